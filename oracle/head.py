@@ -1,0 +1,79 @@
+"""Logprob / KL head oracle: plain float64 restatement (test infrastructure only).
+
+* "GLM Post-Training Beyond SFT", section "IcePop 为什么有两层 ratio":
+  rho_t = pi_train(y_t | s_t) / pi_infer(y_t | s_t) = exp(logp_train - logp_infer)
+  and the trust mask m_t = 1[1/beta <= rho_t <= beta], beta = 2 (keeps
+  rho in [1/2, 2], both ends included).  The rollout pseudo-code in that
+  section computes the train logprob of the exact rollout token ids.
+* Same page, section "动作与概率契约": sampled log-prob precision and the
+  logsumexp reduction must have comparison tests.
+* "Reinforcement Learning: Why Numerical Alignment and MoE Routing Matter So
+  Much", section "混合专家模型更难对齐": k3 is the train/inference divergence
+  metric, with 0.001 as the equivalence threshold.  The page names k3 without
+  its formula; the standard k3 estimator is (r - 1) - log r with
+  r = pi_train / pi_rollout on rollout-sampled tokens (so r = rho), written
+  here as expm1(d) - d with d = logp_train - logp_rollout.
+"""
+import numpy as np
+
+
+def vocab_logits(hidden: np.ndarray, w_vocab: np.ndarray) -> np.ndarray:
+    """Z[t, v] = sum_h hidden[t, h] * Wv[v, h], float64."""
+    return np.asarray(hidden, np.float64) @ np.asarray(w_vocab, np.float64).T
+
+
+def logsumexp_rows(z: np.ndarray) -> np.ndarray:
+    """lse[t] = log sum_v exp(z[t, v]), float64, with the max shift."""
+    z = np.asarray(z, np.float64)
+    m = z.max(axis=1)
+    return m + np.log(np.exp(z - m[:, None]).sum(axis=1))
+
+
+def token_logprob(z: np.ndarray, target: np.ndarray):
+    """log-softmax of row t at the exact target id: z[t, target[t]] - lse[t].
+
+    Returns (logp, lse) in float64.
+    """
+    z = np.asarray(z, np.float64)
+    lse = logsumexp_rows(z)
+    tgt = np.asarray(target, np.int64)
+    logp = z[np.arange(z.shape[0]), tgt] - lse
+    return logp, lse
+
+
+def k3(logp_train, logp_rollout) -> np.ndarray:
+    """k3 = (r - 1) - log r, r = exp(d), d = logp_train - logp_rollout; = expm1(d) - d.
+
+    Exactly 0 when the two logprobs agree; never negative.
+    """
+    d = np.asarray(logp_train, np.float64) - np.asarray(logp_rollout, np.float64)
+    return np.expm1(d) - d
+
+
+def icepop_mask(logp_train, logp_rollout, beta: float = 2.0, dtype=np.float64) -> np.ndarray:
+    """m_t = 1[1/beta <= rho_t <= beta], rho_t = exp(logp_train - logp_rollout).
+
+    ``dtype`` is the precision in which the ratio and the comparison are
+    taken.  Where two implementations must agree on this integer decision they
+    take it in the same precision; the GPU kernel takes it in float32, so the
+    parity tests call this with dtype=np.float32 on the kernel's own float32
+    difference d.
+    """
+    lt = np.asarray(logp_train, dtype)
+    lr = np.asarray(logp_rollout, dtype)
+    d = (lt - lr).astype(dtype)
+    rho = np.exp(d).astype(dtype)
+    b = dtype(beta)
+    lo = dtype(dtype(1.0) / b)
+    return ((lo <= rho) & (rho <= b)).astype(np.uint8)
+
+
+def head_forward(hidden, w_vocab, target, logp_rollout=None, beta=2.0):
+    """Whole head, float64: logits -> lse -> logprob (-> k3, IcePop mask)."""
+    z = vocab_logits(hidden, w_vocab)
+    logp, lse = token_logprob(z, target)
+    out = dict(logits=z, logp=logp, lse=lse)
+    if logp_rollout is not None:
+        out["k3"] = k3(logp, logp_rollout)
+        out["mask"] = icepop_mask(logp, logp_rollout, beta)
+    return out

@@ -1,0 +1,236 @@
+"""MoE layer oracle: plain float64 restatement (test infrastructure only).
+
+What the layer computes, from the pages:
+
+* "位级一致：前沿训练的差异化关键", section "为什么比特级一致是一个复杂的问题":
+  the router and the per-expert matmuls are reductions whose order must depend
+  only on the request; a router near-tie flips which expert fires; the fix is a
+  deterministic tie decision in the router and one fixed kernel choice for the
+  expert matmuls whatever the per-expert token count.
+* "Reinforcement Learning: Why Numerical Alignment and MoE Routing Matter So
+  Much", section "混合专家模型更难对齐": the weighted sum of expert outputs must
+  use the same precision and the same order on both paths.
+* "GLM Post-Training Beyond SFT", section "迁移到 NPU 时": a top-k must pin ties,
+  boundary ties, sort order, NaN handling and the index dtype; compare the
+  index set, its order and the final log-prob.
+
+The method does not change the mathematics of an MoE layer, only the order of
+its floating-point reductions, so the oracle is the textbook definition written
+out in float64 over bf16-rounded inputs.  Readings where the pages are silent
+(gate function, intermediate precisions, NaN rank) are listed in the design doc and
+restated at each function.
+"""
+import numpy as np
+
+from .numerics import bf16_bits_to_f64, round_to_bf16
+
+
+def to_f64(t) -> np.ndarray:
+    """bf16 torch tensor / uint16 array / float array -> float64 numpy array (exact)."""
+    try:
+        import torch
+        if isinstance(t, torch.Tensor):
+            t = t.detach().cpu()
+            if t.dtype == torch.bfloat16:
+                return bf16_bits_to_f64(t.view(torch.int16).numpy().view(np.uint16))
+            return t.to(torch.float64).numpy()
+    except ImportError:  # pragma: no cover - torch is always present in this repo
+        pass
+    a = np.asarray(t)
+    if a.dtype == np.uint16:
+        return bf16_bits_to_f64(a)
+    return a.astype(np.float64)
+
+
+# ----------------------------------------------------------------------------
+# router
+# ----------------------------------------------------------------------------
+
+def router_logits(x: np.ndarray, w_router: np.ndarray) -> np.ndarray:
+    """L[t, e] = sum_h x[t, h] * Wr[e, h], in float64.
+
+    The router is the first reduction the bit-agreement page lists as needing a
+    pinned order; in exact arithmetic it is a plain matrix product.
+    """
+    return np.asarray(x, np.float64) @ np.asarray(w_router, np.float64).T
+
+
+def topk_lowest_index(logits: np.ndarray, k: int) -> np.ndarray:
+    """Per row: the k largest logits, in descending order, exact ties to the lower index.
+
+    Contract (bit-agreement page: "deterministic tie decision in the router";
+    GLM post-training page, "迁移到 NPU 时": ties, sort order and NaN handling
+    must be fixed):
+      * order by logit, largest first;
+      * equal logits (including -0.0 == +0.0) keep ascending expert index;
+      * NaN ranks below every number including -inf; NaNs keep index order.
+    Returns int32 indices of shape [T, k].
+    """
+    L = np.asarray(logits, np.float64)
+    T, E = L.shape
+    if not (0 < k <= E):
+        raise ValueError("need 0 < k <= E")
+    nan = np.isnan(L)
+    neg = np.where(nan, 0.0, -L)              # ascending -L == descending L; -(-0.0) == 0.0 ties
+    idx = np.broadcast_to(np.arange(E), (T, E))
+    # np.lexsort: the last key is the primary key.  Primary: NaN last.
+    order = np.lexsort((idx, neg, nan), axis=-1)
+    return order[:, :k].astype(np.int32)
+
+
+def topk_gates(logits: np.ndarray, topk_idx: np.ndarray) -> np.ndarray:
+    """Gate weights: softmax over the k selected logits (renormalised over top-k).
+
+    The pages do not name the gate function; the workload description fixes
+    "fp32 softmax gating weights renormalised over top-k".  Softmax over the
+    selected logits equals the full softmax renormalised over the selected set.
+    Computed here in float64 with the usual max shift.
+    """
+    L = np.asarray(logits, np.float64)
+    sel = np.take_along_axis(L, topk_idx.astype(np.int64), axis=1)
+    m = sel.max(axis=1, keepdims=True)
+    ex = np.exp(sel - m)
+    return ex / ex.sum(axis=1, keepdims=True)
+
+
+# ----------------------------------------------------------------------------
+# experts
+# ----------------------------------------------------------------------------
+
+def silu(g: np.ndarray) -> np.ndarray:
+    """silu(g) = g * sigmoid(g) = g / (1 + exp(-g)), float64."""
+    g = np.asarray(g, np.float64)
+    with np.errstate(over="ignore"):
+        return g / (1.0 + np.exp(-g))
+
+
+def swiglu_expert(x_rows: np.ndarray, w13: np.ndarray, w2: np.ndarray, F: int,
+                  round_h: bool = True) -> np.ndarray:
+    """One SwiGLU expert on a block of rows, float64.
+
+    w13 is [2F, H]: rows 0..F-1 the gate projection, rows F..2F-1 the up
+    projection; w2 is [H, F] (the down projection).
+        g = x Wg^T,  u = x Wu^T,  h = silu(g) * u,  y = h W2^T.
+    The hidden activation h is the bf16 input of the down projection, so it is
+    rounded to bf16 (nearest-even) before the second product when round_h.
+    """
+    x_rows = np.asarray(x_rows, np.float64)
+    w13 = np.asarray(w13, np.float64)
+    g = x_rows @ w13[:F].T
+    u = x_rows @ w13[F:2 * F].T
+    h = silu(g) * u
+    if round_h:
+        h = round_to_bf16(h)
+    return h @ np.asarray(w2, np.float64).T
+
+
+def expert_outputs(x, topk_idx, w13, w2, F, round_h=True, expert_weights=None):
+    """y[t, j, :] = expert_{idx[t,j]}(x[t]) for every token and slot, float64.
+
+    ``w13``/``w2`` may be float64 arrays [E, 2F, H] / [E, H, F] or a callable
+    ``expert_weights(e) -> (w13_e, w2_e)`` so large configurations can feed one
+    expert at a time.
+    """
+    x = np.asarray(x, np.float64)
+    T, k = topk_idx.shape
+    H = x.shape[1]
+    y = np.zeros((T, k, H), np.float64)
+    for e in np.unique(topk_idx):
+        tok, slot = np.nonzero(topk_idx == e)
+        if expert_weights is not None:
+            w13_e, w2_e = expert_weights(int(e))
+        else:
+            w13_e, w2_e = w13[e], w2[e]
+        y[tok, slot] = swiglu_expert(x[tok], w13_e, w2_e, F, round_h)
+    return y
+
+
+def combine(y_slots: np.ndarray, gates: np.ndarray, y_shared=None) -> np.ndarray:
+    """out[t] = sum_j gates[t, j] * y[t, j] (+ shared-expert output), float64.
+
+    The combine page finding is that precision and order of this weighted sum
+    must match across paths; in float64 the order of the k terms does not
+    matter at the tolerance the GPU path is held to, so the oracle takes the
+    slots in rank order j = 0..k-1 and adds the shared expert last, as the GPU
+    path does.
+    """
+    out = np.zeros(y_slots.shape[0::2], np.float64)
+    for j in range(y_slots.shape[1]):
+        out += gates[:, j:j + 1] * y_slots[:, j]
+    if y_shared is not None:
+        out += y_shared
+    return out
+
+
+def moe_forward(x, w_router, w13, w2, k, F, ws13=None, ws2=None, F_shared=0,
+                round_h=True, expert_weights=None, logits=None):
+    """Whole MoE layer, float64: router -> top-k -> gates -> experts -> combine.
+
+    ``logits`` may be supplied (for example float32 logits produced elsewhere)
+    to re-run only the selection and what follows on them.
+    Returns a dict with logits, idx, gates, y (per slot), y_shared, out.
+    """
+    x = np.asarray(x, np.float64)
+    if logits is None:
+        logits = router_logits(x, w_router)
+    idx = topk_lowest_index(logits, k)
+    gates = topk_gates(logits, idx)
+    y = expert_outputs(x, idx, w13, w2, F, round_h, expert_weights)
+    ys = None
+    if F_shared:
+        ys = swiglu_expert(x, ws13, ws2, F_shared, round_h)
+    out = combine(y, gates, ys)
+    return dict(logits=logits, idx=idx, gates=gates, y=y, y_shared=ys, out=out)
+
+
+def dense_all_experts_then_mask(x, w_router, w13, w2, k, F, round_h=True):
+    """Brute force: run every expert on every token, then keep the top-k.
+
+    out[t] = sum_e 1[e in topk(t)] * gate_e(t) * expert_e(x[t]).
+    Independent of the permutation / dispatch bookkeeping of ``moe_forward``;
+    the two must agree to float64 rounding.
+    """
+    x = np.asarray(x, np.float64)
+    E = w13.shape[0]
+    L = router_logits(x, w_router)
+    idx = topk_lowest_index(L, k)
+    gates = topk_gates(L, idx)
+    T = x.shape[0]
+    gate_full = np.zeros((T, E), np.float64)
+    for j in range(k):
+        gate_full[np.arange(T), idx[:, j]] = gates[:, j]
+    out = np.zeros_like(x)
+    for e in range(E):
+        ye = swiglu_expert(x, w13[e], w2[e], F, round_h)
+        out += (gate_full[:, e] != 0)[:, None] * gate_full[:, e:e + 1] * ye
+    return out
+
+
+# ----------------------------------------------------------------------------
+# dispatch plan (permutation) -- checked as invariants, not recomputed by value
+# ----------------------------------------------------------------------------
+
+def dispatch_plan(topk_idx: np.ndarray, E: int):
+    """Expert-major permutation of the (token, slot) pairs, float-free.
+
+    Rows of expert e occupy [offsets[e], offsets[e+1]); inside an expert the
+    rows follow ascending token index (a stable counting sort).  Returns
+    counts[E], offsets[E+1], row_token[S], slot_row[T, k] (all int64).
+    Implied by the bit-agreement page's "per-expert token count" and its call
+    for one fixed expert-matmul kernel whatever that count.
+    """
+    idx = np.asarray(topk_idx, np.int64)
+    T, k = idx.shape
+    counts = np.bincount(idx.ravel(), minlength=E)
+    offsets = np.zeros(E + 1, np.int64)
+    offsets[1:] = np.cumsum(counts)
+    row_token = np.empty(T * k, np.int64)
+    slot_row = np.empty((T, k), np.int64)
+    fill = offsets[:-1].copy()
+    for t in range(T):                      # ascending token order
+        for j in range(k):
+            e = idx[t, j]
+            row_token[fill[e]] = t
+            slot_row[t, j] = fill[e]
+            fill[e] += 1
+    return counts, offsets, row_token, slot_row

@@ -1,0 +1,222 @@
+"""Pins for oracle.moe against brute force, closed forms and library routines."""
+from fractions import Fraction
+import itertools
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from oracle import moe
+from oracle.numerics import round_to_bf16
+from serve_invariant_moe_gb300 import synth
+
+
+# ---------------------------------------------------------------- router logits
+
+def test_router_logits_exact_on_integers():
+    # brute force in exact rational arithmetic on a tiny integer-valued input
+    rng = np.random.default_rng(3)
+    x = rng.integers(-4, 5, size=(5, 7)).astype(np.float64)
+    w = rng.integers(-4, 5, size=(3, 7)).astype(np.float64)
+    L = moe.router_logits(x, w)
+    assert L.shape == (5, 3)
+    for t in range(5):
+        for e in range(3):
+            ref = sum(Fraction(int(x[t, h])) * Fraction(int(w[e, h])) for h in range(7))
+            assert L[t, e] == float(ref)
+
+
+def test_router_onehot_token_reads_one_column():
+    rng = np.random.default_rng(4)
+    w = rng.standard_normal((6, 9))
+    x = np.eye(9)[[2, 7]]
+    L = moe.router_logits(x, w)
+    assert np.array_equal(L[0], w[:, 2]) and np.array_equal(L[1], w[:, 7])
+
+
+# ---------------------------------------------------------------- top-k contract
+
+def _brute_topk(row, k):
+    """Rank counting: expert e beats f iff (e is not NaN and f is NaN) or
+    L_e > L_f or (L_e == L_f, both or neither NaN, and e < f)."""
+    E = len(row)
+
+    def beats(e, f):
+        ne, nf = np.isnan(row[e]), np.isnan(row[f])
+        if ne != nf:
+            return nf
+        if ne and nf:
+            return e < f
+        if row[e] != row[f]:
+            return row[e] > row[f]
+        return e < f
+
+    rank = [sum(beats(f, e) for f in range(E) if f != e) for e in range(E)]
+    order = sorted(range(E), key=lambda e: rank[e])
+    return order[:k]
+
+
+def test_topk_brute_force_with_ties_nan_inf_signed_zero():
+    rng = np.random.default_rng(5)
+    pool = np.array([-2.0, -1.0, -0.0, 0.0, 1.0, 2.0, np.inf, -np.inf, np.nan])
+    rows = pool[rng.integers(0, len(pool), size=(400, 8))]
+    for k in (1, 2, 3, 8):
+        got = moe.topk_lowest_index(rows, k)
+        for t in range(rows.shape[0]):
+            assert list(got[t]) == _brute_topk(rows[t], k), (rows[t], k)
+
+
+def test_topk_hand_cases():
+    assert list(moe.topk_lowest_index(np.zeros((1, 6)), 4)[0]) == [0, 1, 2, 3]
+    assert list(moe.topk_lowest_index(np.full((1, 4), np.nan), 2)[0]) == [0, 1]
+    row = np.array([[np.nan, -np.inf, 0.0, -0.0]])
+    assert list(moe.topk_lowest_index(row, 4)[0]) == [2, 3, 1, 0]
+    row = np.array([[1.0, 3.0, 3.0, 2.0, 3.0]])
+    assert list(moe.topk_lowest_index(row, 3)[0]) == [1, 2, 4]
+    assert moe.topk_lowest_index(row, 3).dtype == np.int32
+
+
+def test_duplicated_router_rows_tie_to_lower_index():
+    cfg = synth.TINY
+    x, wr = synth.moe_activations(cfg)
+    L = moe.router_logits(moe.to_f64(x), moe.to_f64(wr))
+    assert np.array_equal(L[:, 0::2], L[:, 1::2])          # exact ties
+    idx = moe.topk_lowest_index(L, cfg.k)
+    # each token's top-2 is one duplicated pair, lower index first
+    assert np.all(idx[:, 0] % 2 == 0) and np.all(idx[:, 1] == idx[:, 0] + 1)
+    g = moe.topk_gates(L, idx)
+    assert np.array_equal(g, np.full_like(g, 0.5))
+
+
+# ---------------------------------------------------------------- gates
+
+def test_gates_match_scipy_softmax():
+    rng = np.random.default_rng(6)
+    L = rng.standard_normal((50, 16)) * 3
+    idx = moe.topk_lowest_index(L, 4)
+    g = moe.topk_gates(L, idx)
+    sel = np.take_along_axis(L, idx.astype(np.int64), 1)
+    assert np.allclose(g, scipy.special.softmax(sel, axis=1), rtol=1e-14, atol=0)
+    assert np.allclose(g.sum(1), 1.0, rtol=0, atol=1e-15)
+    # descending logits give non-increasing gates
+    assert np.all(np.diff(g, axis=1) <= 0)
+
+
+def test_gates_equal_logits():
+    g = moe.topk_gates(np.full((3, 8), 1.25), moe.topk_lowest_index(np.full((3, 8), 1.25), 4))
+    assert np.array_equal(g, np.full((3, 4), 0.25))
+
+
+def test_gates_are_full_softmax_renormalised():
+    rng = np.random.default_rng(7)
+    L = rng.standard_normal((20, 10))
+    idx = moe.topk_lowest_index(L, 3)
+    full = scipy.special.softmax(L, axis=1)
+    sel = np.take_along_axis(full, idx.astype(np.int64), 1)
+    assert np.allclose(moe.topk_gates(L, idx), sel / sel.sum(1, keepdims=True), rtol=1e-13)
+
+
+# ---------------------------------------------------------------- SwiGLU expert
+
+def test_silu_matches_scipy():
+    g = np.linspace(-30, 30, 1001)
+    assert np.allclose(moe.silu(g), g * scipy.special.expit(g), rtol=1e-14, atol=1e-300)
+    assert moe.silu(np.array([0.0]))[0] == 0.0
+
+
+def test_swiglu_expert_structure():
+    # gate = identity, up = a constant-one column, down = a permutation:
+    # y = round_bf16(silu(x))[:, perm]  -- catches swapped gate/up and a
+    # transposed down projection (the permutation is not an involution).
+    H = F = 6
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((5, H))
+    x[:, H - 1] = 1.0
+    wg = np.eye(F, H)
+    wu = np.zeros((F, H)); wu[:, H - 1] = 1.0
+    perm = np.array([1, 2, 3, 4, 5, 0])
+    w2 = np.eye(H)[perm]                    # (h @ w2.T)[:, i] = h[:, perm[i]]
+    y = moe.swiglu_expert(x, np.concatenate([wg, wu]), w2, F)
+    h = torch.nn.functional.silu(torch.from_numpy(x)).numpy()
+    h = torch.from_numpy(h.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    # float32 step above is exact for these magnitudes only if h is a float32;
+    # compare against the oracle's single-step rounding of the library silu.
+    ref = round_to_bf16(torch.nn.functional.silu(torch.from_numpy(x)).numpy())[:, perm]
+    assert np.array_equal(y, ref)
+    assert np.allclose(y, h[:, perm], rtol=1e-2)
+
+
+def _tiny_layer(T=24, H=32, E=6, k=2, F=16, seed=9):
+    rng = np.random.default_rng(seed)
+    x = round_to_bf16(rng.standard_normal((T, H)))
+    wr = round_to_bf16(rng.standard_normal((E, H)) * 0.2)
+    w13 = round_to_bf16(rng.standard_normal((E, 2 * F, H)) * 0.2)
+    w2 = round_to_bf16(rng.standard_normal((E, H, F)) * 0.2)
+    return x, wr, w13, w2
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 6])
+def test_sparse_equals_dense_all_experts_then_mask(k):
+    x, wr, w13, w2 = _tiny_layer(k=k)
+    sparse = moe.moe_forward(x, wr, w13, w2, k, 16)["out"]
+    dense = moe.dense_all_experts_then_mask(x, wr, w13, w2, k, 16)
+    assert np.allclose(sparse, dense, rtol=1e-12, atol=1e-12)
+
+
+def test_single_expert_k1_is_plain_mlp():
+    x, wr, w13, w2 = _tiny_layer(E=1, k=1)
+    out = moe.moe_forward(x, wr, w13, w2, 1, 16)["out"]
+    assert np.array_equal(out, moe.swiglu_expert(x, w13[0], w2[0], 16))
+
+
+def test_shared_expert_added():
+    x, wr, w13, w2 = _tiny_layer()
+    rng = np.random.default_rng(10)
+    ws13 = round_to_bf16(rng.standard_normal((2 * 8, 32)) * 0.2)
+    ws2 = round_to_bf16(rng.standard_normal((32, 8)) * 0.2)
+    a = moe.moe_forward(x, wr, w13, w2, 2, 16)["out"]
+    b = moe.moe_forward(x, wr, w13, w2, 2, 16, ws13, ws2, 8)["out"]
+    assert np.allclose(b - a, moe.swiglu_expert(x, ws13, ws2, 8), rtol=1e-12, atol=1e-12)
+
+
+def test_dispatch_plan_invariants():
+    rng = np.random.default_rng(11)
+    T, E, k = 50, 7, 3
+    L = rng.standard_normal((T, E))
+    L[:, 5] = -1e9                      # expert 5 never chosen: an empty segment
+    idx = moe.topk_lowest_index(L, k)
+    counts, offsets, row_token, slot_row = moe.dispatch_plan(idx, E)
+    assert counts.sum() == T * k and counts[5] == 0
+    assert offsets[0] == 0 and offsets[-1] == T * k
+    assert np.array_equal(np.diff(offsets), counts)
+    for e in range(E):
+        seg = row_token[offsets[e]:offsets[e + 1]]
+        assert np.all(np.diff(seg) > 0)              # ascending, no repeats
+        assert set(seg) == set(np.nonzero((idx == e).any(1))[0])
+    for t in range(T):
+        for j in range(k):
+            r = slot_row[t, j]
+            assert row_token[r] == t and offsets[idx[t, j]] <= r < offsets[idx[t, j] + 1]
+    # the multiset of rows is a permutation
+    assert sorted(slot_row.ravel()) == list(range(T * k))
+
+
+def test_combine_is_gate_weighted_sum():
+    rng = np.random.default_rng(12)
+    y = rng.standard_normal((4, 3, 5))
+    g = rng.random((4, 3))
+    ys = rng.standard_normal((4, 5))
+    ref = np.einsum("tj,tjh->th", g, y) + ys
+    assert np.allclose(moe.combine(y, g, ys), ref, rtol=1e-14, atol=1e-14)
+    # a single slot with gate 1 returns that slot's output
+    assert np.array_equal(moe.combine(y[:, :1], np.ones((4, 1))), y[:, 0])
+
+
+def test_skewed_layer_has_busy_experts():
+    cfg = synth.QWEN_MOE
+    x, wr = synth.moe_activations(cfg)
+    idx = moe.topk_lowest_index(moe.router_logits(moe.to_f64(x), moe.to_f64(wr)), cfg.k)
+    counts = np.bincount(idx.ravel(), minlength=cfg.E)
+    assert 1200 <= counts.max() <= 1800
+    assert counts.sum() == cfg.T * cfg.k
