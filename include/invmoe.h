@@ -1,0 +1,198 @@
+/*
+ * invmoe.h -- C ABI of the batch-invariant MoE layer and logprob/KL head (sm_103a).
+ *
+ * What the library computes (sources cited by page title and section):
+ *
+ *   "位级一致：前沿训练的差异化关键" (Fireworks, bit-level agreement for frontier
+ *   training), section "为什么比特级一致是一个复杂的问题": a request must get the
+ *   same bits whatever else shares its batch.  The router and the expert matmuls
+ *   are reductions whose order must depend only on the request; the router needs
+ *   a deterministic tie decision; the expert matmuls need one fixed kernel choice
+ *   whatever the per-expert token count (no split-K: the page notes DeepGEMM
+ *   dropped it because split-K breaks invariance).
+ *
+ *   "Reinforcement Learning: Why Numerical Alignment and MoE Routing Matter So
+ *   Much", section "混合专家模型更难对齐": the weighted sum of expert outputs
+ *   must use a pinned precision and order; k3 is the divergence metric.
+ *
+ *   "GLM Post-Training Beyond SFT", section "IcePop 为什么有两层 ratio": the
+ *   train logprob of the exact rollout token ids, the mismatch ratio
+ *   rho = exp(logp_train - logp_rollout) and the mask 1[1/beta <= rho <= beta].
+ *   Section "迁移到 NPU 时": a top-k must fix ties, order, NaN handling and the
+ *   index dtype.  Section "动作与概率契约": logsumexp needs comparison tests.
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers owned by the caller unless stated otherwise.
+ *     The library allocates no device memory; it keeps only small host-side
+ *     caches (SM count, kernel attributes).
+ *   - bf16 tensors are passed as void* (raw IEEE bfloat16, row-major).
+ *     float is IEEE binary32.  Index tensors are int32.
+ *   - All work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).  Arguments are validated on the
+ *     host before anything is launched; on a validation error nothing is
+ *     launched and the outputs are untouched.
+ *   - Return value: INVMOE_OK (0) or a negative INVMOE_ERR_* code; the last
+ *     error message of the calling thread is available from invmoe_last_error().
+ *   - Device-side faults that the kernels detect themselves (a bounded wait that
+ *     ran out) are recorded in a status word inside `workspace` and reported by
+ *     invmoe_check(); the kernel that detected it stops early and its outputs
+ *     are undefined.
+ *   - Alignment: every tensor pointer must be 16-byte aligned.
+ *   - Batch invariance: for a fixed model shape (H, E, k, F, F_shared, V) the
+ *     bits of every per-token output depend only on that token's inputs, never
+ *     on T, on the other tokens, or on the token's position in the batch.
+ */
+#ifndef INVMOE_H
+#define INVMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define INVMOE_OK                       0
+#define INVMOE_ERR_INVALID_ARG         -1  /* null pointer, negative size, k > E, bad beta ...   */
+#define INVMOE_ERR_UNSUPPORTED_SHAPE   -2  /* a size the kernels do not tile (see each call)     */
+#define INVMOE_ERR_WORKSPACE_TOO_SMALL -3  /* ws_bytes < invmoe_workspace_size(...)              */
+#define INVMOE_ERR_MISALIGNED          -4  /* a pointer is not 16-byte aligned                   */
+#define INVMOE_ERR_CUDA                -5  /* a CUDA runtime/driver call or a launch failed      */
+#define INVMOE_ERR_DEVICE_TIMEOUT      -6  /* a kernel's bounded wait ran out (invmoe_check)     */
+
+/* Library version (major*10000 + minor*100 + patch). */
+int invmoe_version(void);
+
+/* Message describing the last failing call made by this thread ("" if none). */
+const char* invmoe_last_error(void);
+
+/* Number of int32 elements of the dispatch plan for T tokens, E experts, top-k:
+ *   plan = counts[E] | offsets[E+1] | row_token[T*k] | slot_row[T*k]
+ *   counts[e]     tokens routed to expert e
+ *   offsets[e]    first permuted row of expert e (offsets[0] = 0, offsets[E] = T*k);
+ *                 rows of one expert are contiguous and in ascending token order
+ *   row_token[r]  token whose activation sits in permuted row r
+ *   slot_row[t*k + j]  permuted row holding token t's j-th ranked expert
+ * The permuted row count R is exactly T*k (segments are not padded; tiles that
+ * run past a segment end are masked in the kernels). */
+size_t invmoe_plan_len(int T, int E, int k);
+
+/* Bytes of device workspace that every call below accepts for these sizes
+ * (F_shared = 0: no shared expert; V = 0: no head).  One workspace may be
+ * reused by consecutive calls on one stream; calls that may run concurrently
+ * need separate workspaces.  The first 256 bytes hold the status word; the
+ * caller zero-fills the workspace once before first use. */
+size_t invmoe_workspace_size(int T, int H, int E, int k, int F, int F_shared, int V);
+
+/* Synchronise `stream`, read and clear the status word in `workspace`.
+ * Returns INVMOE_OK or INVMOE_ERR_DEVICE_TIMEOUT (a kernel gave up waiting). */
+int invmoe_check(void* workspace, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_route_topk -- router logits, top-k with lowest-index ties, gates, dispatch
+ *
+ *   logits[t, e] = sum_h x[t, h] * w_router[e, h]           (fp32 accumulate,
+ *                  tcgen05 tile 128 x BN x 64, K ascending, no split-K)
+ *   topk_idx[t, 0..k-1]: the k largest logits of row t, largest first; exact
+ *                  ties (and -0 vs +0) go to the lower expert index; NaN ranks
+ *                  below -inf.
+ *   topk_w[t, j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the k selected
+ *                  logits (softmax renormalised over the top-k, fp32, i ascending)
+ *   plan         see invmoe_plan_len (deterministic counting sort; no atomics
+ *                  decide any position)
+ *   xp[r, :]     = x[row_token[r], :]   (bf16 gather, 16-byte vectors)
+ *
+ * x [T, H] bf16, w_router [E, H] bf16, logits [T, E] fp32, topk_idx [T, k] int32,
+ * topk_w [T, k] fp32, plan int32[invmoe_plan_len], xp [T*k, H] bf16.
+ * Shapes: T >= 0, H % 64 == 0, 1 <= E <= 1024, 1 <= k <= min(E, 32).
+ * ------------------------------------------------------------------------- */
+int moe_route_topk(const void* x, const void* w_router, int T, int H, int E, int k,
+                   float* logits, int32_t* topk_idx, float* topk_w, int32_t* plan,
+                   void* xp, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_grouped_ffn -- grouped SwiGLU expert GEMMs (+ optional shared expert)
+ *
+ * For every expert e and each of its permuted rows r in [offsets[e], offsets[e+1]):
+ *   g = xp[r] . Wg_e^T,  u = xp[r] . Wu_e^T      (fp32 in TMEM, K ascending)
+ *   h[r, f] = bf16_rne( silu(g_f) * u_f ),  silu(g) = g / (1 + exp(-g))  (fp32)
+ *   y[r, :] = h[r] . W2_e^T                       (fp32 accumulate, stored fp32)
+ * One tile shape (128 rows x 256 columns x 64 K) for every expert whatever its
+ * row count; K is always walked in ascending order; no split-K.
+ * Shared expert (F_shared > 0): the same two GEMMs over all T tokens of
+ * x_shared with ws13/ws2, result in y_shared [T, H] fp32.
+ *
+ * xp [T*k, H] bf16, plan from moe_route_topk, w13 [E, 2F, H] bf16 (rows 0..F-1
+ * gate, F..2F-1 up), w2 [E, H, F] bf16, h [T*k, F] bf16, y [T*k, H] fp32,
+ * x_shared [T, H] bf16, ws13 [2*F_shared, H] bf16, ws2 [H, F_shared] bf16.
+ * Shapes: H % 64 == 0, F % 128 == 0, F_shared % 128 == 0.
+ * ------------------------------------------------------------------------- */
+int moe_grouped_ffn(const void* xp, const int32_t* plan, const void* w13, const void* w2,
+                    int T, int H, int E, int k, int F, void* h, float* y,
+                    const void* x_shared, const void* ws13, const void* ws2, int F_shared,
+                    float* y_shared, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_combine -- fp32 fixed-order weighted combine
+ *
+ *   out[t, :] = ((w[t,0]*y[slot_row[t,0]] + w[t,1]*y[slot_row[t,1]]) + ...)
+ *               + y_shared[t]      (if y_shared != NULL)
+ * in fp32, slots in rank order j = 0..k-1, every product and sum rounded
+ * separately (no fused multiply-add), shared expert added last.
+ * out_bf16 (nullable) receives bf16_rne(out).
+ * y [T*k, H] fp32, topk_w [T, k] fp32, plan from moe_route_topk, out [T, H] fp32.
+ * Shapes: H % 4 == 0.
+ * ------------------------------------------------------------------------- */
+int moe_combine(const float* y, const float* topk_w, const int32_t* plan, const float* y_shared,
+                int T, int H, int E, int k, float* out, void* out_bf16, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * lm_logprob_kl -- vocab projection, chunked two-pass log-sum-exp, logprob, k3, IcePop
+ *
+ *   logits[t, v] = sum_h hidden[t, h] * w_vocab[v, h]       (fp32, tcgen05 tile)
+ *   pass 1, chunk c = columns [256c, 256c+256):  m_c = max, s_c = sum exp(z - m_c)
+ *           (fixed per-lane order then a fixed butterfly)
+ *   pass 2, c = 0, 1, 2, ... in order:  M' = max(M, m_c);
+ *           S = S*exp(M - M') + s_c*exp(m_c - M');  lse = M + log(S)
+ *   logp[t] = logits[t, target[t]] - lse[t]
+ *   if rollout_logp != NULL:
+ *     d = logp - rollout_logp;  k3 = expm1(d) - d;  rho = exp(d);
+ *     mask = (1/beta <= rho) && (rho <= beta)      (all fp32)
+ * A target outside [0, V) yields logp = NaN for that token.
+ *
+ * hidden [T, H] bf16, w_vocab [V, H] bf16, target [T] int32, rollout_logp [T]
+ * fp32 (nullable: k3/mask not written), logits [T, V] fp32 (written; the
+ * caller's buffer), logp/lse/k3 [T] fp32, mask [T] uint8 (k3, mask nullable).
+ * Shapes: H % 64 == 0, V % 4 == 0, beta >= 1.
+ * ------------------------------------------------------------------------- */
+int lm_logprob_kl(const void* hidden, const void* w_vocab, const int32_t* target,
+                  const float* rollout_logp, int T, int H, int V, float beta,
+                  float* logits, float* logp, float* lse, float* k3, uint8_t* mask,
+                  void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Diagnostics
+ * ------------------------------------------------------------------------- */
+
+/* d[m, n] = sum_k a[m, k] * b[n, k] (fp32 out, ldd = N): the dense tcgen05 GEMM
+ * engine on its own, used by the tests to check the engine at ragged sizes.
+ * variant selects the tile configuration the other calls use:
+ *   0 = 128 x 256 tile, one row tile per unit (vocab projection)
+ *   1 = 128 x 256 tile, two row tiles per unit (expert down projection)
+ *   2 = 128 x 128 tile, 3 = 128 x 64 tile (router logits for E <= 128 / 64)
+ * a [M, K] bf16, b [N, K] bf16.  Shapes: K % 64 == 0, N % 4 == 0. */
+int invmoe_gemm_bf16(const void* a, const void* b, int M, int N, int K, float* d, int variant,
+                     void* workspace, size_t ws_bytes, void* stream);
+
+/* Launch a one-CTA kernel that waits on an mbarrier nothing ever completes,
+ * with a wait limit of `timeout_us` microseconds (1..2000000).  The kernel
+ * gives up, records INVMOE_ERR_DEVICE_TIMEOUT in the status word and returns;
+ * invmoe_check() must then report it.  Exercises the timeout path without
+ * hanging or faulting the GPU. */
+int invmoe_debug_timeout_probe(void* workspace, size_t ws_bytes, int timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* INVMOE_H */

@@ -1,0 +1,126 @@
+"""Prefill and decode entry points over the C ABI.
+
+Both entry points run the same three library calls (moe_route_topk,
+moe_grouped_ffn, moe_combine) with the same kernels and tile shapes; they differ
+only on the host side.  Prefill takes any number of tokens in one call; decode
+serves one token per request from buffers allocated once for a maximum batch.
+Because every reduction in the library is per token with a fixed order, a
+token's output bits do not depend on which entry point served it or on what
+else was in its batch ("位级一致：前沿训练的差异化关键", section "端到端零 KLD":
+the serving engine and the trainer must produce the same numbers whatever the
+batch size or concurrent load).
+"""
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import binding
+
+
+@dataclass
+class MoEWeights:
+    w_router: torch.Tensor            # [E, H] bf16
+    w13: torch.Tensor                 # [E, 2F, H] bf16 (gate rows, then up rows)
+    w2: torch.Tensor                  # [E, H, F] bf16
+    k: int
+    ws13: Optional[torch.Tensor] = None   # [2Fs, H] bf16 shared expert
+    ws2: Optional[torch.Tensor] = None    # [H, Fs] bf16
+
+    @property
+    def E(self):
+        return self.w13.shape[0]
+
+    @property
+    def H(self):
+        return self.w13.shape[2]
+
+    @property
+    def F(self):
+        return self.w13.shape[1] // 2
+
+    @property
+    def F_shared(self):
+        return 0 if self.ws13 is None else self.ws13.shape[0] // 2
+
+
+class MoELayer:
+    """Batch-invariant MoE layer forward on one GPU."""
+
+    def __init__(self, weights: MoEWeights):
+        self.w = weights
+        self._ws = None
+        self._decode = None
+
+    def _workspace(self, T):
+        w = self.w
+        need = binding.workspace_size(T, w.H, w.E, w.k, w.F, w.F_shared, 0)
+        if self._ws is None or self._ws.numel() < need:
+            self._ws = binding.new_workspace(need, device=w.w13.device)
+        return self._ws
+
+    def _run(self, x, ws, bufs=None, out_bf16=None):
+        w = self.w
+        T = x.shape[0]
+        bufs = bufs or {}
+        r = binding.moe_route_topk(x, w.w_router, w.k, ws, logits=bufs.get("logits"), topk_idx=bufs.get("idx"),
+                                   topk_w=bufs.get("w"), plan=bufs.get("plan"), xp=bufs.get("xp"))
+        f = binding.moe_grouped_ffn(r["xp"], r["plan"], w.w13, w.w2, T, w.k, ws, h=bufs.get("h"), y=bufs.get("y"),
+                                    x_shared=x if w.ws13 is not None else None, ws13=w.ws13, ws2=w.ws2,
+                                    y_shared=bufs.get("ys"))
+        out = binding.moe_combine(f["y"], r["topk_w"], r["plan"], T, w.H, w.E, w.k, y_shared=f["y_shared"],
+                                  out=bufs.get("out"), out_bf16=out_bf16)
+        return dict(out=out, **r, **f)
+
+    def prefill(self, x: torch.Tensor, out_bf16: Optional[torch.Tensor] = None, return_all=False):
+        """x [T, H] bf16 -> out [T, H] fp32 (optionally also a bf16 copy)."""
+        res = self._run(x, self._workspace(x.shape[0]), out_bf16=out_bf16)
+        return res if return_all else res["out"]
+
+    def alloc_decode(self, max_batch: int):
+        """Preallocate decode buffers for up to ``max_batch`` concurrent requests."""
+        w = self.w
+        B, dev = max_batch, w.w13.device
+        S = B * w.k
+        self._decode = dict(
+            B=B,
+            logits=torch.empty((B, w.E), dtype=torch.float32, device=dev),
+            idx=torch.empty((B, w.k), dtype=torch.int32, device=dev),
+            w=torch.empty((B, w.k), dtype=torch.float32, device=dev),
+            plan=torch.empty(binding.plan_len(B, w.E, w.k), dtype=torch.int32, device=dev),
+            xp=torch.empty((S, w.H), dtype=torch.bfloat16, device=dev),
+            h=torch.empty((S, w.F), dtype=torch.bfloat16, device=dev),
+            y=torch.empty((S, w.H), dtype=torch.float32, device=dev),
+            ys=torch.empty((B, w.H), dtype=torch.float32, device=dev) if w.ws13 is not None else None,
+            out=torch.empty((B, w.H), dtype=torch.float32, device=dev),
+            ws=binding.new_workspace(binding.workspace_size(B, w.H, w.E, w.k, w.F, w.F_shared, 0), dev),
+        )
+
+    def decode(self, x_tokens: torch.Tensor) -> torch.Tensor:
+        """One token per request: x_tokens [B, H] bf16 -> [B, H] fp32 (a view of the decode buffer)."""
+        B = x_tokens.shape[0]
+        if self._decode is None or self._decode["B"] < B:
+            self.alloc_decode(max(B, 1))
+        d = self._decode
+        w = self.w
+        bufs = dict(logits=d["logits"][:B], idx=d["idx"][:B], w=d["w"][:B], plan=d["plan"], xp=d["xp"],
+                    h=d["h"], y=d["y"], ys=None if d["ys"] is None else d["ys"][:B], out=d["out"][:B])
+        return self._run(x_tokens, d["ws"], bufs)["out"]
+
+
+def moe_prefill(layer: MoELayer, x: torch.Tensor) -> torch.Tensor:
+    return layer.prefill(x)
+
+
+def moe_decode(layer: MoELayer, x_tokens: torch.Tensor) -> torch.Tensor:
+    return layer.decode(x_tokens)
+
+
+def head_logprob_kl(hidden, w_vocab, target, rollout_logp=None, beta=2.0, workspace=None, logits=None):
+    """Token logprobs of the exact target ids, and (with rollout logprobs) k3 and the IcePop mask."""
+    T, H = hidden.shape
+    V = w_vocab.shape[0]
+    if workspace is None:
+        workspace = binding.new_workspace(binding.workspace_size(T, H, V=V), hidden.device)
+    return binding.lm_logprob_kl(hidden, w_vocab, target, workspace, rollout_logp=rollout_logp, beta=beta,
+                                 logits=logits)

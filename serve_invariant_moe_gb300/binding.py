@@ -1,0 +1,165 @@
+"""Python binding of the C ABI: argument marshalling only.
+
+Each function checks dtypes/devices/contiguity, allocates missing outputs with
+torch (device memory only), passes raw pointers and the current CUDA stream to
+libinvmoe.so and raises on a non-zero status.  No arithmetic of the hot path
+happens here: every step runs in the library's kernels.
+"""
+import ctypes
+
+import torch
+
+from ._lib import check, lib
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _req(t, dtype, name, shape=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def plan_len(T, E, k) -> int:
+    return int(lib().invmoe_plan_len(T, E, k))
+
+
+def workspace_size(T, H, E=0, k=0, F=0, F_shared=0, V=0) -> int:
+    return int(lib().invmoe_workspace_size(T, H, E, k, F, F_shared, V))
+
+
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """Zero-filled device workspace (the first 256 bytes are the status word)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def check_status(workspace: torch.Tensor):
+    """Synchronise the current stream and raise if a kernel's bounded wait ran out."""
+    check(lib().invmoe_check(_p(workspace), _stream()))
+
+
+def moe_route_topk(x, w_router, k, workspace, logits=None, topk_idx=None, topk_w=None, plan=None, xp=None):
+    T, H = x.shape
+    E = w_router.shape[0]
+    dev = x.device
+    _req(x, torch.bfloat16, "x")
+    _req(w_router, torch.bfloat16, "w_router", (E, H))
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev) if logits is None else logits
+    topk_idx = torch.empty((T, k), dtype=torch.int32, device=dev) if topk_idx is None else topk_idx
+    topk_w = torch.empty((T, k), dtype=torch.float32, device=dev) if topk_w is None else topk_w
+    plan = torch.empty(plan_len(T, E, k), dtype=torch.int32, device=dev) if plan is None else plan
+    xp = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev) if xp is None else xp
+    _req(logits, torch.float32, "logits", (T, E))
+    _req(topk_idx, torch.int32, "topk_idx", (T, k))
+    _req(topk_w, torch.float32, "topk_w", (T, k))
+    _req(plan, torch.int32, "plan")
+    if plan.numel() < plan_len(T, E, k):
+        raise ValueError("plan is too small")
+    _req(xp, torch.bfloat16, "xp")
+    if xp.numel() < T * k * H:
+        raise ValueError("xp is too small")
+    _req(workspace, torch.uint8, "workspace")
+    check(lib().moe_route_topk(_p(x), _p(w_router), T, H, E, k, _p(logits), _p(topk_idx), _p(topk_w), _p(plan),
+                               _p(xp), _p(workspace), workspace.numel(), _stream()))
+    return dict(logits=logits, topk_idx=topk_idx, topk_w=topk_w, plan=plan, xp=xp)
+
+
+def moe_grouped_ffn(xp, plan, w13, w2, T, k, workspace, h=None, y=None,
+                    x_shared=None, ws13=None, ws2=None, y_shared=None):
+    E, F2, H = w13.shape
+    F = F2 // 2
+    dev = xp.device
+    S = T * k
+    _req(xp, torch.bfloat16, "xp")
+    _req(plan, torch.int32, "plan")
+    _req(w13, torch.bfloat16, "w13")
+    _req(w2, torch.bfloat16, "w2", (E, H, F))
+    h = torch.empty((S, F), dtype=torch.bfloat16, device=dev) if h is None else h
+    y = torch.empty((S, H), dtype=torch.float32, device=dev) if y is None else y
+    _req(h, torch.bfloat16, "h")
+    _req(y, torch.float32, "y")
+    if h.numel() < S * F or y.numel() < S * H:
+        raise ValueError("h / y too small")
+    Fs = 0
+    if ws13 is not None:
+        Fs = ws13.shape[0] // 2
+        _req(x_shared, torch.bfloat16, "x_shared", (T, H))
+        _req(ws13, torch.bfloat16, "ws13", (2 * Fs, H))
+        _req(ws2, torch.bfloat16, "ws2", (H, Fs))
+        y_shared = torch.empty((T, H), dtype=torch.float32, device=dev) if y_shared is None else y_shared
+        _req(y_shared, torch.float32, "y_shared", (T, H))
+    _req(workspace, torch.uint8, "workspace")
+    check(lib().moe_grouped_ffn(_p(xp), _p(plan), _p(w13), _p(w2), T, H, E, k, F, _p(h), _p(y),
+                                _p(x_shared), _p(ws13), _p(ws2), Fs, _p(y_shared), _p(workspace),
+                                workspace.numel(), _stream()))
+    return dict(h=h, y=y, y_shared=y_shared)
+
+
+def moe_combine(y, topk_w, plan, T, H, E, k, y_shared=None, out=None, out_bf16=None):
+    dev = y.device
+    _req(y, torch.float32, "y")
+    _req(topk_w, torch.float32, "topk_w", (T, k))
+    _req(plan, torch.int32, "plan")
+    if y_shared is not None:
+        _req(y_shared, torch.float32, "y_shared", (T, H))
+    out = torch.empty((T, H), dtype=torch.float32, device=dev) if out is None else out
+    _req(out, torch.float32, "out", (T, H))
+    if out_bf16 is not None:
+        _req(out_bf16, torch.bfloat16, "out_bf16", (T, H))
+    check(lib().moe_combine(_p(y), _p(topk_w), _p(plan), _p(y_shared), T, H, E, k, _p(out), _p(out_bf16),
+                            _stream()))
+    return out
+
+
+def lm_logprob_kl(hidden, w_vocab, target, workspace, rollout_logp=None, beta=2.0, logits=None,
+                  logp=None, lse=None, k3=None, mask=None):
+    T, H = hidden.shape
+    V = w_vocab.shape[0]
+    dev = hidden.device
+    _req(hidden, torch.bfloat16, "hidden")
+    _req(w_vocab, torch.bfloat16, "w_vocab", (V, H))
+    _req(target, torch.int32, "target", (T,))
+    logits = torch.empty((T, V), dtype=torch.float32, device=dev) if logits is None else logits
+    _req(logits, torch.float32, "logits", (T, V))
+    logp = torch.empty(T, dtype=torch.float32, device=dev) if logp is None else logp
+    lse = torch.empty(T, dtype=torch.float32, device=dev) if lse is None else lse
+    if rollout_logp is not None:
+        _req(rollout_logp, torch.float32, "rollout_logp", (T,))
+        k3 = torch.empty(T, dtype=torch.float32, device=dev) if k3 is None else k3
+        mask = torch.empty(T, dtype=torch.uint8, device=dev) if mask is None else mask
+    _req(workspace, torch.uint8, "workspace")
+    check(lib().lm_logprob_kl(_p(hidden), _p(w_vocab), _p(target), _p(rollout_logp), T, H, V, float(beta),
+                              _p(logits), _p(logp), _p(lse), _p(k3), _p(mask), _p(workspace), workspace.numel(),
+                              _stream()))
+    return dict(logits=logits, logp=logp, lse=lse, k3=k3, mask=mask)
+
+
+def gemm_bf16(a, b, workspace, variant=0, out=None):
+    """Diagnostic: the dense tcgen05 GEMM engine alone, d = a @ b^T in fp32."""
+    M, K = a.shape
+    N = b.shape[0]
+    _req(a, torch.bfloat16, "a")
+    _req(b, torch.bfloat16, "b", (N, K))
+    out = torch.empty((M, N), dtype=torch.float32, device=a.device) if out is None else out
+    _req(out, torch.float32, "out", (M, N))
+    check(lib().invmoe_gemm_bf16(_p(a), _p(b), M, N, K, _p(out), int(variant), _p(workspace), workspace.numel(),
+                                 _stream()))
+    return out
+
+
+def debug_timeout_probe(workspace, timeout_us=20000):
+    check(lib().invmoe_debug_timeout_probe(_p(workspace), workspace.numel(), int(timeout_us), _stream()))

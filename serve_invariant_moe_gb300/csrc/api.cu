@@ -1,0 +1,262 @@
+// api.cu -- the extern "C" entry points: validation, workspace layout, call order.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace invmoe {
+
+namespace {
+thread_local char g_last_error[512] = "";
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t route_ws(int T, int E) {
+  const size_t NC = (static_cast<size_t>(T) + kDispatchChunk - 1) / kDispatchChunk;
+  return align_up(NC * static_cast<size_t>(E) * sizeof(int32_t), 256);
+}
+size_t ffn_ws(int T, int F_shared) { return align_up(static_cast<size_t>(T) * F_shared * 2, 256); }
+size_t head_ws(int T, int V) {
+  const size_t NCH = (static_cast<size_t>(V) + kLseChunk - 1) / kLseChunk;
+  return align_up(static_cast<size_t>(T) * NCH * sizeof(float2), 256);
+}
+
+unsigned int* status_word(void* ws) { return static_cast<unsigned int*>(ws); }
+uint8_t* scratch(void* ws) { return static_cast<uint8_t*>(ws) + kStatusBytes; }
+}  // namespace
+
+int set_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int check_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return INVMOE_OK;
+  return set_error(INVMOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int device_sm_count(int* out) {
+  static int cache[64] = {};
+  int dev = 0;
+  int rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc) return rc;
+  if (dev < 64 && cache[dev] > 0) {
+    *out = cache[dev];
+    return INVMOE_OK;
+  }
+  int n = 0;
+  rc = check_cuda(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute");
+  if (rc) return rc;
+  if (dev < 64) cache[dev] = n;
+  *out = n;
+  return INVMOE_OK;
+}
+
+}  // namespace invmoe
+
+using namespace invmoe;
+
+#define REQUIRE(cond, code, ...)             \
+  do {                                       \
+    if (!(cond)) return set_error(code, __VA_ARGS__); \
+  } while (0)
+
+#define REQUIRE_PTR(p) REQUIRE((p) != nullptr, INVMOE_ERR_INVALID_ARG, "%s is NULL", #p)
+#define REQUIRE_ALIGNED(p) REQUIRE(aligned16(p), INVMOE_ERR_MISALIGNED, "%s is not 16-byte aligned", #p)
+
+extern "C" {
+
+int invmoe_version(void) { return 100; }
+
+const char* invmoe_last_error(void) { return g_last_error; }
+
+size_t invmoe_plan_len(int T, int E, int k) {
+  if (T < 0 || E <= 0 || k <= 0) return 0;
+  return static_cast<size_t>(2) * E + 1 + static_cast<size_t>(2) * T * k;
+}
+
+size_t invmoe_workspace_size(int T, int H, int E, int k, int F, int F_shared, int V) {
+  (void)H; (void)k; (void)F;
+  if (T < 0) return 0;
+  size_t need = 0;
+  if (E > 0) need = route_ws(T, E) > need ? route_ws(T, E) : need;
+  if (F_shared > 0) need = ffn_ws(T, F_shared) > need ? ffn_ws(T, F_shared) : need;
+  if (V > 0) need = head_ws(T, V) > need ? head_ws(T, V) : need;
+  return kStatusBytes + need;
+}
+
+int invmoe_check(void* workspace, void* stream) {
+  REQUIRE_PTR(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned int v = 0;
+  int rc = check_cuda(cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, st), "cudaMemcpyAsync");
+  if (rc) return rc;
+  if ((rc = check_cuda(cudaStreamSynchronize(st), "cudaStreamSynchronize"))) return rc;
+  if (v != 0) {
+    if ((rc = check_cuda(cudaMemsetAsync(workspace, 0, sizeof(v), st), "cudaMemsetAsync"))) return rc;
+    if ((rc = check_cuda(cudaStreamSynchronize(st), "cudaStreamSynchronize"))) return rc;
+    return set_error(INVMOE_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out (status 0x%x)", v);
+  }
+  return INVMOE_OK;
+}
+
+int moe_route_topk(const void* x, const void* w_router, int T, int H, int E, int k, float* logits,
+                   int32_t* topk_idx, float* topk_w, int32_t* plan, void* xp, void* workspace, size_t ws_bytes,
+                   void* stream) {
+  REQUIRE(T >= 0 && H > 0 && E > 0 && k > 0, INVMOE_ERR_INVALID_ARG, "need T >= 0, H, E, k > 0");
+  REQUIRE(E <= 1024, INVMOE_ERR_UNSUPPORTED_SHAPE, "E=%d > 1024", E);
+  REQUIRE(k <= E && k <= 32, INVMOE_ERR_INVALID_ARG, "need k <= min(E, 32) (k=%d, E=%d)", k, E);
+  REQUIRE(H % 64 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "H=%d is not a multiple of 64", H);
+  REQUIRE_PTR(plan); REQUIRE_PTR(workspace);
+  REQUIRE(ws_bytes >= kStatusBytes + route_ws(T, E), INVMOE_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    return check_cuda(cudaMemsetAsync(plan, 0, (2 * static_cast<size_t>(E) + 1) * sizeof(int32_t), st),
+                      "cudaMemsetAsync");
+  }
+  REQUIRE_PTR(x); REQUIRE_PTR(w_router); REQUIRE_PTR(logits); REQUIRE_PTR(topk_idx); REQUIRE_PTR(topk_w);
+  REQUIRE_PTR(xp);
+  REQUIRE_ALIGNED(x); REQUIRE_ALIGNED(w_router); REQUIRE_ALIGNED(logits); REQUIRE_ALIGNED(xp);
+  REQUIRE_ALIGNED(workspace);
+
+  GemmCall g{};
+  g.variant = E <= 64 ? GV_F32_BN64_MT1 : (E <= 128 ? GV_F32_BN128_MT1 : GV_F32_BN256_MT1);
+  g.A = x; g.a_rows = T; g.B = w_router; g.b_rows = E; g.K = H; g.N = E; g.M = T; g.G = 0;
+  g.out = logits; g.ldo = E; g.status = status_word(workspace);
+  // the fp32 epilogue stores 4 columns at a time; E % 4 != 0 would need a scalar tail
+  REQUIRE(E % 4 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "E=%d is not a multiple of 4", E);
+  int rc = gemm_run(g, st);
+  if (rc) return rc;
+  return route_launch(logits, T, E, k, H, x, topk_idx, topk_w, plan, xp,
+                      reinterpret_cast<int32_t*>(scratch(workspace)), st);
+}
+
+int moe_grouped_ffn(const void* xp, const int32_t* plan, const void* w13, const void* w2, int T, int H, int E,
+                    int k, int F, void* h, float* y, const void* x_shared, const void* ws13, const void* ws2,
+                    int F_shared, float* y_shared, void* workspace, size_t ws_bytes, void* stream) {
+  REQUIRE(T >= 0 && H > 0 && E > 0 && k > 0 && F > 0 && F_shared >= 0, INVMOE_ERR_INVALID_ARG, "bad sizes");
+  REQUIRE(E <= 1024 && k <= E, INVMOE_ERR_INVALID_ARG, "need k <= E <= 1024");
+  REQUIRE(H % 64 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "H=%d is not a multiple of 64", H);
+  REQUIRE(F % 128 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "F=%d is not a multiple of 128", F);
+  REQUIRE(F_shared % 128 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "F_shared=%d is not a multiple of 128", F_shared);
+  REQUIRE_PTR(workspace);
+  REQUIRE(ws_bytes >= kStatusBytes + (F_shared > 0 ? ffn_ws(T, F_shared) : 0), INVMOE_ERR_WORKSPACE_TOO_SMALL,
+          "workspace too small");
+  if (T == 0) return INVMOE_OK;
+  REQUIRE_PTR(xp); REQUIRE_PTR(plan); REQUIRE_PTR(w13); REQUIRE_PTR(w2); REQUIRE_PTR(h); REQUIRE_PTR(y);
+  REQUIRE_ALIGNED(xp); REQUIRE_ALIGNED(w13); REQUIRE_ALIGNED(w2); REQUIRE_ALIGNED(h); REQUIRE_ALIGNED(y);
+  REQUIRE_ALIGNED(plan); REQUIRE_ALIGNED(workspace);
+  if (F_shared > 0) {
+    REQUIRE_PTR(x_shared); REQUIRE_PTR(ws13); REQUIRE_PTR(ws2); REQUIRE_PTR(y_shared);
+    REQUIRE_ALIGNED(x_shared); REQUIRE_ALIGNED(ws13); REQUIRE_ALIGNED(ws2); REQUIRE_ALIGNED(y_shared);
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const long long S = static_cast<long long>(T) * k;
+  const int32_t* counts = plan;
+  const int32_t* offsets = plan + E;
+  unsigned int* status = status_word(workspace);
+
+  GemmCall g1{};
+  g1.variant = GV_SWIGLU_BN256_MT2;
+  g1.A = xp; g1.a_rows = S; g1.B = w13; g1.b_rows = static_cast<long long>(E) * 2 * F; g1.K = H;
+  g1.N = F; g1.G = E; g1.counts = counts; g1.offsets = offsets; g1.b_group_rows = 2 * F; g1.b_up_rows = F;
+  g1.out = h; g1.ldo = F; g1.status = status;
+  int rc = gemm_run(g1, st);
+  if (rc) return rc;
+
+  GemmCall g2{};
+  g2.variant = GV_F32_BN256_MT2;
+  g2.A = h; g2.a_rows = S; g2.B = w2; g2.b_rows = static_cast<long long>(E) * H; g2.K = F;
+  g2.N = H; g2.G = E; g2.counts = counts; g2.offsets = offsets; g2.b_group_rows = H;
+  g2.out = y; g2.ldo = H; g2.status = status;
+  if ((rc = gemm_run(g2, st))) return rc;
+
+  if (F_shared > 0) {
+    void* hs = scratch(workspace);
+    GemmCall s1{};
+    s1.variant = GV_SWIGLU_BN256_MT2;
+    s1.A = x_shared; s1.a_rows = T; s1.B = ws13; s1.b_rows = 2LL * F_shared; s1.K = H;
+    s1.N = F_shared; s1.M = T; s1.G = 0; s1.b_group_rows = 0; s1.b_up_rows = F_shared;
+    s1.out = hs; s1.ldo = F_shared; s1.status = status;
+    if ((rc = gemm_run(s1, st))) return rc;
+    GemmCall s2{};
+    s2.variant = GV_F32_BN256_MT2;
+    s2.A = hs; s2.a_rows = T; s2.B = ws2; s2.b_rows = H; s2.K = F_shared;
+    s2.N = H; s2.M = T; s2.G = 0;
+    s2.out = y_shared; s2.ldo = H; s2.status = status;
+    if ((rc = gemm_run(s2, st))) return rc;
+  }
+  return INVMOE_OK;
+}
+
+int moe_combine(const float* y, const float* topk_w, const int32_t* plan, const float* y_shared, int T, int H, int E,
+                int k, float* out, void* out_bf16, void* stream) {
+  REQUIRE(T >= 0 && H > 0 && E > 0 && k > 0 && k <= E, INVMOE_ERR_INVALID_ARG, "bad sizes");
+  REQUIRE(H % 4 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "H=%d is not a multiple of 4", H);
+  if (T == 0) return INVMOE_OK;
+  REQUIRE_PTR(y); REQUIRE_PTR(topk_w); REQUIRE_PTR(plan); REQUIRE_PTR(out);
+  REQUIRE_ALIGNED(y); REQUIRE_ALIGNED(out);
+  if (y_shared) REQUIRE_ALIGNED(y_shared);
+  if (out_bf16) REQUIRE(((uintptr_t)out_bf16 & 7u) == 0, INVMOE_ERR_MISALIGNED, "out_bf16 is not 8-byte aligned");
+  const int32_t* slot_row = plan + 2 * E + 1 + static_cast<long long>(T) * k;
+  return combine_launch(y, topk_w, slot_row, y_shared, T, H, k, out, out_bf16, static_cast<cudaStream_t>(stream));
+}
+
+int lm_logprob_kl(const void* hidden, const void* w_vocab, const int32_t* target, const float* rollout_logp, int T,
+                  int H, int V, float beta, float* logits, float* logp, float* lse, float* k3, uint8_t* mask,
+                  void* workspace, size_t ws_bytes, void* stream) {
+  REQUIRE(T >= 0 && H > 0 && V > 0, INVMOE_ERR_INVALID_ARG, "bad sizes");
+  REQUIRE(beta >= 1.0f, INVMOE_ERR_INVALID_ARG, "beta must be >= 1");
+  REQUIRE(H % 64 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "H=%d is not a multiple of 64", H);
+  REQUIRE(V % 4 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "V=%d is not a multiple of 4", V);
+  REQUIRE_PTR(workspace);
+  REQUIRE(ws_bytes >= kStatusBytes + head_ws(T, V), INVMOE_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
+  if (T == 0) return INVMOE_OK;
+  REQUIRE_PTR(hidden); REQUIRE_PTR(w_vocab); REQUIRE_PTR(target); REQUIRE_PTR(logits); REQUIRE_PTR(logp);
+  REQUIRE_ALIGNED(hidden); REQUIRE_ALIGNED(w_vocab); REQUIRE_ALIGNED(logits); REQUIRE_ALIGNED(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  GemmCall g{};
+  g.variant = GV_F32_BN256_MT1;
+  g.A = hidden; g.a_rows = T; g.B = w_vocab; g.b_rows = V; g.K = H; g.N = V; g.M = T; g.G = 0;
+  g.n_major = 1; g.out = logits; g.ldo = V; g.status = status_word(workspace);
+  int rc = gemm_run(g, st);
+  if (rc) return rc;
+  return lse_launch(logits, target, rollout_logp, T, V, beta, reinterpret_cast<float2*>(scratch(workspace)), logp,
+                    lse, k3, mask, st);
+}
+
+int invmoe_gemm_bf16(const void* a, const void* b, int M, int N, int K, float* d, int variant, void* workspace,
+                     size_t ws_bytes, void* stream) {
+  REQUIRE(M >= 0 && N > 0 && K > 0, INVMOE_ERR_INVALID_ARG, "bad sizes");
+  REQUIRE(K % 64 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 64", K);
+  REQUIRE(N % 4 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "N=%d is not a multiple of 4", N);
+  REQUIRE(variant >= 0 && variant <= 3, INVMOE_ERR_INVALID_ARG, "variant must be 0..3");
+  REQUIRE_PTR(workspace);
+  REQUIRE(ws_bytes >= kStatusBytes, INVMOE_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
+  if (M == 0) return INVMOE_OK;
+  REQUIRE_PTR(a); REQUIRE_PTR(b); REQUIRE_PTR(d);
+  REQUIRE_ALIGNED(a); REQUIRE_ALIGNED(b); REQUIRE_ALIGNED(d);
+  GemmCall g{};
+  g.variant = static_cast<GemmVariant>(variant);
+  g.A = a; g.a_rows = M; g.B = b; g.b_rows = N; g.K = K; g.N = N; g.M = M; g.G = 0;
+  g.n_major = (variant == 0) ? 1 : 0;
+  g.out = d; g.ldo = N; g.status = status_word(workspace);
+  return gemm_run(g, static_cast<cudaStream_t>(stream));
+}
+
+int invmoe_debug_timeout_probe(void* workspace, size_t ws_bytes, int timeout_us, void* stream) {
+  REQUIRE_PTR(workspace);
+  REQUIRE(ws_bytes >= kStatusBytes, INVMOE_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
+  REQUIRE(timeout_us >= 1 && timeout_us <= 2000000, INVMOE_ERR_INVALID_ARG, "timeout_us must be 1..2000000");
+  return timeout_probe_launch(status_word(workspace), static_cast<unsigned long long>(timeout_us) * 1000ull,
+                              static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

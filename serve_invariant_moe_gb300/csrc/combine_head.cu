@@ -1,0 +1,197 @@
+// combine_head.cu -- fp32 fixed-order combine; chunked two-pass log-sum-exp,
+// token logprob, k3 and the IcePop mask; the bounded-wait probe.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace invmoe {
+
+namespace {
+
+// out[t, :] = ((w0*y0 + w1*y1) + ...) + y_shared, fp32, slots in rank order,
+// every product and sum rounded on its own ("Reinforcement Learning: Why
+// Numerical Alignment and MoE Routing Matter So Much", section
+// "混合专家模型更难对齐": the precision and order of the weighted expert sum
+// must be pinned).  One thread per 4 columns, 16-byte loads and stores.
+__global__ void combine_kernel(const float4* __restrict__ y, const float* __restrict__ w,
+                               const int32_t* __restrict__ slot_row, const float4* __restrict__ y_shared, int T,
+                               int H4, int k, float4* __restrict__ out, uint2* __restrict__ out_bf16) {
+  const long long total = static_cast<long long>(T) * H4;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long t = i / H4;
+    const int c = static_cast<int>(i - t * H4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const float wj = w[t * k + j];
+      const float4 v = y[static_cast<long long>(slot_row[t * k + j]) * H4 + c];
+      const float4 pr = make_float4(__fmul_rn(wj, v.x), __fmul_rn(wj, v.y), __fmul_rn(wj, v.z), __fmul_rn(wj, v.w));
+      if (j == 0) {
+        acc = pr;
+      } else {
+        acc = make_float4(__fadd_rn(acc.x, pr.x), __fadd_rn(acc.y, pr.y), __fadd_rn(acc.z, pr.z),
+                          __fadd_rn(acc.w, pr.w));
+      }
+    }
+    if (y_shared != nullptr) {
+      const float4 s = y_shared[i];
+      acc = make_float4(__fadd_rn(acc.x, s.x), __fadd_rn(acc.y, s.y), __fadd_rn(acc.z, s.z), __fadd_rn(acc.w, s.w));
+    }
+    out[i] = acc;
+    if (out_bf16 != nullptr) {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+      out_bf16[i] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    }
+  }
+}
+
+// Pass 1 ("GLM Post-Training Beyond SFT", section "动作与概率契约": logsumexp
+// needs comparison tests; the chunking fixes its order).  One warp per
+// (token, group of 4 chunks); chunk c covers columns [256c, 256c + 256).
+// Lane l holds columns 256c + 4l .. +3 and 256c + 128 + 4l .. +3.
+//   m_c = max of the chunk
+//   s_c = sum exp(z - m_c): each lane adds its 8 terms left to right, then a
+//         xor butterfly over lanes 16, 8, 4, 2, 1 (the same on every lane).
+constexpr int kChunksPerWarp = 4;
+
+__global__ void lse_partial_kernel(const float* __restrict__ z, int T, int V, int NCH, float2* __restrict__ part) {
+  const long long gw = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int groups = (NCH + kChunksPerWarp - 1) / kChunksPerWarp;
+  if (gw >= static_cast<long long>(T) * groups) return;
+  const long long t = gw / groups;
+  const int c0 = static_cast<int>(gw - t * groups) * kChunksPerWarp;
+  const float* row = z + t * V;
+  float4 a[kChunksPerWarp], b[kChunksPerWarp];
+  const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+#pragma unroll
+  for (int i = 0; i < kChunksPerWarp; ++i) {
+    const int col_a = (c0 + i) * kLseChunk + 4 * lane;
+    const int col_b = col_a + 128;
+    a[i] = (c0 + i < NCH && col_a < V) ? __ldcs(reinterpret_cast<const float4*>(row + col_a)) : ninf;
+    b[i] = (c0 + i < NCH && col_b < V) ? __ldcs(reinterpret_cast<const float4*>(row + col_b)) : ninf;
+  }
+#pragma unroll
+  for (int i = 0; i < kChunksPerWarp; ++i) {
+    if (c0 + i >= NCH) break;
+    float m = fmaxf(fmaxf(fmaxf(a[i].x, a[i].y), fmaxf(a[i].z, a[i].w)),
+                    fmaxf(fmaxf(b[i].x, b[i].y), fmaxf(b[i].z, b[i].w)));
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+    float s = 0.0f;
+    if (m != -INFINITY) {
+      s = __fadd_rn(s, expf(a[i].x - m));
+      s = __fadd_rn(s, expf(a[i].y - m));
+      s = __fadd_rn(s, expf(a[i].z - m));
+      s = __fadd_rn(s, expf(a[i].w - m));
+      s = __fadd_rn(s, expf(b[i].x - m));
+      s = __fadd_rn(s, expf(b[i].y - m));
+      s = __fadd_rn(s, expf(b[i].z - m));
+      s = __fadd_rn(s, expf(b[i].w - m));
+    }
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, d));
+    if (lane == 0) part[t * NCH + (c0 + i)] = make_float2(m, s);
+  }
+}
+
+// Pass 2: one thread per token merges the partials in ascending chunk order,
+//   M' = max(M, m_c);  S = S*exp(M - M') + s_c*exp(m_c - M');  lse = M + log S,
+// then logp = z[target] - lse and, with rollout logprobs ("GLM Post-Training
+// Beyond SFT", section "IcePop 为什么有两层 ratio"), d = logp - rollout,
+// k3 = expm1(d) - d, rho = exp(d), mask = 1/beta <= rho <= beta.
+__global__ void lse_merge_kernel(const float2* __restrict__ part, const float* __restrict__ z,
+                                 const int32_t* __restrict__ target, const float* __restrict__ rollout, int T, int V,
+                                 int NCH, float beta, float* __restrict__ logp, float* __restrict__ lse,
+                                 float* __restrict__ k3, uint8_t* __restrict__ mask) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  const float2* pt = part + static_cast<long long>(t) * NCH;
+  float M = -INFINITY, S = 0.0f;
+  for (int c = 0; c < NCH; ++c) {
+    const float2 ms = pt[c];
+    if (ms.x > M) {
+      S = __fadd_rn(__fmul_rn(S, expf(M - ms.x)), ms.y);
+      M = ms.x;
+    } else if (ms.x != -INFINITY) {
+      S = __fadd_rn(S, __fmul_rn(ms.y, expf(ms.x - M)));
+    }
+  }
+  const float l = __fadd_rn(M, logf(S));
+  const int tg = target[t];
+  const float lp = (tg >= 0 && tg < V) ? __fsub_rn(z[static_cast<long long>(t) * V + tg], l)
+                                       : __uint_as_float(0x7fc00000u);
+  logp[t] = lp;
+  if (lse != nullptr) lse[t] = l;
+  if (rollout != nullptr) {
+    const float d = __fsub_rn(lp, rollout[t]);
+    if (k3 != nullptr) k3[t] = __fsub_rn(expm1f(d), d);
+    if (mask != nullptr) {
+      const float rho = expf(d);
+      const float lo = __fdiv_rn(1.0f, beta);
+      mask[t] = (lo <= rho && rho <= beta) ? 1 : 0;
+    }
+  }
+}
+
+// Waits on an mbarrier that nothing completes, with a short limit; records the
+// timeout in the status word and returns.
+__global__ void timeout_probe_kernel(unsigned int* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    WaitCtl w{&abort_flag, status, limit_ns};
+    mbar_wait(&bar, 0, w);
+    // release the barrier so the shared word is left in a completed state
+    mbar_arrive(&bar);
+  }
+}
+
+}  // namespace
+
+int combine_launch(const float* y, const float* topk_w, const int32_t* slot_row, const float* y_shared, int T,
+                   int H, int k, float* out, void* out_bf16, cudaStream_t st) {
+  int sms = 0, rc;
+  if ((rc = device_sm_count(&sms))) return rc;
+  const int H4 = H / 4;
+  const long long total = static_cast<long long>(T) * H4;
+  long long blocks = (total + 255) / 256;
+  if (blocks > static_cast<long long>(sms) * 16) blocks = static_cast<long long>(sms) * 16;
+  if (blocks == 0) return INVMOE_OK;
+  combine_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(
+      reinterpret_cast<const float4*>(y), topk_w, slot_row, reinterpret_cast<const float4*>(y_shared), T, H4, k,
+      reinterpret_cast<float4*>(out), reinterpret_cast<uint2*>(out_bf16));
+  return check_cuda(cudaGetLastError(), "combine_kernel");
+}
+
+int lse_launch(const float* logits, const int32_t* target, const float* rollout_logp, int T, int V, float beta,
+               float2* partials, float* logp, float* lse, float* k3, uint8_t* mask, cudaStream_t st) {
+  int rc;
+  const int NCH = (V + kLseChunk - 1) / kLseChunk;
+  const int groups = (NCH + kChunksPerWarp - 1) / kChunksPerWarp;
+  const long long warps = static_cast<long long>(T) * groups;
+  const long long blocks = (warps * 32 + 255) / 256;
+  if (blocks == 0) return INVMOE_OK;
+  lse_partial_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(logits, T, V, NCH, partials);
+  if ((rc = check_cuda(cudaGetLastError(), "lse_partial_kernel"))) return rc;
+  lse_merge_kernel<<<(T + 127) / 128, 128, 0, st>>>(partials, logits, target, rollout_logp, T, V, NCH, beta, logp,
+                                                   lse, k3, mask);
+  return check_cuda(cudaGetLastError(), "lse_merge_kernel");
+}
+
+int timeout_probe_launch(unsigned int* status, unsigned long long limit_ns, cudaStream_t st) {
+  timeout_probe_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+  return check_cuda(cudaGetLastError(), "timeout_probe_kernel");
+}
+
+}  // namespace invmoe

@@ -1,0 +1,111 @@
+// gemm.cu -- host side of the tcgen05 GEMM engine: tensor maps, launch shapes.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "tc_gemm.cuh"
+
+namespace invmoe {
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// Row-major bf16 [rows, inner] matrix; box = 64 elements (128 B, one swizzle row) x box_rows.
+int make_tmap(CUtensorMap* m, const void* base, long long inner, long long rows, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return set_error(INVMOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(INVMOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return INVMOE_OK;
+}
+
+template <int BN, int MT, int EPI, int STAGES>
+int launch(const GemmCall& c, cudaStream_t st) {
+  using S = GemmShape<BN, MT, EPI, STAGES>;
+  if (c.G > S::MAX_GROUPS) return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "more than %d groups", S::MAX_GROUPS);
+  CUtensorMap ta, tb;
+  int rc = make_tmap(&ta, c.A, c.K, c.a_rows, kBM);
+  if (rc) return rc;
+  rc = make_tmap(&tb, c.B, c.K, c.b_rows, EPI == EPI_SWIGLU ? BN / 2 : BN);
+  if (rc) return rc;
+
+  int dev = 0;
+  if ((rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice"))) return rc;
+  static bool attr_set[64] = {};
+  if (dev < 64 && !attr_set[dev]) {
+    rc = check_cuda(cudaFuncSetAttribute(tc_gemm_kernel<BN, MT, EPI, STAGES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES),
+                    "cudaFuncSetAttribute");
+    if (rc) return rc;
+    attr_set[dev] = true;
+  }
+  int sms = 0;
+  if ((rc = device_sm_count(&sms))) return rc;
+
+  GemmParams p;
+  p.K = c.K;
+  p.N = c.N;
+  const int nb_cols = (EPI == EPI_SWIGLU) ? BN / 2 : BN;
+  p.n_blocks = (c.N + nb_cols - 1) / nb_cols;
+  p.M = c.M;
+  p.G = c.G;
+  p.counts = c.counts;
+  p.offsets = c.offsets;
+  p.b_group_rows = c.b_group_rows;
+  p.b_up_rows = c.b_up_rows;
+  p.n_major = c.n_major;
+  p.out = c.out;
+  p.ldo = c.ldo;
+  p.status = c.status;
+  p.timeout_ns = kTimeoutNs;
+
+  constexpr long long CH = static_cast<long long>(MT) * kBM;
+  long long max_chunks = (c.G > 0) ? (c.a_rows + CH - 1) / CH + c.G : (c.M + CH - 1) / CH;
+  long long max_units = max_chunks * p.n_blocks;
+  if (max_units <= 0) return INVMOE_OK;
+  const int grid = static_cast<int>(max_units < sms ? max_units : sms);
+  tc_gemm_kernel<BN, MT, EPI, STAGES><<<grid, 192, S::SMEM_BYTES, st>>>(ta, tb, p);
+  return check_cuda(cudaGetLastError(), "tc_gemm_kernel launch");
+}
+
+}  // namespace
+
+int gemm_run(const GemmCall& c, cudaStream_t st) {
+  if (c.a_rows <= 0 || (c.G == 0 && c.M <= 0)) return INVMOE_OK;
+  if (c.K % kBK != 0) return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 64", c.K);
+  switch (c.variant) {
+    case GV_F32_BN256_MT1: return launch<256, 1, EPI_F32, 4>(c, st);
+    case GV_F32_BN256_MT2: return launch<256, 2, EPI_F32, 3>(c, st);
+    case GV_F32_BN128_MT1: return launch<128, 1, EPI_F32, 6>(c, st);
+    case GV_F32_BN64_MT1: return launch<64, 1, EPI_F32, 8>(c, st);
+    case GV_SWIGLU_BN256_MT2: return launch<256, 2, EPI_SWIGLU, 3>(c, st);
+  }
+  return set_error(INVMOE_ERR_INVALID_ARG, "unknown GEMM variant %d", (int)c.variant);
+}
+
+}  // namespace invmoe

@@ -1,0 +1,71 @@
+// internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/invmoe.h"
+
+namespace invmoe {
+
+// Wait limit for every bounded device wait (1 s).
+constexpr unsigned long long kTimeoutNs = 1000000000ull;
+
+// Fixed chunk sizes (part of the numerical definition; never derived from T).
+constexpr int kDispatchChunk = 64;   // tokens per dispatch-count chunk
+constexpr int kLseChunk = 256;       // vocabulary columns per log-sum-exp partial
+
+// Workspace: [0, 256) status block, then per-call scratch.
+constexpr size_t kStatusBytes = 256;
+
+int set_error(int code, const char* fmt, ...);
+int check_cuda(cudaError_t e, const char* what);
+int device_sm_count(int* out);
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- GEMM engine
+enum GemmVariant : int {
+  GV_F32_BN256_MT1 = 0,   // dense fp32-out, 4-stage ring, double-buffered TMEM (LM head)
+  GV_F32_BN256_MT2 = 1,   // grouped/dense fp32-out, 2 row tiles per unit (expert down projection)
+  GV_F32_BN128_MT1 = 2,
+  GV_F32_BN64_MT1 = 3,
+  GV_SWIGLU_BN256_MT2 = 4 // grouped/dense gate+up with SwiGLU epilogue -> bf16
+};
+
+struct GemmCall {
+  GemmVariant variant;
+  const void* A;       // [a_rows, K] bf16
+  long long a_rows;
+  const void* B;       // [b_rows, K] bf16
+  long long b_rows;
+  int K;
+  int N;               // valid output columns
+  int M;               // dense rows (ignored when G > 0)
+  int G;               // groups (0 = dense)
+  const int* counts;
+  const int* offsets;
+  int b_group_rows;
+  int b_up_rows;
+  int n_major;
+  void* out;
+  long long ldo;
+  unsigned int* status;
+};
+
+int gemm_run(const GemmCall& c, cudaStream_t st);
+
+// ---------------------------------------------------------------- routing
+int route_launch(const float* logits, int T, int E, int k, int H, const void* x, int32_t* topk_idx,
+                 float* topk_w, int32_t* plan, void* xp, int32_t* chunk_counts, cudaStream_t st);
+
+// ---------------------------------------------------------------- combine / head
+int combine_launch(const float* y, const float* topk_w, const int32_t* slot_row, const float* y_shared,
+                   int T, int H, int k, float* out, void* out_bf16, cudaStream_t st);
+int lse_launch(const float* logits, const int32_t* target, const float* rollout_logp, int T, int V,
+               float beta, float2* partials, float* logp, float* lse, float* k3, uint8_t* mask,
+               cudaStream_t st);
+int timeout_probe_launch(unsigned int* status, unsigned long long limit_ns, cudaStream_t st);
+
+}  // namespace invmoe

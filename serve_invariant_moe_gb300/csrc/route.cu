@@ -1,0 +1,228 @@
+// route.cu -- top-k with lowest-index ties, gates, deterministic dispatch, gather.
+//
+// Sources: "位级一致：前沿训练的差异化关键", section "为什么比特级一致是一个复杂的问题"
+// (a router near-tie flips which expert fires; fix: a deterministic tie
+// decision); "GLM Post-Training Beyond SFT", section "迁移到 NPU 时" (a top-k must
+// fix ties, boundary ties, sort order, NaN handling and the index dtype).
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace invmoe {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Total order key: larger = ranks earlier.  NaN -> 0 (below every number,
+// including -inf); -0.0 and +0.0 map to the same key (a tie).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  if (v != v) return 0u;
+  uint32_t b = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+  if (key == 0u) return __uint_as_float(0x7fc00000u);
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// One warp per token.  Lane l holds experts l, l+32, ... (EPL of them).  Each of
+// the k rounds takes the warp-wide maximum of (key, ~expert): a larger logit
+// wins, an exact tie goes to the lower expert index.  The gate softmax is taken
+// over the k selected logits in rank order, in fp32.
+template <int EPL>
+__global__ void topk_gate_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx,
+                                 float* __restrict__ w) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const float* row = logits + static_cast<long long>(t) * E;
+  uint64_t key[EPL];
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = i * 32 + lane;
+    key[i] = (e < E) ? ((static_cast<uint64_t>(order_key(row[e])) << 32) | static_cast<uint32_t>(~e)) : 0ull;
+    // a NaN logit keeps key 0 in its high half but a non-zero low half, so it
+    // still outranks an absent entry (key 0) and ties among NaNs go by index
+  }
+  int my_e = 0;
+  float my_v = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    uint64_t best = 0ull;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) best = key[i] > best ? key[i] : best;
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+      const uint64_t o = __shfl_xor_sync(kFull, best, d);
+      best = o > best ? o : best;
+    }
+    const int e = static_cast<int>(~static_cast<uint32_t>(best));
+    const float v = key_value(static_cast<uint32_t>(best >> 32));
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)
+      if (i * 32 + lane == e) key[i] = 0ull;
+    if (lane == j) {
+      my_e = e;
+      my_v = v;
+    }
+  }
+  // gates: w_j = exp(v_j - v_0) / sum_{i<k} exp(v_i - v_0), the sum in rank order
+  const float v0 = __shfl_sync(kFull, my_v, 0);
+  const float ex = (lane < k) ? expf(my_v - v0) : 0.0f;
+  float s = 0.0f;
+  for (int j = 0; j < k; ++j) s = __fadd_rn(s, __shfl_sync(kFull, ex, j));
+  if (lane < k) {
+    idx[static_cast<long long>(t) * k + lane] = my_e;
+    w[static_cast<long long>(t) * k + lane] = __fdiv_rn(ex, s);
+  }
+}
+
+// Per chunk of kDispatchChunk tokens: how many of its (token, slot) pairs go to each expert.
+__global__ void dispatch_count_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
+                                      int32_t* __restrict__ chunk_counts) {
+  extern __shared__ int hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int c = blockIdx.x;
+  const long long p0 = static_cast<long long>(c) * kDispatchChunk * k;
+  const long long p1 = min(static_cast<long long>(T), static_cast<long long>(c + 1) * kDispatchChunk) * k;
+  for (long long p = p0 + threadIdx.x; p < p1; p += blockDim.x) atomicAdd(&hist[idx[p]], 1);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[static_cast<long long>(c) * E + e] = hist[e];
+}
+
+// One block: per expert an exclusive scan over chunks (in place), the expert
+// totals, and an exclusive scan over experts for the segment offsets.
+__global__ void dispatch_scan_kernel(int32_t* __restrict__ chunk_counts, int NC, int E, int32_t* __restrict__ counts,
+                                     int32_t* __restrict__ offsets) {
+  __shared__ int warp_tot[32];
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E) {
+    for (int c = 0; c < NC; ++c) {
+      const long long i = static_cast<long long>(c) * E + e;
+      const int v = chunk_counts[i];
+      chunk_counts[i] = run;
+      run += v;
+    }
+    counts[e] = run;
+  }
+  // block exclusive scan of run over e (blockDim.x = 1024)
+  const int lane = e & 31, wid = e >> 5;
+  int incl = run;
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(kFull, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int t = warp_tot[lane];
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(kFull, t, d);
+      if (lane >= d) t += v;
+    }
+    warp_tot[lane] = t;  // inclusive over warps
+  }
+  __syncthreads();
+  const int excl = incl - run + (wid > 0 ? warp_tot[wid - 1] : 0);
+  if (e < E) offsets[e] = excl;
+  if (e == E - 1) offsets[E] = excl + run;
+}
+
+// One warp per chunk: walk the chunk's pairs p = t*k + j in ascending order, 32 at
+// a time.  Lanes holding the same expert are ranked by lane (match_any), and a
+// per-expert running count in shared memory carries the rank across batches, so
+// each expert's rows come out in ascending token order (a token never picks the
+// same expert twice).
+__global__ void dispatch_scatter_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
+                                        const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
+                                        int32_t* __restrict__ row_token, int32_t* __restrict__ slot_row) {
+  extern __shared__ int run[];
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) run[e] = 0;
+  __syncwarp();
+  const int c = blockIdx.x;
+  const long long p0 = static_cast<long long>(c) * kDispatchChunk * k;
+  const long long p1 = min(static_cast<long long>(T), static_cast<long long>(c + 1) * kDispatchChunk) * k;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (long long pb = p0; pb < p1; pb += 32) {
+    const long long p = pb + lane;
+    const int e = (p < p1) ? idx[p] : -1;
+    const unsigned m = __match_any_sync(kFull, e);
+    const int rank = __popc(m & lt_mask);
+    if (e >= 0) {
+      const int pos = offsets[e] + chunk_base[static_cast<long long>(c) * E + e] + run[e] + rank;
+      row_token[pos] = static_cast<int32_t>(p / k);
+      slot_row[p] = pos;
+    }
+    __syncwarp();
+    if (e >= 0 && rank == 0) run[e] += __popc(m);
+    __syncwarp();
+  }
+}
+
+// xp[r, :] = x[row_token[r], :] in 16-byte vectors.
+__global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row_token, long long R,
+                                   int vec_per_row, uint4* __restrict__ xp) {
+  const long long total = R * vec_per_row;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = i / vec_per_row;
+    const int c = static_cast<int>(i - r * vec_per_row);
+    xp[i] = x[static_cast<long long>(row_token[r]) * vec_per_row + c];
+  }
+}
+
+}  // namespace
+
+int route_launch(const float* logits, int T, int E, int k, int H, const void* x, int32_t* topk_idx,
+                 float* topk_w, int32_t* plan, void* xp, int32_t* chunk_counts, cudaStream_t st) {
+  int rc;
+  int32_t* counts = plan;
+  int32_t* offsets = plan + E;
+  const long long S = static_cast<long long>(T) * k;
+  int32_t* row_token = plan + 2 * E + 1;
+  int32_t* slot_row = row_token + S;
+
+  // top-k + gates
+  {
+    const int threads = 256;
+    const long long blocks = (static_cast<long long>(T) * 32 + threads - 1) / threads;
+    const int epl = (E + 31) / 32;
+    if (epl <= 1) topk_gate_kernel<1><<<blocks, threads, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
+    else if (epl <= 2) topk_gate_kernel<2><<<blocks, threads, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
+    else if (epl <= 4) topk_gate_kernel<4><<<blocks, threads, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
+    else if (epl <= 8) topk_gate_kernel<8><<<blocks, threads, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
+    else if (epl <= 16) topk_gate_kernel<16><<<blocks, threads, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
+    else topk_gate_kernel<32><<<blocks, threads, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
+    if ((rc = check_cuda(cudaGetLastError(), "topk_gate_kernel"))) return rc;
+  }
+  // dispatch plan
+  const int NC = (T + kDispatchChunk - 1) / kDispatchChunk;
+  dispatch_count_kernel<<<NC, 256, E * sizeof(int), st>>>(topk_idx, T, E, k, chunk_counts);
+  if ((rc = check_cuda(cudaGetLastError(), "dispatch_count_kernel"))) return rc;
+  dispatch_scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, NC, E, counts, offsets);
+  if ((rc = check_cuda(cudaGetLastError(), "dispatch_scan_kernel"))) return rc;
+  dispatch_scatter_kernel<<<NC, 32, E * sizeof(int), st>>>(topk_idx, T, E, k, chunk_counts, offsets, row_token,
+                                                           slot_row);
+  if ((rc = check_cuda(cudaGetLastError(), "dispatch_scatter_kernel"))) return rc;
+  // permute
+  const int vec_per_row = H / 8;
+  const long long total = S * vec_per_row;
+  int sms = 0;
+  if ((rc = device_sm_count(&sms))) return rc;
+  long long blocks = (total + 255) / 256;
+  const long long cap = static_cast<long long>(sms) * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks > 0) {
+    gather_rows_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(static_cast<const uint4*>(x), row_token, S,
+                                                                  vec_per_row, static_cast<uint4*>(xp));
+    if ((rc = check_cuda(cudaGetLastError(), "gather_rows_kernel"))) return rc;
+  }
+  return INVMOE_OK;
+}
+
+}  // namespace invmoe

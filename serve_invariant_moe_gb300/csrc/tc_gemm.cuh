@@ -1,0 +1,375 @@
+// tc_gemm.cuh -- the fixed-tile tcgen05 GEMM engine (sm_103a).
+//
+//   D[r, n] = sum_k A[r, k] * B[n, k]      A, B bf16 K-major, D accumulated in fp32 TMEM
+//
+// Batch invariance ("位级一致：前沿训练的差异化关键", section
+// "为什么比特级一致是一个复杂的问题": one fixed kernel choice for the expert
+// matmuls whatever the per-expert token count; DeepGEMM dropped split-K because
+// it breaks invariance):
+//   * one tile shape per call site (BM = 128 rows, BN columns, BK = 64), chosen
+//     from the model shape only, never from T or from a group's row count;
+//   * every output element is produced by exactly one CTA that walks K from 0
+//     upward in 64-wide blocks, each block as four K=16 MMAs in ascending order,
+//     accumulating in TMEM; no split-K, no stream-K;
+//   * which CTA handles which tile (the persistent schedule) varies freely: it
+//     never changes the order of any element's reduction;
+//   * rows of a tile that belong to another group, or lie past the end of A,
+//     are loaded (TMA fills out-of-range rows with zeros) and multiplied, but
+//     never stored: an MMA row depends only on its own A row.
+//
+// Grouped mode: groups g = 0..G-1 own the A rows [offsets[g], offsets[g]+counts[g])
+// and the B rows [g*b_group_rows, (g+1)*b_group_rows).  A group's rows are cut
+// into chunks of MT*128 rows; a work unit is (chunk, column block).  Each unit
+// streams its B tile once per K block and multiplies it against up to MT row
+// tiles, so an expert with at most MT*128 tokens reads its weights once.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over units):
+//   warp 0      TMA producer (one lane): A row tiles + B tile per K block into
+//               a STAGES-deep shared-memory ring (128-byte swizzle)
+//   warp 1      TMEM owner + MMA issuer (one lane): tcgen05.mma kind::f16,
+//               commit frees a ring slot / publishes a finished accumulator
+//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time, convert,
+//               store to global (fp32 rows, or SwiGLU -> bf16)
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace invmoe {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+
+enum Epilogue : int { EPI_F32 = 0, EPI_SWIGLU = 1 };
+
+struct GemmParams {
+  int K;                  // reduction length (multiple of 64)
+  int N;                  // valid output columns (F32: of D; SwiGLU: of h)
+  int n_blocks;           // column blocks per row chunk
+  int M;                  // dense mode: rows of A and D
+  int G;                  // groups (0 = dense)
+  const int* counts;      // [G] rows per group (device)
+  const int* offsets;     // [G+1] first A row per group (device)
+  int b_group_rows;       // B rows per group
+  int b_up_rows;          // SwiGLU: offset of the up-projection rows inside a group
+  int n_major;            // 1: consecutive units walk row chunks of one column block
+  void* out;              // D (fp32) or h (bf16)
+  long long ldo;          // output row stride, elements
+  unsigned int* status;   // status word (bit 0: a bounded wait ran out)
+  unsigned long long timeout_ns;
+};
+
+template <int BN, int MT, int EPI, int STAGES>
+struct GemmShape {
+  static constexpr int A_BYTES = kBM * kBK * 2;                 // 16 KB per 128-row tile
+  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int STAGE_BYTES = MT * A_BYTES + B_BYTES;
+  static constexpr int ACC_COLS = MT * BN;                      // fp32 TMEM columns per accumulator
+  static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int TMEM_NEED = ACC_STAGES * ACC_COLS;
+  static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128
+                                   : TMEM_NEED <= 256 ? 256 : 512;
+  static constexpr int MAX_GROUPS = 1024;
+  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * ACC_STAGES + 1);
+  static constexpr int MISC_BYTES = 16;
+  static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + BAR_BYTES + MISC_BYTES +
+                                    4 * (MAX_GROUPS + 1);
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+  static_assert(EPI != EPI_SWIGLU || BN % 64 == 0, "SwiGLU splits BN into gate/up halves");
+  static_assert(TMEM_NEED <= 512, "TMEM");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+struct Unit {
+  int row0;    // first A / D row of the chunk
+  int rows;    // valid rows in the chunk (1 .. MT*128)
+  int b_row;   // first B row of the column block (gate rows for SwiGLU)
+  int nb;      // column block
+};
+
+template <int MT, int EPI, int BN>
+__device__ __forceinline__ Unit decode_unit(int u, const GemmParams& p, const int* s_prefix, int total_chunks) {
+  int chunk, nb;
+  if (p.n_major) {
+    nb = u / total_chunks;
+    chunk = u - nb * total_chunks;
+  } else {
+    chunk = u / p.n_blocks;
+    nb = u - chunk * p.n_blocks;
+  }
+  constexpr int CH = MT * kBM;
+  Unit U;
+  int g = 0;
+  if (p.G > 0) {
+    int lo = 0, hi = p.G;  // s_prefix[lo] <= chunk < s_prefix[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_prefix[mid] <= chunk) lo = mid; else hi = mid;
+    }
+    g = lo;
+    const int local = chunk - s_prefix[g];
+    U.row0 = __ldg(p.offsets + g) + local * CH;
+    U.rows = min(CH, __ldg(p.counts + g) - local * CH);
+  } else {
+    U.row0 = chunk * CH;
+    U.rows = min(CH, p.M - U.row0);
+  }
+  constexpr int NB_ROWS = (EPI == EPI_SWIGLU) ? BN / 2 : BN;
+  U.b_row = g * p.b_group_rows + nb * NB_ROWS;
+  U.nb = nb;
+  return U;
+}
+
+__device__ __forceinline__ float silu_f32(float g) {
+  // silu(g) = g / (1 + exp(-g)), IEEE division
+  return g / (1.0f + expf(-g));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int BN, int MT, int EPI, int STAGES>
+__global__ void __launch_bounds__(192, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+  using S = GemmShape<BN, MT, EPI, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* accf_bar = empty_bar + STAGES;
+  uint64_t* acce_bar = accf_bar + S::ACC_STAGES;
+  uint64_t* final_bar = acce_bar + S::ACC_STAGES;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(final_bar + 1);
+  uint32_t* tmem_slot = misc;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 1);
+  int* s_total = reinterpret_cast<int*>(misc + 2);
+  int* s_prefix = reinterpret_cast<int*>(misc + 4);  // [G+1]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < S::ACC_STAGES; ++a) {
+      mbar_init(&accf_bar[a], 1);
+      mbar_init(&acce_bar[a], 128);
+    }
+    mbar_init(final_bar, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, S::TMEM_COLS);
+
+  // Row-chunk prefix over groups (warp 2; G <= 1024): s_prefix[g] = sum_{g'<g} ceil(counts[g'] / (MT*128)).
+  constexpr int CH = MT * kBM;
+  if (warp == 2) {
+    if (p.G > 0) {
+      const int per = (p.G + 31) / 32;
+      const int g0 = lane * per;
+      int local = 0;
+      for (int i = 0; i < per; ++i) {
+        const int g = g0 + i;
+        if (g < p.G) local += (__ldg(p.counts + g) + CH - 1) / CH;
+      }
+      int incl = local;
+      for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+      }
+      int run = incl - local;
+      for (int i = 0; i < per; ++i) {
+        const int g = g0 + i;
+        if (g < p.G) {
+          s_prefix[g] = run;
+          run += (__ldg(p.counts + g) + CH - 1) / CH;
+        }
+      }
+      if (lane == 31) {
+        s_prefix[p.G] = incl;
+        *s_total = incl;
+      }
+    } else if (lane == 0) {
+      *s_total = (p.M + CH - 1) / CH;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_chunks = *s_total;
+  const int total_units = total_chunks * p.n_blocks;
+  const int num_kb = p.K / kBK;
+  WaitCtl wc{s_abort, p.status, p.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int filled_phase[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) filled_phase[s] = -1;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const Unit U = decode_unit<MT, EPI, BN>(u, p, s_prefix, total_chunks);
+        const int ntile = (U.rows + kBM - 1) / kBM;
+        const uint32_t bytes = ntile * S::A_BYTES + S::B_BYTES;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wc)) { ok = false; break; }
+          uint8_t* st = ring + stage * S::STAGE_BYTES;
+          mbar_arrive_expect_tx(&full_bar[stage], bytes);
+          for (int t = 0; t < ntile; ++t)
+            tma_load_2d(st + t * S::A_BYTES, &tmA, &full_bar[stage], kb * kBK, U.row0 + t * kBM);
+          if (EPI == EPI_SWIGLU) {
+            tma_load_2d(st + MT * S::A_BYTES, &tmB, &full_bar[stage], kb * kBK, U.b_row);
+            tma_load_2d(st + MT * S::A_BYTES + S::B_BYTES / 2, &tmB, &full_bar[stage], kb * kBK,
+                        U.b_row + p.b_up_rows);
+          } else {
+            tma_load_2d(st + MT * S::A_BYTES, &tmB, &full_bar[stage], kb * kBK, U.b_row);
+          }
+          filled_phase[stage] = static_cast<int>(phase);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // Let every copy this thread issued land before the CTA can exit.
+      WaitCtl drain{nullptr, p.status, p.timeout_ns};
+      for (int s = 0; s < STAGES; ++s)
+        if (filled_phase[s] >= 0) mbar_wait(&full_bar[s], static_cast<uint32_t>(filled_phase[s]), drain);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16_f32(kBM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+        const Unit U = decode_unit<MT, EPI, BN>(u, p, s_prefix, total_chunks);
+        const int ntile = (U.rows + kBM - 1) / kBM;
+        if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1u, wc)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * S::ACC_COLS);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, wc)) { ok = false; break; }
+          tc_fence_after();
+          uint8_t* st = ring + stage * S::STAGE_BYTES;
+          const uint64_t bdesc = sdesc_k_sw128(smem_u32(st + MT * S::A_BYTES));
+          for (int t = 0; t < ntile; ++t) {
+            const uint64_t adesc = sdesc_k_sw128(smem_u32(st + t * S::A_BYTES));
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              // +32 bytes along K inside the 128-byte swizzle row = +2 in the encoded address
+              umma_bf16(d0 + static_cast<uint32_t>(t * BN), adesc + 2u * kk, bdesc + 2u * kk, IDESC,
+                        (kb | kk) != 0 ? 1u : 0u);
+            }
+          }
+          umma_commit(&empty_bar[stage]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(&accf_bar[acc]);
+        if (++acc == S::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
+      }
+      // Every MMA this thread issued must finish before TMEM is released.
+      umma_commit(final_bar);
+      WaitCtl drain{nullptr, p.status, p.timeout_ns};
+      mbar_wait(final_bar, 0, drain);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int r_in_tile = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+      const Unit U = decode_unit<MT, EPI, BN>(u, p, s_prefix, total_chunks);
+      const int ntile = (U.rows + kBM - 1) / kBM;
+      // every lane waits; the warp proceeds only if all lanes saw the phase
+      // complete, so the .sync.aligned TMEM loads below never run diverged
+      const bool ok = mbar_wait(&accf_bar[acc], acc_phase, wc);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      for (int t = 0; t < ntile; ++t) {
+        const int row_local = t * kBM + r_in_tile;
+        const bool valid = row_local < U.rows;
+        const long long row = static_cast<long long>(U.row0) + row_local;
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                               static_cast<uint32_t>(acc * S::ACC_COLS + t * BN);
+        if (EPI == EPI_F32) {
+          const int n0 = U.nb * BN;
+          float* orow = static_cast<float*>(p.out) + row * p.ldo + n0;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tbase + c * 32, v);
+            tmem_ld_wait();
+            if (valid) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int col = n0 + c * 32 + j * 4;
+                if (col < p.N) {
+                  float4 f = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                         __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+                  *reinterpret_cast<float4*>(orow + c * 32 + j * 4) = f;
+                }
+              }
+            }
+          }
+        } else {
+          constexpr int HALF = BN / 2;
+          const int n0 = U.nb * HALF;
+          __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + row * p.ldo + n0;
+#pragma unroll 1
+          for (int c = 0; c < HALF / 32; ++c) {
+            uint32_t gv[32], uv[32];
+            tmem_ld32(tbase + c * 32, gv);
+            tmem_ld32(tbase + HALF + c * 32, uv);
+            tmem_ld_wait();
+            if (valid) {
+              uint32_t packed[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float h0 = __fmul_rn(silu_f32(__uint_as_float(gv[2 * j])), __uint_as_float(uv[2 * j]));
+                const float h1 =
+                    __fmul_rn(silu_f32(__uint_as_float(gv[2 * j + 1])), __uint_as_float(uv[2 * j + 1]));
+                packed[j] = pack_bf16x2(h0, h1);
+              }
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<uint4*>(orow + c * 32 + j * 8) =
+                    make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acce_bar[acc]);
+      if (++acc == S::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::TMEM_COLS);
+  }
+}
+
+}  // namespace invmoe

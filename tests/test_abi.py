@@ -1,0 +1,67 @@
+"""CPU-side checks of the C ABI: the library builds, loads without a GPU and
+exports every function include/invmoe.h declares; host-side validation."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char\s*\*|void)\s*\**\s*(\w+)\s*\(", src, re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from serve_invariant_moe_gb300 import build, _lib
+    build.build()
+    return _lib.lib()
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("moe_route_topk", "moe_grouped_ffn", "moe_combine", "lm_logprob_kl",
+              "invmoe_workspace_size", "invmoe_last_error", "invmoe_plan_len", "invmoe_check"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in _declared():
+        assert hasattr(lib, n), n
+    from serve_invariant_moe_gb300 import _lib
+    assert set(_lib.PROTOTYPES) == set(_declared())
+
+
+def test_sizes(lib):
+    assert lib.invmoe_plan_len(64, 8, 2) == 2 * 8 + 1 + 2 * 64 * 2
+    ws = lib.invmoe_workspace_size(8192, 6144, 256, 8, 2048, 2048, 151552)
+    assert ws >= 256 + 8192 * 592 * 8
+    assert lib.invmoe_version() >= 100
+
+
+def test_validation_rejects_before_any_launch(lib):
+    # invalid arguments return an error code without touching the (absent) GPU
+    null = None
+    rc = lib.moe_route_topk(null, null, 64, 256, 8, 9, null, null, null, null, null, null, 0, null)
+    assert rc == -1 and b"k <=" in lib.invmoe_last_error()
+    rc = lib.moe_route_topk(null, null, 64, 100, 8, 2, null, null, null, null, null, null, 0, null)
+    assert rc == -2
+    rc = lib.moe_grouped_ffn(null, null, null, null, 64, 256, 8, 2, 96, null, null,
+                             null, null, null, 0, null, null, 0, null)
+    assert rc == -2 and b"F=96" in lib.invmoe_last_error()
+    rc = lib.lm_logprob_kl(null, null, null, null, 4, 256, 4096, ctypes.c_float(0.5), null, null, null,
+                           null, null, null, 0, null)
+    assert rc == -1 and b"beta" in lib.invmoe_last_error()
+    rc = lib.lm_logprob_kl(null, null, null, null, 4, 256, 4096, ctypes.c_float(2.0), null, null, null,
+                           null, null, ctypes.c_void_p(256), 10, null)
+    assert rc == -3
+    rc = lib.invmoe_debug_timeout_probe(ctypes.c_void_p(256), 4096, 0, null)
+    assert rc == -1
