@@ -1,0 +1,492 @@
+"""Benchmark of the batch-invariant MoE layer + logprob/KL head on GB300.
+
+One step = one pass of the whole hot path over one batch of T = 8192 tokens:
+the GLM-scale MoE layer (hidden 6144, 256 experts top-8, SwiGLU ffn 2048, one
+shared expert of ffn 2048): router GEMM -> top-k/gates -> dispatch + permute ->
+grouped SwiGLU GEMM -> grouped down GEMM (+ shared expert) -> fp32 combine;
+then the logprob/KL head on the layer's output (vocab 151552): LM-head GEMM ->
+chunked two-pass log-sum-exp -> token logprob -> k3 -> IcePop mask (beta = 2).
+The metric is tokens/s of that whole step.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+N > 1 runs under torchrun, one rank per GPU; every rank processes its own
+batch (token data parallelism: no collective on the data path), so the value is
+the sum over ranks (weak scaling).  ``--impl reference`` times the float64 CPU
+oracle on a bounded token sample of the same workload.
+"""
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+_ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, _ROOT)
+
+METRIC = "invariant MoE-layer + logprob/KL head tokens/s (T=8192 GLM-scale layer + 151552-vocab head)"
+UNIT = "tokens/s"
+WORKLOAD = "glm_scale_moe(T=8192,H=6144,E=256,k=8,F=2048,shared F=2048) + glm_scale_head(V=151552)"
+
+
+def _peaks():
+    p = os.path.join(_ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d.get("bf16_tflops_sustained"),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _smi_id(device):
+    """nvidia-smi --id for a torch device: its UUID when torch exposes it, else the index."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(device.index or 0)
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _max_over_ranks(v, ws, device):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.item()
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- ours
+
+class Step:
+    """Device-resident inputs, weights and buffers of one step; run() is the hot path."""
+
+    def __init__(self, device, seed_offset=0):
+        import torch
+        from serve_invariant_moe_gb300 import api, binding, synth
+        self.torch, self.api, self.binding = torch, api, binding
+        mc, hc = synth.GLM_MOE, synth.GLM_HEAD
+        self.mc, self.hc = mc, hc
+        T = mc.T
+        x, wr = synth.moe_activations(mc, seed_offset=seed_offset)
+        w13, w2 = synth.expert_weights(mc, device)
+        ws13, ws2 = synth.shared_expert_weights(mc, device)
+        _, wv, target, noise, _ = synth.head_inputs(hc, device, T=T, seed_offset=seed_offset)
+        self.layer = api.MoELayer(api.MoEWeights(wr.to(device), w13, w2, mc.k, ws13, ws2))
+        self.x_host = x
+        self.x = x.to(device)
+        self.wv = wv
+        self.target_host = target
+        self.target = target.to(device)
+        self.noise = noise
+        self.hidden = torch.empty((T, mc.H), dtype=torch.bfloat16, device=device)
+        self.logits = torch.empty((T, hc.V), dtype=torch.float32, device=device)
+        self.ws_head = binding.new_workspace(binding.workspace_size(T, mc.H, V=hc.V), device)
+        self.layer.alloc_decode(T)          # preallocated buffers reused by every step
+        self.rollout = None
+
+    def run(self, x=None, target=None, rollout=None):
+        """MoE layer (bf16 copy of its output feeds the head) + head; returns the head dict."""
+        d = self.layer._decode
+        w = self.layer.w
+        x = self.x if x is None else x
+        target = self.target if target is None else target
+        rollout = self.rollout if rollout is None else rollout
+        bufs = dict(logits=d["logits"], idx=d["idx"], w=d["w"], plan=d["plan"], xp=d["xp"], h=d["h"],
+                    y=d["y"], ys=d["ys"], out=d["out"])
+        self.layer._run(x, d["ws"], bufs, out_bf16=self.hidden)
+        return self.binding.lm_logprob_kl(self.hidden, self.wv, target, self.ws_head, rollout_logp=rollout,
+                                          beta=2.0, logits=self.logits)
+
+
+def _work_table(mc, hc, counts):
+    """Algorithmic work per launch, by kernel name: ('tensor', flop) or ('hbm', bytes)."""
+    T, H, E, k, F, Fs, V = mc.T, mc.H, mc.E, mc.k, mc.F, mc.F_shared, hc.V
+    S = T * k
+    active = int((counts > 0).sum())
+    return {
+        "router_gemm": ("tensor", 2.0 * T * E * H),
+        "expert_gemm1_swiglu": ("tensor", 2.0 * S * 2 * F * H),
+        "expert_gemm2": ("tensor", 2.0 * S * H * F),
+        "shared_gemm1_swiglu": ("tensor", 2.0 * T * 2 * Fs * H),
+        "shared_gemm2": ("tensor", 2.0 * T * H * Fs),
+        "lm_head_gemm": ("tensor", 2.0 * T * V * H),
+        "topk_gate": ("hbm", T * E * 4 + T * k * 8),
+        "dispatch_count": ("hbm", T * k * 4),
+        "dispatch_scan": ("hbm", 2 * (T // 64) * E * 4),
+        "dispatch_scatter": ("hbm", T * k * 4 * 3),
+        "gather_rows": ("hbm", S * H * 2 * 2 + S * 4),
+        "combine": ("hbm", S * H * 4 + T * H * 4 + T * H * 4 + T * H * 2 + T * k * 8),
+        "lse_partial": ("hbm", T * V * 4 + T * math.ceil(V / 256) * 8),
+        "lse_merge": ("hbm", T * math.ceil(V / 256) * 8 + T * 16),
+        # weight bytes that bound the expert GEMMs (not used for the roofline bound choice)
+        "_expert_weight_bytes": ("hbm", active * (2 * F * H + H * F) * 2),
+    }
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    from serve_invariant_moe_gb300 import _lib, binding, build
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    build.build()
+    lib = _lib.lib()
+    st = Step(device, seed_offset=rank)
+    T = st.mc.T
+
+    # rollout logprobs: the step's own logprob perturbed by N(0, 0.05)
+    first = st.run(rollout=None)
+    torch.cuda.synchronize()
+    st.rollout = (first["logp"] + (st.noise * st.hc.noise_std).to(device)).contiguous()
+    binding.check_status(st.ws_head)
+    binding.check_status(st.layer._decode["ws"])
+
+    for _ in range(args.warmup):
+        st.run()
+    torch.cuda.synchronize()
+
+    # ---------------- timed region: device-resident inputs
+    clocks = ClockSampler(_smi_id(device))
+    clocks.start()
+    time.sleep(0.3)
+    lib.invmoe_profile_enable(1)
+    stream = torch.cuda.current_stream()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    _barrier(ws)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        st.run()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    lib.invmoe_profile_enable(0)
+    ms_total = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    import ctypes
+    maxn = 64
+    names = ctypes.create_string_buffer(48 * maxn)
+    tot = (ctypes.c_float * maxn)()
+    cnt = (ctypes.c_int * maxn)()
+    n = lib.invmoe_profile_collect(names, tot, cnt, maxn)
+    kern = {}
+    for i in range(max(n, 0)):
+        nm = names.raw[48 * i:48 * i + 48].split(b"\0")[0].decode()
+        kern[nm] = (tot[i], cnt[i])
+    binding.check_status(st.ws_head)
+    binding.check_status(st.layer._decode["ws"])
+
+    ms_step = _max_over_ranks(ms_total / args.steps, ws, device)
+    value = ws * T / (ms_step / 1e3)
+
+    # ---------------- end to end: host inputs in pinned memory, results back to the host
+    x_pin = st.x_host.pin_memory()
+    t_pin = st.target_host.pin_memory()
+    r_pin = st.rollout.cpu().pin_memory()
+    out_logp = torch.empty(T, dtype=torch.float32).pin_memory()
+    out_k3 = torch.empty(T, dtype=torch.float32).pin_memory()
+    out_mask = torch.empty(T, dtype=torch.uint8).pin_memory()
+    x_dev = torch.empty_like(st.x)
+    t_dev = torch.empty_like(st.target)
+    r_dev = torch.empty_like(st.rollout)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 10))
+    _barrier(ws)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        x_dev.copy_(x_pin, non_blocking=True)
+        t_dev.copy_(t_pin, non_blocking=True)
+        r_dev.copy_(r_pin, non_blocking=True)
+        res = st.run(x=x_dev, target=t_dev, rollout=r_dev)
+        out_logp.copy_(res["logp"], non_blocking=True)
+        out_k3.copy_(res["k3"], non_blocking=True)
+        out_mask.copy_(res["mask"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, ws, device)
+    h2d = x_pin.numel() * 2 + t_pin.numel() * 4 + r_pin.numel() * 4
+    d2h = T * 4 + T * 4 + T * 1
+
+    # ---------------- roofline of the dominant kernel (from the timed region)
+    counts = st.layer._decode["plan"][:st.mc.E].cpu().numpy()
+    work = _work_table(st.mc, st.hc, counts)
+    peaks = _peaks()
+    per_kernel = {}
+    for nm, (msum, c) in kern.items():
+        if nm not in work or c == 0:
+            continue
+        kind, amount = work[nm]
+        avg_ms = msum / c
+        if kind == "tensor":
+            ach = amount / (avg_ms / 1e3) / 1e12
+            per_kernel[nm] = dict(ms=round(avg_ms, 4), launches=c, bound="tensor", achieved=round(ach, 1),
+                                  unit="TFLOP/s", frac=round(ach / peaks["bf16"], 4))
+        else:
+            ach = amount / (avg_ms / 1e3) / 1e9
+            per_kernel[nm] = dict(ms=round(avg_ms, 4), launches=c, bound="hbm", achieved=round(ach, 1),
+                                  unit="GB/s", frac=round(ach / peaks["hbm"], 4))
+    dom = max(kern.items(), key=lambda kv: kv[1][0])[0] if kern else None
+    roof = None
+    if dom in per_kernel:
+        pk = per_kernel[dom]
+        roof = dict(kernel=dom, bound=pk["bound"], achieved=pk["achieved"],
+                    peak=peaks["bf16"] if pk["bound"] == "tensor" else peaks["hbm"], unit=pk["unit"],
+                    frac=pk["frac"], traffic=None, peak_source=peaks["src"] + " (burst)")
+    launches = sum(c for (_, c) in kern.values())
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(st, samples=args.cpu_sample_tokens)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 inputs/weights, fp32 accumulate",
+            "data": "synthetic (seeded), random-init weights",
+            "config": {"workload": WORKLOAD, "tokens_per_step_per_gpu": T, "parallelism": f"token-dp{ws}",
+                       "l2": "inputs larger than L2 (19.3 GB expert weights, 1.86 GB vocab weights)"},
+            "e2e": {"value": round(ws * T / (e2e_ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "roofline": roof,
+            "kernels": per_kernel,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- oracle (CPU)
+
+def _oracle_sample(x, wr, expert, ws13, ws2, wv, target, rollout, mc, tokens):
+    """The float64 oracle on a token sample: MoE layer, then the head on the layer output.
+
+    Inputs are the bf16 tensors of the workload (CPU); the oracle's own exact
+    bf16 -> float64 conversion is part of the timed work.  ``expert(e)`` returns
+    expert e's bf16 (W13_e, W2_e).  The vocabulary is fed to the oracle in
+    blocks of 16384 rows to bound host memory.
+    """
+    import numpy as np
+    from oracle import head as ohead
+    from oracle import moe as omoe
+    from oracle.numerics import round_to_bf16
+
+    def ew(e):
+        a, b = expert(e)
+        return omoe.to_f64(a), omoe.to_f64(b)
+    xs = omoe.to_f64(x[tokens])
+    res = omoe.moe_forward(xs, omoe.to_f64(wr), None, None, mc.k, mc.F, omoe.to_f64(ws13), omoe.to_f64(ws2),
+                           mc.F_shared, expert_weights=ew)
+    hs = round_to_bf16(res["out"])          # the head reads the layer's bf16 copy
+    V = wv.shape[0]
+    z = np.empty((len(tokens), V))
+    for v0 in range(0, V, 16384):
+        z[:, v0:v0 + 16384] = ohead.vocab_logits(hs, omoe.to_f64(wv[v0:v0 + 16384]))
+    logp, lse = ohead.token_logprob(z, target[tokens])
+    return logp, ohead.k3(logp, rollout[tokens])
+
+
+def cpu_baseline(st, samples=4):
+    """Time the float64 oracle on `samples` tokens of the same step (bounded, ~10-30 s)."""
+    from oracle import moe as omoe
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    tokens = list(range(samples))
+    mc = st.mc
+    wr = st.layer.w.w_router.cpu()
+    L = omoe.router_logits(omoe.to_f64(st.x_host[tokens]), omoe.to_f64(wr))
+    need = sorted(set(omoe.topk_lowest_index(L, mc.k).ravel().tolist()))
+    bank = {e: (st.layer.w.w13[e].cpu(), st.layer.w.w2[e].cpu()) for e in need}
+    ws13, ws2 = st.layer.w.ws13.cpu(), st.layer.w.ws2.cpu()
+    wv = st.wv.cpu()
+    target = st.target_host.numpy()
+    rollout = st.rollout.double().cpu().numpy()
+    t0 = time.perf_counter()
+    _oracle_sample(st.x_host, wr, bank.__getitem__, ws13, ws2, wv, target, rollout, mc, tokens)
+    dt = time.perf_counter() - t0
+    return {"value": round(samples / dt, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{samples} tokens of the same step (MoE layer + head), float64 numpy, "
+                      f"including the oracle's bf16->float64 conversion; {dt:.1f} s"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: K timed steps, each a bounded token sample."""
+    ws, rank, local = _dist()
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+    from oracle import moe as omoe
+    from serve_invariant_moe_gb300 import synth
+    mc, hc = synth.GLM_MOE, synth.GLM_HEAD
+    per_step = args.ref_tokens_per_step
+    n_tok = per_step * (args.steps + args.warmup)
+    # inputs of the same workload drawn on the CPU; only the experts the sample touches are drawn
+    x, wr = synth.moe_activations(mc)
+    L = omoe.router_logits(omoe.to_f64(x[:n_tok]), omoe.to_f64(wr))
+    need = sorted(set(omoe.topk_lowest_index(L, mc.k).ravel().tolist()))
+    bank = {e: synth.one_expert(mc, e) for e in need}
+    ws13, ws2 = synth.shared_expert_weights(mc)
+    _, wv, target, noise, _ = synth.head_inputs(hc, "cpu", T=mc.T)
+    rollout = np.full(mc.T, -math.log(hc.V)) + noise.double().numpy() * hc.noise_std
+    tgt = target.numpy()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    times = []
+    for s in range(args.warmup + args.steps):
+        tokens = list(range(s * per_step, (s + 1) * per_step))
+        t0 = time.perf_counter()
+        _oracle_sample(x, wr, bank.__getitem__, ws13, ws2, wv, tgt, rollout, mc, tokens)
+        times.append(time.perf_counter() - t0)
+    t = sum(times[args.warmup:])
+    value = per_step * args.steps / t
+    sample = (f"{per_step} token(s) per step of the T=8192 step (MoE layer + head), float64 numpy on "
+              f"{cores} host cores, including the oracle's bf16->float64 conversion")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded), random-init weights",
+        "config": {"workload": WORKLOAD, "tokens_per_step": per_step},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_profile_case(args):
+    """A small launch of one hot kernel for an ncu capture (inputs > L2, a few GB on the device).
+
+    lm_head:  vocab-projection GEMM + LSE at T=2048, H=6144, V=32768 (Wv 403 MB, logits 268 MB).
+    experts:  the grouped expert GEMMs at T=2048, H=6144, E=32, k=8, F=2048 (weights 2.4 GB).
+    """
+    import torch
+    from serve_invariant_moe_gb300 import api, binding, build, synth
+    build.build()
+    dev = torch.device("cuda:0")
+    if args.profile_case == "lm_head":
+        import dataclasses
+        hc = dataclasses.replace(synth.GLM_HEAD, T=2048, V=32768)
+        hidden, wv, target, _, _ = synth.head_inputs(hc, dev)
+        ws = binding.new_workspace(binding.workspace_size(hc.T, hc.H, V=hc.V), dev)
+        for _ in range(3):
+            binding.lm_logprob_kl(hidden.to(dev), wv, target.to(dev), ws)
+        binding.check_status(ws)
+    else:
+        import dataclasses
+        mc = dataclasses.replace(synth.GLM_MOE, T=2048, E=32)
+        x, wr = synth.moe_activations(mc)
+        w13, w2 = synth.expert_weights(mc, dev)
+        ws13, ws2 = synth.shared_expert_weights(mc, dev)
+        layer = api.MoELayer(api.MoEWeights(wr.to(dev), w13, w2, mc.k, ws13, ws2))
+        for _ in range(3):
+            layer.prefill(x.to(dev))
+        binding.check_status(layer._ws)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": args.profile_case, "ok": True}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--profile-case", choices=["lm_head", "experts"], default=None)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=4)
+    ap.add_argument("--ref-tokens-per-step", type=int, default=1)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -177,12 +177,23 @@ int lm_logprob_kl(const void* hidden, const void* w_vocab, const int32_t* target
 /* d[m, n] = sum_k a[m, k] * b[n, k] (fp32 out, ldd = N): the dense tcgen05 GEMM
  * engine on its own, used by the tests to check the engine at ragged sizes.
  * variant selects the tile configuration the other calls use:
- *   0 = 128 x 256 tile, one row tile per unit (vocab projection)
- *   1 = 128 x 256 tile, two row tiles per unit (expert down projection)
+ *   0 = 128 x 256 tile, one row tile per unit
+ *   1 = 128 x 256 tile, two row tiles per unit (vocab and expert down projections)
  *   2 = 128 x 128 tile, 3 = 128 x 64 tile (router logits for E <= 128 / 64)
+ * plus 256 to order the work units column-block-major (the vocab projection's order).
  * a [M, K] bf16, b [N, K] bf16.  Shapes: K % 64 == 0, N % 4 == 0. */
 int invmoe_gemm_bf16(const void* a, const void* b, int M, int N, int K, float* d, int variant,
                      void* workspace, size_t ws_bytes, void* stream);
+
+/* Per-kernel timing.  While enabled, every kernel launch made by this library
+ * is bracketed by a pair of CUDA events recorded on the launch stream (events
+ * come from a host-side pool; no device memory is allocated).
+ * invmoe_profile_collect() waits for the recorded events, writes up to
+ * max_entries aggregated rows -- kernel name (NUL-terminated, at most 47 chars,
+ * in a 48-byte slot of `names`), total milliseconds and launch count -- drops
+ * the records and returns the number of rows (negative on error). */
+int invmoe_profile_enable(int on);
+int invmoe_profile_collect(char* names, float* total_ms, int* launches, int max_entries);
 
 /* Launch a one-CTA kernel that waits on an mbarrier nothing ever completes,
  * with a wait limit of `timeout_us` microseconds (1..2000000).  The kernel

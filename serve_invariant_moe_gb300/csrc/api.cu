@@ -5,6 +5,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 
@@ -57,6 +58,44 @@ int device_sm_count(int* out) {
   if (dev < 64) cache[dev] = n;
   *out = n;
   return INVMOE_OK;
+}
+
+namespace {
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_recs;
+std::vector<cudaEvent_t> g_prof_pool;
+
+cudaEvent_t take_event() {
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+}  // namespace
+
+ProfScope::ProfScope(const char* name, cudaStream_t st) : idx_(-1), st_(st) {
+  if (!g_prof_on) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  ProfRec r{name, take_event(), take_event()};
+  if (!r.a || !r.b) return;
+  cudaEventRecord(r.a, st);
+  g_prof_recs.push_back(r);
+  idx_ = static_cast<long>(g_prof_recs.size()) - 1;
+}
+
+ProfScope::~ProfScope() {
+  if (idx_ < 0) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (idx_ < static_cast<long>(g_prof_recs.size())) cudaEventRecord(g_prof_recs[idx_].b, st_);
 }
 
 }  // namespace invmoe
@@ -127,6 +166,7 @@ int moe_route_topk(const void* x, const void* w_router, int T, int H, int E, int
   REQUIRE_ALIGNED(workspace);
 
   GemmCall g{};
+  g.name = "router_gemm";
   g.variant = E <= 64 ? GV_F32_BN64_MT1 : (E <= 128 ? GV_F32_BN128_MT1 : GV_F32_BN256_MT1);
   g.A = x; g.a_rows = T; g.B = w_router; g.b_rows = E; g.K = H; g.N = E; g.M = T; g.G = 0;
   g.out = logits; g.ldo = E; g.status = status_word(workspace);
@@ -164,6 +204,7 @@ int moe_grouped_ffn(const void* xp, const int32_t* plan, const void* w13, const 
   unsigned int* status = status_word(workspace);
 
   GemmCall g1{};
+  g1.name = "expert_gemm1_swiglu";
   g1.variant = GV_SWIGLU_BN256_MT2;
   g1.A = xp; g1.a_rows = S; g1.B = w13; g1.b_rows = static_cast<long long>(E) * 2 * F; g1.K = H;
   g1.N = F; g1.G = E; g1.counts = counts; g1.offsets = offsets; g1.b_group_rows = 2 * F; g1.b_up_rows = F;
@@ -172,6 +213,7 @@ int moe_grouped_ffn(const void* xp, const int32_t* plan, const void* w13, const 
   if (rc) return rc;
 
   GemmCall g2{};
+  g2.name = "expert_gemm2";
   g2.variant = GV_F32_BN256_MT2;
   g2.A = h; g2.a_rows = S; g2.B = w2; g2.b_rows = static_cast<long long>(E) * H; g2.K = F;
   g2.N = H; g2.G = E; g2.counts = counts; g2.offsets = offsets; g2.b_group_rows = H;
@@ -181,12 +223,14 @@ int moe_grouped_ffn(const void* xp, const int32_t* plan, const void* w13, const 
   if (F_shared > 0) {
     void* hs = scratch(workspace);
     GemmCall s1{};
+    s1.name = "shared_gemm1_swiglu";
     s1.variant = GV_SWIGLU_BN256_MT2;
     s1.A = x_shared; s1.a_rows = T; s1.B = ws13; s1.b_rows = 2LL * F_shared; s1.K = H;
     s1.N = F_shared; s1.M = T; s1.G = 0; s1.b_group_rows = 0; s1.b_up_rows = F_shared;
     s1.out = hs; s1.ldo = F_shared; s1.status = status;
     if ((rc = gemm_run(s1, st))) return rc;
     GemmCall s2{};
+    s2.name = "shared_gemm2";
     s2.variant = GV_F32_BN256_MT2;
     s2.A = hs; s2.a_rows = T; s2.B = ws2; s2.b_rows = H; s2.K = F_shared;
     s2.N = H; s2.M = T; s2.G = 0;
@@ -223,7 +267,8 @@ int lm_logprob_kl(const void* hidden, const void* w_vocab, const int32_t* target
   REQUIRE_ALIGNED(hidden); REQUIRE_ALIGNED(w_vocab); REQUIRE_ALIGNED(logits); REQUIRE_ALIGNED(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   GemmCall g{};
-  g.variant = GV_F32_BN256_MT1;
+  g.name = "lm_head_gemm";
+  g.variant = GV_F32_BN256_MT2;
   g.A = hidden; g.a_rows = T; g.B = w_vocab; g.b_rows = V; g.K = H; g.N = V; g.M = T; g.G = 0;
   g.n_major = 1; g.out = logits; g.ldo = V; g.status = status_word(workspace);
   int rc = gemm_run(g, st);
@@ -237,18 +282,57 @@ int invmoe_gemm_bf16(const void* a, const void* b, int M, int N, int K, float* d
   REQUIRE(M >= 0 && N > 0 && K > 0, INVMOE_ERR_INVALID_ARG, "bad sizes");
   REQUIRE(K % 64 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 64", K);
   REQUIRE(N % 4 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "N=%d is not a multiple of 4", N);
-  REQUIRE(variant >= 0 && variant <= 3, INVMOE_ERR_INVALID_ARG, "variant must be 0..3");
+  const int n_major = (variant >> 8) & 1;
+  variant &= 0xff;
+  REQUIRE(variant >= 0 && variant <= 3, INVMOE_ERR_INVALID_ARG, "variant must be 0..3 (+256 for n-major)");
   REQUIRE_PTR(workspace);
   REQUIRE(ws_bytes >= kStatusBytes, INVMOE_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
   if (M == 0) return INVMOE_OK;
   REQUIRE_PTR(a); REQUIRE_PTR(b); REQUIRE_PTR(d);
   REQUIRE_ALIGNED(a); REQUIRE_ALIGNED(b); REQUIRE_ALIGNED(d);
   GemmCall g{};
+  g.name = "gemm_bf16";
   g.variant = static_cast<GemmVariant>(variant);
   g.A = a; g.a_rows = M; g.B = b; g.b_rows = N; g.K = K; g.N = N; g.M = M; g.G = 0;
-  g.n_major = (variant == 0) ? 1 : 0;
+  g.n_major = n_major;
   g.out = d; g.ldo = N; g.status = status_word(workspace);
   return gemm_run(g, static_cast<cudaStream_t>(stream));
+}
+
+int invmoe_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = on != 0;
+  return INVMOE_OK;
+}
+
+int invmoe_profile_collect(char* names, float* total_ms, int* launches, int max_entries) {
+  REQUIRE_PTR(names); REQUIRE_PTR(total_ms); REQUIRE_PTR(launches);
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  int n = 0;
+  int rc = INVMOE_OK;
+  for (const ProfRec& r : g_prof_recs) {
+    float ms = 0.f;
+    if (!rc) rc = check_cuda(cudaEventSynchronize(r.b), "cudaEventSynchronize");
+    if (!rc) rc = check_cuda(cudaEventElapsedTime(&ms, r.a, r.b), "cudaEventElapsedTime");
+    int slot = -1;
+    for (int i = 0; i < n; ++i)
+      if (strncmp(names + 48 * i, r.name, 47) == 0) { slot = i; break; }
+    if (slot < 0 && n < max_entries) {
+      slot = n++;
+      strncpy(names + 48 * slot, r.name, 47);
+      names[48 * slot + 47] = 0;
+      total_ms[slot] = 0.f;
+      launches[slot] = 0;
+    }
+    if (slot >= 0) {
+      total_ms[slot] += ms;
+      launches[slot] += 1;
+    }
+    g_prof_pool.push_back(r.a);
+    g_prof_pool.push_back(r.b);
+  }
+  g_prof_recs.clear();
+  return rc ? rc : n;
 }
 
 int invmoe_debug_timeout_probe(void* workspace, size_t ws_bytes, int timeout_us, void* stream) {

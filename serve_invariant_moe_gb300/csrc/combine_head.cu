@@ -168,6 +168,7 @@ int combine_launch(const float* y, const float* topk_w, const int32_t* slot_row,
   long long blocks = (total + 255) / 256;
   if (blocks > static_cast<long long>(sms) * 16) blocks = static_cast<long long>(sms) * 16;
   if (blocks == 0) return INVMOE_OK;
+  ProfScope prof("combine", st);
   combine_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(
       reinterpret_cast<const float4*>(y), topk_w, slot_row, reinterpret_cast<const float4*>(y_shared), T, H4, k,
       reinterpret_cast<float4*>(out), reinterpret_cast<uint2*>(out_bf16));
@@ -182,8 +183,12 @@ int lse_launch(const float* logits, const int32_t* target, const float* rollout_
   const long long warps = static_cast<long long>(T) * groups;
   const long long blocks = (warps * 32 + 255) / 256;
   if (blocks == 0) return INVMOE_OK;
+  {
+  ProfScope prof1("lse_partial", st);
   lse_partial_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(logits, T, V, NCH, partials);
+  }
   if ((rc = check_cuda(cudaGetLastError(), "lse_partial_kernel"))) return rc;
+  ProfScope prof2("lse_merge", st);
   lse_merge_kernel<<<(T + 127) / 128, 128, 0, st>>>(partials, logits, target, rollout_logp, T, V, NCH, beta, logp,
                                                    lse, k3, mask);
   return check_cuda(cudaGetLastError(), "lse_merge_kernel");

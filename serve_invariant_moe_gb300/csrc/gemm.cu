@@ -82,6 +82,8 @@ int launch(const GemmCall& c, cudaStream_t st) {
   p.out = c.out;
   p.ldo = c.ldo;
   p.status = c.status;
+  // the dynamic-schedule counter lives in the workspace's status block, after the status word
+  p.sched = reinterpret_cast<int*>(reinterpret_cast<char*>(c.status) + 64);
   p.timeout_ns = kTimeoutNs;
 
   constexpr long long CH = static_cast<long long>(MT) * kBM;
@@ -89,7 +91,9 @@ int launch(const GemmCall& c, cudaStream_t st) {
   long long max_units = max_chunks * p.n_blocks;
   if (max_units <= 0) return INVMOE_OK;
   const int grid = static_cast<int>(max_units < sms ? max_units : sms);
-  tc_gemm_kernel<BN, MT, EPI, STAGES><<<grid, 192, S::SMEM_BYTES, st>>>(ta, tb, p);
+  if ((rc = check_cuda(cudaMemsetAsync(p.sched, 0, sizeof(int), st), "cudaMemsetAsync"))) return rc;
+  ProfScope prof(c.name ? c.name : "tc_gemm", st);
+  tc_gemm_kernel<BN, MT, EPI, STAGES><<<grid, S::THREADS, S::SMEM_BYTES, st>>>(ta, tb, p);
   return check_cuda(cudaGetLastError(), "tc_gemm_kernel launch");
 }
 

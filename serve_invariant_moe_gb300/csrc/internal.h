@@ -20,6 +20,16 @@ constexpr int kLseChunk = 256;       // vocabulary columns per log-sum-exp parti
 constexpr size_t kStatusBytes = 256;
 
 int set_error(int code, const char* fmt, ...);
+
+// Brackets one kernel launch with CUDA events while profiling is enabled.
+class ProfScope {
+ public:
+  ProfScope(const char* name, cudaStream_t st);
+  ~ProfScope();
+ private:
+  long idx_;
+  cudaStream_t st_;
+};
 int check_cuda(cudaError_t e, const char* what);
 int device_sm_count(int* out);
 
@@ -35,6 +45,7 @@ enum GemmVariant : int {
 };
 
 struct GemmCall {
+  const char* name;    // kernel label for the profiler
   GemmVariant variant;
   const void* A;       // [a_rows, K] bf16
   long long a_rows;

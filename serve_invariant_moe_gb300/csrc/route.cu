@@ -192,6 +192,7 @@ int route_launch(const float* logits, int T, int E, int k, int H, const void* x,
     const int threads = 256;
     const long long blocks = (static_cast<long long>(T) * 32 + threads - 1) / threads;
     const int epl = (E + 31) / 32;
+    ProfScope prof("topk_gate", st);
     if (epl <= 1) topk_gate_kernel<1><<<blocks, threads, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
     else if (epl <= 2) topk_gate_kernel<2><<<blocks, threads, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
     else if (epl <= 4) topk_gate_kernel<4><<<blocks, threads, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
@@ -202,12 +203,21 @@ int route_launch(const float* logits, int T, int E, int k, int H, const void* x,
   }
   // dispatch plan
   const int NC = (T + kDispatchChunk - 1) / kDispatchChunk;
-  dispatch_count_kernel<<<NC, 256, E * sizeof(int), st>>>(topk_idx, T, E, k, chunk_counts);
+  {
+    ProfScope prof("dispatch_count", st);
+    dispatch_count_kernel<<<NC, 256, E * sizeof(int), st>>>(topk_idx, T, E, k, chunk_counts);
+  }
   if ((rc = check_cuda(cudaGetLastError(), "dispatch_count_kernel"))) return rc;
-  dispatch_scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, NC, E, counts, offsets);
+  {
+    ProfScope prof("dispatch_scan", st);
+    dispatch_scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, NC, E, counts, offsets);
+  }
   if ((rc = check_cuda(cudaGetLastError(), "dispatch_scan_kernel"))) return rc;
-  dispatch_scatter_kernel<<<NC, 32, E * sizeof(int), st>>>(topk_idx, T, E, k, chunk_counts, offsets, row_token,
-                                                           slot_row);
+  {
+    ProfScope prof("dispatch_scatter", st);
+    dispatch_scatter_kernel<<<NC, 32, E * sizeof(int), st>>>(topk_idx, T, E, k, chunk_counts, offsets, row_token,
+                                                             slot_row);
+  }
   if ((rc = check_cuda(cudaGetLastError(), "dispatch_scatter_kernel"))) return rc;
   // permute
   const int vec_per_row = H / 8;
@@ -218,6 +228,7 @@ int route_launch(const float* logits, int T, int E, int k, int H, const void* x,
   const long long cap = static_cast<long long>(sms) * 16;
   if (blocks > cap) blocks = cap;
   if (blocks > 0) {
+    ProfScope prof("gather_rows", st);
     gather_rows_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(static_cast<const uint4*>(x), row_token, S,
                                                                   vec_per_row, static_cast<uint4*>(xp));
     if ((rc = check_cuda(cudaGetLastError(), "gather_rows_kernel"))) return rc;

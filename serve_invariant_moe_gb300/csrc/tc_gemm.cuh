@@ -58,6 +58,7 @@ struct GemmParams {
   void* out;              // D (fp32) or h (bf16)
   long long ldo;          // output row stride, elements
   unsigned int* status;   // status word (bit 0: a bounded wait ran out)
+  int* sched;             // unit counter for the dynamic schedule (zero before launch)
   unsigned long long timeout_ns;
 };
 
@@ -71,13 +72,16 @@ struct GemmShape {
   static constexpr int TMEM_NEED = ACC_STAGES * ACC_COLS;
   static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128
                                    : TMEM_NEED <= 256 ? 256 : 512;
+  static constexpr int EPI_WARPS = 8;                           // two warps per TMEM lane quadrant
+  static constexpr int EPI_THREADS = 32 * EPI_WARPS;
+  static constexpr int THREADS = 64 + EPI_THREADS;
+  static constexpr int QDEPTH = 4;                              // scheduled-unit queue depth
   static constexpr int MAX_GROUPS = 1024;
-  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * ACC_STAGES + 1);
-  static constexpr int MISC_BYTES = 16;
+  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * ACC_STAGES + 1 + 2 * QDEPTH);
+  static constexpr int MISC_BYTES = 16 + 4 * QDEPTH;
   static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + BAR_BYTES + MISC_BYTES +
                                     4 * (MAX_GROUPS + 1);
-  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
-  static_assert(EPI != EPI_SWIGLU || BN % 64 == 0, "SwiGLU splits BN into gate/up halves");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(TMEM_NEED <= 512, "TMEM");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
@@ -132,8 +136,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Work units are handed out dynamically: the producer thread takes the next
+// unit index from a global counter and publishes it through a small shared
+// queue to the MMA thread and the epilogue warps.  Which CTA computes which
+// tile therefore varies from run to run; the arithmetic of every tile does not.
 template <int BN, int MT, int EPI, int STAGES>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
   using S = GemmShape<BN, MT, EPI, STAGES>;
@@ -145,11 +153,14 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* accf_bar = empty_bar + STAGES;
   uint64_t* acce_bar = accf_bar + S::ACC_STAGES;
   uint64_t* final_bar = acce_bar + S::ACC_STAGES;
-  uint32_t* misc = reinterpret_cast<uint32_t*>(final_bar + 1);
+  uint64_t* qfull_bar = final_bar + 1;
+  uint64_t* qempty_bar = qfull_bar + S::QDEPTH;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(qempty_bar + S::QDEPTH);
   uint32_t* tmem_slot = misc;
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 1);
   int* s_total = reinterpret_cast<int*>(misc + 2);
-  int* s_prefix = reinterpret_cast<int*>(misc + 4);  // [G+1]
+  volatile int* s_queue = reinterpret_cast<volatile int*>(misc + 4);    // [QDEPTH]
+  int* s_prefix = reinterpret_cast<int*>(misc + 4 + S::QDEPTH);         // [G+1]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -161,9 +172,13 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < S::ACC_STAGES; ++a) {
       mbar_init(&accf_bar[a], 1);
-      mbar_init(&acce_bar[a], 128);
+      mbar_init(&acce_bar[a], S::EPI_THREADS);
     }
     mbar_init(final_bar, 1);
+    for (int q = 0; q < S::QDEPTH; ++q) {
+      mbar_init(&qfull_bar[q], 1);
+      mbar_init(&qempty_bar[q], 1 + S::EPI_THREADS);
+    }
     *s_abort = 0;
     fence_barrier_init();
   }
@@ -216,18 +231,27 @@ __global__ void __launch_bounds__(192, 1)
   WaitCtl wc{s_abort, p.status, p.timeout_ns};
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producer + scheduler
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
+      int qi = 0;
+      uint32_t qphase = 0;
       int filled_phase[STAGES];
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) filled_phase[s] = -1;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+      while (true) {
+        int u = atomicAdd(p.sched, 1);
+        if (u >= total_units) u = -1;
+        if (!mbar_wait(&qempty_bar[qi], qphase ^ 1u, wc)) break;
+        s_queue[qi] = u;
+        mbar_arrive(&qfull_bar[qi]);
+        if (++qi == S::QDEPTH) { qi = 0; qphase ^= 1u; }
+        if (u < 0) break;
         const Unit U = decode_unit<MT, EPI, BN>(u, p, s_prefix, total_chunks);
         const int ntile = (U.rows + kBM - 1) / kBM;
         const uint32_t bytes = ntile * S::A_BYTES + S::B_BYTES;
+        bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wc)) { ok = false; break; }
           uint8_t* st = ring + stage * S::STAGE_BYTES;
@@ -244,6 +268,7 @@ __global__ void __launch_bounds__(192, 1)
           filled_phase[stage] = static_cast<int>(phase);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
+        if (!ok) break;
       }
       // Let every copy this thread issued land before the CTA can exit.
       WaitCtl drain{nullptr, p.status, p.timeout_ns};
@@ -258,13 +283,20 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+      int qi = 0;
+      uint32_t qphase = 0;
+      while (true) {
+        if (!mbar_wait(&qfull_bar[qi], qphase, wc)) break;
+        const int u = s_queue[qi];
+        mbar_arrive(&qempty_bar[qi]);
+        if (++qi == S::QDEPTH) { qi = 0; qphase ^= 1u; }
+        if (u < 0) break;
         const Unit U = decode_unit<MT, EPI, BN>(u, p, s_prefix, total_chunks);
         const int ntile = (U.rows + kBM - 1) / kBM;
-        if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1u, wc)) { ok = false; break; }
+        if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1u, wc)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * S::ACC_COLS);
+        bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, wc)) { ok = false; break; }
           tc_fence_after();
@@ -293,11 +325,21 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int ew = warp - 2;                 // 0 .. EPI_WARPS-1
+    const int q = warp & 3;                  // TMEM lane quadrant this warp may access
+    const int half = ew >> 2;                // which half of the column chunks this warp converts
     const int r_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    int qi = 0;
+    uint32_t qphase = 0;
+    while (true) {
+      const bool okq = mbar_wait(&qfull_bar[qi], qphase, wc);
+      if (!__all_sync(0xffffffffu, okq)) break;
+      const int u = s_queue[qi];
+      mbar_arrive(&qempty_bar[qi]);
+      if (++qi == S::QDEPTH) { qi = 0; qphase ^= 1u; }
+      if (u < 0) break;
       const Unit U = decode_unit<MT, EPI, BN>(u, p, s_prefix, total_chunks);
       const int ntile = (U.rows + kBM - 1) / kBM;
       // every lane waits; the warp proceeds only if all lanes saw the phase
@@ -315,7 +357,7 @@ __global__ void __launch_bounds__(192, 1)
           const int n0 = U.nb * BN;
           float* orow = static_cast<float*>(p.out) + row * p.ldo + n0;
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
+          for (int c = half; c < BN / 32; c += 2) {
             uint32_t v[32];
             tmem_ld32(tbase + c * 32, v);
             tmem_ld_wait();
@@ -336,7 +378,7 @@ __global__ void __launch_bounds__(192, 1)
           const int n0 = U.nb * HALF;
           __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + row * p.ldo + n0;
 #pragma unroll 1
-          for (int c = 0; c < HALF / 32; ++c) {
+          for (int c = half; c < HALF / 32; c += 2) {
             uint32_t gv[32], uv[32];
             tmem_ld32(tbase + c * 32, gv);
             tmem_ld32(tbase + HALF + c * 32, uv);

@@ -117,17 +117,24 @@ def moe_activations(cfg: MoEConfig, T: int = None, seed_offset: int = 0):
     return x, wr
 
 
+def one_expert(cfg: MoEConfig, e: int, device="cpu"):
+    """Weights of expert e alone (its own generator), bf16: W13_e [2F, H], W2_e [H, F]."""
+    g = _gen(cfg.seed * 7919 + 101 + 7 * e, device)
+    w13 = to_bf16(normal((2 * cfg.F, cfg.H), cfg.w_std, g, device))
+    w2 = to_bf16(normal((cfg.H, cfg.F), cfg.w_std, g, device))
+    return w13, w2
+
+
 def expert_weights(cfg: MoEConfig, device="cpu"):
     """Expert weight banks, bf16: W13 [E, 2F, H] (gate rows then up rows), W2 [E, H, F].
 
-    Drawn one expert at a time to bound the float32 temporary.
+    Drawn one expert at a time (each from its own seeded generator, so any one
+    expert can be re-drawn alone) to bound the float32 temporary.
     """
-    g = _gen(cfg.seed * 7919 + 101, device)
     w13 = torch.empty((cfg.E, 2 * cfg.F, cfg.H), dtype=torch.bfloat16, device=device)
     w2 = torch.empty((cfg.E, cfg.H, cfg.F), dtype=torch.bfloat16, device=device)
     for e in range(cfg.E):
-        w13[e] = to_bf16(normal((2 * cfg.F, cfg.H), cfg.w_std, g, device))
-        w2[e] = to_bf16(normal((cfg.H, cfg.F), cfg.w_std, g, device))
+        w13[e], w2[e] = one_expert(cfg, e, device)
     return w13, w2
 
 
