@@ -149,20 +149,22 @@ int moe_combine(const float* y, const float* topk_w, const int32_t* plan, const 
 /* ---------------------------------------------------------------------------
  * lm_logprob_kl -- vocab projection, chunked two-pass log-sum-exp, logprob, k3, IcePop
  *
- *   logits[t, v] = sum_h hidden[t, h] * w_vocab[v, h]       (fp32, tcgen05 tile)
- *   pass 1, chunk c = columns [256c, 256c+256):  m_c = max, s_c = sum exp(z - m_c)
- *           (fixed per-lane order then a fixed butterfly)
+ *   z[t, v] = sum_h hidden[t, h] * w_vocab[v, h]     (fp32 in TMEM, tcgen05 tile 128 x 256 x 64)
+ *   pass 1, in the projection's epilogue, chunk c = columns [256c, 256c+256):
+ *           m_c = max z;  s_c = sum of exp(z - m_c): column j of the chunk is added,
+ *           in ascending j, to accumulator j mod 8, then s_c = ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7))
  *   pass 2, c = 0, 1, 2, ... in order:  M' = max(M, m_c);
  *           S = S*exp(M - M') + s_c*exp(m_c - M');  lse = M + log(S)
- *   logp[t] = logits[t, target[t]] - lse[t]
+ *   logp[t] = z[t, target[t]] - lse[t]
  *   if rollout_logp != NULL:
  *     d = logp - rollout_logp;  k3 = expm1(d) - d;  rho = exp(d);
  *     mask = (1/beta <= rho) && (rho <= beta)      (all fp32)
  * A target outside [0, V) yields logp = NaN for that token.
  *
  * hidden [T, H] bf16, w_vocab [V, H] bf16, target [T] int32, rollout_logp [T]
- * fp32 (nullable: k3/mask not written), logits [T, V] fp32 (written; the
- * caller's buffer), logp/lse/k3 [T] fp32, mask [T] uint8 (k3, mask nullable).
+ * fp32 (nullable: k3/mask not written), logits [T, V] fp32 (nullable: the logits
+ * are then never written to memory), logp [T] fp32, lse/k3 [T] fp32 and mask [T]
+ * uint8 (nullable).
  * Shapes: H % 64 == 0, V % 4 == 0, beta >= 1.
  * ------------------------------------------------------------------------- */
 int lm_logprob_kl(const void* hidden, const void* w_vocab, const int32_t* target,
@@ -180,6 +182,7 @@ int lm_logprob_kl(const void* hidden, const void* w_vocab, const int32_t* target
  *   0 = 128 x 256 tile, one row tile per unit
  *   1 = 128 x 256 tile, two row tiles per unit (vocab and expert down projections)
  *   2 = 128 x 128 tile, 3 = 128 x 64 tile (router logits for E <= 128 / 64)
+ *   4 = 256 x 256 tile computed by a CTA pair (cta_group::2) on two SMs
  * plus 256 to order the work units column-block-major (the vocab projection's order).
  * a [M, K] bf16, b [N, K] bf16.  Shapes: K % 64 == 0, N % 4 == 0. */
 int invmoe_gemm_bf16(const void* a, const void* b, int M, int N, int K, float* d, int variant,

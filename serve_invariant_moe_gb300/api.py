@@ -116,11 +116,12 @@ def moe_decode(layer: MoELayer, x_tokens: torch.Tensor) -> torch.Tensor:
     return layer.decode(x_tokens)
 
 
-def head_logprob_kl(hidden, w_vocab, target, rollout_logp=None, beta=2.0, workspace=None, logits=None):
+def head_logprob_kl(hidden, w_vocab, target, rollout_logp=None, beta=2.0, workspace=None, logits=None,
+                    write_logits=False):
     """Token logprobs of the exact target ids, and (with rollout logprobs) k3 and the IcePop mask."""
     T, H = hidden.shape
     V = w_vocab.shape[0]
     if workspace is None:
         workspace = binding.new_workspace(binding.workspace_size(T, H, V=V), hidden.device)
     return binding.lm_logprob_kl(hidden, w_vocab, target, workspace, rollout_logp=rollout_logp, beta=beta,
-                                 logits=logits)
+                                 logits=logits, write_logits=write_logits)

@@ -126,15 +126,18 @@ def moe_combine(y, topk_w, plan, T, H, E, k, y_shared=None, out=None, out_bf16=N
 
 
 def lm_logprob_kl(hidden, w_vocab, target, workspace, rollout_logp=None, beta=2.0, logits=None,
-                  logp=None, lse=None, k3=None, mask=None):
+                  logp=None, lse=None, k3=None, mask=None, write_logits=False):
+    """logits are written only if a buffer is passed or write_logits is set."""
     T, H = hidden.shape
     V = w_vocab.shape[0]
     dev = hidden.device
     _req(hidden, torch.bfloat16, "hidden")
     _req(w_vocab, torch.bfloat16, "w_vocab", (V, H))
     _req(target, torch.int32, "target", (T,))
-    logits = torch.empty((T, V), dtype=torch.float32, device=dev) if logits is None else logits
-    _req(logits, torch.float32, "logits", (T, V))
+    if logits is None and write_logits:
+        logits = torch.empty((T, V), dtype=torch.float32, device=dev)
+    if logits is not None:
+        _req(logits, torch.float32, "logits", (T, V))
     logp = torch.empty(T, dtype=torch.float32, device=dev) if logp is None else logp
     lse = torch.empty(T, dtype=torch.float32, device=dev) if lse is None else lse
     if rollout_logp is not None:

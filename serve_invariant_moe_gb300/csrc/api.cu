@@ -21,10 +21,11 @@ size_t route_ws(int T, int E) {
   return align_up(NC * static_cast<size_t>(E) * sizeof(int32_t), 256);
 }
 size_t ffn_ws(int T, int F_shared) { return align_up(static_cast<size_t>(T) * F_shared * 2, 256); }
-size_t head_ws(int T, int V) {
+size_t head_part_bytes(int T, int V) {
   const size_t NCH = (static_cast<size_t>(V) + kLseChunk - 1) / kLseChunk;
   return align_up(static_cast<size_t>(T) * NCH * sizeof(float2), 256);
 }
+size_t head_ws(int T, int V) { return head_part_bytes(T, V) + align_up(static_cast<size_t>(T) * 4, 256); }
 
 unsigned int* status_word(void* ws) { return static_cast<unsigned int*>(ws); }
 uint8_t* scratch(void* ws) { return static_cast<uint8_t*>(ws) + kStatusBytes; }
@@ -263,18 +264,21 @@ int lm_logprob_kl(const void* hidden, const void* w_vocab, const int32_t* target
   REQUIRE_PTR(workspace);
   REQUIRE(ws_bytes >= kStatusBytes + head_ws(T, V), INVMOE_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
   if (T == 0) return INVMOE_OK;
-  REQUIRE_PTR(hidden); REQUIRE_PTR(w_vocab); REQUIRE_PTR(target); REQUIRE_PTR(logits); REQUIRE_PTR(logp);
-  REQUIRE_ALIGNED(hidden); REQUIRE_ALIGNED(w_vocab); REQUIRE_ALIGNED(logits); REQUIRE_ALIGNED(workspace);
+  REQUIRE_PTR(hidden); REQUIRE_PTR(w_vocab); REQUIRE_PTR(target); REQUIRE_PTR(logp);
+  REQUIRE_ALIGNED(hidden); REQUIRE_ALIGNED(w_vocab); REQUIRE_ALIGNED(workspace);
+  if (logits) REQUIRE_ALIGNED(logits);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float2* part = reinterpret_cast<float2*>(scratch(workspace));
+  float* tgt_logit = reinterpret_cast<float*>(scratch(workspace) + head_part_bytes(T, V));
   GemmCall g{};
-  g.name = "lm_head_gemm";
-  g.variant = GV_F32_BN256_MT2;
+  g.name = "lm_head_gemm_lse";
+  g.variant = GV_LSE_BN256_MT2;
   g.A = hidden; g.a_rows = T; g.B = w_vocab; g.b_rows = V; g.K = H; g.N = V; g.M = T; g.G = 0;
   g.n_major = 1; g.out = logits; g.ldo = V; g.status = status_word(workspace);
+  g.part = part; g.target = target; g.tgt_logit = tgt_logit;
   int rc = gemm_run(g, st);
   if (rc) return rc;
-  return lse_launch(logits, target, rollout_logp, T, V, beta, reinterpret_cast<float2*>(scratch(workspace)), logp,
-                    lse, k3, mask, st);
+  return lse_merge_launch(part, tgt_logit, target, rollout_logp, T, V, beta, logp, lse, k3, mask, st);
 }
 
 int invmoe_gemm_bf16(const void* a, const void* b, int M, int N, int K, float* d, int variant, void* workspace,
@@ -284,7 +288,7 @@ int invmoe_gemm_bf16(const void* a, const void* b, int M, int N, int K, float* d
   REQUIRE(N % 4 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "N=%d is not a multiple of 4", N);
   const int n_major = (variant >> 8) & 1;
   variant &= 0xff;
-  REQUIRE(variant >= 0 && variant <= 3, INVMOE_ERR_INVALID_ARG, "variant must be 0..3 (+256 for n-major)");
+  REQUIRE(variant >= 0 && variant <= 4, INVMOE_ERR_INVALID_ARG, "variant must be 0..4 (+256 for n-major)");
   REQUIRE_PTR(workspace);
   REQUIRE(ws_bytes >= kStatusBytes, INVMOE_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
   if (M == 0) return INVMOE_OK;
@@ -292,7 +296,7 @@ int invmoe_gemm_bf16(const void* a, const void* b, int M, int N, int K, float* d
   REQUIRE_ALIGNED(a); REQUIRE_ALIGNED(b); REQUIRE_ALIGNED(d);
   GemmCall g{};
   g.name = "gemm_bf16";
-  g.variant = static_cast<GemmVariant>(variant);
+  g.variant = variant == 4 ? GV_PAIR_F32 : static_cast<GemmVariant>(variant);
   g.A = a; g.a_rows = M; g.B = b; g.b_rows = N; g.K = K; g.N = N; g.M = M; g.G = 0;
   g.n_major = n_major;
   g.out = d; g.ldo = N; g.status = status_word(workspace);

@@ -49,62 +49,17 @@ __global__ void combine_kernel(const float4* __restrict__ y, const float* __rest
   }
 }
 
-// Pass 1 ("GLM Post-Training Beyond SFT", section "动作与概率契约": logsumexp
-// needs comparison tests; the chunking fixes its order).  One warp per
-// (token, group of 4 chunks); chunk c covers columns [256c, 256c + 256).
-// Lane l holds columns 256c + 4l .. +3 and 256c + 128 + 4l .. +3.
-//   m_c = max of the chunk
-//   s_c = sum exp(z - m_c): each lane adds its 8 terms left to right, then a
-//         xor butterfly over lanes 16, 8, 4, 2, 1 (the same on every lane).
-constexpr int kChunksPerWarp = 4;
-
-__global__ void lse_partial_kernel(const float* __restrict__ z, int T, int V, int NCH, float2* __restrict__ part) {
-  const long long gw = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  const int groups = (NCH + kChunksPerWarp - 1) / kChunksPerWarp;
-  if (gw >= static_cast<long long>(T) * groups) return;
-  const long long t = gw / groups;
-  const int c0 = static_cast<int>(gw - t * groups) * kChunksPerWarp;
-  const float* row = z + t * V;
-  float4 a[kChunksPerWarp], b[kChunksPerWarp];
-  const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-#pragma unroll
-  for (int i = 0; i < kChunksPerWarp; ++i) {
-    const int col_a = (c0 + i) * kLseChunk + 4 * lane;
-    const int col_b = col_a + 128;
-    a[i] = (c0 + i < NCH && col_a < V) ? __ldcs(reinterpret_cast<const float4*>(row + col_a)) : ninf;
-    b[i] = (c0 + i < NCH && col_b < V) ? __ldcs(reinterpret_cast<const float4*>(row + col_b)) : ninf;
-  }
-#pragma unroll
-  for (int i = 0; i < kChunksPerWarp; ++i) {
-    if (c0 + i >= NCH) break;
-    float m = fmaxf(fmaxf(fmaxf(a[i].x, a[i].y), fmaxf(a[i].z, a[i].w)),
-                    fmaxf(fmaxf(b[i].x, b[i].y), fmaxf(b[i].z, b[i].w)));
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
-    float s = 0.0f;
-    if (m != -INFINITY) {
-      s = __fadd_rn(s, expf(a[i].x - m));
-      s = __fadd_rn(s, expf(a[i].y - m));
-      s = __fadd_rn(s, expf(a[i].z - m));
-      s = __fadd_rn(s, expf(a[i].w - m));
-      s = __fadd_rn(s, expf(b[i].x - m));
-      s = __fadd_rn(s, expf(b[i].y - m));
-      s = __fadd_rn(s, expf(b[i].z - m));
-      s = __fadd_rn(s, expf(b[i].w - m));
-    }
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, d));
-    if (lane == 0) part[t * NCH + (c0 + i)] = make_float2(m, s);
-  }
-}
-
-// Pass 2: one thread per token merges the partials in ascending chunk order,
+// Pass 2 of the chunked log-sum-exp ("GLM Post-Training Beyond SFT", section
+// "动作与概率契约": logsumexp needs comparison tests; the chunking fixes its
+// order).  Pass 1 runs in the vocabulary-projection epilogue: for the 256-column
+// chunk c of row t, m_c = max z and s_c = sum of exp(z - m_c) over the chunk's
+// columns in a fixed eight-accumulator order.  Here one thread per token merges the partials in
+// ascending chunk order,
 //   M' = max(M, m_c);  S = S*exp(M - M') + s_c*exp(m_c - M');  lse = M + log S,
 // then logp = z[target] - lse and, with rollout logprobs ("GLM Post-Training
 // Beyond SFT", section "IcePop 为什么有两层 ratio"), d = logp - rollout,
 // k3 = expm1(d) - d, rho = exp(d), mask = 1/beta <= rho <= beta.
-__global__ void lse_merge_kernel(const float2* __restrict__ part, const float* __restrict__ z,
+__global__ void lse_merge_kernel(const float2* __restrict__ part, const float* __restrict__ tgt_logit,
                                  const int32_t* __restrict__ target, const float* __restrict__ rollout, int T, int V,
                                  int NCH, float beta, float* __restrict__ logp, float* __restrict__ lse,
                                  float* __restrict__ k3, uint8_t* __restrict__ mask) {
@@ -123,8 +78,7 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, const float* _
   }
   const float l = __fadd_rn(M, logf(S));
   const int tg = target[t];
-  const float lp = (tg >= 0 && tg < V) ? __fsub_rn(z[static_cast<long long>(t) * V + tg], l)
-                                       : __uint_as_float(0x7fc00000u);
+  const float lp = (tg >= 0 && tg < V) ? __fsub_rn(tgt_logit[t], l) : __uint_as_float(0x7fc00000u);
   logp[t] = lp;
   if (lse != nullptr) lse[t] = l;
   if (rollout != nullptr) {
@@ -175,22 +129,14 @@ int combine_launch(const float* y, const float* topk_w, const int32_t* slot_row,
   return check_cuda(cudaGetLastError(), "combine_kernel");
 }
 
-int lse_launch(const float* logits, const int32_t* target, const float* rollout_logp, int T, int V, float beta,
-               float2* partials, float* logp, float* lse, float* k3, uint8_t* mask, cudaStream_t st) {
-  int rc;
+int lse_merge_launch(const float2* partials, const float* tgt_logit, const int32_t* target,
+                     const float* rollout_logp, int T, int V, float beta, float* logp, float* lse, float* k3,
+                     uint8_t* mask, cudaStream_t st) {
   const int NCH = (V + kLseChunk - 1) / kLseChunk;
-  const int groups = (NCH + kChunksPerWarp - 1) / kChunksPerWarp;
-  const long long warps = static_cast<long long>(T) * groups;
-  const long long blocks = (warps * 32 + 255) / 256;
-  if (blocks == 0) return INVMOE_OK;
-  {
-  ProfScope prof1("lse_partial", st);
-  lse_partial_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(logits, T, V, NCH, partials);
-  }
-  if ((rc = check_cuda(cudaGetLastError(), "lse_partial_kernel"))) return rc;
-  ProfScope prof2("lse_merge", st);
-  lse_merge_kernel<<<(T + 127) / 128, 128, 0, st>>>(partials, logits, target, rollout_logp, T, V, NCH, beta, logp,
-                                                   lse, k3, mask);
+  if (T == 0) return INVMOE_OK;
+  ProfScope prof("lse_merge", st);
+  lse_merge_kernel<<<(T + 127) / 128, 128, 0, st>>>(partials, tgt_logit, target, rollout_logp, T, V, NCH, beta,
+                                                   logp, lse, k3, mask);
   return check_cuda(cudaGetLastError(), "lse_merge_kernel");
 }
 

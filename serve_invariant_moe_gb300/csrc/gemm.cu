@@ -6,6 +6,7 @@
 
 #include "internal.h"
 #include "tc_gemm.cuh"
+#include "tc_gemm2.cuh"
 
 namespace invmoe {
 
@@ -85,6 +86,10 @@ int launch(const GemmCall& c, cudaStream_t st) {
   // the dynamic-schedule counter lives in the workspace's status block, after the status word
   p.sched = reinterpret_cast<int*>(reinterpret_cast<char*>(c.status) + 64);
   p.timeout_ns = kTimeoutNs;
+  p.part = c.part;
+  p.nch = (c.N + 255) / 256;
+  p.target = c.target;
+  p.tgt_logit = c.tgt_logit;
 
   constexpr long long CH = static_cast<long long>(MT) * kBM;
   long long max_chunks = (c.G > 0) ? (c.a_rows + CH - 1) / CH + c.G : (c.M + CH - 1) / CH;
@@ -95,6 +100,76 @@ int launch(const GemmCall& c, cudaStream_t st) {
   ProfScope prof(c.name ? c.name : "tc_gemm", st);
   tc_gemm_kernel<BN, MT, EPI, STAGES><<<grid, S::THREADS, S::SMEM_BYTES, st>>>(ta, tb, p);
   return check_cuda(cudaGetLastError(), "tc_gemm_kernel launch");
+}
+
+GemmParams make_params(const GemmCall& c, int nb_cols) {
+  GemmParams p;
+  p.K = c.K;
+  p.N = c.N;
+  p.n_blocks = (c.N + nb_cols - 1) / nb_cols;
+  p.M = c.M;
+  p.G = c.G;
+  p.counts = c.counts;
+  p.offsets = c.offsets;
+  p.b_group_rows = c.b_group_rows;
+  p.b_up_rows = c.b_up_rows;
+  p.n_major = c.n_major;
+  p.out = c.out;
+  p.ldo = c.ldo;
+  p.status = c.status;
+  p.sched = reinterpret_cast<int*>(reinterpret_cast<char*>(c.status) + 64);
+  p.timeout_ns = kTimeoutNs;
+  p.part = c.part;
+  p.nch = (c.N + 255) / 256;
+  p.target = c.target;
+  p.tgt_logit = c.tgt_logit;
+  return p;
+}
+
+// CTA-pair engine: clusters of 2, grid = 2 x min(units, SMs / 2).
+template <int EPI, int STAGES>
+int launch_pair(const GemmCall& c, cudaStream_t st) {
+  using S = PairShape<EPI, STAGES>;
+  if (c.G > S::MAX_GROUPS) return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "more than %d groups", S::MAX_GROUPS);
+  CUtensorMap ta, tb;
+  int rc = make_tmap(&ta, c.A, c.K, c.a_rows, kBM);
+  if (rc) return rc;
+  rc = make_tmap(&tb, c.B, c.K, c.b_rows, kBM);
+  if (rc) return rc;
+  int dev = 0;
+  if ((rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice"))) return rc;
+  static bool attr_set[64] = {};
+  if (dev < 64 && !attr_set[dev]) {
+    rc = check_cuda(cudaFuncSetAttribute(tc_gemm_pair_kernel<EPI, STAGES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES),
+                    "cudaFuncSetAttribute");
+    if (rc) return rc;
+    attr_set[dev] = true;
+  }
+  int sms = 0;
+  if ((rc = device_sm_count(&sms))) return rc;
+  const GemmParams p = make_params(c, EPI == EPI_SWIGLU ? 128 : 256);
+  constexpr long long CH = 2LL * kBM;
+  long long max_chunks = (c.G > 0) ? (c.a_rows + CH - 1) / CH + c.G : (c.M + CH - 1) / CH;
+  long long max_units = max_chunks * p.n_blocks;
+  if (max_units <= 0) return INVMOE_OK;
+  const long long pairs = max_units < sms / 2 ? max_units : sms / 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(S::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = S::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  ProfScope prof(c.name ? c.name : "tc_gemm_pair", st);
+  rc = check_cuda(cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<EPI, STAGES>, ta, tb, p), "cudaLaunchKernelEx");
+  if (rc) return rc;
+  return check_cuda(cudaGetLastError(), "tc_gemm_pair_kernel launch");
 }
 
 }  // namespace
@@ -108,6 +183,10 @@ int gemm_run(const GemmCall& c, cudaStream_t st) {
     case GV_F32_BN128_MT1: return launch<128, 1, EPI_F32, 6>(c, st);
     case GV_F32_BN64_MT1: return launch<64, 1, EPI_F32, 8>(c, st);
     case GV_SWIGLU_BN256_MT2: return launch<256, 2, EPI_SWIGLU, 3>(c, st);
+    case GV_LSE_BN256_MT2: return launch<256, 2, EPI_LSE, 3>(c, st);
+    case GV_PAIR_F32: return launch_pair<EPI_F32, 6>(c, st);
+    case GV_PAIR_LSE: return launch_pair<EPI_LSE, 6>(c, st);
+    case GV_PAIR_SWIGLU: return launch_pair<EPI_SWIGLU, 6>(c, st);
   }
   return set_error(INVMOE_ERR_INVALID_ARG, "unknown GEMM variant %d", (int)c.variant);
 }

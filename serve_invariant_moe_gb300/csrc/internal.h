@@ -41,7 +41,11 @@ enum GemmVariant : int {
   GV_F32_BN256_MT2 = 1,   // grouped/dense fp32-out, 2 row tiles per unit (expert down projection)
   GV_F32_BN128_MT1 = 2,
   GV_F32_BN64_MT1 = 3,
-  GV_SWIGLU_BN256_MT2 = 4 // grouped/dense gate+up with SwiGLU epilogue -> bf16
+  GV_SWIGLU_BN256_MT2 = 4, // grouped/dense gate+up with SwiGLU epilogue -> bf16
+  GV_LSE_BN256_MT2 = 5,    // dense vocab projection with per-chunk log-sum-exp partials
+  GV_PAIR_F32 = 6,         // CTA-pair 256 x 256 tile, fp32 out
+  GV_PAIR_LSE = 7,         // CTA-pair tile, log-sum-exp epilogue
+  GV_PAIR_SWIGLU = 8       // CTA-pair tile, SwiGLU epilogue
 };
 
 struct GemmCall {
@@ -63,6 +67,9 @@ struct GemmCall {
   void* out;
   long long ldo;
   unsigned int* status;
+  float2* part;          // GV_LSE only
+  const int* target;     // GV_LSE only
+  float* tgt_logit;      // GV_LSE only
 };
 
 int gemm_run(const GemmCall& c, cudaStream_t st);
@@ -74,9 +81,9 @@ int route_launch(const float* logits, int T, int E, int k, int H, const void* x,
 // ---------------------------------------------------------------- combine / head
 int combine_launch(const float* y, const float* topk_w, const int32_t* slot_row, const float* y_shared,
                    int T, int H, int k, float* out, void* out_bf16, cudaStream_t st);
-int lse_launch(const float* logits, const int32_t* target, const float* rollout_logp, int T, int V,
-               float beta, float2* partials, float* logp, float* lse, float* k3, uint8_t* mask,
-               cudaStream_t st);
+int lse_merge_launch(const float2* partials, const float* tgt_logit, const int32_t* target,
+                     const float* rollout_logp, int T, int V, float beta, float* logp, float* lse, float* k3,
+                     uint8_t* mask, cudaStream_t st);
 int timeout_probe_launch(unsigned int* status, unsigned long long limit_ns, cudaStream_t st);
 
 }  // namespace invmoe

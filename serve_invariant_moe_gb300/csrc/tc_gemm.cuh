@@ -42,7 +42,7 @@ namespace invmoe {
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 
-enum Epilogue : int { EPI_F32 = 0, EPI_SWIGLU = 1 };
+enum Epilogue : int { EPI_F32 = 0, EPI_SWIGLU = 1, EPI_LSE = 2 };
 
 struct GemmParams {
   int K;                  // reduction length (multiple of 64)
@@ -60,6 +60,11 @@ struct GemmParams {
   unsigned int* status;   // status word (bit 0: a bounded wait ran out)
   int* sched;             // unit counter for the dynamic schedule (zero before launch)
   unsigned long long timeout_ns;
+  // EPI_LSE only: per (row, column block) log-sum-exp partials and the target logit
+  float2* part;           // [rows, nch] (max, sum exp(z - max)) of each 256-column chunk
+  int nch;                // column blocks = ceil(N / 256)
+  const int* target;      // [rows] target column of each row
+  float* tgt_logit;       // [rows] z[row, target[row]] (written by the block holding it)
 };
 
 template <int BN, int MT, int EPI, int STAGES>
@@ -82,6 +87,7 @@ struct GemmShape {
   static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + BAR_BYTES + MISC_BYTES +
                                     4 * (MAX_GROUPS + 1);
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+  static_assert(EPI != EPI_LSE || (MT == 2 && BN == 256), "LSE epilogue: one tile per warp half, 256-column chunks");
   static_assert(TMEM_NEED <= 512, "TMEM");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
@@ -353,7 +359,62 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
         const long long row = static_cast<long long>(U.row0) + row_local;
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                static_cast<uint32_t>(acc * S::ACC_COLS + t * BN);
-        if (EPI == EPI_F32) {
+        if (EPI == EPI_LSE) {
+          // Two warps share each TMEM lane quadrant: warp half h takes tile t == h,
+          // so every thread owns one full 256-column row of its tile.
+          if (t != half) continue;
+          const int n0 = U.nb * BN;
+          float* orow = p.out != nullptr ? static_cast<float*>(p.out) + row * p.ldo + n0 : nullptr;
+          const int tg = valid ? __ldg(p.target + row) - n0 : -1;   // target column inside this block
+          // max over the chunk (exact in any order), eight running maxima for ILP
+          float mx[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+          float tv = 0.0f;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tbase + c * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float z = __uint_as_float(v[j]);
+              if (n0 + c * 32 + j < p.N) mx[j & 7] = fmaxf(mx[j & 7], z);
+              if (tg == c * 32 + j) tv = z;
+            }
+            if (valid && orow != nullptr) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                if (n0 + c * 32 + j * 4 < p.N)
+                  *reinterpret_cast<float4*>(orow + c * 32 + j * 4) =
+                      make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+              }
+            }
+          }
+          const float m = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+          // s = sum of exp(z - m) over the chunk: column j of the chunk goes to
+          // accumulator j mod 8 in ascending j; then ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7))
+          float acc8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc8[i] = 0.0f;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tbase + c * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (n0 + c * 32 + j < p.N) acc8[j & 7] = __fadd_rn(acc8[j & 7], expf(__uint_as_float(v[j]) - m));
+          }
+          const float sum = __fadd_rn(__fadd_rn(__fadd_rn(acc8[0], acc8[1]), __fadd_rn(acc8[2], acc8[3])),
+                                      __fadd_rn(__fadd_rn(acc8[4], acc8[5]), __fadd_rn(acc8[6], acc8[7])));
+          if (valid) {
+            p.part[row * p.nch + U.nb] = make_float2(m, sum);
+            if (tg >= 0 && tg < BN && n0 + tg < p.N) p.tgt_logit[row] = tv;
+          }
+        } else if (EPI == EPI_F32) {
           const int n0 = U.nb * BN;
           float* orow = static_cast<float*>(p.out) + row * p.ldo + n0;
 #pragma unroll 1

@@ -64,3 +64,19 @@ def test_identical_b_rows_give_identical_columns(ws):
     b[1::2] = b[0::2]
     d = binding.gemm_bf16(a, b.cuda(), ws, variant=3).cpu()
     assert torch.equal(d[:, 0::2], d[:, 1::2])
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 64), (256, 256, 64), (300, 520, 192), (777, 1028, 512), (1000, 64, 256)])
+def test_pair_tile_matches_oracle_and_single_cta_bits(ws, M, N, K):
+    """The CTA-pair (cta_group::2) 256 x 256 tile: within the fp32 bound of the oracle
+    and bit-identical to the single-CTA 128 x 256 tile."""
+    from serve_invariant_moe_gb300 import binding
+    a = _rand((M, K), 3 + M + K)
+    b = _rand((N, K), 4 + N + K, 0.05)
+    d = binding.gemm_bf16(a.cuda(), b.cuda(), ws, variant=4)
+    d1 = binding.gemm_bf16(a.cuda(), b.cuda(), ws, variant=1)
+    binding.check_status(ws)
+    a64, b64 = f64(a), f64(b)
+    err = np.abs(d.double().cpu().numpy() - omoe.router_logits(a64, b64))
+    assert (err <= dot_bound(a64, b64, K)).all()
+    assert torch.equal(d, d1)

@@ -21,7 +21,7 @@ def _build():
 def _run(hidden, wv, target, rollout=None, beta=2.0):
     from serve_invariant_moe_gb300 import api
     r = api.head_logprob_kl(hidden.cuda(), wv.cuda(), target.cuda(),
-                            None if rollout is None else rollout.cuda(), beta)
+                            None if rollout is None else rollout.cuda(), beta, write_logits=True)
     torch.cuda.synchronize()
     return r
 
@@ -76,6 +76,23 @@ def test_identical_logprobs_give_zero_k3_and_keep_all():
     assert torch.all(r2["k3"] == 0) and torch.all(r2["mask"] == 1)
 
 
+def test_logits_buffer_is_optional_and_changes_nothing():
+    T, H, V = 77, 256, 3000
+    g = torch.Generator().manual_seed(5)
+    hidden = torch.randn((T, H), generator=g).to(torch.bfloat16).cuda()
+    wv = (torch.randn((V, H), generator=g) * 0.02).to(torch.bfloat16).cuda()
+    target = torch.randint(0, V, (T,), generator=g, dtype=torch.int32).cuda()
+    from serve_invariant_moe_gb300 import api
+    a = api.head_logprob_kl(hidden, wv, target)
+    b = api.head_logprob_kl(hidden, wv, target, write_logits=True)
+    torch.cuda.synchronize()
+    assert a["logits"] is None
+    assert torch.equal(a["logp"], b["logp"]) and torch.equal(a["lse"], b["lse"])
+    # the target logit the epilogue captured is the stored logit
+    zt = b["logits"].gather(1, target.long()[:, None])[:, 0]
+    assert torch.equal(b["logp"], zt - b["lse"])
+
+
 def test_target_out_of_range_gives_nan():
     T, H, V = 4, 128, 512
     hidden = torch.randn((T, H)).to(torch.bfloat16)
@@ -105,7 +122,7 @@ def test_full_size_head_sampled_tokens():
     # rollout: the oracle's logprob + N(0, 0.05) on the sampled tokens, -log V + noise elsewhere
     rollout = torch.full((cfg.T,), -math.log(cfg.V)) + noise * cfg.noise_std
     rollout[sample] = torch.from_numpy(logp_ref).float() + noise[sample] * cfg.noise_std
-    r = api.head_logprob_kl(hidden.cuda(), wv, target.cuda(), rollout.cuda(), 2.0)
+    r = api.head_logprob_kl(hidden.cuda(), wv, target.cuda(), rollout.cuda(), 2.0, write_logits=True)
     torch.cuda.synchronize()
     z = r["logits"][sample].double().cpu().numpy()
     assert (np.abs(z - z_ref) <= bound).all()
