@@ -438,7 +438,8 @@ def run_profile_case(args):
     """A small launch of one hot kernel for an ncu capture (inputs > L2, a few GB on the device).
 
     lm_head:  vocab-projection GEMM + LSE at T=2048, H=6144, V=32768 (Wv 403 MB, logits 268 MB).
-    experts:  the grouped expert GEMMs at T=2048, H=6144, E=32, k=8, F=2048 (weights 2.4 GB).
+    experts:  the grouped expert GEMMs at T=1024, H=6144, E=32, k=8, F=2048 + shared (weights 2.4 GB);
+              256 token-slots per expert on average, as in the T=8192, E=256 layer.
     """
     import torch
     from serve_invariant_moe_gb300 import api, binding, build, synth
@@ -454,7 +455,7 @@ def run_profile_case(args):
         binding.check_status(ws)
     else:
         import dataclasses
-        mc = dataclasses.replace(synth.GLM_MOE, T=2048, E=32)
+        mc = dataclasses.replace(synth.GLM_MOE, T=1024, E=32)
         x, wr = synth.moe_activations(mc)
         w13, w2 = synth.expert_weights(mc, dev)
         ws13, ws2 = synth.shared_expert_weights(mc, dev)

@@ -225,14 +225,14 @@ int moe_grouped_ffn(const void* xp, const int32_t* plan, const void* w13, const 
     void* hs = scratch(workspace);
     GemmCall s1{};
     s1.name = "shared_gemm1_swiglu";
-    s1.variant = GV_SWIGLU_BN256_MT2;
+    s1.variant = GV_PAIR_SWIGLU;
     s1.A = x_shared; s1.a_rows = T; s1.B = ws13; s1.b_rows = 2LL * F_shared; s1.K = H;
     s1.N = F_shared; s1.M = T; s1.G = 0; s1.b_group_rows = 0; s1.b_up_rows = F_shared;
     s1.out = hs; s1.ldo = F_shared; s1.status = status;
     if ((rc = gemm_run(s1, st))) return rc;
     GemmCall s2{};
     s2.name = "shared_gemm2";
-    s2.variant = GV_F32_BN256_MT2;
+    s2.variant = GV_PAIR_F32;
     s2.A = hs; s2.a_rows = T; s2.B = ws2; s2.b_rows = H; s2.K = F_shared;
     s2.N = H; s2.M = T; s2.G = 0;
     s2.out = y_shared; s2.ldo = H; s2.status = status;
@@ -272,7 +272,7 @@ int lm_logprob_kl(const void* hidden, const void* w_vocab, const int32_t* target
   float* tgt_logit = reinterpret_cast<float*>(scratch(workspace) + head_part_bytes(T, V));
   GemmCall g{};
   g.name = "lm_head_gemm_lse";
-  g.variant = GV_LSE_BN256_MT2;
+  g.variant = GV_PAIR_LSE;
   g.A = hidden; g.a_rows = T; g.B = w_vocab; g.b_rows = V; g.K = H; g.N = V; g.M = T; g.G = 0;
   g.n_major = 1; g.out = logits; g.ldo = V; g.status = status_word(workspace);
   g.part = part; g.target = target; g.tgt_logit = tgt_logit;

@@ -52,7 +52,7 @@ int launch(const GemmCall& c, cudaStream_t st) {
   CUtensorMap ta, tb;
   int rc = make_tmap(&ta, c.A, c.K, c.a_rows, kBM);
   if (rc) return rc;
-  rc = make_tmap(&tb, c.B, c.K, c.b_rows, EPI == EPI_SWIGLU ? BN / 2 : BN);
+  rc = make_tmap(&tb, c.B, c.K, c.b_rows, BN >= 128 ? 128 : BN);
   if (rc) return rc;
 
   int dev = 0;
@@ -166,6 +166,7 @@ int launch_pair(const GemmCall& c, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if ((rc = check_cuda(cudaMemsetAsync(p.sched, 0, sizeof(int), st), "cudaMemsetAsync"))) return rc;
   ProfScope prof(c.name ? c.name : "tc_gemm_pair", st);
   rc = check_cuda(cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<EPI, STAGES>, ta, tb, p), "cudaLaunchKernelEx");
   if (rc) return rc;

@@ -44,16 +44,28 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// One potentially-suspending probe of the phase with parity `parity`.
+// One potentially-suspending probe of the phase with parity `parity`.  With
+// CLUSTER the acquire is cluster-scoped (arrivals released by the peer CTA).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(200000u)  // suspend hint: 200 us
-      : "memory");
+  if (CLUSTER) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(200000u)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(200000u)  // suspend hint: 200 us
+        : "memory");
+  }
   return done != 0;
 }
 
@@ -66,11 +78,12 @@ struct WaitCtl {
 // Bounded wait for the phase with parity `parity` of `bar`.  Returns false if
 // the limit ran out (status recorded, abort flag raised) or if another role of
 // the CTA raised the abort flag.
+template <bool CLUSTER = false>
 static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WaitCtl w) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it < (1u << 28); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     if (w.abort != nullptr && *w.abort) return false;
     if (global_timer_ns() - t0 > w.limit_ns) break;
   }

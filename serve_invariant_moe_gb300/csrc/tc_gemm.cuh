@@ -99,30 +99,38 @@ struct Unit {
   int nb;      // column block
 };
 
+// Unit order.  Grouped: group by group; inside a group column-block-major, so
+// all row chunks of one (group, column block) are consecutive units and share
+// the weight tile while it is in L2.  Dense: row-chunk-major, or column-block-
+// major when n_major (consecutive units then share a weight tile).
 template <int MT, int EPI, int BN>
 __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& p, const int* s_prefix, int total_chunks) {
-  int chunk, nb;
-  if (p.n_major) {
-    nb = u / total_chunks;
-    chunk = u - nb * total_chunks;
-  } else {
-    chunk = u / p.n_blocks;
-    nb = u - chunk * p.n_blocks;
-  }
   constexpr int CH = MT * kBM;
   Unit U;
-  int g = 0;
+  int g = 0, nb;
   if (p.G > 0) {
-    int lo = 0, hi = p.G;  // s_prefix[lo] <= chunk < s_prefix[hi]
+    const int NB = p.n_blocks;
+    int lo = 0, hi = p.G;  // NB*s_prefix[lo] <= u < NB*s_prefix[hi]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (s_prefix[mid] <= chunk) lo = mid; else hi = mid;
+      if (NB * s_prefix[mid] <= u) lo = mid; else hi = mid;
     }
     g = lo;
-    const int local = chunk - s_prefix[g];
-    U.row0 = __ldg(p.offsets + g) + local * CH;
-    U.rows = min(CH, __ldg(p.counts + g) - local * CH);
+    const int nch = s_prefix[g + 1] - s_prefix[g];
+    const int local = u - NB * s_prefix[g];
+    nb = local / nch;
+    const int c = local - nb * nch;
+    U.row0 = __ldg(p.offsets + g) + c * CH;
+    U.rows = min(CH, __ldg(p.counts + g) - c * CH);
   } else {
+    int chunk;
+    if (p.n_major) {
+      nb = u / total_chunks;
+      chunk = u - nb * total_chunks;
+    } else {
+      chunk = u / p.n_blocks;
+      nb = u - chunk * p.n_blocks;
+    }
     U.row0 = chunk * CH;
     U.rows = min(CH, p.M - U.row0);
   }
@@ -246,9 +254,12 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
       int filled_phase[STAGES];
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) filled_phase[s] = -1;
+      // the next unit index is fetched one unit ahead so the atomic's latency hides
+      // behind the current unit's loads
+      int next = atomicAdd(p.sched, 1);
       while (true) {
-        int u = atomicAdd(p.sched, 1);
-        if (u >= total_units) u = -1;
+        int u = next < total_units ? next : -1;
+        if (u >= 0) next = atomicAdd(p.sched, 1);
         if (!mbar_wait(&qempty_bar[qi], qphase ^ 1u, wc)) break;
         s_queue[qi] = u;
         mbar_arrive(&qfull_bar[qi]);
@@ -258,16 +269,26 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
         const int ntile = (U.rows + kBM - 1) / kBM;
         const uint32_t bytes = ntile * S::A_BYTES + S::B_BYTES;
         bool ok = true;
+        // B row blocks of 128 this unit streams (SwiGLU: gate block, up block)
+        constexpr int NBB = BN >= 128 ? BN / 128 : 1;
+        int brow[NBB];
+        if (EPI == EPI_SWIGLU) {
+          brow[0] = U.b_row;
+          brow[NBB - 1] = U.b_row + p.b_up_rows;
+        } else {
+#pragma unroll
+          for (int i = 0; i < NBB; ++i) brow[i] = U.b_row + i * 128;
+        }
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wc)) { ok = false; break; }
           uint8_t* st = ring + stage * S::STAGE_BYTES;
           mbar_arrive_expect_tx(&full_bar[stage], bytes);
           for (int t = 0; t < ntile; ++t)
             tma_load_2d(st + t * S::A_BYTES, &tmA, &full_bar[stage], kb * kBK, U.row0 + t * kBM);
-          if (EPI == EPI_SWIGLU) {
-            tma_load_2d(st + MT * S::A_BYTES, &tmB, &full_bar[stage], kb * kBK, U.b_row);
-            tma_load_2d(st + MT * S::A_BYTES + S::B_BYTES / 2, &tmB, &full_bar[stage], kb * kBK,
-                        U.b_row + p.b_up_rows);
+          if (BN >= 128) {
+#pragma unroll
+            for (int i = 0; i < NBB; ++i)
+              tma_load_2d(st + MT * S::A_BYTES + i * (kBM * kBK * 2), &tmB, &full_bar[stage], kb * kBK, brow[i]);
           } else {
             tma_load_2d(st + MT * S::A_BYTES, &tmB, &full_bar[stage], kb * kBK, U.b_row);
           }

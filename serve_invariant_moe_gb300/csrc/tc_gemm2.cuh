@@ -38,9 +38,10 @@ struct PairShape {
   static constexpr int EPI_WARPS = 8;
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
   static constexpr int THREADS = 64 + EPI_THREADS;
+  static constexpr int QDEPTH = 4;              // scheduled-unit queue depth
   static constexpr int MAX_GROUPS = 1024;
-  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * ACC_STAGES + 1);
-  static constexpr int MISC_BYTES = 16;
+  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * ACC_STAGES + 1 + 2 * QDEPTH);
+  static constexpr int MISC_BYTES = 16 + 4 * QDEPTH;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + MISC_BYTES + 4 * (MAX_GROUPS + 1);
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
@@ -59,18 +60,19 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
   uint64_t* accf_bar = empty_bar + STAGES;
   uint64_t* acce_bar = accf_bar + S::ACC_STAGES;
   uint64_t* final_bar = acce_bar + S::ACC_STAGES;
-  uint32_t* misc = reinterpret_cast<uint32_t*>(final_bar + 1);
+  uint64_t* qfull_bar = final_bar + 1;
+  uint64_t* qempty_bar = qfull_bar + S::QDEPTH;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(qempty_bar + S::QDEPTH);
   uint32_t* tmem_slot = misc;
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 1);
   int* s_total = reinterpret_cast<int*>(misc + 2);
-  int* s_prefix = reinterpret_cast<int*>(misc + 4);  // [G+1]
+  volatile int* s_queue = reinterpret_cast<volatile int*>(misc + 4);    // [QDEPTH]
+  int* s_prefix = reinterpret_cast<int*>(misc + 4 + S::QDEPTH);         // [G+1]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();          // 0 = leader (issues the MMAs), 1 = follower
   const uint32_t peer = rank ^ 1u;
-  const int pair = blockIdx.x >> 1;
-  const int npairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -82,6 +84,12 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
       mbar_init(&acce_bar[a], 2 * S::EPI_THREADS);
     }
     mbar_init(final_bar, 1);
+    for (int qq = 0; qq < S::QDEPTH; ++qq) {
+      mbar_init(&qfull_bar[qq], 1);
+      // consumers of a queue slot: per CTA its epilogue threads, plus the
+      // leader's MMA thread and the follower's producer thread
+      mbar_init(&qempty_bar[qq], 2 + 2 * S::EPI_THREADS);
+    }
     *s_abort = 0;
     fence_barrier_init();
   }
@@ -133,6 +141,10 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
   const int num_kb = p.K / kBK;
   WaitCtl wc{s_abort, p.status, p.timeout_ns};
   const uint32_t peer_abort = mapa_shared(smem_u32(const_cast<int*>(s_abort)), peer);
+  const uint32_t qempty_leader0 = mapa_shared(smem_u32(&qempty_bar[0]), 0);
+  // Units are handed out dynamically by the leader's producer: it takes the next
+  // index from a global counter and publishes it into both CTAs' queues.  Every
+  // consumer releases a slot on the leader's qempty barrier.
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
@@ -143,7 +155,28 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) filled_phase[s] = -1;
       bool ok = true;
-      for (int u = pair; ok && u < total_units; u += npairs) {
+      int qi = 0;
+      uint32_t qphase = 0;
+      const uint32_t q_peer0 = mapa_shared(smem_u32(const_cast<int*>(s_queue)), peer);
+      const uint32_t qfull_peer0 = mapa_shared(smem_u32(&qfull_bar[0]), peer);
+      int next = rank == 0 ? atomicAdd(p.sched, 1) : 0;
+      while (ok) {
+        int u;
+        if (rank == 0) {
+          u = next < total_units ? next : -1;
+          if (u >= 0) next = atomicAdd(p.sched, 1);
+          if (!mbar_wait<true>(&qempty_bar[qi], qphase ^ 1u, wc)) { ok = false; break; }
+          s_queue[qi] = u;
+          mbar_arrive(&qfull_bar[qi]);
+          st_shared_remote_u32(q_peer0 + 4u * qi, static_cast<uint32_t>(u));
+          mbar_arrive_remote(qfull_peer0 + 8u * qi);
+        } else {
+          if (!mbar_wait<true>(&qfull_bar[qi], qphase, wc)) { ok = false; break; }
+          u = s_queue[qi];
+          mbar_arrive_remote(qempty_leader0 + 8u * qi);
+        }
+        if (++qi == S::QDEPTH) { qi = 0; qphase ^= 1u; }
+        if (u < 0) break;
         const Unit U = decode_unit<2, EPI, BN>(u, p, s_prefix, total_chunks);
         const int a_row = U.row0 + static_cast<int>(rank) * kBM;
         const int b_row = (EPI == EPI_SWIGLU) ? U.b_row + static_cast<int>(rank) * p.b_up_rows
@@ -176,8 +209,15 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int u = pair; ok && u < total_units; u += npairs) {
-        if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1u, wc)) { ok = false; break; }
+      int qi = 0;
+      uint32_t qphase = 0;
+      while (ok) {
+        if (!mbar_wait(&qfull_bar[qi], qphase, wc)) { ok = false; break; }
+        const int u = s_queue[qi];
+        mbar_arrive(&qempty_bar[qi]);
+        if (++qi == S::QDEPTH) { qi = 0; qphase ^= 1u; }
+        if (u < 0) break;
+        if (!mbar_wait<true>(&acce_bar[acc], acc_phase ^ 1u, wc)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * S::ACC_COLS);
         for (int kb = 0; kb < num_kb; ++kb) {
@@ -210,7 +250,15 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
     const uint32_t acce_leader0 = mapa_shared(smem_u32(&acce_bar[0]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = pair; u < total_units; u += npairs) {
+    int qi = 0;
+    uint32_t qphase = 0;
+    while (true) {
+      const bool okq = mbar_wait<true>(&qfull_bar[qi], qphase, wc);
+      if (!__all_sync(0xffffffffu, okq)) break;
+      const int u = s_queue[qi];
+      mbar_arrive_remote(qempty_leader0 + 8u * qi);
+      if (++qi == S::QDEPTH) { qi = 0; qphase ^= 1u; }
+      if (u < 0) break;
       const Unit U = decode_unit<2, EPI, BN>(u, p, s_prefix, total_chunks);
       const bool ok = mbar_wait(&accf_bar[acc], acc_phase, wc);
       if (!__all_sync(0xffffffffu, ok)) break;
