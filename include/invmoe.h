@@ -173,6 +173,33 @@ int lm_logprob_kl(const void* hidden, const void* w_vocab, const int32_t* target
                   void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_route_topk_noalloc -- moe_route_topk for callers that cannot allocate
+ *
+ * The source pages have no counterpart of this call; it exists for callers that
+ * may not allocate device memory where they route tokens (a serving loop under a
+ * fixed memory budget, where cudaMalloc could fail or stall the device, or a
+ * plain-C host that only holds the buffers it was given).  It computes exactly
+ * what moe_route_topk computes, with the same kernels, but takes no workspace:
+ * its scratch (status word, schedule counter, per-chunk expert counts) is one
+ * fixed array of 1 MiB + 256 bytes inside the library, held by every GPU that
+ * loads the library until the process exits.
+ *   - Limit: ceil(T/64) * E <= 262144 (for example T <= 65536 at E = 256);
+ *     larger sizes return INVMOE_ERR_UNSUPPORTED_SHAPE and launch nothing.
+ *   - No cudaMalloc, cudaFree or other allocating call is made.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents (the status word is cleared at the start of every call): calls
+ *     that overlap on the GPU (other streams, other host threads) race.
+ *   - status (nullable, 4-byte aligned device pointer, caller-owned): receives
+ *     the call's status word (non-zero = a bounded device wait ran out).
+ * Other arguments, layouts and errors: as moe_route_topk.
+ * ------------------------------------------------------------------------- */
+int moe_route_topk_noalloc(const void* x, const void* w_router, int T, int H, int E, int k,
+                           float* logits, int32_t* topk_idx, float* topk_w, int32_t* plan,
+                           void* xp, unsigned int* status, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Diagnostics
  * ------------------------------------------------------------------------- */
 

@@ -22,6 +22,7 @@ PROTOTYPES = {
     "invmoe_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
     "invmoe_check": (_i, [_vp, _vp]),
     "moe_route_topk": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_route_topk_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_grouped_ffn": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp,
                              _vp, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
     "moe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp]),
