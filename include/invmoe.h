@@ -92,7 +92,8 @@ int invmoe_check(void* workspace, void* stream);
  * moe_route_topk -- router logits, top-k with lowest-index ties, gates, dispatch
  *
  *   logits[t, e] = sum_h x[t, h] * w_router[e, h]           (fp32 accumulate,
- *                  tcgen05 tile 128 x BN x 64, K ascending, no split-K)
+ *                  tcgen05 tile 128 x BN x 64 with BN = 64 for E <= 64, else 128;
+ *                  K ascending, no split-K)
  *   topk_idx[t, 0..k-1]: the k largest logits of row t, largest first; exact
  *                  ties (and -0 vs +0) go to the lower expert index; NaN ranks
  *                  below -inf.
@@ -153,8 +154,10 @@ int moe_combine(const float* y, const float* topk_w, const int32_t* plan, const 
  *   pass 1, in the projection's epilogue, chunk c = columns [256c, 256c+256):
  *           m_c = max z;  s_c = sum of exp(z - m_c): column j of the chunk is added,
  *           in ascending j, to accumulator j mod 8, then s_c = ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7))
- *   pass 2, c = 0, 1, 2, ... in order:  M' = max(M, m_c);
- *           S = S*exp(M - M') + s_c*exp(m_c - M');  lse = M + log(S)
+ *   pass 2, partials folded as (M, S) + (m, s) = (M', S*exp(M - M') + s*exp(m - M')),
+ *           M' = max(M, m), in a fixed order: lane l of a warp folds chunks
+ *           [l*P, (l+1)*P), P = ceil(V/256/32), in ascending order, then the 32 lane
+ *           results fold by a xor butterfly (16, 8, 4, 2, 1);  lse = M + log(S)
  *   logp[t] = z[t, target[t]] - lse[t]
  *   if rollout_logp != NULL:
  *     d = logp - rollout_logp;  k3 = expm1(d) - d;  rho = exp(d);

@@ -168,7 +168,8 @@ int moe_route_topk(const void* x, const void* w_router, int T, int H, int E, int
 
   GemmCall g{};
   g.name = "router_gemm";
-  g.variant = E <= 64 ? GV_F32_BN64_MT1 : (E <= 128 ? GV_F32_BN128_MT1 : GV_F32_BN256_MT1);
+  // narrow tiles so that even E = 256 spreads over twice as many SMs as a 256-wide tile
+  g.variant = E <= 64 ? GV_F32_BN64_MT1 : GV_F32_BN128_MT1;
   g.A = x; g.a_rows = T; g.B = w_router; g.b_rows = E; g.K = H; g.N = E; g.M = T; g.G = 0;
   g.out = logits; g.ldo = E; g.status = status_word(workspace);
   // the fp32 epilogue stores 4 columns at a time; E % 4 != 0 would need a scalar tail
@@ -274,7 +275,9 @@ int lm_logprob_kl(const void* hidden, const void* w_vocab, const int32_t* target
   g.name = "lm_head_gemm_lse";
   g.variant = GV_PAIR_LSE;
   g.A = hidden; g.a_rows = T; g.B = w_vocab; g.b_rows = V; g.K = H; g.N = V; g.M = T; g.G = 0;
-  g.n_major = 1; g.out = logits; g.ldo = V; g.status = status_word(workspace);
+  // column-block-major in bands of 16 row chunks (4096 tokens, 50 MB of hidden
+  // states at H = 6144): the band stays in L2 while every vocabulary tile streams past
+  g.n_major = 1; g.m_group = 16; g.out = logits; g.ldo = V; g.status = status_word(workspace);
   g.part = part; g.target = target; g.tgt_logit = tgt_logit;
   int rc = gemm_run(g, st);
   if (rc) return rc;

@@ -52,30 +52,54 @@ __global__ void combine_kernel(const float4* __restrict__ y, const float* __rest
 // Pass 2 of the chunked log-sum-exp ("GLM Post-Training Beyond SFT", section
 // "动作与概率契约": logsumexp needs comparison tests; the chunking fixes its
 // order).  Pass 1 runs in the vocabulary-projection epilogue: for the 256-column
-// chunk c of row t, m_c = max z and s_c = sum of exp(z - m_c) over the chunk's
-// columns in a fixed eight-accumulator order.  Here one thread per token merges the partials in
-// ascending chunk order,
-//   M' = max(M, m_c);  S = S*exp(M - M') + s_c*exp(m_c - M');  lse = M + log S,
-// then logp = z[target] - lse and, with rollout logprobs ("GLM Post-Training
-// Beyond SFT", section "IcePop 为什么有两层 ratio"), d = logp - rollout,
-// k3 = expm1(d) - d, rho = exp(d), mask = 1/beta <= rho <= beta.
+// chunk c of row t it gives m_c = max z and s_c = sum of exp(z - m_c).
+// Two partials combine as
+//   (M, S) + (m, s) = (max(M, m), S*exp(M - max) + s*exp(m - max))
+// with the factor for the larger maximum being exactly 1 (so one exp per step);
+// the operation is commutative bit for bit.  Fixed order: one warp per token;
+// lane l folds chunks [l*P, (l+1)*P), P = ceil(NCH / 32), in ascending order;
+// the 32 lane results are then folded by a xor butterfly over lane distances
+// 16, 8, 4, 2, 1.  The order depends only on V, never on the batch.
+// Then lse = M + log S, logp = z[target] - lse and, with rollout logprobs
+// ("GLM Post-Training Beyond SFT", section "IcePop 为什么有两层 ratio"),
+// d = logp - rollout, k3 = expm1(d) - d, rho = exp(d), mask = 1/beta <= rho <= beta.
+__device__ __forceinline__ void lse_fold(float& M, float& S, float m, float s) {
+  if (m == -INFINITY) return;
+  if (M == -INFINITY) {
+    M = m;
+    S = s;
+  } else if (m > M) {
+    S = __fadd_rn(__fmul_rn(S, expf(M - m)), s);
+    M = m;
+  } else {
+    S = __fadd_rn(S, __fmul_rn(s, expf(m - M)));
+  }
+}
+
+constexpr int kMergeWarps = 4;
+
 __global__ void lse_merge_kernel(const float2* __restrict__ part, const float* __restrict__ tgt_logit,
                                  const int32_t* __restrict__ target, const float* __restrict__ rollout, int T, int V,
                                  int NCH, float beta, float* __restrict__ logp, float* __restrict__ lse,
                                  float* __restrict__ k3, uint8_t* __restrict__ mask) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   if (t >= T) return;
   const float2* pt = part + static_cast<long long>(t) * NCH;
+  const int P = (NCH + 31) / 32;
+  const int c1 = min(NCH, (lane + 1) * P);
   float M = -INFINITY, S = 0.0f;
-  for (int c = 0; c < NCH; ++c) {
+  for (int c = lane * P; c < c1; ++c) {
     const float2 ms = pt[c];
-    if (ms.x > M) {
-      S = __fadd_rn(__fmul_rn(S, expf(M - ms.x)), ms.y);
-      M = ms.x;
-    } else if (ms.x != -INFINITY) {
-      S = __fadd_rn(S, __fmul_rn(ms.y, expf(ms.x - M)));
-    }
+    lse_fold(M, S, ms.x, ms.y);
   }
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) {
+    const float m = __shfl_xor_sync(0xffffffffu, M, d);
+    const float s = __shfl_xor_sync(0xffffffffu, S, d);
+    lse_fold(M, S, m, s);
+  }
+  if (lane != 0) return;
   const float l = __fadd_rn(M, logf(S));
   const int tg = target[t];
   const float lp = (tg >= 0 && tg < V) ? __fsub_rn(tgt_logit[t], l) : __uint_as_float(0x7fc00000u);
@@ -135,8 +159,8 @@ int lse_merge_launch(const float2* partials, const float* tgt_logit, const int32
   const int NCH = (V + kLseChunk - 1) / kLseChunk;
   if (T == 0) return INVMOE_OK;
   ProfScope prof("lse_merge", st);
-  lse_merge_kernel<<<(T + 127) / 128, 128, 0, st>>>(partials, tgt_logit, target, rollout_logp, T, V, NCH, beta,
-                                                   logp, lse, k3, mask);
+  lse_merge_kernel<<<(T + kMergeWarps - 1) / kMergeWarps, 32 * kMergeWarps, 0, st>>>(
+      partials, tgt_logit, target, rollout_logp, T, V, NCH, beta, logp, lse, k3, mask);
   return check_cuda(cudaGetLastError(), "lse_merge_kernel");
 }
 

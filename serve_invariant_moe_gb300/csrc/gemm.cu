@@ -90,6 +90,7 @@ int launch(const GemmCall& c, cudaStream_t st) {
   p.nch = (c.N + 255) / 256;
   p.target = c.target;
   p.tgt_logit = c.tgt_logit;
+  p.m_group = c.m_group > 0 ? c.m_group : (1 << 30);
 
   constexpr long long CH = static_cast<long long>(MT) * kBM;
   long long max_chunks = (c.G > 0) ? (c.a_rows + CH - 1) / CH + c.G : (c.M + CH - 1) / CH;
@@ -123,6 +124,7 @@ GemmParams make_params(const GemmCall& c, int nb_cols) {
   p.nch = (c.N + 255) / 256;
   p.target = c.target;
   p.tgt_logit = c.tgt_logit;
+  p.m_group = c.m_group > 0 ? c.m_group : (1 << 30);
   return p;
 }
 

@@ -70,6 +70,7 @@ struct GemmCall {
   float2* part;          // GV_LSE only
   const int* target;     // GV_LSE only
   float* tgt_logit;      // GV_LSE only
+  int m_group;           // dense column-block-major order: row chunks per band (0 = all)
 };
 
 int gemm_run(const GemmCall& c, cudaStream_t st);

@@ -65,13 +65,15 @@ struct GemmParams {
   int nch;                // column blocks = ceil(N / 256)
   const int* target;      // [rows] target column of each row
   float* tgt_logit;       // [rows] z[row, target[row]] (written by the block holding it)
+  int m_group;            // dense column-block-major order: row chunks per band (>= 1)
 };
 
 template <int BN, int MT, int EPI, int STAGES>
 struct GemmShape {
   static constexpr int A_BYTES = kBM * kBK * 2;                 // 16 KB per 128-row tile
   static constexpr int B_BYTES = BN * kBK * 2;
-  static constexpr int STAGE_BYTES = MT * A_BYTES + B_BYTES;
+  static constexpr int STAGE_BYTES = MT * A_BYTES + B_BYTES;    // one ring stage: A row tiles + B tile
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
   static constexpr int ACC_COLS = MT * BN;                      // fp32 TMEM columns per accumulator
   static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
   static constexpr int TMEM_NEED = ACC_STAGES * ACC_COLS;
@@ -84,7 +86,7 @@ struct GemmShape {
   static constexpr int MAX_GROUPS = 1024;
   static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * ACC_STAGES + 1 + 2 * QDEPTH);
   static constexpr int MISC_BYTES = 16 + 4 * QDEPTH;
-  static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + STAGES * STAGE_BYTES + BAR_BYTES + MISC_BYTES +
+  static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + RING_BYTES + BAR_BYTES + MISC_BYTES +
                                     4 * (MAX_GROUPS + 1);
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(EPI != EPI_LSE || (MT == 2 && BN == 256), "LSE epilogue: one tile per warp half, 256-column chunks");
@@ -125,8 +127,15 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& p, const in
   } else {
     int chunk;
     if (p.n_major) {
-      nb = u / total_chunks;
-      chunk = u - nb * total_chunks;
+      // bands of m_group row chunks; inside a band column-block-major, so the
+      // band's A rows stay in L2 while every B tile streams past them once
+      const int gm = min(max(p.m_group, 1), total_chunks);
+      const int band = u / (gm * p.n_blocks);
+      const int c0 = band * gm;
+      const int gsize = min(gm, total_chunks - c0);
+      const int local = u - band * gm * p.n_blocks;
+      nb = local / gsize;
+      chunk = c0 + (local - nb * gsize);
     } else {
       chunk = u / p.n_blocks;
       nb = u - chunk * p.n_blocks;
@@ -162,7 +171,7 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + S::RING_BYTES);
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* accf_bar = empty_bar + STAGES;
   uint64_t* acce_bar = accf_bar + S::ACC_STAGES;
@@ -191,7 +200,7 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
     mbar_init(final_bar, 1);
     for (int q = 0; q < S::QDEPTH; ++q) {
       mbar_init(&qfull_bar[q], 1);
-      mbar_init(&qempty_bar[q], 1 + S::EPI_THREADS);
+      mbar_init(&qempty_bar[q], 1 + S::EPI_THREADS);   // consumers: MMA thread + epilogue threads
     }
     *s_abort = 0;
     fence_barrier_init();
@@ -288,7 +297,8 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
           if (BN >= 128) {
 #pragma unroll
             for (int i = 0; i < NBB; ++i)
-              tma_load_2d(st + MT * S::A_BYTES + i * (kBM * kBK * 2), &tmB, &full_bar[stage], kb * kBK, brow[i]);
+              tma_load_2d(st + MT * S::A_BYTES + i * (kBM * kBK * 2), &tmB, &full_bar[stage], kb * kBK,
+                               brow[i]);
           } else {
             tma_load_2d(st + MT * S::A_BYTES, &tmB, &full_bar[stage], kb * kBK, U.b_row);
           }
@@ -354,7 +364,8 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;                 // 0 .. EPI_WARPS-1
     const int q = warp & 3;                  // TMEM lane quadrant this warp may access
-    const int half = ew >> 2;                // which half of the column chunks this warp converts
+    constexpr int NPART = S::EPI_WARPS / 4;  // warps sharing one lane quadrant
+    const int half = ew >> 2;                // which of them this warp is (column chunks c = half mod NPART)
     const int r_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -439,7 +450,7 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
           const int n0 = U.nb * BN;
           float* orow = static_cast<float*>(p.out) + row * p.ldo + n0;
 #pragma unroll 1
-          for (int c = half; c < BN / 32; c += 2) {
+          for (int c = half; c < BN / 32; c += NPART) {
             uint32_t v[32];
             tmem_ld32(tbase + c * 32, v);
             tmem_ld_wait();
@@ -460,7 +471,7 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
           const int n0 = U.nb * HALF;
           __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + row * p.ldo + n0;
 #pragma unroll 1
-          for (int c = half; c < HALF / 32; c += 2) {
+          for (int c = half; c < HALF / 32; c += NPART) {
             uint32_t gv[32], uv[32];
             tmem_ld32(tbase + c * 32, gv);
             tmem_ld32(tbase + HALF + c * 32, uv);

@@ -1,0 +1,42 @@
+"""The decode entry point captured into a CUDA graph and replayed: the same bits as
+the eager decode path (no host synchronisation or allocation inside the path)."""
+import dataclasses
+
+import pytest
+import torch
+
+from serve_invariant_moe_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def test_decode_graph_replay_matches_eager():
+    from serve_invariant_moe_gb300 import api, build
+    build.build()
+    cfg = dataclasses.replace(synth.GLM_MOE, name="graph_small", H=512, E=32, k=8, F=256, F_shared=256, seed=41)
+    _, wr = synth.moe_activations(cfg, T=1)
+    w13, w2 = synth.expert_weights(cfg, "cuda")
+    ws13, ws2 = synth.shared_expert_weights(cfg, "cuda")
+    layer = api.MoELayer(api.MoEWeights(wr.cuda(), w13, w2, cfg.k, ws13, ws2))
+    B = 48
+    layer.alloc_decode(B)
+    static_x = torch.zeros((B, cfg.H), dtype=torch.bfloat16, device="cuda")
+    g = torch.Generator().manual_seed(7)
+    batches = [synth.to_bf16(torch.randn((B, cfg.H), generator=g)).cuda() for _ in range(3)]
+    eager = [layer.decode(x).clone() for x in batches]
+    torch.cuda.synchronize()
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        static_x.copy_(batches[0])
+        layer.decode(static_x)                      # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        static_out = layer.decode(static_x)
+    for x, ref in zip(batches, eager):
+        static_x.copy_(x)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(static_out, ref)

@@ -1,0 +1,119 @@
+"""Planted mistakes: each replaces one oracle function with a plausible wrong
+version (on the CPU) and checks that a pin of the oracle tests catches it."""
+import numpy as np
+import pytest
+import scipy.special
+import scipy.stats
+import torch
+
+from oracle import head, moe, numerics
+
+
+def _pin_topk(topk):
+    pool = np.array([-1.0, 0.0, 1.0, np.nan, -np.inf])
+    rng = np.random.default_rng(0)
+    rows = pool[rng.integers(0, len(pool), size=(200, 6))]
+    from test_oracle_moe import _brute_topk
+    got = topk(rows, 3)
+    for t in range(rows.shape[0]):
+        assert list(got[t]) == _brute_topk(rows[t], 3)
+
+
+def _pin_gates(gates_fn):
+    rng = np.random.default_rng(1)
+    L = rng.standard_normal((20, 8))
+    idx = moe.topk_lowest_index(L, 3)
+    sel = np.take_along_axis(L, idx.astype(np.int64), 1)
+    assert np.allclose(gates_fn(L, idx), scipy.special.softmax(sel, axis=1), rtol=1e-13)
+
+
+def _pin_swiglu(expert):
+    H = F = 6
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((4, H)); x[:, H - 1] = 1.0
+    wg = np.eye(F, H); wu = np.zeros((F, H)); wu[:, H - 1] = 1.0
+    perm = np.array([1, 2, 3, 4, 5, 0])
+    y = expert(x, np.concatenate([wg, wu]), np.eye(H)[perm], F)
+    ref = numerics.round_to_bf16(torch.nn.functional.silu(torch.from_numpy(x)).numpy())[:, perm]
+    assert np.array_equal(y, ref)
+
+
+def _pin_k3(k3_fn):
+    rng = np.random.default_rng(3)
+    p = rng.dirichlet(np.ones(30)); q = rng.dirichlet(np.ones(30))
+    assert abs(np.sum(q * k3_fn(np.log(p), np.log(q))) - scipy.stats.entropy(q, p)) < 1e-12
+
+
+def _pin_round(round_fn):
+    x = np.random.default_rng(4).standard_normal(5000).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(round_fn(x.astype(np.float64)), ref)
+
+
+def _pin_lse(lse_fn):
+    z = np.random.default_rng(5).standard_normal((5, 300)) * 30 + 1000.0   # large logits
+    assert np.allclose(lse_fn(z), scipy.special.logsumexp(z, axis=1), rtol=1e-13, atol=1e-12)
+
+
+def test_pins_pass_on_the_real_oracle():
+    _pin_topk(moe.topk_lowest_index)
+    _pin_gates(moe.topk_gates)
+    _pin_swiglu(moe.swiglu_expert)
+    _pin_k3(head.k3)
+    _pin_round(numerics.round_to_bf16)
+    _pin_lse(head.logsumexp_rows)
+
+
+def _topk_high_index_ties(L, k):            # ties to the higher index
+    L = np.asarray(L, np.float64)
+    E = L.shape[1]
+    nan = np.isnan(L)
+    idx = np.broadcast_to(-np.arange(E), L.shape)
+    return np.lexsort((idx, np.where(nan, 0.0, -L), nan), axis=-1)[:, :k].astype(np.int32)
+
+
+def _topk_nan_first(L, k):                  # NaN treated as the largest value
+    L = np.asarray(L, np.float64)
+    return moe.topk_lowest_index(np.where(np.isnan(L), np.inf, L), k)
+
+
+def _gates_not_renormalised(L, idx):        # full softmax, not renormalised over the top-k
+    full = scipy.special.softmax(np.asarray(L, np.float64), axis=1)
+    return np.take_along_axis(full, idx.astype(np.int64), 1)
+
+
+def _swiglu_swapped(x, w13, w2, F, round_h=True):   # gate and up exchanged
+    return moe.swiglu_expert(x, np.concatenate([w13[F:2 * F], w13[:F]]), w2, F, round_h)
+
+
+def _swiglu_down_transposed(x, w13, w2, F, round_h=True):
+    return moe.swiglu_expert(x, w13, np.asarray(w2).T, F, round_h)
+
+
+def _k3_reversed(lt, lr):                  # ratio taken the other way round
+    return head.k3(lr, lt)
+
+
+def _round_truncate(x):                    # truncation instead of round-to-nearest-even
+    x = np.asarray(x, np.float64).astype(np.float32)
+    b = (x.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32)
+    return b.astype(np.float64)
+
+
+def _lse_no_shift(z):                      # forgot the max shift (overflows / underflows)
+    return np.log(np.exp(np.asarray(z, np.float64)).sum(axis=1))
+
+
+@pytest.mark.parametrize("pin, wrong", [
+    (_pin_topk, _topk_high_index_ties),
+    (_pin_topk, _topk_nan_first),
+    (_pin_gates, _gates_not_renormalised),
+    (_pin_swiglu, _swiglu_swapped),
+    (_pin_swiglu, _swiglu_down_transposed),
+    (_pin_k3, _k3_reversed),
+    (_pin_round, _round_truncate),
+    (_pin_lse, _lse_no_shift),
+])
+def test_planted_mistake_is_caught(pin, wrong):
+    with pytest.raises(AssertionError), np.errstate(all="ignore"):
+        pin(wrong)
