@@ -319,6 +319,13 @@ def run_ours(args):
                     frac=pk["frac"], traffic=TRAFFIC_BYTES.get(dom), peak_source=peaks["src"] + " (burst)")
     launches = sum(c for (_, c) in kern.values())
 
+    inv = invariance_check(st, device) if rank == 0 else None
+    moe_names = ["router_gemm", "topk_gate", "dispatch_count", "dispatch_scan", "dispatch_scatter", "gather_rows",
+                 "expert_gemm1_swiglu", "expert_gemm2", "shared_gemm1_swiglu", "shared_gemm2", "combine"]
+    head_names = ["lm_head_gemm_lse", "lse_merge"]
+    moe_ms = sum(kern[n][0] / kern[n][1] for n in moe_names if n in kern)
+    head_ms = sum(kern[n][0] / kern[n][1] for n in head_names if n in kern)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(st, samples=args.cpu_sample_tokens)
@@ -334,6 +341,9 @@ def run_ours(args):
             "e2e": {"value": round(ws * T / (e2e_ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
+            "moe_layer_tokens_per_s": round(T / (moe_ms / 1e3), 1) if moe_ms else None,
+            "head_tokens_per_s": round(T / (head_ms / 1e3), 1) if head_ms else None,
+            "invariance": inv,
             "roofline": roof,
             "kernels": per_kernel,
             "clocks": clk,
@@ -343,6 +353,45 @@ def run_ours(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def invariance_check(st, device):
+    """k3 == 0 evidence on the bench's own layer and head (outside the timed region).
+
+    A fixed 32-token probe request goes through the step twice: inside the
+    8192-token batch (prefill), and one token per call (decode).  Reports how
+    many output values and logprobs differ (must be 0) and the mean k3 that the
+    library's head computes between the two paths (must be exactly 0.0).
+    """
+    import torch
+    from serve_invariant_moe_gb300 import api, synth
+    mc = st.mc
+    probe = synth.probe_tokens(mc).to(device)
+    tgt = st.target[:32].clone()
+    off = 1000
+    x = st.x.clone()
+    x[off:off + 32] = probe
+    tb = st.target.clone()
+    tb[off:off + 32] = tgt
+    res = st.run(x=x, target=tb, rollout=torch.zeros_like(st.rollout))
+    out_a = st.layer._decode["out"][off:off + 32].clone()
+    logp_a = res["logp"][off:off + 32].clone()
+    outs, hid = [], torch.empty((1, mc.H), dtype=torch.bfloat16, device=device)
+    logp_b = torch.empty(32, dtype=torch.float32, device=device)
+    for i in range(32):
+        outs.append(st.layer.decode(probe[i:i + 1], out_bf16=hid).clone())
+        logp_b[i:i + 1] = api.head_logprob_kl(hid, st.wv, tgt[i:i + 1])["logp"]
+    out_b = torch.cat(outs)
+    # k3 and IcePop mask computed by the library between the two paths
+    hid_all = torch.empty((32, mc.H), dtype=torch.bfloat16, device=device)
+    st.layer.decode(probe, out_bf16=hid_all)
+    r = api.head_logprob_kl(hid_all, st.wv, tgt, rollout_logp=logp_b)
+    torch.cuda.synchronize()
+    return {"probe_tokens": 32, "batch_tokens": mc.T,
+            "moe_out_values_differing": int((out_a != out_b).sum().item()),
+            "logp_differing": int((logp_a != logp_b).sum().item()),
+            "k3_mean_prefill_vs_decode": float(r["k3"].double().mean().item()),
+            "icepop_kept": int(r["mask"].sum().item())}
 
 
 # --------------------------------------------------------------------------- oracle (CPU)

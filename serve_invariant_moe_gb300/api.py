@@ -96,8 +96,9 @@ class MoELayer:
             ws=binding.new_workspace(binding.workspace_size(B, w.H, w.E, w.k, w.F, w.F_shared, 0), dev),
         )
 
-    def decode(self, x_tokens: torch.Tensor) -> torch.Tensor:
-        """One token per request: x_tokens [B, H] bf16 -> [B, H] fp32 (a view of the decode buffer)."""
+    def decode(self, x_tokens: torch.Tensor, out_bf16: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """One token per request: x_tokens [B, H] bf16 -> [B, H] fp32 (a view of the decode buffer);
+        out_bf16 [B, H] (optional) receives the bf16 copy the head reads."""
         B = x_tokens.shape[0]
         if self._decode is None or self._decode["B"] < B:
             self.alloc_decode(max(B, 1))
@@ -105,7 +106,7 @@ class MoELayer:
         w = self.w
         bufs = dict(logits=d["logits"][:B], idx=d["idx"][:B], w=d["w"][:B], plan=d["plan"], xp=d["xp"],
                     h=d["h"], y=d["y"], ys=None if d["ys"] is None else d["ys"][:B], out=d["out"][:B])
-        return self._run(x_tokens, d["ws"], bufs)["out"]
+        return self._run(x_tokens, d["ws"], bufs, out_bf16=out_bf16)["out"]
 
 
 def moe_prefill(layer: MoELayer, x: torch.Tensor) -> torch.Tensor:

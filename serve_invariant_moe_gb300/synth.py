@@ -167,17 +167,28 @@ def head_inputs(cfg: HeadConfig, device="cpu", T: int = None, seed_offset: int =
     return hidden, wv, target, noise, noise_wide
 
 
-def probe_and_batch(cfg: MoEConfig, n_other: int, trial: int, probe_len: int = 32):
+def probe_tokens(cfg: MoEConfig, probe_len: int = 32) -> torch.Tensor:
+    """The fixed probe request of the batch-invariance sweep (seed 1234), bf16 [probe_len, H]."""
+    return to_bf16(normal((probe_len, cfg.H), cfg.x_std, _gen(1234)))
+
+
+def probe_and_batch(cfg: MoEConfig, n_other: int, trial: int, probe_len: int = 32, skew: bool = False):
     """Batch-invariance sweep input: a fixed probe request embedded in other traffic.
 
     Returns (x_batch [n_other + probe_len, H] bf16, probe_offset, lengths) where
     the probe's tokens are always the same seeded draw (seed 1234) and the other
     tokens, their request lengths and the probe's offset vary with ``trial``.
+    With ``skew`` the other tokens are perturbed copies of probe tokens, so they
+    route to the probe's experts and push the probe's rows to other positions
+    inside those experts' tiles.
     """
-    gp = _gen(1234)
-    probe = to_bf16(normal((probe_len, cfg.H), cfg.x_std, gp))
-    g = _gen(100003 + trial * 31 + n_other)
-    other = to_bf16(normal((n_other, cfg.H), cfg.x_std, g))
+    probe = probe_tokens(cfg, probe_len)
+    g = _gen(100003 + trial * 31 + n_other + (7 if skew else 0))
+    other = normal((n_other, cfg.H), cfg.x_std, g)
+    if skew and n_other > 0:
+        src = torch.randint(0, probe_len, (n_other,), generator=g)
+        other = probe.float()[src] + 0.05 * other
+    other = to_bf16(other)
     # random request lengths: 1 = a decode token, >1 = a prefill chunk
     lengths = []
     left = n_other

@@ -38,11 +38,13 @@ def _sweep(cfg, sizes, trials):
     n_runs = 0
     for n in sizes:
         for trial in range(trials):
-            x, off, lengths = synth.probe_and_batch(cfg, n, trial)
-            out = layer.prefill(x.cuda())
-            probe = out[off:off + 32]
-            assert torch.equal(probe, ref), f"n_other={n} trial={trial}: {(probe != ref).sum().item()} bits differ"
-            n_runs += 1
+            for skew in (False, True):
+                x, off, lengths = synth.probe_and_batch(cfg, n, trial, skew=skew)
+                out = layer.prefill(x.cuda())
+                probe = out[off:off + 32]
+                assert torch.equal(probe, ref), (
+                    f"n_other={n} trial={trial} skew={skew}: {(probe != ref).sum().item()} values differ")
+                n_runs += 1
     # decode path: the probe's tokens one per request, alongside other decode tokens
     for B in (1, 2, 7, 64):
         g = torch.Generator().manual_seed(B)
@@ -59,9 +61,14 @@ def test_invariance_small_layer():
     assert _sweep(SMALL, [1, 2, 3, 7, 31, 32, 33, 127, 128, 129, 255, 257, 1000], 2) > 0
 
 
+GLM_SIZES = [1, 2, 3, 7, 31, 32, 33, 127, 128, 129, 255, 256, 257, 511, 1000, 2047, 4096]
+
+
 @pytest.mark.slow
 def test_invariance_glm_scale_layer():
-    _sweep(synth.GLM_MOE, [1, 3, 33, 129, 1000, 4096], 2)
+    """The glm-scale layer: 17 batch sizes x 2 trials x (random, skewed) other traffic = 68
+    batches through prefill, plus the probe through decode at several batch sizes."""
+    assert _sweep(synth.GLM_MOE, GLM_SIZES, 2) == len(GLM_SIZES) * 4
 
 
 def test_head_logprob_invariant_and_k3_zero():
