@@ -320,6 +320,7 @@ def run_ours(args):
     launches = sum(c for (_, c) in kern.values())
 
     inv = invariance_check(st, device) if rank == 0 else None
+    nxt = next_rows_timing(st, device) if rank == 0 else None
     moe_names = ["router_gemm", "topk_gate", "dispatch_count", "dispatch_scan", "dispatch_scatter", "gather_rows",
                  "expert_gemm1_swiglu", "expert_gemm2", "shared_gemm1_swiglu", "shared_gemm2", "combine"]
     head_names = ["lm_head_gemm_lse", "lse_merge"]
@@ -344,6 +345,7 @@ def run_ours(args):
             "moe_layer_tokens_per_s": round(T / (moe_ms / 1e3), 1) if moe_ms else None,
             "head_tokens_per_s": round(T / (head_ms / 1e3), 1) if head_ms else None,
             "invariance": inv,
+            "next_rows": nxt,
             "roofline": roof,
             "kernels": per_kernel,
             "clocks": clk,
@@ -392,6 +394,38 @@ def invariance_check(st, device):
             "logp_differing": int((logp_a != logp_b).sum().item()),
             "k3_mean_prefill_vs_decode": float(r["k3"].double().mean().item()),
             "icepop_kept": int(r["mask"].sum().item())}
+
+
+def next_rows_timing(st, device, reps=5):
+    """Device time of the rows beyond the step on the same workload (outside the timed region):
+    router replay of the step's own choices, and the IcePop-masked policy loss + DIS weights."""
+    import torch
+    from serve_invariant_moe_gb300 import binding
+    d = st.layer._decode
+    w = st.layer.w
+    idx = d["idx"].clone()
+    lt = st.rollout.clone()
+    lr = lt + (st.noise.to(device) * 0.5)
+    adv = torch.linspace(-1, 1, lt.numel(), device=device)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    replay_ms = timed(lambda: binding.moe_route_replay(st.x, w.w_router, idx, d["ws"], logits=d["logits"],
+                                                       topk_w=d["w"], plan=d["plan"], xp=d["xp"]))
+    loss_ms = timed(lambda: binding.rl_token_loss(lt, lr, adv))
+    binding.check_status(d["ws"])
+    T = st.mc.T
+    return {"route_replay_ms": round(replay_ms, 4), "route_replay_tokens_per_s": round(T / (replay_ms / 1e3), 1),
+            "rl_token_loss_ms": round(loss_ms, 4), "rl_token_loss_tokens_per_s": round(T / (loss_ms / 1e3), 1)}
 
 
 # --------------------------------------------------------------------------- oracle (CPU)

@@ -85,7 +85,8 @@ size_t invmoe_plan_len(int T, int E, int k);
 size_t invmoe_workspace_size(int T, int H, int E, int k, int F, int F_shared, int V);
 
 /* Synchronise `stream`, read and clear the status word in `workspace`.
- * Returns INVMOE_OK or INVMOE_ERR_DEVICE_TIMEOUT (a kernel gave up waiting). */
+ * Returns INVMOE_OK, INVMOE_ERR_DEVICE_TIMEOUT (a kernel gave up waiting) or
+ * INVMOE_ERR_INVALID_ARG (moe_route_replay was given an invalid expert index). */
 int invmoe_check(void* workspace, void* stream);
 
 /* ---------------------------------------------------------------------------
@@ -110,6 +111,29 @@ int invmoe_check(void* workspace, void* stream);
 int moe_route_topk(const void* x, const void* w_router, int T, int H, int E, int k,
                    float* logits, int32_t* topk_idx, float* topk_w, int32_t* plan,
                    void* xp, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_route_replay -- router replay: given expert choices, fresh gates and dispatch
+ *
+ * "Reinforcement Learning: Why Numerical Alignment and MoE Routing Matter So
+ * Much", sections "MoE 路由会放大这种不匹配" and "Fireworks 保持训练循环一致":
+ * router replay records the experts chosen during rollout and makes the trainer
+ * reuse them; matching the choice is not enough, the outputs' computation and
+ * combine must also match.  This call takes the recorded choices topk_idx
+ * [T, k] int32 (input, not modified) instead of selecting them:
+ *   logits     as moe_route_topk (same router GEMM)
+ *   topk_w[t, j] = exp(l_j - l_max) / sum_i exp(l_i - l_max) over the given
+ *              experts, the sum in slot order -- bit-identical to moe_route_topk's
+ *              gates when the given experts are its own choice
+ *   plan, xp   as moe_route_topk, for the given experts
+ * A token whose list holds an index outside [0, E) or a repeated index is
+ * routed to experts 0..k-1 with NaN gates (nothing is read out of bounds) and
+ * invmoe_check() then reports INVMOE_ERR_INVALID_ARG.
+ * Workspace: invmoe_workspace_size(T, H, E, k, ...) bytes.
+ * ------------------------------------------------------------------------- */
+int moe_route_replay(const void* x, const void* w_router, const int32_t* topk_idx, int T, int H, int E, int k,
+                     float* logits, float* topk_w, int32_t* plan, void* xp,
+                     void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
  * moe_grouped_ffn -- grouped SwiGLU expert GEMMs (+ optional shared expert)
@@ -201,6 +225,27 @@ int lm_logprob_kl(const void* hidden, const void* w_vocab, const int32_t* target
 int moe_route_topk_noalloc(const void* x, const void* w_router, int T, int H, int E, int k,
                            float* logits, int32_t* topk_idx, float* topk_w, int32_t* plan,
                            void* xp, unsigned int* status, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * rl_token_loss -- IcePop-masked clipped policy loss and DIS weights per token
+ *
+ * "GLM Post-Training Beyond SFT", sections "GRPO 在优化什么" (clipped objective
+ * min(r A, clip(r, 1-eps_l, 1+eps_h) A), eps_l = 0.2, eps_h = 0.28),
+ * "IcePop 为什么有两层 ratio" (the trust mask multiplies the token loss) and
+ * "Direct Double-Sided Importance Sampling" (f(r) = r inside (1-eps_l, 1+eps_h),
+ * else 0).  Per token, fp32:
+ *   rho = exp(logp_train - logp_rollout);  r = exp(logp_train - logp_old)
+ *   icepop_mask = 1/beta <= rho <= beta
+ *   loss = icepop_mask ? -min(r*A, clip(r, 1-eps_low, 1+eps_high)*A) : 0
+ *   dis_weight = (1-eps_low < rho < 1+eps_high) ? rho : 0
+ * loss_mean (nullable, [1]) = sum(loss) / T in a fixed order (one block: thread i
+ * adds elements i, i+1024, ... ascending, then xor butterflies inside and across
+ * warps).  logp_old nullable (then r = rho); icepop_mask, dis_weight nullable.
+ * All [T] device arrays; fp32 except icepop_mask (uint8).
+ * ------------------------------------------------------------------------- */
+int rl_token_loss(const float* logp_train, const float* logp_old, const float* logp_rollout,
+                  const float* advantage, int T, float beta, float eps_low, float eps_high,
+                  uint8_t* icepop_mask, float* dis_weight, float* loss, float* loss_mean, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Diagnostics

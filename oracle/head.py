@@ -77,3 +77,36 @@ def head_forward(hidden, w_vocab, target, logp_rollout=None, beta=2.0):
         out["k3"] = k3(logp, logp_rollout)
         out["mask"] = icepop_mask(logp, logp_rollout, beta)
     return out
+
+
+def ppo_icepop_loss(logp_train, logp_old, logp_rollout, advantage, beta=2.0, eps_low=0.2, eps_high=0.28,
+                    dtype=np.float64):
+    """IcePop-masked clipped policy loss per token, and its mean over tokens.
+
+    "GLM Post-Training Beyond SFT", section "GRPO 在优化什么": with the ratio
+    r_t = pi_theta / pi_old the clipped objective is
+    min(r_t A, clip(r_t, 1 - eps_l, 1 + eps_h) A), eps_l = 0.2, eps_h = 0.28
+    (section "IcePop 为什么有两层 ratio"); the same section multiplies the trust
+    mask m_t = 1[1/beta <= rho_t <= beta], rho_t = pi_train / pi_infer, into the
+    token loss, which is the negated objective:
+        loss_t = -m_t * min(r_t A_t, clip(r_t, 1 - eps_l, 1 + eps_h) A_t).
+    The mask decision is taken in ``dtype`` (see icepop_mask).  Returns
+    (loss_t [T] float64, mean loss float64).
+    """
+    lt = np.asarray(logp_train, np.float64)
+    lo = np.asarray(logp_old, np.float64)
+    A = np.asarray(advantage, np.float64)
+    r = np.exp(lt - lo)
+    m = icepop_mask(logp_train, logp_rollout, beta, dtype).astype(np.float64)
+    obj = np.minimum(r * A, np.clip(r, 1.0 - eps_low, 1.0 + eps_high) * A)
+    loss = -m * obj
+    return loss, float(loss.mean()) if loss.size else 0.0
+
+
+def dis_weight(logp_train, logp_rollout, eps_low=0.2, eps_high=0.28):
+    """Direct double-sided importance weight ("GLM Post-Training Beyond SFT",
+    section "Direct Double-Sided Importance Sampling"):
+    r_t = exp(logp_theta - logp_rollout);  f(r_t) = r_t if 1 - eps_l < r_t < 1 + eps_h, else 0
+    (both ends excluded; 0 means the token gives no gradient)."""
+    r = np.exp(np.asarray(logp_train, np.float64) - np.asarray(logp_rollout, np.float64))
+    return np.where((1.0 - eps_low < r) & (r < 1.0 + eps_high), r, 0.0)

@@ -163,17 +163,21 @@ def combine(y_slots: np.ndarray, gates: np.ndarray, y_shared=None) -> np.ndarray
 
 
 def moe_forward(x, w_router, w13, w2, k, F, ws13=None, ws2=None, F_shared=0,
-                round_h=True, expert_weights=None, logits=None):
+                round_h=True, expert_weights=None, logits=None, replay_idx=None):
     """Whole MoE layer, float64: router -> top-k -> gates -> experts -> combine.
 
     ``logits`` may be supplied (for example float32 logits produced elsewhere)
-    to re-run only the selection and what follows on them.
+    to re-run only the selection and what follows on them.  ``replay_idx``
+    [T, k] replaces the selection by recorded expert choices (router replay,
+    "Reinforcement Learning: Why Numerical Alignment and MoE Routing Matter So
+    Much", section "MoE 路由会放大这种不匹配"); the gates are then the softmax
+    of the logits of the given experts.
     Returns a dict with logits, idx, gates, y (per slot), y_shared, out.
     """
     x = np.asarray(x, np.float64)
     if logits is None:
         logits = router_logits(x, w_router)
-    idx = topk_lowest_index(logits, k)
+    idx = topk_lowest_index(logits, k) if replay_idx is None else np.asarray(replay_idx, np.int32)
     gates = topk_gates(logits, idx)
     y = expert_outputs(x, idx, w13, w2, F, round_h, expert_weights)
     ys = None

@@ -23,10 +23,12 @@ PROTOTYPES = {
     "invmoe_check": (_i, [_vp, _vp]),
     "moe_route_topk": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_route_topk_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "moe_route_replay": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_grouped_ffn": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp,
                              _vp, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
     "moe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp]),
     "lm_logprob_kl": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "rl_token_loss": (_i, [_vp, _vp, _vp, _vp, _i, _f, _f, _f, _vp, _vp, _vp, _vp, _vp]),
     "invmoe_gemm_bf16": (_i, [_vp, _vp, _i, _i, _i, _vp, _i, _vp, _sz, _vp]),
     "invmoe_debug_timeout_probe": (_i, [_vp, _sz, _i, _vp]),
     "invmoe_profile_enable": (_i, [_i]),

@@ -59,12 +59,16 @@ class MoELayer:
             self._ws = binding.new_workspace(need, device=w.w13.device)
         return self._ws
 
-    def _run(self, x, ws, bufs=None, out_bf16=None):
+    def _run(self, x, ws, bufs=None, out_bf16=None, replay_idx=None):
         w = self.w
         T = x.shape[0]
         bufs = bufs or {}
-        r = binding.moe_route_topk(x, w.w_router, w.k, ws, logits=bufs.get("logits"), topk_idx=bufs.get("idx"),
-                                   topk_w=bufs.get("w"), plan=bufs.get("plan"), xp=bufs.get("xp"))
+        if replay_idx is None:
+            r = binding.moe_route_topk(x, w.w_router, w.k, ws, logits=bufs.get("logits"), topk_idx=bufs.get("idx"),
+                                       topk_w=bufs.get("w"), plan=bufs.get("plan"), xp=bufs.get("xp"))
+        else:
+            r = binding.moe_route_replay(x, w.w_router, replay_idx, ws, logits=bufs.get("logits"),
+                                         topk_w=bufs.get("w"), plan=bufs.get("plan"), xp=bufs.get("xp"))
         f = binding.moe_grouped_ffn(r["xp"], r["plan"], w.w13, w.w2, T, w.k, ws, h=bufs.get("h"), y=bufs.get("y"),
                                     x_shared=x if w.ws13 is not None else None, ws13=w.ws13, ws2=w.ws2,
                                     y_shared=bufs.get("ys"))
@@ -72,9 +76,11 @@ class MoELayer:
                                   out=bufs.get("out"), out_bf16=out_bf16)
         return dict(out=out, **r, **f)
 
-    def prefill(self, x: torch.Tensor, out_bf16: Optional[torch.Tensor] = None, return_all=False):
-        """x [T, H] bf16 -> out [T, H] fp32 (optionally also a bf16 copy)."""
-        res = self._run(x, self._workspace(x.shape[0]), out_bf16=out_bf16)
+    def prefill(self, x: torch.Tensor, out_bf16: Optional[torch.Tensor] = None, return_all=False,
+                replay_idx: Optional[torch.Tensor] = None):
+        """x [T, H] bf16 -> out [T, H] fp32 (optionally also a bf16 copy).  With replay_idx [T, k]
+        int32 the recorded expert choices are used instead of the router's own top-k."""
+        res = self._run(x, self._workspace(x.shape[0]), out_bf16=out_bf16, replay_idx=replay_idx)
         return res if return_all else res["out"]
 
     def alloc_decode(self, max_batch: int):

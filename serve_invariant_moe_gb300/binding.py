@@ -78,6 +78,31 @@ def moe_route_topk(x, w_router, k, workspace, logits=None, topk_idx=None, topk_w
     return dict(logits=logits, topk_idx=topk_idx, topk_w=topk_w, plan=plan, xp=xp)
 
 
+def moe_route_replay(x, w_router, topk_idx, workspace, logits=None, topk_w=None, plan=None, xp=None):
+    """Router replay: the given experts [T, k] int32, fresh gates, plan and permuted rows."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    k = topk_idx.shape[1]
+    dev = x.device
+    _req(x, torch.bfloat16, "x")
+    _req(w_router, torch.bfloat16, "w_router", (E, H))
+    _req(topk_idx, torch.int32, "topk_idx", (T, k))
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev) if logits is None else logits
+    topk_w = torch.empty((T, k), dtype=torch.float32, device=dev) if topk_w is None else topk_w
+    plan = torch.empty(plan_len(T, E, k), dtype=torch.int32, device=dev) if plan is None else plan
+    xp = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev) if xp is None else xp
+    _req(logits, torch.float32, "logits", (T, E))
+    _req(topk_w, torch.float32, "topk_w", (T, k))
+    _req(plan, torch.int32, "plan")
+    _req(xp, torch.bfloat16, "xp")
+    if plan.numel() < plan_len(T, E, k) or xp.numel() < T * k * H:
+        raise ValueError("plan / xp too small")
+    _req(workspace, torch.uint8, "workspace")
+    check(lib().moe_route_replay(_p(x), _p(w_router), _p(topk_idx), T, H, E, k, _p(logits), _p(topk_w), _p(plan),
+                                 _p(xp), _p(workspace), workspace.numel(), _stream()))
+    return dict(logits=logits, topk_idx=topk_idx, topk_w=topk_w, plan=plan, xp=xp)
+
+
 def moe_grouped_ffn(xp, plan, w13, w2, T, k, workspace, h=None, y=None,
                     x_shared=None, ws13=None, ws2=None, y_shared=None):
     E, F2, H = w13.shape
@@ -149,6 +174,24 @@ def lm_logprob_kl(hidden, w_vocab, target, workspace, rollout_logp=None, beta=2.
                               _p(logits), _p(logp), _p(lse), _p(k3), _p(mask), _p(workspace), workspace.numel(),
                               _stream()))
     return dict(logits=logits, logp=logp, lse=lse, k3=k3, mask=mask)
+
+
+def rl_token_loss(logp_train, logp_rollout, advantage, logp_old=None, beta=2.0, eps_low=0.2, eps_high=0.28):
+    """IcePop-masked clipped policy loss per token (+ fixed-order mean), IcePop mask, DIS weights."""
+    T = logp_train.shape[0]
+    dev = logp_train.device
+    for name, t in (("logp_train", logp_train), ("logp_rollout", logp_rollout), ("advantage", advantage)):
+        _req(t, torch.float32, name, (T,))
+    if logp_old is not None:
+        _req(logp_old, torch.float32, "logp_old", (T,))
+    out = dict(loss=torch.empty(T, dtype=torch.float32, device=dev),
+               loss_mean=torch.empty(1, dtype=torch.float32, device=dev),
+               icepop_mask=torch.empty(T, dtype=torch.uint8, device=dev),
+               dis_weight=torch.empty(T, dtype=torch.float32, device=dev))
+    check(lib().rl_token_loss(_p(logp_train), _p(logp_old), _p(logp_rollout), _p(advantage), T, float(beta),
+                              float(eps_low), float(eps_high), _p(out["icepop_mask"]), _p(out["dis_weight"]),
+                              _p(out["loss"]), _p(out["loss_mean"]), _stream()))
+    return out
 
 
 def gemm_bf16(a, b, workspace, variant=0, out=None):

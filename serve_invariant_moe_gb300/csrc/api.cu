@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace invmoe {
 
@@ -19,6 +20,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t route_ws(int T, int E) {
   const size_t NC = (static_cast<size_t>(T) + kDispatchChunk - 1) / kDispatchChunk;
   return align_up(NC * static_cast<size_t>(E) * sizeof(int32_t), 256);
+}
+size_t replay_ws(int T, int E, int k) {
+  return route_ws(T, E) + align_up(static_cast<size_t>(T) * k * sizeof(int32_t), 256);
 }
 size_t ffn_ws(int T, int F_shared) { return align_up(static_cast<size_t>(T) * F_shared * 2, 256); }
 size_t head_part_bytes(int T, int V) {
@@ -123,10 +127,10 @@ size_t invmoe_plan_len(int T, int E, int k) {
 }
 
 size_t invmoe_workspace_size(int T, int H, int E, int k, int F, int F_shared, int V) {
-  (void)H; (void)k; (void)F;
+  (void)H; (void)F;
   if (T < 0) return 0;
   size_t need = 0;
-  if (E > 0) need = route_ws(T, E) > need ? route_ws(T, E) : need;
+  if (E > 0 && k > 0) need = replay_ws(T, E, k) > need ? replay_ws(T, E, k) : need;
   if (F_shared > 0) need = ffn_ws(T, F_shared) > need ? ffn_ws(T, F_shared) : need;
   if (V > 0) need = head_ws(T, V) > need ? head_ws(T, V) : need;
   return kStatusBytes + need;
@@ -142,7 +146,10 @@ int invmoe_check(void* workspace, void* stream) {
   if (v != 0) {
     if ((rc = check_cuda(cudaMemsetAsync(workspace, 0, sizeof(v), st), "cudaMemsetAsync"))) return rc;
     if ((rc = check_cuda(cudaStreamSynchronize(st), "cudaStreamSynchronize"))) return rc;
-    return set_error(INVMOE_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out (status 0x%x)", v);
+    if (v & kStatusTimeout)
+      return set_error(INVMOE_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out (status 0x%x)", v);
+    return set_error(INVMOE_ERR_INVALID_ARG,
+                     "router replay: an expert index was out of range or repeated within a token (status 0x%x)", v);
   }
   return INVMOE_OK;
 }
@@ -178,6 +185,38 @@ int moe_route_topk(const void* x, const void* w_router, int T, int H, int E, int
   if (rc) return rc;
   return route_launch(logits, T, E, k, H, x, topk_idx, topk_w, plan, xp,
                       reinterpret_cast<int32_t*>(scratch(workspace)), st);
+}
+
+int moe_route_replay(const void* x, const void* w_router, const int32_t* topk_idx, int T, int H, int E, int k,
+                     float* logits, float* topk_w, int32_t* plan, void* xp, void* workspace, size_t ws_bytes,
+                     void* stream) {
+  REQUIRE(T >= 0 && H > 0 && E > 0 && k > 0, INVMOE_ERR_INVALID_ARG, "need T >= 0, H, E, k > 0");
+  REQUIRE(E <= 1024, INVMOE_ERR_UNSUPPORTED_SHAPE, "E=%d > 1024", E);
+  REQUIRE(k <= E && k <= 32, INVMOE_ERR_INVALID_ARG, "need k <= min(E, 32) (k=%d, E=%d)", k, E);
+  REQUIRE(H % 64 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "H=%d is not a multiple of 64", H);
+  REQUIRE(E % 4 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "E=%d is not a multiple of 4", E);
+  REQUIRE_PTR(plan); REQUIRE_PTR(workspace);
+  REQUIRE(ws_bytes >= kStatusBytes + replay_ws(T, E, k), INVMOE_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    return check_cuda(cudaMemsetAsync(plan, 0, (2 * static_cast<size_t>(E) + 1) * sizeof(int32_t), st),
+                      "cudaMemsetAsync");
+  }
+  REQUIRE_PTR(x); REQUIRE_PTR(w_router); REQUIRE_PTR(topk_idx); REQUIRE_PTR(logits); REQUIRE_PTR(topk_w);
+  REQUIRE_PTR(xp);
+  REQUIRE_ALIGNED(x); REQUIRE_ALIGNED(w_router); REQUIRE_ALIGNED(logits); REQUIRE_ALIGNED(xp);
+  REQUIRE_ALIGNED(workspace);
+  GemmCall g{};
+  g.name = "router_gemm";
+  g.variant = E <= 64 ? GV_F32_BN64_MT1 : GV_F32_BN128_MT1;
+  g.A = x; g.a_rows = T; g.B = w_router; g.b_rows = E; g.K = H; g.N = E; g.M = T; g.G = 0;
+  g.out = logits; g.ldo = E; g.status = status_word(workspace);
+  int rc = gemm_run(g, st);
+  if (rc) return rc;
+  int32_t* counts = reinterpret_cast<int32_t*>(scratch(workspace));
+  int32_t* idx_safe = reinterpret_cast<int32_t*>(scratch(workspace) + route_ws(T, E));
+  return replay_launch(logits, topk_idx, T, E, k, H, x, idx_safe, topk_w, plan, xp, counts,
+                       status_word(workspace), st);
 }
 
 int moe_grouped_ffn(const void* xp, const int32_t* plan, const void* w13, const void* w2, int T, int H, int E,
@@ -282,6 +321,19 @@ int lm_logprob_kl(const void* hidden, const void* w_vocab, const int32_t* target
   int rc = gemm_run(g, st);
   if (rc) return rc;
   return lse_merge_launch(part, tgt_logit, target, rollout_logp, T, V, beta, logp, lse, k3, mask, st);
+}
+
+int rl_token_loss(const float* logp_train, const float* logp_old, const float* logp_rollout, const float* advantage,
+                  int T, float beta, float eps_low, float eps_high, uint8_t* icepop_mask, float* dis_weight,
+                  float* loss, float* loss_mean, void* stream) {
+  REQUIRE(T >= 0, INVMOE_ERR_INVALID_ARG, "T must be >= 0");
+  REQUIRE(beta >= 1.0f, INVMOE_ERR_INVALID_ARG, "beta must be >= 1");
+  REQUIRE(eps_low >= 0.0f && eps_low < 1.0f && eps_high >= 0.0f, INVMOE_ERR_INVALID_ARG,
+          "need 0 <= eps_low < 1 and eps_high >= 0");
+  if (T == 0) return INVMOE_OK;
+  REQUIRE_PTR(logp_train); REQUIRE_PTR(logp_rollout); REQUIRE_PTR(advantage); REQUIRE_PTR(loss);
+  return rl_loss_launch(logp_train, logp_old, logp_rollout, advantage, T, beta, eps_low, eps_high, icepop_mask,
+                        dis_weight, loss, loss_mean, static_cast<cudaStream_t>(stream));
 }
 
 int invmoe_gemm_bf16(const void* a, const void* b, int M, int N, int K, float* d, int variant, void* workspace,

@@ -116,6 +116,51 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, const float* _
   }
 }
 
+// Per-token policy-loss terms ("GLM Post-Training Beyond SFT", sections "GRPO
+// 在优化什么", "IcePop 为什么有两层 ratio", "Direct Double-Sided Importance
+// Sampling"), fp32:
+//   rho = exp(lt - lr)            mismatch ratio train / rollout
+//   r   = exp(lt - lo)            PPO ratio train / old train (lo = lr when absent)
+//   m   = 1/beta <= rho <= beta   IcePop trust mask
+//   loss = m ? -min(r*A, clip(r, 1-el, 1+eh)*A) : 0
+//   dis  = (1-el < rho < 1+eh) ? rho : 0
+__global__ void rl_token_kernel(const float* __restrict__ lt, const float* __restrict__ lo,
+                                const float* __restrict__ lr, const float* __restrict__ adv, int T, float beta,
+                                float el, float eh, uint8_t* __restrict__ mask, float* __restrict__ dis,
+                                float* __restrict__ loss) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  const float rho = expf(__fsub_rn(lt[t], lr[t]));
+  const float r = expf(__fsub_rn(lt[t], lo != nullptr ? lo[t] : lr[t]));
+  const float lo_clip = __fsub_rn(1.0f, el), hi_clip = __fadd_rn(1.0f, eh);
+  const bool m = (__fdiv_rn(1.0f, beta) <= rho) && (rho <= beta);
+  const float a = adv[t];
+  const float obj = fminf(__fmul_rn(r, a), __fmul_rn(fminf(fmaxf(r, lo_clip), hi_clip), a));
+  loss[t] = m ? -obj : 0.0f;
+  if (mask != nullptr) mask[t] = m ? 1 : 0;
+  if (dis != nullptr) dis[t] = (lo_clip < rho && rho < hi_clip) ? rho : 0.0f;
+}
+
+// Mean of loss[0..T) in a fixed order: thread i of one 1024-thread block adds
+// loss[i], loss[i + 1024], ... in ascending order; the 1024 partial sums are
+// folded by a xor butterfly inside each warp (16, 8, 4, 2, 1) and then across
+// the 32 warp sums the same way; the total is divided by T.
+__global__ void fixed_order_mean_kernel(const float* __restrict__ v, int T, float* __restrict__ out) {
+  __shared__ float warp_sum[32];
+  float s = 0.0f;
+  for (int i = threadIdx.x; i < T; i += 1024) s = __fadd_rn(s, v[i]);
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, d));
+  if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float w = warp_sum[threadIdx.x];
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) w = __fadd_rn(w, __shfl_xor_sync(0xffffffffu, w, d));
+    if (threadIdx.x == 0) *out = __fdiv_rn(w, static_cast<float>(T));
+  }
+}
+
 // Waits on an mbarrier that nothing completes, with a short limit; records the
 // timeout in the status word and returns.
 __global__ void timeout_probe_kernel(unsigned int* status, unsigned long long limit_ns) {
@@ -162,6 +207,20 @@ int lse_merge_launch(const float2* partials, const float* tgt_logit, const int32
   lse_merge_kernel<<<(T + kMergeWarps - 1) / kMergeWarps, 32 * kMergeWarps, 0, st>>>(
       partials, tgt_logit, target, rollout_logp, T, V, NCH, beta, logp, lse, k3, mask);
   return check_cuda(cudaGetLastError(), "lse_merge_kernel");
+}
+
+int rl_loss_launch(const float* lt, const float* lo, const float* lr, const float* adv, int T, float beta,
+                   float el, float eh, uint8_t* mask, float* dis, float* loss, float* loss_mean, cudaStream_t st) {
+  int rc;
+  {
+    ProfScope prof("rl_token_loss", st);
+    rl_token_kernel<<<(T + 255) / 256, 256, 0, st>>>(lt, lo, lr, adv, T, beta, el, eh, mask, dis, loss);
+    if ((rc = check_cuda(cudaGetLastError(), "rl_token_kernel"))) return rc;
+  }
+  if (loss_mean == nullptr) return INVMOE_OK;
+  ProfScope prof("fixed_order_mean", st);
+  fixed_order_mean_kernel<<<1, 1024, 0, st>>>(loss, T, loss_mean);
+  return check_cuda(cudaGetLastError(), "fixed_order_mean_kernel");
 }
 
 int timeout_probe_launch(unsigned int* status, unsigned long long limit_ns, cudaStream_t st) {

@@ -79,12 +79,20 @@ int gemm_run(const GemmCall& c, cudaStream_t st);
 int route_launch(const float* logits, int T, int E, int k, int H, const void* x, int32_t* topk_idx,
                  float* topk_w, int32_t* plan, void* xp, int32_t* chunk_counts, cudaStream_t st);
 
+int dispatch_launch(const int32_t* topk_idx, int T, int E, int k, int H, const void* x, int32_t* plan, void* xp,
+                    int32_t* chunk_counts, cudaStream_t st);
+int replay_launch(const float* logits, const int32_t* idx_in, int T, int E, int k, int H, const void* x,
+                  int32_t* idx_safe, float* topk_w, int32_t* plan, void* xp, int32_t* chunk_counts,
+                  unsigned int* status, cudaStream_t st);
+
 // ---------------------------------------------------------------- combine / head
 int combine_launch(const float* y, const float* topk_w, const int32_t* slot_row, const float* y_shared,
                    int T, int H, int k, float* out, void* out_bf16, cudaStream_t st);
 int lse_merge_launch(const float2* partials, const float* tgt_logit, const int32_t* target,
                      const float* rollout_logp, int T, int V, float beta, float* logp, float* lse, float* k3,
                      uint8_t* mask, cudaStream_t st);
+int rl_loss_launch(const float* lt, const float* lo, const float* lr, const float* adv, int T, float beta,
+                   float el, float eh, uint8_t* mask, float* dis, float* loss, float* loss_mean, cudaStream_t st);
 int timeout_probe_launch(unsigned int* status, unsigned long long limit_ns, cudaStream_t st);
 
 }  // namespace invmoe

@@ -8,6 +8,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace invmoe {
 
@@ -75,6 +76,46 @@ __global__ void topk_gate_kernel(const float* __restrict__ logits, int T, int E,
   for (int j = 0; j < k; ++j) s = __fadd_rn(s, __shfl_sync(kFull, ex, j));
   if (lane < k) {
     idx[static_cast<long long>(t) * k + lane] = my_e;
+    w[static_cast<long long>(t) * k + lane] = __fdiv_rn(ex, s);
+  }
+}
+
+// Router replay ("Reinforcement Learning: Why Numerical Alignment and MoE Routing
+// Matter So Much", section "MoE 路由会放大这种不匹配": router replay records the
+// rollout's expert choices and reuses them in training; the same page notes that
+// the outputs' computation and combine must still match).  One warp per token:
+// the k given experts are checked (in range, distinct); gates are the softmax of
+// their logits, w_j = exp(l_j - l_max) / sum_i exp(l_i - l_max) with the sum in
+// slot order -- for experts given in descending-logit order this is exactly the
+// arithmetic of topk_gate_kernel.  A token with an invalid list gets experts
+// 0..k-1 and NaN gates, and the status word records kStatusBadIndex.
+__global__ void replay_gate_kernel(const float* __restrict__ logits, const int32_t* __restrict__ idx_in, int T,
+                                   int E, int k, int32_t* __restrict__ idx_out, float* __restrict__ w,
+                                   unsigned int* __restrict__ status) {
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int e = lane < k ? idx_in[static_cast<long long>(t) * k + lane] : -1;
+  const unsigned m = __match_any_sync(kFull, e);
+  const bool bad_lane = lane < k && (e < 0 || e >= E || __popc(m) > 1);
+  const bool bad = __any_sync(kFull, bad_lane);
+  if (bad) {
+    if (lane == 0) atomicOr(status, kStatusBadIndex);
+    if (lane < k) {
+      idx_out[static_cast<long long>(t) * k + lane] = lane;
+      w[static_cast<long long>(t) * k + lane] = __uint_as_float(0x7fc00000u);
+    }
+    return;
+  }
+  const float v = lane < k ? logits[static_cast<long long>(t) * E + e] : -INFINITY;
+  float vmax = v;
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, d));
+  const float ex = (lane < k) ? expf(v - vmax) : 0.0f;
+  float s = 0.0f;
+  for (int j = 0; j < k; ++j) s = __fadd_rn(s, __shfl_sync(kFull, ex, j));
+  if (lane < k) {
+    idx_out[static_cast<long long>(t) * k + lane] = e;
     w[static_cast<long long>(t) * k + lane] = __fdiv_rn(ex, s);
   }
 }
@@ -181,12 +222,6 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* _
 int route_launch(const float* logits, int T, int E, int k, int H, const void* x, int32_t* topk_idx,
                  float* topk_w, int32_t* plan, void* xp, int32_t* chunk_counts, cudaStream_t st) {
   int rc;
-  int32_t* counts = plan;
-  int32_t* offsets = plan + E;
-  const long long S = static_cast<long long>(T) * k;
-  int32_t* row_token = plan + 2 * E + 1;
-  int32_t* slot_row = row_token + S;
-
   // top-k + gates
   {
     const int threads = 256;
@@ -201,6 +236,31 @@ int route_launch(const float* logits, int T, int E, int k, int H, const void* x,
     else topk_gate_kernel<32><<<blocks, threads, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
     if ((rc = check_cuda(cudaGetLastError(), "topk_gate_kernel"))) return rc;
   }
+  return dispatch_launch(topk_idx, T, E, k, H, x, plan, xp, chunk_counts, st);
+}
+
+int replay_launch(const float* logits, const int32_t* idx_in, int T, int E, int k, int H, const void* x,
+                  int32_t* idx_safe, float* topk_w, int32_t* plan, void* xp, int32_t* chunk_counts,
+                  unsigned int* status, cudaStream_t st) {
+  int rc;
+  {
+    const int threads = 256;
+    const long long blocks = (static_cast<long long>(T) * 32 + threads - 1) / threads;
+    ProfScope prof("replay_gate", st);
+    replay_gate_kernel<<<blocks, threads, 0, st>>>(logits, idx_in, T, E, k, idx_safe, topk_w, status);
+    if ((rc = check_cuda(cudaGetLastError(), "replay_gate_kernel"))) return rc;
+  }
+  return dispatch_launch(idx_safe, T, E, k, H, x, plan, xp, chunk_counts, st);
+}
+
+int dispatch_launch(const int32_t* topk_idx, int T, int E, int k, int H, const void* x, int32_t* plan, void* xp,
+                    int32_t* chunk_counts, cudaStream_t st) {
+  int rc;
+  int32_t* counts = plan;
+  int32_t* offsets = plan + E;
+  const long long S = static_cast<long long>(T) * k;
+  int32_t* row_token = plan + 2 * E + 1;
+  int32_t* slot_row = row_token + S;
   // dispatch plan
   const int NC = (T + kDispatchChunk - 1) / kDispatchChunk;
   {

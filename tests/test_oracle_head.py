@@ -102,3 +102,31 @@ def test_k3_golden_threshold_consistency():
     assert round(g["bad_path_k3"] / g["equivalence_threshold"], -2) == g["ratio_to_threshold_approx"]
     lp = np.array([-1.0, -2.0])
     assert head.k3(lp, lp).mean() == g["aligned_k3"] < g["equivalence_threshold"]
+
+
+def test_ppo_icepop_loss_hand_cases():
+    g = json.load(open(os.path.join(GOLDEN, "icepop_beta2.json")))
+    el, eh = g["ppo_clip_eps_low"], g["ppo_clip_eps_high"]
+    # identical policies: r = 1, rho = 1 -> loss = -A
+    lt = np.array([-1.0, -2.0, -3.0])
+    loss, mean = head.ppo_icepop_loss(lt, lt, lt, np.array([1.0, -0.5, 2.0]), 2.0, el, eh)
+    assert np.array_equal(loss, np.array([-1.0, 0.5, -2.0])) and abs(mean - (-2.5 / 3)) < 1e-15
+    # positive advantage: the ratio is capped at 1 + eps_h; negative: floored at 1 - eps_l
+    lo = np.zeros(4)
+    lt = np.log(np.array([1.5, 1.5, 0.5, 0.5]))
+    A = np.array([1.0, -1.0, 1.0, -1.0])
+    loss, _ = head.ppo_icepop_loss(lt, lo, lt, A, 2.0, el, eh)      # rollout == train: mask 1
+    assert np.allclose(loss, [-(1 + eh), 1.5, -0.5, 1 - el], rtol=0, atol=1e-15)
+    # the IcePop mask removes a token whose train/infer ratio is outside [1/2, 2]
+    loss, _ = head.ppo_icepop_loss(np.zeros(2), np.zeros(2), np.log([3.0, 1.9]), np.ones(2), 2.0, el, eh)
+    assert loss[0] == 0.0 and loss[1] == -1.0
+
+
+def test_dis_weight_window():
+    g = json.load(open(os.path.join(GOLDEN, "icepop_beta2.json")))
+    el, eh = g["ppo_clip_eps_low"], g["ppo_clip_eps_high"]
+    r = np.array([0.79, 0.8, 0.81, 1.0, 1.27, 1.28, 1.3])
+    w = head.dis_weight(np.log(r), np.zeros_like(r), el, eh)
+    # open interval (0.8, 1.28); exp(log(r)) may land an ulp away from r at the two ends
+    assert w[0] == 0 and w[6] == 0 and np.allclose(w[[2, 3, 4]], r[[2, 3, 4]], rtol=1e-15)
+    assert head.dis_weight(np.log([0.8 - 1e-9, 1.28 + 1e-9]), np.zeros(2), el, eh).tolist() == [0.0, 0.0]

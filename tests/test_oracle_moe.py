@@ -220,3 +220,20 @@ def test_skewed_layer_has_busy_experts():
     counts = np.bincount(idx.ravel(), minlength=cfg.E)
     assert 1200 <= counts.max() <= 1800
     assert counts.sum() == cfg.T * cfg.k
+
+
+def test_replay_of_own_choice_is_the_plain_forward():
+    x, wr, w13, w2 = _tiny_layer(k=3)
+    a = moe.moe_forward(x, wr, w13, w2, 3, 16)
+    b = moe.moe_forward(x, wr, w13, w2, 3, 16, replay_idx=a["idx"])
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["gates"], b["gates"])
+    # replaying other experts changes the output but keeps gates a distribution over them
+    idx = (a["idx"] + 1) % 6
+    c = moe.moe_forward(x, wr, w13, w2, 3, 16, replay_idx=idx)
+    assert np.array_equal(c["idx"], idx) and np.allclose(c["gates"].sum(1), 1.0)
+    dense = np.zeros_like(x)
+    for e in range(6):
+        ye = moe.swiglu_expert(x, w13[e], w2[e], 16)
+        for j in range(3):
+            dense += ((idx[:, j] == e) * c["gates"][:, j])[:, None] * ye
+    assert np.allclose(c["out"], dense, rtol=1e-12, atol=1e-12)
