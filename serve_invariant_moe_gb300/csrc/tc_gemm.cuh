@@ -263,12 +263,12 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
       int filled_phase[STAGES];
 #pragma unroll
       for (int s = 0; s < STAGES; ++s) filled_phase[s] = -1;
-      // the next unit index is fetched one unit ahead so the atomic's latency hides
-      // behind the current unit's loads
-      int next = atomicAdd(p.sched, 1);
+      // the unit index is taken only when its loads are about to be issued: units
+      // with neighbouring indices (the row chunks of one expert's column block,
+      // which share the weight tile) then start close together and share it in L2
       while (true) {
-        int u = next < total_units ? next : -1;
-        if (u >= 0) next = atomicAdd(p.sched, 1);
+        int u = atomicAdd(p.sched, 1);
+        if (u >= total_units) u = -1;
         if (!mbar_wait(&qempty_bar[qi], qphase ^ 1u, wc)) break;
         s_queue[qi] = u;
         mbar_arrive(&qfull_bar[qi]);

@@ -159,12 +159,11 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
       uint32_t qphase = 0;
       const uint32_t q_peer0 = mapa_shared(smem_u32(const_cast<int*>(s_queue)), peer);
       const uint32_t qfull_peer0 = mapa_shared(smem_u32(&qfull_bar[0]), peer);
-      int next = rank == 0 ? atomicAdd(p.sched, 1) : 0;
       while (ok) {
         int u;
         if (rank == 0) {
-          u = next < total_units ? next : -1;
-          if (u >= 0) next = atomicAdd(p.sched, 1);
+          u = atomicAdd(p.sched, 1);
+          if (u >= total_units) u = -1;
           if (!mbar_wait<true>(&qempty_bar[qi], qphase ^ 1u, wc)) { ok = false; break; }
           s_queue[qi] = u;
           mbar_arrive(&qfull_bar[qi]);
