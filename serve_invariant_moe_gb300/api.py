@@ -115,6 +115,49 @@ class MoELayer:
         return self._run(x_tokens, d["ws"], bufs, out_bf16=out_bf16)["out"]
 
 
+class DecodeGraphs:
+    """Decode steps captured as CUDA graphs, one per batch-size bucket.
+
+    Every kernel of the decode path takes its sizes and buffers at capture time,
+    so a step for a bucket of B requests replays as one graph launch; batches
+    smaller than a bucket are padded with zero tokens, which changes no other
+    row's bits (every row is computed on its own).  The captured kernels are the
+    same as the eager ones, so a replayed step gives the same bits as
+    MoELayer.decode on the same tokens.
+    """
+
+    def __init__(self, layer: MoELayer, buckets=(1, 2, 4, 8, 16, 32, 64, 128)):
+        self.layer = layer
+        self.buckets = sorted(buckets)
+        w = layer.w
+        dev = w.w13.device
+        layer.alloc_decode(self.buckets[-1])
+        self.inp = {B: torch.zeros((B, w.H), dtype=torch.bfloat16, device=dev) for B in self.buckets}
+        self.out = {}
+        self.graphs = {}
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            for B in self.buckets:
+                layer.decode(self.inp[B])          # warm-up outside capture (kernel attributes, caches)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        for B in self.buckets:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.out[B] = layer.decode(self.inp[B])
+            self.graphs[B] = g
+
+    def __call__(self, x_tokens: torch.Tensor) -> torch.Tensor:
+        """x_tokens [b, H] bf16 (b <= largest bucket) -> [b, H] fp32 (a view of the graph's output)."""
+        b = x_tokens.shape[0]
+        B = next(B for B in self.buckets if B >= b)
+        self.inp[B][:b].copy_(x_tokens)
+        if b < B:
+            self.inp[B][b:].zero_()
+        self.graphs[B].replay()
+        return self.out[B][:b]
+
+
 def moe_prefill(layer: MoELayer, x: torch.Tensor) -> torch.Tensor:
     return layer.prefill(x)
 

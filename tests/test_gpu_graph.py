@@ -40,3 +40,22 @@ def test_decode_graph_replay_matches_eager():
         graph.replay()
         torch.cuda.synchronize()
         assert torch.equal(static_out, ref)
+
+
+def test_decode_graph_buckets_match_eager_decode():
+    from serve_invariant_moe_gb300 import api, build
+    build.build()
+    cfg = dataclasses.replace(synth.GLM_MOE, name="graph_buckets", H=512, E=32, k=8, F=256, F_shared=256, seed=42)
+    _, wr = synth.moe_activations(cfg, T=1)
+    w13, w2 = synth.expert_weights(cfg, "cuda")
+    ws13, ws2 = synth.shared_expert_weights(cfg, "cuda")
+    layer = api.MoELayer(api.MoEWeights(wr.cuda(), w13, w2, cfg.k, ws13, ws2))
+    graphs = api.DecodeGraphs(layer, buckets=(1, 4, 16))
+    eager_layer = api.MoELayer(api.MoEWeights(wr.cuda(), w13, w2, cfg.k, ws13, ws2))
+    g = torch.Generator().manual_seed(11)
+    for b in (1, 3, 4, 9, 16):
+        x = synth.to_bf16(torch.randn((b, cfg.H), generator=g)).cuda()
+        ref = eager_layer.decode(x).clone()
+        got = graphs(x).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref), b
