@@ -24,13 +24,18 @@ Sources (cited by page title and section):
   mask m_t = 1[1/beta <= rho_t <= beta] with beta = 2; sections "迁移到 NPU 时"
   and "动作与概率契约": the top-k tie / order / NaN contract and the
   logsumexp comparison contract.
+* Same bit-agreement page, section "端到端零 KLD": the trainer follows the same
+  bit-exact standard as the serving path; the head backward here is the chain
+  rule of the forward definition, written out.
 
 Modules:
     numerics  -- exact bf16 <-> float64 conversion and round-to-nearest-even.
     moe       -- router logits, top-k with lowest-index ties, gates, SwiGLU
                  experts, dispatch plan invariants, fixed-order combine, and the
                  dense-all-experts-then-mask brute force.
-    head      -- vocab projection, log-sum-exp, token logprob, k3, IcePop mask.
+    head      -- vocab projection, log-sum-exp, token logprob, k3, IcePop mask,
+                 the IcePop-masked clipped loss and its gradient, DIS weights,
+                 and the head backward (dlogits, d hidden, d vocab weights).
 
 Every function here is parity-pinned by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_*.py`` against closed forms, library routines, brute force

@@ -110,3 +110,63 @@ def dis_weight(logp_train, logp_rollout, eps_low=0.2, eps_high=0.28):
     (both ends excluded; 0 means the token gives no gradient)."""
     r = np.exp(np.asarray(logp_train, np.float64) - np.asarray(logp_rollout, np.float64))
     return np.where((1.0 - eps_low < r) & (r < 1.0 + eps_high), r, 0.0)
+
+
+# ----------------------------------------------------------------------------
+# backward of the head (the trainer's side of the same definition)
+# ----------------------------------------------------------------------------
+
+def ppo_icepop_grad(logp_train, logp_old, logp_rollout, advantage, beta=2.0, eps_low=0.2, eps_high=0.28,
+                    dtype=np.float64):
+    """Derivative of the mean IcePop-masked clipped loss with respect to each logp_train.
+
+    From ``ppo_icepop_loss``: loss_t = -m_t * min(r_t A_t, clip(r_t) A_t) with
+    r_t = exp(logp_train_t - logp_old_t), mean over the T tokens.  The mask
+    m_t is an indicator (piecewise constant in logp_train), so it is held fixed.
+    Where the unclipped term attains the minimum (r A <= clip(r) A, which
+    includes every r inside the clip window) d(r A)/d logp_train = r A; where the
+    clipped term is strictly smaller it is a constant and the derivative is 0:
+        g_t = -(1/T) * m_t * r_t * A_t * 1[r_t A_t <= clip(r_t) A_t].
+    Returns g [T] float64.
+    """
+    lt = np.asarray(logp_train, np.float64)
+    lo = np.asarray(logp_old, np.float64)
+    A = np.asarray(advantage, np.float64)
+    T = lt.shape[0]
+    if T == 0:
+        return np.zeros(0)
+    r = np.exp(lt - lo)
+    m = icepop_mask(logp_train, logp_rollout, beta, dtype).astype(np.float64)
+    unclipped = r * A <= np.clip(r, 1.0 - eps_low, 1.0 + eps_high) * A
+    return np.where(unclipped, -(m * r * A) / T, 0.0)
+
+
+def dlogits(z, target, grad_logp):
+    """dL/dz[t, v] for L = sum_t g_t * logp_t, logp_t = z[t, target_t] - lse(z_t):
+        dz[t, v] = g_t * (1[v == target_t] - softmax(z_t)_v),
+    float64.  A token with g_t = 0 (dropped by the IcePop mask, or clipped)
+    contributes nothing."""
+    z = np.asarray(z, np.float64)
+    g = np.asarray(grad_logp, np.float64)
+    lse = logsumexp_rows(z)
+    p = np.exp(z - lse[:, None])
+    onehot = np.zeros_like(z)
+    onehot[np.arange(z.shape[0]), np.asarray(target, np.int64)] = 1.0
+    return g[:, None] * (onehot - p)
+
+
+def head_backward(hidden, w_vocab, target, grad_logp, round_dz=True):
+    """Gradients of L = sum_t g_t * logp_t through the vocabulary projection, float64.
+
+        Z = Hs Wv^T,  dZ = dlogits(Z),  dHs = dZ Wv,  dWv = dZ^T Hs.
+    dZ is the bf16 operand of the two gradient products, so it is rounded to
+    bf16 (nearest-even) first when round_dz, as the forward rounds h.
+    Returns dict(dz, d_hidden, d_wvocab).
+    """
+    from .numerics import round_to_bf16
+    hs = np.asarray(hidden, np.float64)
+    wv = np.asarray(w_vocab, np.float64)
+    dz = dlogits(vocab_logits(hs, wv), target, grad_logp)
+    if round_dz:
+        dz = round_to_bf16(dz)
+    return dict(dz=dz, d_hidden=dz @ wv, d_wvocab=dz.T @ hs)

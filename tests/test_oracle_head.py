@@ -6,6 +6,7 @@ import os
 import numpy as np
 import scipy.special
 import scipy.stats
+import torch
 
 from oracle import head
 
@@ -130,3 +131,116 @@ def test_dis_weight_window():
     # open interval (0.8, 1.28); exp(log(r)) may land an ulp away from r at the two ends
     assert w[0] == 0 and w[6] == 0 and np.allclose(w[[2, 3, 4]], r[[2, 3, 4]], rtol=1e-15)
     assert head.dis_weight(np.log([0.8 - 1e-9, 1.28 + 1e-9]), np.zeros(2), el, eh).tolist() == [0.0, 0.0]
+
+
+# ---------------------------------------------------------------- backward
+
+def _f_logp(hs, wv, target, g):
+    """sum_t g_t * logp_t as a plain function of (hidden, vocab weights)."""
+    logp, _ = head.token_logprob(head.vocab_logits(hs, wv), target)
+    return float(np.dot(g, logp))
+
+
+def test_dlogits_central_differences_and_row_sums():
+    rng = np.random.default_rng(20)
+    z = rng.standard_normal((4, 9)) * 2
+    tgt = np.array([0, 8, 3, 3])
+    g = np.array([1.0, -0.7, 0.0, 2.5])
+    dz = head.dlogits(z, tgt, g)
+    eps = 1e-5
+    for t in range(4):
+        for v in range(9):
+            zp, zm = z.copy(), z.copy()
+            zp[t, v] += eps; zm[t, v] -= eps
+            fd = (np.dot(g, head.token_logprob(zp, tgt)[0]) - np.dot(g, head.token_logprob(zm, tgt)[0])) / (2 * eps)
+            assert abs(fd - dz[t, v]) < 1e-9
+    assert np.allclose(dz.sum(1), 0.0, atol=1e-15)          # softmax and one-hot both sum to one
+    assert np.array_equal(dz[2], np.zeros(9))                # g = 0: the token contributes nothing
+    assert dz[0, 0] > 0 and np.all(dz[0, 1:] < 0)            # g > 0 raises the target, lowers the rest
+
+
+def test_dlogits_matches_torch_autograd():
+    rng = np.random.default_rng(21)
+    z = torch.from_numpy(rng.standard_normal((6, 40)) * 3).requires_grad_(True)
+    tgt = torch.from_numpy(rng.integers(0, 40, 6))
+    g = torch.from_numpy(rng.standard_normal(6))
+    (torch.log_softmax(z, 1).gather(1, tgt[:, None])[:, 0] * g).sum().backward()
+    assert np.allclose(head.dlogits(z.detach().numpy(), tgt.numpy(), g.numpy()), z.grad.numpy(),
+                       rtol=1e-13, atol=1e-15)
+
+
+def test_head_backward_central_differences():
+    # every element of both gradients against a central difference of sum_t g_t logp_t;
+    # a transposed operand, a dropped one-hot or a sign error fails here
+    rng = np.random.default_rng(22)
+    T, H, V = 3, 5, 7
+    hs = rng.standard_normal((T, H))
+    wv = rng.standard_normal((V, H)) * 0.5
+    tgt = np.array([6, 0, 2])
+    g = np.array([0.5, -1.25, 2.0])
+    out = head.head_backward(hs, wv, tgt, g, round_dz=False)
+    assert out["d_hidden"].shape == (T, H) and out["d_wvocab"].shape == (V, H)
+    eps = 1e-6
+    for name, arr, grad in (("hidden", hs, out["d_hidden"]), ("wvocab", wv, out["d_wvocab"])):
+        for i in np.ndindex(arr.shape):
+            ap, am = arr.copy(), arr.copy()
+            ap[i] += eps; am[i] -= eps
+            if name == "hidden":
+                fd = (_f_logp(ap, wv, tgt, g) - _f_logp(am, wv, tgt, g)) / (2 * eps)
+            else:
+                fd = (_f_logp(hs, ap, tgt, g) - _f_logp(hs, am, tgt, g)) / (2 * eps)
+            assert abs(fd - grad[i]) < 1e-7 * max(1.0, abs(fd)), (name, i, fd, grad[i])
+
+
+def test_head_backward_bf16_rounding_of_dz():
+    rng = np.random.default_rng(23)
+    hs = rng.standard_normal((8, 16)); wv = rng.standard_normal((50, 16)) * 0.3
+    tgt = rng.integers(0, 50, 8); g = rng.standard_normal(8)
+    a = head.head_backward(hs, wv, tgt, g, round_dz=False)
+    b = head.head_backward(hs, wv, tgt, g)
+    # dz is rounded to bf16 (8 significant bits): relative change at most 2^-8 per element
+    assert np.all(np.abs(b["dz"] - a["dz"]) <= 2.0 ** -8 * np.abs(a["dz"]))
+    from oracle.numerics import round_to_bf16
+    assert np.array_equal(round_to_bf16(b["dz"]), b["dz"])
+    assert np.allclose(b["d_hidden"], b["dz"] @ wv, rtol=1e-14) and np.allclose(b["d_wvocab"], b["dz"].T @ hs, rtol=1e-14)
+
+
+def test_ppo_icepop_grad_hand_cases():
+    g = json.load(open(os.path.join(GOLDEN, "icepop_beta2.json")))
+    el, eh = g["ppo_clip_eps_low"], g["ppo_clip_eps_high"]
+    lo = np.zeros(6)
+    r = np.array([1.0, 1.5, 0.5, 0.5, 1.5, 1.0])
+    A = np.array([1.0, 1.0, 1.0, -1.0, -1.0, 0.0])
+    lt = np.log(r)
+    gr = head.ppo_icepop_grad(lt, lo, lt, A, 2.0, el, eh)           # mask 1 everywhere
+    # inside the window: -r A / T; A > 0 above the window and A < 0 below it are clipped: 0;
+    # A > 0 below and A < 0 above stay unclipped
+    want = np.array([-1.0, 0.0, -0.5, 0.0, 1.5, 0.0]) / 6
+    assert np.allclose(gr, want, rtol=1e-15, atol=0)
+    # a token the IcePop mask drops gives no gradient
+    gm = head.ppo_icepop_grad(np.zeros(2), np.zeros(2), np.log([3.0, 1.0]), np.ones(2), 2.0, el, eh)
+    assert gm[0] == 0.0 and gm[1] == -0.5
+
+
+def test_ppo_icepop_grad_central_differences():
+    # away from the clip edges and the mask edges the loss is smooth in logp_train
+    rng = np.random.default_rng(24)
+    T = 400
+    lo = rng.standard_normal(T) * 0.1
+    lt = lo + rng.standard_normal(T) * 0.3
+    lr = lt + rng.standard_normal(T) * 0.4
+    A = rng.standard_normal(T)
+    r = np.exp(lt - lo)
+    rho = np.exp(lt - lr)
+    ok = (np.abs(r - 0.8) > 1e-3) & (np.abs(r - 1.28) > 1e-3) & (np.abs(rho - 0.5) > 1e-3) & (np.abs(rho - 2) > 1e-3)
+    gr = head.ppo_icepop_grad(lt, lo, lr, A)
+    eps = 1e-7
+    for t in np.nonzero(ok)[0][:200]:
+        p, m = lt.copy(), lt.copy()
+        p[t] += eps; m[t] -= eps
+        # the mask is held at its value at lt (an indicator has no derivative)
+        lrp, lrm = lr.copy(), lr.copy()
+        lrp[t] += eps; lrm[t] -= eps
+        fd = (head.ppo_icepop_loss(p, lo, lrp, A)[1] - head.ppo_icepop_loss(m, lo, lrm, A)[1]) / (2 * eps)
+        assert abs(fd - gr[t]) < 1e-7, (t, fd, gr[t])
+    assert (gr == 0).sum() > 10 and (gr != 0).sum() > 200     # both regimes exercised

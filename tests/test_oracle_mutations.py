@@ -55,7 +55,47 @@ def _pin_lse(lse_fn):
     assert np.allclose(lse_fn(z), scipy.special.logsumexp(z, axis=1), rtol=1e-13, atol=1e-12)
 
 
+def _pin_head_backward(hb):
+    rng = np.random.default_rng(6)
+    T, H, V = 2, 4, 5
+    hs = rng.standard_normal((T, H)); wv = rng.standard_normal((V, H)) * 0.5
+    tgt = np.array([4, 1]); g = np.array([0.75, -1.5])
+
+    def f(a, b):
+        logp, _ = head.token_logprob(head.vocab_logits(a, b), tgt)
+        return float(np.dot(g, logp))
+
+    out = hb(hs, wv, tgt, g, round_dz=False)
+    eps = 1e-6
+    for i in np.ndindex(hs.shape):
+        p, m = hs.copy(), hs.copy(); p[i] += eps; m[i] -= eps
+        assert abs((f(p, wv) - f(m, wv)) / (2 * eps) - out["d_hidden"][i]) < 1e-7
+    for i in np.ndindex(wv.shape):
+        p, m = wv.copy(), wv.copy(); p[i] += eps; m[i] -= eps
+        assert abs((f(hs, p) - f(hs, m)) / (2 * eps) - out["d_wvocab"][i]) < 1e-7
+
+
+def _pin_ppo_grad(gfn):
+    rng = np.random.default_rng(7)
+    T = 300
+    lo = rng.standard_normal(T) * 0.1
+    lt = lo + rng.standard_normal(T) * 0.3
+    lr = lt + rng.standard_normal(T) * 0.4
+    A = rng.standard_normal(T)
+    r, rho = np.exp(lt - lo), np.exp(lt - lr)
+    ok = (np.abs(r - 0.8) > 1e-3) & (np.abs(r - 1.28) > 1e-3) & (np.abs(rho - 0.5) > 1e-3) & (np.abs(rho - 2) > 1e-3)
+    gr = gfn(lt, lo, lr, A)
+    eps = 1e-7
+    for t in np.nonzero(ok)[0]:
+        p, m = lt.copy(), lt.copy(); p[t] += eps; m[t] -= eps
+        lp, lm = lr.copy(), lr.copy(); lp[t] += eps; lm[t] -= eps
+        fd = (head.ppo_icepop_loss(p, lo, lp, A)[1] - head.ppo_icepop_loss(m, lo, lm, A)[1]) / (2 * eps)
+        assert abs(fd - gr[t]) < 1e-7
+
+
 def test_pins_pass_on_the_real_oracle():
+    _pin_head_backward(head.head_backward)
+    _pin_ppo_grad(head.ppo_icepop_grad)
     _pin_topk(moe.topk_lowest_index)
     _pin_gates(moe.topk_gates)
     _pin_swiglu(moe.swiglu_expert)
@@ -104,7 +144,45 @@ def _lse_no_shift(z):                      # forgot the max shift (overflows / u
     return np.log(np.exp(np.asarray(z, np.float64)).sum(axis=1))
 
 
+def _hb_sign_flipped(hs, wv, tgt, g, round_dz=True):    # softmax - onehot without the minus of g
+    out = head.head_backward(hs, wv, tgt, g, round_dz)
+    return {k: -v for k, v in out.items()}
+
+
+def _hb_no_onehot(hs, wv, tgt, g, round_dz=True):        # dropped the one-hot term
+    hs = np.asarray(hs, np.float64); wv = np.asarray(wv, np.float64)
+    z = head.vocab_logits(hs, wv)
+    dz = -np.asarray(g)[:, None] * np.exp(z - head.logsumexp_rows(z)[:, None])
+    return dict(dz=dz, d_hidden=dz @ wv, d_wvocab=dz.T @ hs)
+
+
+def _hb_unscaled(hs, wv, tgt, g, round_dz=True):         # forgot the per-token upstream gradient
+    return head.head_backward(hs, wv, tgt, np.ones_like(np.asarray(g, np.float64)), round_dz)
+
+
+def _ppo_grad_no_ratio(lt, lo, lr, A, *a):               # d(r A)/d logp taken as A, not r A
+    r = np.exp(np.asarray(lt) - np.asarray(lo))
+    g = head.ppo_icepop_grad(lt, lo, lr, A, *a)
+    return g / r
+
+
+def _ppo_grad_no_clip(lt, lo, lr, A, beta=2.0, *a):      # ignored the clipped branch
+    r = np.exp(np.asarray(lt) - np.asarray(lo))
+    m = head.icepop_mask(lt, lr, beta).astype(np.float64)
+    return -(m * r * np.asarray(A)) / len(r)
+
+
+def _ppo_grad_no_mask(lt, lo, lr, A, *a):                # ignored the IcePop mask
+    return head.ppo_icepop_grad(lt, lo, lt, A, *a)
+
+
 @pytest.mark.parametrize("pin, wrong", [
+    (_pin_head_backward, _hb_sign_flipped),
+    (_pin_head_backward, _hb_no_onehot),
+    (_pin_head_backward, _hb_unscaled),
+    (_pin_ppo_grad, _ppo_grad_no_ratio),
+    (_pin_ppo_grad, _ppo_grad_no_clip),
+    (_pin_ppo_grad, _ppo_grad_no_mask),
     (_pin_topk, _topk_high_index_ties),
     (_pin_topk, _topk_nan_first),
     (_pin_gates, _gates_not_renormalised),
