@@ -245,16 +245,7 @@ def run_ours(args):
     lib.invmoe_profile_enable(0)
     ms_total = ev0.elapsed_time(ev1)
     clk = clocks.stop()
-    import ctypes
-    maxn = 64
-    names = ctypes.create_string_buffer(48 * maxn)
-    tot = (ctypes.c_float * maxn)()
-    cnt = (ctypes.c_int * maxn)()
-    n = lib.invmoe_profile_collect(names, tot, cnt, maxn)
-    kern = {}
-    for i in range(max(n, 0)):
-        nm = names.raw[48 * i:48 * i + 48].split(b"\0")[0].decode()
-        kern[nm] = (tot[i], cnt[i])
+    kern = _profile_collect(lib)
     binding.check_status(st.ws_head)
     binding.check_status(st.layer._decode["ws"])
 
@@ -321,6 +312,8 @@ def run_ours(args):
 
     inv = invariance_check(st, device) if rank == 0 else None
     nxt = next_rows_timing(st, device) if rank == 0 else None
+    if nxt is not None and not args.no_backward:
+        nxt.update(head_backward_timing(st, device, peaks))
     moe_names = ["router_gemm", "topk_gate", "dispatch_count", "dispatch_scan", "dispatch_scatter", "gather_rows",
                  "expert_gemm1_swiglu", "expert_gemm2", "shared_gemm1_swiglu", "shared_gemm2", "combine"]
     head_names = ["lm_head_gemm_lse", "lse_merge"]
@@ -394,6 +387,70 @@ def invariance_check(st, device):
             "logp_differing": int((logp_a != logp_b).sum().item()),
             "k3_mean_prefill_vs_decode": float(r["k3"].double().mean().item()),
             "icepop_kept": int(r["mask"].sum().item())}
+
+
+def _profile_collect(lib):
+    """Per-kernel (total ms, launches) recorded by the library's CUDA-event profiler."""
+    import ctypes
+    maxn = 64
+    names = ctypes.create_string_buffer(48 * maxn)
+    tot = (ctypes.c_float * maxn)()
+    cnt = (ctypes.c_int * maxn)()
+    n = lib.invmoe_profile_collect(names, tot, cnt, maxn)
+    kern = {}
+    for i in range(max(n, 0)):
+        nm = names.raw[48 * i:48 * i + 48].split(b"\0")[0].decode()
+        kern[nm] = (tot[i], cnt[i])
+    return kern
+
+
+def head_backward_timing(st, device, peaks, reps=3):
+    """The head backward on the step's own batch (T = 8192, H = 6144, V = 151552), outside the
+    timed region: upstream gradient from the IcePop-masked policy loss, then dlogits, d_hidden and
+    d_wvocab.  Per-kernel device time from the library's profiler; each of the three kernels is a
+    2*T*V*H-flop contraction."""
+    import torch
+    from serve_invariant_moe_gb300 import _lib, binding
+    lib = _lib.lib()
+    T, H, V = st.mc.T, st.mc.H, st.hc.V
+    fwd = st.run()
+    lt = fwd["logp"].clone()
+    lse = fwd["lse"].clone()
+    lr = lt + (st.noise.to(device) * 0.5)
+    adv = torch.linspace(-1, 1, T, device=device)
+    grad = binding.rl_token_loss(lt, lr, adv)["grad_logp"]
+    ws = binding.new_workspace(4096, device)
+    dz = torch.empty((T, V), dtype=torch.bfloat16, device=device)
+    dh = torch.empty((T, H), dtype=torch.float32, device=device)
+    dw = torch.empty((V, H), dtype=torch.float32, device=device)
+
+    def call():
+        binding.lm_head_backward(st.hidden, st.wv, st.target, lse, grad, ws, dlogits=dz, d_hidden=dh, d_wvocab=dw)
+
+    call()
+    torch.cuda.synchronize()
+    lib.invmoe_profile_enable(1)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    lib.invmoe_profile_enable(0)
+    kern = _profile_collect(lib)
+    binding.check_status(ws)
+    ms = e0.elapsed_time(e1) / reps
+    flop = 2.0 * T * V * H
+    out = {"head_backward_ms": round(ms, 3), "head_backward_tokens_per_s": round(T / (ms / 1e3), 1),
+           "head_backward_tflops": round(3 * flop / (ms / 1e3) / 1e12, 1)}
+    for nm in ("lm_head_dlogits", "lm_head_dhidden", "lm_head_dwvocab"):
+        if nm in kern and kern[nm][1]:
+            kms = kern[nm][0] / kern[nm][1]
+            ach = flop / (kms / 1e3) / 1e12
+            out[nm] = dict(ms=round(kms, 4), achieved=round(ach, 1), unit="TFLOP/s",
+                           frac=round(ach / peaks["bf16"], 4))
+    del dz, dw, dh
+    return out
 
 
 def next_rows_timing(st, device, reps=5):
@@ -564,6 +621,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true", help="skip the head-backward timing (next rows)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)
     ap.add_argument("--ref-tokens-per-step", type=int, default=1)
     args = ap.parse_args()

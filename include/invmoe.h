@@ -227,6 +227,37 @@ int moe_route_topk_noalloc(const void* x, const void* w_router, int T, int H, in
                            void* xp, unsigned int* status, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * lm_head_backward -- deterministic backward of the vocabulary projection
+ *
+ * The trainer's side of the same definition ("位级一致：前沿训练的差异化关键",
+ * section "端到端零 KLD": the trainer follows the same bit-exact standard as the
+ * serving path).  For the per-token loss L = sum_t g[t] * logp[t] (g = dL/dlogp,
+ * e.g. rl_token_loss's grad_logp; g[t] = 0 for a token the IcePop mask drops):
+ *   z[t, v]   recomputed exactly as lm_logprob_kl computes it (same tile, same
+ *             K order, so bit-identical)
+ *   dz[t, v]  = bf16_rne( g[t] * (onehot(v == target[t]) - exp(z[t, v] - lse[t])) )
+ *             fp32: p = exp(z - lse); 1 - p at the target column, -p elsewhere;
+ *             one fp32 multiply by g[t]; then rounded to bf16
+ *   d_hidden[t, h] = sum_v dz[t, v] * w_vocab[v, h]       v ascending in 64-wide blocks
+ *   d_wvocab[v, h] = sum_t dz[t, v] * hidden[t, h]        t ascending in 64-wide blocks
+ * Each output element is produced by one CTA pair that walks its reduction in
+ * the same order on every call (no split reduction, no atomics), so repeated
+ * calls give identical bits whatever the schedule; a row of d_hidden depends on
+ * its own token only (batch-invariant), as in the forward.
+ *
+ * hidden [T, H] bf16, w_vocab [V, H] bf16, target [T] int32 (in [0, V)), lse [T]
+ * fp32 (from lm_logprob_kl), grad_logp [T] fp32; outputs (device, caller-owned):
+ * dlogits [T, V] bf16, d_hidden [T, H] fp32 (nullable: not computed),
+ * d_wvocab [V, H] fp32 (nullable: not computed).  All 16-byte aligned.
+ * workspace: invmoe_workspace_size(T, H, 0, 0, 0, 0, V) bytes suffice (only the
+ * status block is used).
+ * Shapes: H % 64 == 0, V % 8 == 0.  T may be any size >= 0.
+ * ------------------------------------------------------------------------- */
+int lm_head_backward(const void* hidden, const void* w_vocab, const int32_t* target, const float* lse,
+                     const float* grad_logp, int T, int H, int V, void* dlogits, float* d_hidden,
+                     float* d_wvocab, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * rl_token_loss -- IcePop-masked clipped policy loss and DIS weights per token
  *
  * "GLM Post-Training Beyond SFT", sections "GRPO 在优化什么" (clipped objective
@@ -241,11 +272,16 @@ int moe_route_topk_noalloc(const void* x, const void* w_router, int T, int H, in
  * loss_mean (nullable, [1]) = sum(loss) / T in a fixed order (one block: thread i
  * adds elements i, i+1024, ... ascending, then xor butterflies inside and across
  * warps).  logp_old nullable (then r = rho); icepop_mask, dis_weight nullable.
+ * grad_logp (nullable) = d loss_mean / d logp_train, the mask held fixed:
+ *   icepop_mask && r*A <= clip(r)*A ? -(r*A) / T : 0
+ * (the unclipped term is the minimum, which holds for every r inside the clip
+ * window; where the clipped term is strictly smaller it is constant in r).
  * All [T] device arrays; fp32 except icepop_mask (uint8).
  * ------------------------------------------------------------------------- */
 int rl_token_loss(const float* logp_train, const float* logp_old, const float* logp_rollout,
                   const float* advantage, int T, float beta, float eps_low, float eps_high,
-                  uint8_t* icepop_mask, float* dis_weight, float* loss, float* loss_mean, void* stream);
+                  uint8_t* icepop_mask, float* dis_weight, float* loss, float* loss_mean,
+                  float* grad_logp, void* stream);
 
 /* ---------------------------------------------------------------------------
  * Diagnostics
@@ -258,8 +294,11 @@ int rl_token_loss(const float* logp_train, const float* logp_old, const float* l
  *   1 = 128 x 256 tile, two row tiles per unit (vocab and expert down projections)
  *   2 = 128 x 128 tile, 3 = 128 x 64 tile (router logits for E <= 128 / 64)
  *   4 = 256 x 256 tile computed by a CTA pair (cta_group::2) on two SMs
+ *   5 = as 4 with b MN-major: b is [K, N] (d = a * b), K % 8 == 0, N % 8 == 0
+ *   6 = as 4 with a and b MN-major: a is [K, M], b is [K, N] (d = a^T * b),
+ *       any K >= 1, M % 8 == 0, N % 8 == 0
  * plus 256 to order the work units column-block-major (the vocab projection's order).
- * a [M, K] bf16, b [N, K] bf16.  Shapes: K % 64 == 0, N % 4 == 0. */
+ * a [M, K] bf16, b [N, K] bf16 unless stated.  Shapes (0..4): K % 64 == 0, N % 4 == 0. */
 int invmoe_gemm_bf16(const void* a, const void* b, int M, int N, int K, float* d, int variant,
                      void* workspace, size_t ws_bytes, void* stream);
 

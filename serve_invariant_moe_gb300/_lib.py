@@ -28,7 +28,8 @@ PROTOTYPES = {
                              _vp, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
     "moe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp]),
     "lm_logprob_kl": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
-    "rl_token_loss": (_i, [_vp, _vp, _vp, _vp, _i, _f, _f, _f, _vp, _vp, _vp, _vp, _vp]),
+    "rl_token_loss": (_i, [_vp, _vp, _vp, _vp, _i, _f, _f, _f, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "lm_head_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "invmoe_gemm_bf16": (_i, [_vp, _vp, _i, _i, _i, _vp, _i, _vp, _sz, _vp]),
     "invmoe_debug_timeout_probe": (_i, [_vp, _sz, _i, _vp]),
     "invmoe_profile_enable": (_i, [_i]),

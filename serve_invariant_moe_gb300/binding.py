@@ -187,19 +187,59 @@ def rl_token_loss(logp_train, logp_rollout, advantage, logp_old=None, beta=2.0, 
     out = dict(loss=torch.empty(T, dtype=torch.float32, device=dev),
                loss_mean=torch.empty(1, dtype=torch.float32, device=dev),
                icepop_mask=torch.empty(T, dtype=torch.uint8, device=dev),
-               dis_weight=torch.empty(T, dtype=torch.float32, device=dev))
+               dis_weight=torch.empty(T, dtype=torch.float32, device=dev),
+               grad_logp=torch.empty(T, dtype=torch.float32, device=dev))
     check(lib().rl_token_loss(_p(logp_train), _p(logp_old), _p(logp_rollout), _p(advantage), T, float(beta),
                               float(eps_low), float(eps_high), _p(out["icepop_mask"]), _p(out["dis_weight"]),
-                              _p(out["loss"]), _p(out["loss_mean"]), _stream()))
+                              _p(out["loss"]), _p(out["loss_mean"]), _p(out["grad_logp"]), _stream()))
     return out
 
 
+def lm_head_backward(hidden, w_vocab, target, lse, grad_logp, workspace, dlogits=None, d_hidden=True,
+                     d_wvocab=True):
+    """Head backward: dlogits [T, V] bf16, d_hidden [T, H] fp32, d_wvocab [V, H] fp32.
+
+    d_hidden / d_wvocab: a tensor to write into, True to allocate one, False to skip it."""
+    T, H = hidden.shape
+    V = w_vocab.shape[0]
+    dev = hidden.device
+    _req(hidden, torch.bfloat16, "hidden")
+    _req(w_vocab, torch.bfloat16, "w_vocab", (V, H))
+    _req(target, torch.int32, "target", (T,))
+    _req(lse, torch.float32, "lse", (T,))
+    _req(grad_logp, torch.float32, "grad_logp", (T,))
+    _req(workspace, torch.uint8, "workspace")
+    dlogits = torch.empty((T, V), dtype=torch.bfloat16, device=dev) if dlogits is None else dlogits
+    _req(dlogits, torch.bfloat16, "dlogits", (T, V))
+    if d_hidden is True:
+        d_hidden = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if d_wvocab is True:
+        d_wvocab = torch.empty((V, H), dtype=torch.float32, device=dev)
+    d_hidden = None if d_hidden is False else d_hidden
+    d_wvocab = None if d_wvocab is False else d_wvocab
+    if d_hidden is not None:
+        _req(d_hidden, torch.float32, "d_hidden", (T, H))
+    if d_wvocab is not None:
+        _req(d_wvocab, torch.float32, "d_wvocab", (V, H))
+    check(lib().lm_head_backward(_p(hidden), _p(w_vocab), _p(target), _p(lse), _p(grad_logp), T, H, V,
+                                 _p(dlogits), _p(d_hidden), _p(d_wvocab), _p(workspace), workspace.numel(),
+                                 _stream()))
+    return dict(dlogits=dlogits, d_hidden=d_hidden, d_wvocab=d_wvocab)
+
+
 def gemm_bf16(a, b, workspace, variant=0, out=None):
-    """Diagnostic: the dense tcgen05 GEMM engine alone, d = a @ b^T in fp32."""
-    M, K = a.shape
-    N = b.shape[0]
+    """Diagnostic: the dense tcgen05 GEMM engine alone, d = a @ b^T in fp32.
+
+    variant 5 takes b as [K, N] (d = a @ b); variant 6 takes a as [K, M] and b as
+    [K, N] (d = a^T @ b)."""
+    v = int(variant) & 0xff
+    if v == 6:
+        K, M = a.shape
+    else:
+        M, K = a.shape
+    N = b.shape[1] if v in (5, 6) else b.shape[0]
     _req(a, torch.bfloat16, "a")
-    _req(b, torch.bfloat16, "b", (N, K))
+    _req(b, torch.bfloat16, "b", (K, N) if v in (5, 6) else (N, K))
     out = torch.empty((M, N), dtype=torch.float32, device=a.device) if out is None else out
     _req(out, torch.float32, "out", (M, N))
     check(lib().invmoe_gemm_bf16(_p(a), _p(b), M, N, K, _p(out), int(variant), _p(workspace), workspace.numel(),

@@ -117,7 +117,7 @@ using namespace invmoe;
 
 extern "C" {
 
-int invmoe_version(void) { return 100; }
+int invmoe_version(void) { return 110; }
 
 const char* invmoe_last_error(void) { return g_last_error; }
 
@@ -323,9 +323,62 @@ int lm_logprob_kl(const void* hidden, const void* w_vocab, const int32_t* target
   return lse_merge_launch(part, tgt_logit, target, rollout_logp, T, V, beta, logp, lse, k3, mask, st);
 }
 
+int lm_head_backward(const void* hidden, const void* w_vocab, const int32_t* target, const float* lse,
+                     const float* grad_logp, int T, int H, int V, void* dlogits, float* d_hidden, float* d_wvocab,
+                     void* workspace, size_t ws_bytes, void* stream) {
+  REQUIRE(T >= 0 && H > 0 && V > 0, INVMOE_ERR_INVALID_ARG, "bad sizes");
+  REQUIRE(H % 64 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "H=%d is not a multiple of 64", H);
+  REQUIRE(V % 8 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "V=%d is not a multiple of 8", V);
+  REQUIRE_PTR(workspace);
+  REQUIRE(ws_bytes >= kStatusBytes, INVMOE_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
+  if (T == 0) {
+    // no token: d_wvocab is a sum over nothing
+    if (d_wvocab != nullptr)
+      return check_cuda(cudaMemsetAsync(d_wvocab, 0, static_cast<size_t>(V) * H * sizeof(float),
+                                        static_cast<cudaStream_t>(stream)),
+                        "cudaMemsetAsync");
+    return INVMOE_OK;
+  }
+  REQUIRE_PTR(hidden); REQUIRE_PTR(w_vocab); REQUIRE_PTR(target); REQUIRE_PTR(lse); REQUIRE_PTR(grad_logp);
+  REQUIRE_PTR(dlogits);
+  REQUIRE_ALIGNED(hidden); REQUIRE_ALIGNED(w_vocab); REQUIRE_ALIGNED(workspace); REQUIRE_ALIGNED(dlogits);
+  if (d_hidden) REQUIRE_ALIGNED(d_hidden);
+  if (d_wvocab) REQUIRE_ALIGNED(d_wvocab);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // dz: the forward's vocabulary projection (same engine, tile and order) with the gradient epilogue
+  GemmCall g{};
+  g.name = "lm_head_dlogits";
+  g.variant = GV_PAIR_DLOGITS;
+  g.A = hidden; g.a_rows = T; g.B = w_vocab; g.b_rows = V; g.K = H; g.N = V; g.M = T; g.G = 0;
+  g.n_major = 1; g.m_group = 16; g.out = dlogits; g.ldo = V; g.status = status_word(workspace);
+  g.target = target; g.row_lse = lse; g.row_scale = grad_logp;
+  int rc = gemm_run(g, st);
+  if (rc) return rc;
+  if (d_hidden) {
+    // d_hidden = dz [T, V] (K-major) x w_vocab [V, H] (MN-major); a row chunk's
+    // column blocks are consecutive units, so they stream the same dz rows together
+    GemmCall b{};
+    b.name = "lm_head_dhidden";
+    b.variant = GV_PAIR_F32_BMN;
+    b.A = dlogits; b.a_rows = T; b.B = w_vocab; b.b_rows = H; b.K = V; b.N = H; b.M = T; b.G = 0;
+    b.out = d_hidden; b.ldo = H; b.status = status_word(workspace);
+    if ((rc = gemm_run(b, st))) return rc;
+  }
+  if (d_wvocab) {
+    // d_wvocab = dz^T: dz [T, V] read MN-major as a [V x T] operand, hidden [T, H] MN-major
+    GemmCall w{};
+    w.name = "lm_head_dwvocab";
+    w.variant = GV_PAIR_F32_AMN_BMN;
+    w.A = dlogits; w.a_rows = V; w.B = hidden; w.b_rows = H; w.K = T; w.N = H; w.M = V; w.G = 0;
+    w.out = d_wvocab; w.ldo = H; w.status = status_word(workspace);
+    if ((rc = gemm_run(w, st))) return rc;
+  }
+  return INVMOE_OK;
+}
+
 int rl_token_loss(const float* logp_train, const float* logp_old, const float* logp_rollout, const float* advantage,
                   int T, float beta, float eps_low, float eps_high, uint8_t* icepop_mask, float* dis_weight,
-                  float* loss, float* loss_mean, void* stream) {
+                  float* loss, float* loss_mean, float* grad_logp, void* stream) {
   REQUIRE(T >= 0, INVMOE_ERR_INVALID_ARG, "T must be >= 0");
   REQUIRE(beta >= 1.0f, INVMOE_ERR_INVALID_ARG, "beta must be >= 1");
   REQUIRE(eps_low >= 0.0f && eps_low < 1.0f && eps_high >= 0.0f, INVMOE_ERR_INVALID_ARG,
@@ -333,17 +386,23 @@ int rl_token_loss(const float* logp_train, const float* logp_old, const float* l
   if (T == 0) return INVMOE_OK;
   REQUIRE_PTR(logp_train); REQUIRE_PTR(logp_rollout); REQUIRE_PTR(advantage); REQUIRE_PTR(loss);
   return rl_loss_launch(logp_train, logp_old, logp_rollout, advantage, T, beta, eps_low, eps_high, icepop_mask,
-                        dis_weight, loss, loss_mean, static_cast<cudaStream_t>(stream));
+                        dis_weight, loss, loss_mean, grad_logp, static_cast<cudaStream_t>(stream));
 }
 
 int invmoe_gemm_bf16(const void* a, const void* b, int M, int N, int K, float* d, int variant, void* workspace,
                      size_t ws_bytes, void* stream) {
   REQUIRE(M >= 0 && N > 0 && K > 0, INVMOE_ERR_INVALID_ARG, "bad sizes");
-  REQUIRE(K % 64 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 64", K);
-  REQUIRE(N % 4 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "N=%d is not a multiple of 4", N);
   const int n_major = (variant >> 8) & 1;
   variant &= 0xff;
-  REQUIRE(variant >= 0 && variant <= 4, INVMOE_ERR_INVALID_ARG, "variant must be 0..4 (+256 for n-major)");
+  REQUIRE(variant >= 0 && variant <= 6, INVMOE_ERR_INVALID_ARG, "variant must be 0..6 (+256 for n-major)");
+  if (variant <= 4) {
+    REQUIRE(K % 64 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 64", K);
+    REQUIRE(N % 4 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "N=%d is not a multiple of 4", N);
+  } else {
+    REQUIRE(N % 8 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "N=%d is not a multiple of 8", N);
+    if (variant == 5) REQUIRE(K % 8 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 8", K);
+    if (variant == 6) REQUIRE(M % 8 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "M=%d is not a multiple of 8", M);
+  }
   REQUIRE_PTR(workspace);
   REQUIRE(ws_bytes >= kStatusBytes, INVMOE_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
   if (M == 0) return INVMOE_OK;
@@ -351,7 +410,8 @@ int invmoe_gemm_bf16(const void* a, const void* b, int M, int N, int K, float* d
   REQUIRE_ALIGNED(a); REQUIRE_ALIGNED(b); REQUIRE_ALIGNED(d);
   GemmCall g{};
   g.name = "gemm_bf16";
-  g.variant = variant == 4 ? GV_PAIR_F32 : static_cast<GemmVariant>(variant);
+  g.variant = variant == 4 ? GV_PAIR_F32 : variant == 5 ? GV_PAIR_F32_BMN : variant == 6 ? GV_PAIR_F32_AMN_BMN
+                                                                                 : static_cast<GemmVariant>(variant);
   g.A = a; g.a_rows = M; g.B = b; g.b_rows = N; g.K = K; g.N = N; g.M = M; g.G = 0;
   g.n_major = n_major;
   g.out = d; g.ldo = N; g.status = status_word(workspace);

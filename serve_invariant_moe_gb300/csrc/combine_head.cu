@@ -127,7 +127,7 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, const float* _
 __global__ void rl_token_kernel(const float* __restrict__ lt, const float* __restrict__ lo,
                                 const float* __restrict__ lr, const float* __restrict__ adv, int T, float beta,
                                 float el, float eh, uint8_t* __restrict__ mask, float* __restrict__ dis,
-                                float* __restrict__ loss) {
+                                float* __restrict__ loss, float* __restrict__ grad) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   const float rho = expf(__fsub_rn(lt[t], lr[t]));
@@ -139,6 +139,12 @@ __global__ void rl_token_kernel(const float* __restrict__ lt, const float* __res
   loss[t] = m ? -obj : 0.0f;
   if (mask != nullptr) mask[t] = m ? 1 : 0;
   if (dis != nullptr) dis[t] = (lo_clip < rho && rho < hi_clip) ? rho : 0.0f;
+  if (grad != nullptr) {
+    // d mean / d logp_train with the mask held fixed: -(r A) / T where the unclipped term is the minimum
+    const float ra = __fmul_rn(r, a);
+    const bool unclipped = ra <= __fmul_rn(fminf(fmaxf(r, lo_clip), hi_clip), a);
+    grad[t] = (m && unclipped) ? -__fdiv_rn(ra, static_cast<float>(T)) : 0.0f;
+  }
 }
 
 // Mean of loss[0..T) in a fixed order: thread i of one 1024-thread block adds
@@ -210,11 +216,12 @@ int lse_merge_launch(const float2* partials, const float* tgt_logit, const int32
 }
 
 int rl_loss_launch(const float* lt, const float* lo, const float* lr, const float* adv, int T, float beta,
-                   float el, float eh, uint8_t* mask, float* dis, float* loss, float* loss_mean, cudaStream_t st) {
+                   float el, float eh, uint8_t* mask, float* dis, float* loss, float* loss_mean, float* grad,
+                   cudaStream_t st) {
   int rc;
   {
     ProfScope prof("rl_token_loss", st);
-    rl_token_kernel<<<(T + 255) / 256, 256, 0, st>>>(lt, lo, lr, adv, T, beta, el, eh, mask, dis, loss);
+    rl_token_kernel<<<(T + 255) / 256, 256, 0, st>>>(lt, lo, lr, adv, T, beta, el, eh, mask, dis, loss, grad);
     if ((rc = check_cuda(cudaGetLastError(), "rl_token_kernel"))) return rc;
   }
   if (loss_mean == nullptr) return INVMOE_OK;

@@ -45,6 +45,34 @@ int make_tmap(CUtensorMap* m, const void* base, long long inner, long long rows,
   return INVMOE_OK;
 }
 
+GemmParams make_params(const GemmCall& c, int nb_cols) {
+  GemmParams p{};
+  p.K = c.K;
+  p.N = c.N;
+  p.n_blocks = (c.N + nb_cols - 1) / nb_cols;
+  p.M = c.M;
+  p.G = c.G;
+  p.counts = c.counts;
+  p.offsets = c.offsets;
+  p.b_group_rows = c.b_group_rows;
+  p.b_up_rows = c.b_up_rows;
+  p.n_major = c.n_major;
+  p.out = c.out;
+  p.ldo = c.ldo;
+  p.status = c.status;
+  // the dynamic-schedule counter lives in the workspace's status block, after the status word
+  p.sched = reinterpret_cast<int*>(reinterpret_cast<char*>(c.status) + 64);
+  p.timeout_ns = kTimeoutNs;
+  p.part = c.part;
+  p.nch = (c.N + 255) / 256;
+  p.target = c.target;
+  p.tgt_logit = c.tgt_logit;
+  p.m_group = c.m_group > 0 ? c.m_group : (1 << 30);
+  p.row_lse = c.row_lse;
+  p.row_scale = c.row_scale;
+  return p;
+}
+
 template <int BN, int MT, int EPI, int STAGES>
 int launch(const GemmCall& c, cudaStream_t st) {
   using S = GemmShape<BN, MT, EPI, STAGES>;
@@ -68,29 +96,7 @@ int launch(const GemmCall& c, cudaStream_t st) {
   int sms = 0;
   if ((rc = device_sm_count(&sms))) return rc;
 
-  GemmParams p;
-  p.K = c.K;
-  p.N = c.N;
-  const int nb_cols = (EPI == EPI_SWIGLU) ? BN / 2 : BN;
-  p.n_blocks = (c.N + nb_cols - 1) / nb_cols;
-  p.M = c.M;
-  p.G = c.G;
-  p.counts = c.counts;
-  p.offsets = c.offsets;
-  p.b_group_rows = c.b_group_rows;
-  p.b_up_rows = c.b_up_rows;
-  p.n_major = c.n_major;
-  p.out = c.out;
-  p.ldo = c.ldo;
-  p.status = c.status;
-  // the dynamic-schedule counter lives in the workspace's status block, after the status word
-  p.sched = reinterpret_cast<int*>(reinterpret_cast<char*>(c.status) + 64);
-  p.timeout_ns = kTimeoutNs;
-  p.part = c.part;
-  p.nch = (c.N + 255) / 256;
-  p.target = c.target;
-  p.tgt_logit = c.tgt_logit;
-  p.m_group = c.m_group > 0 ? c.m_group : (1 << 30);
+  const GemmParams p = make_params(c, (EPI == EPI_SWIGLU) ? BN / 2 : BN);
 
   constexpr long long CH = static_cast<long long>(MT) * kBM;
   long long max_chunks = (c.G > 0) ? (c.a_rows + CH - 1) / CH + c.G : (c.M + CH - 1) / CH;
@@ -103,46 +109,24 @@ int launch(const GemmCall& c, cudaStream_t st) {
   return check_cuda(cudaGetLastError(), "tc_gemm_kernel launch");
 }
 
-GemmParams make_params(const GemmCall& c, int nb_cols) {
-  GemmParams p;
-  p.K = c.K;
-  p.N = c.N;
-  p.n_blocks = (c.N + nb_cols - 1) / nb_cols;
-  p.M = c.M;
-  p.G = c.G;
-  p.counts = c.counts;
-  p.offsets = c.offsets;
-  p.b_group_rows = c.b_group_rows;
-  p.b_up_rows = c.b_up_rows;
-  p.n_major = c.n_major;
-  p.out = c.out;
-  p.ldo = c.ldo;
-  p.status = c.status;
-  p.sched = reinterpret_cast<int*>(reinterpret_cast<char*>(c.status) + 64);
-  p.timeout_ns = kTimeoutNs;
-  p.part = c.part;
-  p.nch = (c.N + 255) / 256;
-  p.target = c.target;
-  p.tgt_logit = c.tgt_logit;
-  p.m_group = c.m_group > 0 ? c.m_group : (1 << 30);
-  return p;
-}
 
-// CTA-pair engine: clusters of 2, grid = 2 x min(units, SMs / 2).
-template <int EPI, int STAGES>
+// CTA-pair engine: clusters of 2, grid = 2 x min(units, SMs / 2).  A K-major
+// operand is [rows, K] (box 64 K x 128 rows); an MN-major one is [K, rows]
+// (box 64 rows x 64 K, two per 128-row half tile).
+template <int EPI, int STAGES, bool A_MN = false, bool B_MN = false>
 int launch_pair(const GemmCall& c, cudaStream_t st) {
   using S = PairShape<EPI, STAGES>;
   if (c.G > S::MAX_GROUPS) return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "more than %d groups", S::MAX_GROUPS);
   CUtensorMap ta, tb;
-  int rc = make_tmap(&ta, c.A, c.K, c.a_rows, kBM);
+  int rc = A_MN ? make_tmap(&ta, c.A, c.a_rows, c.K, 64) : make_tmap(&ta, c.A, c.K, c.a_rows, kBM);
   if (rc) return rc;
-  rc = make_tmap(&tb, c.B, c.K, c.b_rows, kBM);
+  rc = B_MN ? make_tmap(&tb, c.B, c.b_rows, c.K, 64) : make_tmap(&tb, c.B, c.K, c.b_rows, kBM);
   if (rc) return rc;
   int dev = 0;
   if ((rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice"))) return rc;
   static bool attr_set[64] = {};
   if (dev < 64 && !attr_set[dev]) {
-    rc = check_cuda(cudaFuncSetAttribute(tc_gemm_pair_kernel<EPI, STAGES>,
+    rc = check_cuda(cudaFuncSetAttribute(tc_gemm_pair_kernel<EPI, STAGES, A_MN, B_MN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES),
                     "cudaFuncSetAttribute");
     if (rc) return rc;
@@ -170,7 +154,8 @@ int launch_pair(const GemmCall& c, cudaStream_t st) {
   cfg.numAttrs = 1;
   if ((rc = check_cuda(cudaMemsetAsync(p.sched, 0, sizeof(int), st), "cudaMemsetAsync"))) return rc;
   ProfScope prof(c.name ? c.name : "tc_gemm_pair", st);
-  rc = check_cuda(cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<EPI, STAGES>, ta, tb, p), "cudaLaunchKernelEx");
+  rc = check_cuda(cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<EPI, STAGES, A_MN, B_MN>, ta, tb, p),
+                  "cudaLaunchKernelEx");
   if (rc) return rc;
   return check_cuda(cudaGetLastError(), "tc_gemm_pair_kernel launch");
 }
@@ -179,7 +164,13 @@ int launch_pair(const GemmCall& c, cudaStream_t st) {
 
 int gemm_run(const GemmCall& c, cudaStream_t st) {
   if (c.a_rows <= 0 || (c.G == 0 && c.M <= 0)) return INVMOE_OK;
-  if (c.K % kBK != 0) return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 64", c.K);
+  if (c.K <= 0) return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "K=%d", c.K);
+  // the MN-major variants take any K (zero-filled tail); every other one needs K % 64 == 0
+  const bool ragged_k_ok = c.variant == GV_PAIR_F32_BMN || c.variant == GV_PAIR_F32_AMN_BMN;
+  if (!ragged_k_ok && c.K % kBK != 0)
+    return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 64", c.K);
+  if (c.variant == GV_PAIR_F32_BMN && c.K % 8 != 0)
+    return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 8 (row stride of A)", c.K);
   switch (c.variant) {
     case GV_F32_BN256_MT1: return launch<256, 1, EPI_F32, 4>(c, st);
     case GV_F32_BN256_MT2: return launch<256, 2, EPI_F32, 3>(c, st);
@@ -190,6 +181,9 @@ int gemm_run(const GemmCall& c, cudaStream_t st) {
     case GV_PAIR_F32: return launch_pair<EPI_F32, 6>(c, st);
     case GV_PAIR_LSE: return launch_pair<EPI_LSE, 6>(c, st);
     case GV_PAIR_SWIGLU: return launch_pair<EPI_SWIGLU, 6>(c, st);
+    case GV_PAIR_DLOGITS: return launch_pair<EPI_DLOGITS, 6>(c, st);
+    case GV_PAIR_F32_BMN: return launch_pair<EPI_F32, 6, false, true>(c, st);
+    case GV_PAIR_F32_AMN_BMN: return launch_pair<EPI_F32, 6, true, true>(c, st);
   }
   return set_error(INVMOE_ERR_INVALID_ARG, "unknown GEMM variant %d", (int)c.variant);
 }

@@ -45,15 +45,18 @@ enum GemmVariant : int {
   GV_LSE_BN256_MT2 = 5,    // dense vocab projection with per-chunk log-sum-exp partials
   GV_PAIR_F32 = 6,         // CTA-pair 256 x 256 tile, fp32 out
   GV_PAIR_LSE = 7,         // CTA-pair tile, log-sum-exp epilogue
-  GV_PAIR_SWIGLU = 8       // CTA-pair tile, SwiGLU epilogue
+  GV_PAIR_SWIGLU = 8,      // CTA-pair tile, SwiGLU epilogue
+  GV_PAIR_DLOGITS = 9,     // CTA-pair tile, bf16 g * (onehot - softmax) epilogue (head backward)
+  GV_PAIR_F32_BMN = 10,    // CTA-pair tile, fp32 out, B MN-major ([K, N]), any K % 8 == 0
+  GV_PAIR_F32_AMN_BMN = 11 // CTA-pair tile, fp32 out, A ([K, M]) and B ([K, N]) MN-major, any K
 };
 
 struct GemmCall {
   const char* name;    // kernel label for the profiler
   GemmVariant variant;
-  const void* A;       // [a_rows, K] bf16
+  const void* A;       // [a_rows, K] bf16 (MN-major variants: [K, a_rows])
   long long a_rows;
-  const void* B;       // [b_rows, K] bf16
+  const void* B;       // [b_rows, K] bf16 (MN-major variants: [K, b_rows])
   long long b_rows;
   int K;
   int N;               // valid output columns
@@ -71,6 +74,8 @@ struct GemmCall {
   const int* target;     // GV_LSE only
   float* tgt_logit;      // GV_LSE only
   int m_group;           // dense column-block-major order: row chunks per band (0 = all)
+  const float* row_lse;  // GV_PAIR_DLOGITS only
+  const float* row_scale;
 };
 
 int gemm_run(const GemmCall& c, cudaStream_t st);
@@ -92,7 +97,8 @@ int lse_merge_launch(const float2* partials, const float* tgt_logit, const int32
                      const float* rollout_logp, int T, int V, float beta, float* logp, float* lse, float* k3,
                      uint8_t* mask, cudaStream_t st);
 int rl_loss_launch(const float* lt, const float* lo, const float* lr, const float* adv, int T, float beta,
-                   float el, float eh, uint8_t* mask, float* dis, float* loss, float* loss_mean, cudaStream_t st);
+                   float el, float eh, uint8_t* mask, float* dis, float* loss, float* loss_mean, float* grad,
+                   cudaStream_t st);
 int timeout_probe_launch(unsigned int* status, unsigned long long limit_ns, cudaStream_t st);
 
 }  // namespace invmoe

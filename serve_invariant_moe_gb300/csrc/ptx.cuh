@@ -148,11 +148,29 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16 with bf16 A/B, fp32 D, both K-major.
+// Shared-memory matrix descriptor for an MN-major operand tile (the M or N
+// index contiguous in memory) written by TMA with 128-byte swizzle as boxes of
+// 64 MN elements (128 B) x 64 K rows, 8 KB each, stored one after another:
+//   stride byte offset  1024 B between consecutive groups of 8 K rows
+//   leading byte offset 8192 B between consecutive 64-element MN atoms (boxes)
+// A K = 16 step advances the start address by 16 rows x 128 B = 2048 B.
+constexpr uint32_t kMnBoxBytes = 64 * 64 * 2;
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(kMnBoxBytes >> 4) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16 with bf16 A/B, fp32 D.
 //   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format (1 = bf16);
-//   15/16 A/B major (0 = K); 17-22 N >> 3; 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+//   15/16 A/B major (0 = K-major, 1 = MN-major); 17-22 N >> 3; 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = false, bool b_mn = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 

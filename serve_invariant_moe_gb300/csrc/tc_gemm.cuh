@@ -42,7 +42,7 @@ namespace invmoe {
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 
-enum Epilogue : int { EPI_F32 = 0, EPI_SWIGLU = 1, EPI_LSE = 2 };
+enum Epilogue : int { EPI_F32 = 0, EPI_SWIGLU = 1, EPI_LSE = 2, EPI_DLOGITS = 3 };
 
 struct GemmParams {
   int K;                  // reduction length (multiple of 64)
@@ -66,6 +66,9 @@ struct GemmParams {
   const int* target;      // [rows] target column of each row
   float* tgt_logit;       // [rows] z[row, target[row]] (written by the block holding it)
   int m_group;            // dense column-block-major order: row chunks per band (>= 1)
+  // EPI_DLOGITS only (target as above): out = bf16 g[row] * (onehot - exp(z - lse[row]))
+  const float* row_lse;   // [rows] log-sum-exp of each row of Z
+  const float* row_scale; // [rows] upstream gradient g of each row's logprob
 };
 
 template <int BN, int MT, int EPI, int STAGES>

@@ -17,6 +17,14 @@
 // keeps two 256-column accumulators per CTA, so the epilogue of one tile
 // overlaps the main loop of the next.  The pairing changes only which SM holds
 // which row; every element's reduction is the same K-ascending chain.
+//
+// Operand majorness (A_MN / B_MN): a K-major operand is stored [rows, K] and
+// arrives as one 128-row x 64-K box per stage; an MN-major operand is stored
+// [K, rows] (its row index contiguous, as Wv is for dHs = dZ Wv, and as dZ and
+// Hs are for dWv = dZ^T Hs) and arrives as two 64-row x 64-K boxes.  Only the
+// shared-memory layout and the descriptors change; the MMAs, their K order and
+// the accumulation are the same.  A reduction length K that is not a multiple
+// of 64 is padded by the tensor map's zero fill (0 * 0 adds nothing).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -46,12 +54,21 @@ struct PairShape {
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-template <int EPI, int STAGES>
+__device__ __forceinline__ uint32_t dlogit_bf16x2(float z0, float z1, bool t0, bool t1, float lse, float g) {
+  // d = g * (onehot - p), p = exp(z - lse); the target column takes 1 - p
+  const float p0 = expf(z0 - lse), p1 = expf(z1 - lse);
+  const float d0 = __fmul_rn(g, t0 ? __fsub_rn(1.0f, p0) : -p0);
+  const float d1 = __fmul_rn(g, t1 ? __fsub_rn(1.0f, p1) : -p1);
+  return pack_bf16x2(d0, d1);
+}
+
+template <int EPI, int STAGES, bool A_MN = false, bool B_MN = false>
 __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmParams p) {
   using S = PairShape<EPI, STAGES>;
   constexpr int BN = S::BN;
+  static_assert(!(B_MN && EPI == EPI_SWIGLU), "SwiGLU reads gate/up row blocks of a K-major B");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -138,7 +155,7 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int total_chunks = *s_total;
   const int total_units = total_chunks * p.n_blocks;
-  const int num_kb = p.K / kBK;
+  const int num_kb = (p.K + kBK - 1) / kBK;
   WaitCtl wc{s_abort, p.status, p.timeout_ns};
   const uint32_t peer_abort = mapa_shared(smem_u32(const_cast<int*>(s_abort)), peer);
   const uint32_t qempty_leader0 = mapa_shared(smem_u32(&qempty_bar[0]), 0);
@@ -185,8 +202,18 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
           uint8_t* st = ring + stage * S::STAGE_BYTES;
           const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * S::STAGE_BYTES);
-          tma_load_2d_pair(st, &tmA, fb, kb * kBK, a_row);
-          tma_load_2d_pair(st + S::TILE_BYTES, &tmB, fb, kb * kBK, b_row);
+          if (A_MN) {
+            tma_load_2d_pair(st, &tmA, fb, a_row, kb * kBK);
+            tma_load_2d_pair(st + kMnBoxBytes, &tmA, fb, a_row + 64, kb * kBK);
+          } else {
+            tma_load_2d_pair(st, &tmA, fb, kb * kBK, a_row);
+          }
+          if (B_MN) {
+            tma_load_2d_pair(st + S::TILE_BYTES, &tmB, fb, b_row, kb * kBK);
+            tma_load_2d_pair(st + S::TILE_BYTES + kMnBoxBytes, &tmB, fb, b_row + 64, kb * kBK);
+          } else {
+            tma_load_2d_pair(st + S::TILE_BYTES, &tmB, fb, kb * kBK, b_row);
+          }
           filled_phase[stage] = static_cast<int>(phase);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -202,7 +229,10 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader only)
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t IDESC = idesc_bf16_f32(2 * kBM, BN);
+      constexpr uint32_t IDESC = idesc_bf16_f32(2 * kBM, BN, A_MN, B_MN);
+      // per K = 16 step: +32 B inside a K-major swizzle row, +2048 B (16 rows) MN-major; encoded >> 4
+      constexpr uint64_t A_STEP = A_MN ? 128u : 2u;
+      constexpr uint64_t B_STEP = B_MN ? 128u : 2u;
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -223,11 +253,12 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
           if (!mbar_wait(&full_bar[stage], phase, wc)) { ok = false; break; }
           tc_fence_after();
           uint8_t* st = ring + stage * S::STAGE_BYTES;
-          const uint64_t adesc = sdesc_k_sw128(smem_u32(st));
-          const uint64_t bdesc = sdesc_k_sw128(smem_u32(st + S::TILE_BYTES));
+          const uint64_t adesc = A_MN ? sdesc_mn_sw128(smem_u32(st)) : sdesc_k_sw128(smem_u32(st));
+          const uint64_t bdesc = B_MN ? sdesc_mn_sw128(smem_u32(st + S::TILE_BYTES))
+                                      : sdesc_k_sw128(smem_u32(st + S::TILE_BYTES));
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_bf16_pair(d0, adesc + 2u * kk, bdesc + 2u * kk, IDESC, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16_pair(d0, adesc + A_STEP * kk, bdesc + B_STEP * kk, IDESC, (kb | kk) != 0 ? 1u : 0u);
           umma_commit_pair(&empty_bar[stage], 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -315,6 +346,32 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
           if (valid) {
             p.part[row * p.nch + U.nb] = make_float2(m, sum);
             if (tg >= 0 && tg < BN && n0 + tg < p.N) p.tgt_logit[row] = tv;
+          }
+        }
+      } else if (EPI == EPI_DLOGITS) {
+        // one bf16 gradient row segment per thread; N is a multiple of 8, so each
+        // 8-column group is either wholly inside the matrix or wholly past it
+        const int n0 = U.nb * BN;
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + row * p.ldo + n0;
+        const float lse = valid ? __ldg(p.row_lse + row) : 0.0f;
+        const float g = valid ? __ldg(p.row_scale + row) : 0.0f;
+        const int tg = valid ? __ldg(p.target + row) - n0 : -1;
+#pragma unroll 1
+        for (int c = half; c < BN / 32; c += 2) {
+          uint32_t v[32];
+          tmem_ld32(tbase + c * 32, v);
+          tmem_ld_wait();
+          if (valid) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              packed[j] = dlogit_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]),
+                                        tg == c * 32 + 2 * j, tg == c * 32 + 2 * j + 1, lse, g);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (n0 + c * 32 + j * 8 < p.N)
+                *reinterpret_cast<uint4*>(orow + c * 32 + j * 8) =
+                    make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
           }
         }
       } else if (EPI == EPI_F32) {

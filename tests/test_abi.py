@@ -65,3 +65,22 @@ def test_validation_rejects_before_any_launch(lib):
     assert rc == -3
     rc = lib.invmoe_debug_timeout_probe(ctypes.c_void_p(256), 4096, 0, null)
     assert rc == -1
+    # head backward: vocabulary not a multiple of 8, hidden not a multiple of 64, no workspace
+    rc = lib.lm_head_backward(null, null, null, null, null, 4, 256, 1001, null, null, null, ctypes.c_void_p(256),
+                              4096, null)
+    assert rc == -2 and b"V=1001" in lib.invmoe_last_error()
+    rc = lib.lm_head_backward(null, null, null, null, null, 4, 100, 1024, null, null, null, ctypes.c_void_p(256),
+                              4096, null)
+    assert rc == -2
+    rc = lib.lm_head_backward(null, null, null, null, null, 4, 256, 1024, null, null, null, null, 0, null)
+    assert rc == -1
+    rc = lib.lm_head_backward(null, null, null, null, null, 4, 256, 1024, null, null, null, ctypes.c_void_p(256),
+                              4096, null)
+    assert rc == -1                                   # missing input pointers
+    # MN-major GEMM test entry: shape rules of variants 5 and 6
+    rc = lib.invmoe_gemm_bf16(null, null, 64, 64, 12, null, 5, ctypes.c_void_p(256), 4096, null)
+    assert rc == -2
+    rc = lib.invmoe_gemm_bf16(null, null, 12, 64, 64, null, 6, ctypes.c_void_p(256), 4096, null)
+    assert rc == -2
+    rc = lib.invmoe_gemm_bf16(null, null, 64, 64, 64, null, 7, ctypes.c_void_p(256), 4096, null)
+    assert rc == -1

@@ -35,7 +35,7 @@ def test_empty_batch_through_every_entry_point():
     assert lib.moe_combine(None, None, binding._p(plan), None, 0, H, E, k, None, None, stream) == 0
     assert lib.lm_logprob_kl(None, None, None, None, 0, H, V, 2.0, None, None, None, None, None,
                              binding._p(ws), ws.numel(), stream) == 0
-    assert lib.rl_token_loss(None, None, None, None, 0, 2.0, 0.2, 0.28, None, None, None, None, stream) == 0
+    assert lib.rl_token_loss(None, None, None, None, 0, 2.0, 0.2, 0.28, None, None, None, None, None, stream) == 0
     binding.check_status(ws)
 
 

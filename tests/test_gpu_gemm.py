@@ -80,3 +80,39 @@ def test_pair_tile_matches_oracle_and_single_cta_bits(ws, M, N, K):
     err = np.abs(d.double().cpu().numpy() - omoe.router_logits(a64, b64))
     assert (err <= dot_bound(a64, b64, K)).all()
     assert torch.equal(d, d1)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 64), (256, 256, 128), (300, 520, 192), (777, 1032, 512)])
+def test_mn_major_operands_give_the_k_major_bits(ws, M, N, K):
+    """MN-major operand tiles (b stored [K, N]; a stored [K, M]) give bit-identical
+    results to the K-major tiles of the same matrices: only the shared-memory layout
+    and the descriptors differ, not the MMAs or their order."""
+    from serve_invariant_moe_gb300 import binding
+    a = _rand((M, K), 30 + M + K)
+    b = _rand((N, K), 31 + N + K, 0.05)
+    ref = binding.gemm_bf16(a.cuda(), b.cuda(), ws, variant=4)
+    d5 = binding.gemm_bf16(a.cuda(), b.t().contiguous().cuda(), ws, variant=5)
+    binding.check_status(ws)
+    assert torch.equal(d5, ref)
+    if M % 8 == 0:
+        d6 = binding.gemm_bf16(a.t().contiguous().cuda(), b.t().contiguous().cuda(), ws, variant=6)
+        binding.check_status(ws)
+        assert torch.equal(d6, ref)
+
+
+@pytest.mark.parametrize("variant,M,N,K", [(5, 300, 264, 200), (5, 129, 64, 8), (6, 264, 520, 77),
+                                           (6, 1000, 256, 1), (6, 8, 8, 300)])
+def test_mn_major_ragged_k_matches_oracle(ws, variant, M, N, K):
+    """A reduction length that is not a multiple of 64 (zero-filled tail)."""
+    from serve_invariant_moe_gb300 import binding
+    a = _rand((M, K), 40 + M + K)
+    b = _rand((N, K), 41 + N + K, 0.05)
+    if variant == 5:
+        d = binding.gemm_bf16(a.cuda(), b.t().contiguous().cuda(), ws, variant=5)
+    else:
+        d = binding.gemm_bf16(a.t().contiguous().cuda(), b.t().contiguous().cuda(), ws, variant=6)
+    binding.check_status(ws)
+    a64, b64 = f64(a), f64(b)
+    err = np.abs(d.double().cpu().numpy() - omoe.router_logits(a64, b64))
+    bound = dot_bound(a64, b64, K)
+    assert (err <= bound).all(), f"max err/bound {(err / bound).max():.3f}"
