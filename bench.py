@@ -586,6 +586,9 @@ def run_profile_case(args):
     lm_head:  vocab-projection GEMM + LSE at T=2048, H=6144, V=32768 (Wv 403 MB, logits 268 MB).
     experts:  the grouped expert GEMMs at T=1024, H=6144, E=32, k=8, F=2048 + shared (weights 2.4 GB);
               256 token-slots per expert on average, as in the T=8192, E=256 layer.
+    head_backward: one forward for lse, then the head backward twice at T=2048, H=6144, V=32768
+              (dlogits 134 MB bf16, d_wvocab 805 MB fp32); the pair-engine launches in order are
+              lm_head_gemm_lse, then (lm_head_dlogits, lm_head_dhidden, lm_head_dwvocab) per backward.
     """
     import torch
     from serve_invariant_moe_gb300 import api, binding, build, synth
@@ -598,6 +601,17 @@ def run_profile_case(args):
         ws = binding.new_workspace(binding.workspace_size(hc.T, hc.H, V=hc.V), dev)
         for _ in range(3):
             binding.lm_logprob_kl(hidden.to(dev), wv, target.to(dev), ws)
+        binding.check_status(ws)
+    elif args.profile_case == "head_backward":
+        import dataclasses
+        hc = dataclasses.replace(synth.GLM_HEAD, T=2048, V=32768)
+        hidden, wv, target, noise, _ = synth.head_inputs(hc, dev)
+        hs, tg = hidden.to(dev), target.to(dev)
+        ws = binding.new_workspace(binding.workspace_size(hc.T, hc.H, V=hc.V), dev)
+        fwd = binding.lm_logprob_kl(hs, wv, tg, ws)
+        grad = (noise / hc.T).to(dev)
+        for _ in range(2):
+            binding.lm_head_backward(hs, wv, tg, fwd["lse"], grad, ws)
         binding.check_status(ws)
     else:
         import dataclasses
@@ -615,7 +629,7 @@ def run_profile_case(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile-case", choices=["lm_head", "experts"], default=None)
+    ap.add_argument("--profile-case", choices=["lm_head", "experts", "head_backward"], default=None)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)

@@ -71,6 +71,34 @@ struct GemmParams {
   const float* row_scale; // [rows] upstream gradient g of each row's logprob
 };
 
+// Epilogue stores.  After tcgen05.ld.32x32b each lane of a warp holds one row
+// of the tile (lane = row), so a direct store from registers writes 32 rows x
+// 16 bytes per instruction.  Instead each warp writes a 32-row x 64-byte
+// segment into its own 2 KB of shared memory and stores it back out with four
+// lanes per row: 8 rows x 64 contiguous bytes per instruction.  The 16-byte
+// chunk q of row r sits at r*64 + (q ^ ((r >> 1) & 3))*16, so both the
+// row-wise writes and the chunk-wise reads are free of bank conflicts.
+constexpr int kOutStageBytes = 32 * 64;
+
+__device__ __forceinline__ void stage_store_rows64(uint8_t* stage, const uint32_t (&v)[16], uint8_t* out_row0,
+                                                   long long ld_bytes, int rows_valid, int bytes_valid) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(stage + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) =
+        make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  __syncwarp();
+  const int q = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + (lane >> 2);
+    const uint4 w = *reinterpret_cast<const uint4*>(stage + r * 64 + ((q ^ ((r >> 1) & 3)) << 4));
+    if (r < rows_valid && q * 16 < bytes_valid)
+      *reinterpret_cast<uint4*>(out_row0 + r * ld_bytes + q * 16) = w;
+  }
+  __syncwarp();
+}
+
 template <int BN, int MT, int EPI, int STAGES>
 struct GemmShape {
   static constexpr int A_BYTES = kBM * kBK * 2;                 // 16 KB per 128-row tile
@@ -89,8 +117,9 @@ struct GemmShape {
   static constexpr int MAX_GROUPS = 1024;
   static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * ACC_STAGES + 1 + 2 * QDEPTH);
   static constexpr int MISC_BYTES = 16 + 4 * QDEPTH;
-  static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + RING_BYTES + BAR_BYTES + MISC_BYTES +
-                                    4 * (MAX_GROUPS + 1);
+  static constexpr int OSTAGE_BYTES = EPI_WARPS * kOutStageBytes;   // epilogue store staging
+  static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + RING_BYTES + OSTAGE_BYTES + BAR_BYTES +
+                                    MISC_BYTES + 4 * (MAX_GROUPS + 1);
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(EPI != EPI_LSE || (MT == 2 && BN == 256), "LSE epilogue: one tile per warp half, 256-column chunks");
   static_assert(TMEM_NEED <= 512, "TMEM");
@@ -174,7 +203,8 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + S::RING_BYTES);
+  uint8_t* ostage = smem + S::RING_BYTES;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + S::RING_BYTES + S::OSTAGE_BYTES);
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* accf_bar = empty_bar + STAGES;
   uint64_t* acce_bar = accf_bar + S::ACC_STAGES;
@@ -450,36 +480,43 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
             if (tg >= 0 && tg < BN && n0 + tg < p.N) p.tgt_logit[row] = tv;
           }
         } else if (EPI == EPI_F32) {
+          // the warp's 32 rows start at tile row q*32; lane L stores row r of them
           const int n0 = U.nb * BN;
-          float* orow = static_cast<float*>(p.out) + row * p.ldo + n0;
+          const int rows_valid = U.rows - (t * kBM + q * 32);
+          uint8_t* obase = rows_valid > 0 ? reinterpret_cast<uint8_t*>(static_cast<float*>(p.out) +
+                                                (static_cast<long long>(U.row0) + t * kBM + q * 32) * p.ldo + n0)
+                                          : nullptr;
+          uint8_t* stg = ostage + ew * kOutStageBytes;
 #pragma unroll 1
           for (int c = half; c < BN / 32; c += NPART) {
             uint32_t v[32];
             tmem_ld32(tbase + c * 32, v);
             tmem_ld_wait();
-            if (valid) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const int col = n0 + c * 32 + j * 4;
-                if (col < p.N) {
-                  float4 f = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                         __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-                  *reinterpret_cast<float4*>(orow + c * 32 + j * 4) = f;
-                }
-              }
+            if (rows_valid > 0) {
+              const int bytes_valid = (p.N - (n0 + c * 32)) * 4;
+              stage_store_rows64(stg, *reinterpret_cast<uint32_t(*)[16]>(&v[0]), obase + c * 128, p.ldo * 4,
+                                 rows_valid, bytes_valid);
+              stage_store_rows64(stg, *reinterpret_cast<uint32_t(*)[16]>(&v[16]), obase + c * 128 + 64, p.ldo * 4,
+                                 rows_valid, bytes_valid - 64);
             }
           }
         } else {
           constexpr int HALF = BN / 2;
           const int n0 = U.nb * HALF;
-          __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + row * p.ldo + n0;
+          const int rows_valid = U.rows - (t * kBM + q * 32);
+          uint8_t* obase = rows_valid > 0
+                               ? reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                            (static_cast<long long>(U.row0) + t * kBM + q * 32) * p.ldo +
+                                                            n0)
+                               : nullptr;
+          uint8_t* stg = ostage + ew * kOutStageBytes;
 #pragma unroll 1
           for (int c = half; c < HALF / 32; c += NPART) {
             uint32_t gv[32], uv[32];
             tmem_ld32(tbase + c * 32, gv);
             tmem_ld32(tbase + HALF + c * 32, uv);
             tmem_ld_wait();
-            if (valid) {
+            if (rows_valid > 0) {
               uint32_t packed[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
@@ -488,10 +525,7 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
                     __fmul_rn(silu_f32(__uint_as_float(gv[2 * j + 1])), __uint_as_float(uv[2 * j + 1]));
                 packed[j] = pack_bf16x2(h0, h1);
               }
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<uint4*>(orow + c * 32 + j * 8) =
-                    make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+              stage_store_rows64(stg, packed, obase + c * 64, p.ldo * 2, rows_valid, (p.N - (n0 + c * 32)) * 2);
             }
           }
         }

@@ -50,7 +50,9 @@ struct PairShape {
   static constexpr int MAX_GROUPS = 1024;
   static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 * ACC_STAGES + 1 + 2 * QDEPTH);
   static constexpr int MISC_BYTES = 16 + 4 * QDEPTH;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + MISC_BYTES + 4 * (MAX_GROUPS + 1);
+  static constexpr int OSTAGE_BYTES = EPI_WARPS * kOutStageBytes;   // epilogue store staging
+  static constexpr int SMEM_BYTES =
+      1024 + STAGES * STAGE_BYTES + OSTAGE_BYTES + BAR_BYTES + MISC_BYTES + 4 * (MAX_GROUPS + 1);
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -72,7 +74,8 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES);
+  uint8_t* ostage = smem + STAGES * S::STAGE_BYTES;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * S::STAGE_BYTES + S::OSTAGE_BYTES);
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* accf_bar = empty_bar + STAGES;
   uint64_t* acce_bar = accf_bar + S::ACC_STAGES;
@@ -352,57 +355,67 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
         // one bf16 gradient row segment per thread; N is a multiple of 8, so each
         // 8-column group is either wholly inside the matrix or wholly past it
         const int n0 = U.nb * BN;
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + row * p.ldo + n0;
         const float lse = valid ? __ldg(p.row_lse + row) : 0.0f;
         const float g = valid ? __ldg(p.row_scale + row) : 0.0f;
         const int tg = valid ? __ldg(p.target + row) - n0 : -1;
+        const int rows_valid = U.rows - (static_cast<int>(rank) * kBM + q * 32);
+        uint8_t* obase = rows_valid > 0
+                             ? reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                          (static_cast<long long>(U.row0) + rank * kBM + q * 32) *
+                                                              p.ldo + n0)
+                             : nullptr;
+        uint8_t* stg = ostage + ew * kOutStageBytes;
 #pragma unroll 1
         for (int c = half; c < BN / 32; c += 2) {
           uint32_t v[32];
           tmem_ld32(tbase + c * 32, v);
           tmem_ld_wait();
-          if (valid) {
+          if (rows_valid > 0) {
             uint32_t packed[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               packed[j] = dlogit_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]),
                                         tg == c * 32 + 2 * j, tg == c * 32 + 2 * j + 1, lse, g);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (n0 + c * 32 + j * 8 < p.N)
-                *reinterpret_cast<uint4*>(orow + c * 32 + j * 8) =
-                    make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+            stage_store_rows64(stg, packed, obase + c * 64, p.ldo * 2, rows_valid, (p.N - (n0 + c * 32)) * 2);
           }
         }
       } else if (EPI == EPI_F32) {
         const int n0 = U.nb * BN;
-        float* orow = static_cast<float*>(p.out) + row * p.ldo + n0;
+        const int rows_valid = U.rows - (static_cast<int>(rank) * kBM + q * 32);
+        uint8_t* obase = rows_valid > 0 ? reinterpret_cast<uint8_t*>(static_cast<float*>(p.out) +
+                                              (static_cast<long long>(U.row0) + rank * kBM + q * 32) * p.ldo + n0)
+                                        : nullptr;
+        uint8_t* stg = ostage + ew * kOutStageBytes;
 #pragma unroll 1
         for (int c = half; c < BN / 32; c += 2) {
           uint32_t v[32];
           tmem_ld32(tbase + c * 32, v);
           tmem_ld_wait();
-          if (valid) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (n0 + c * 32 + j * 4 < p.N)
-                *reinterpret_cast<float4*>(orow + c * 32 + j * 4) =
-                    make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-            }
+          if (rows_valid > 0) {
+            const int bytes_valid = (p.N - (n0 + c * 32)) * 4;
+            stage_store_rows64(stg, *reinterpret_cast<uint32_t(*)[16]>(&v[0]), obase + c * 128, p.ldo * 4,
+                               rows_valid, bytes_valid);
+            stage_store_rows64(stg, *reinterpret_cast<uint32_t(*)[16]>(&v[16]), obase + c * 128 + 64, p.ldo * 4,
+                               rows_valid, bytes_valid - 64);
           }
         }
       } else {
         constexpr int HALF = BN / 2;
         const int n0 = U.nb * HALF;
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) + row * p.ldo + n0;
+        const int rows_valid = U.rows - (static_cast<int>(rank) * kBM + q * 32);
+        uint8_t* obase = rows_valid > 0
+                             ? reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                          (static_cast<long long>(U.row0) + rank * kBM + q * 32) *
+                                                              p.ldo + n0)
+                             : nullptr;
+        uint8_t* stg = ostage + ew * kOutStageBytes;
 #pragma unroll 1
         for (int c = half; c < HALF / 32; c += 2) {
           uint32_t gv[32], uv[32];
           tmem_ld32(tbase + c * 32, gv);
           tmem_ld32(tbase + HALF + c * 32, uv);
           tmem_ld_wait();
-          if (valid) {
+          if (rows_valid > 0) {
             uint32_t packed[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -410,10 +423,7 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
               const float h1 = __fmul_rn(silu_f32(__uint_as_float(gv[2 * j + 1])), __uint_as_float(uv[2 * j + 1]));
               packed[j] = pack_bf16x2(h0, h1);
             }
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              *reinterpret_cast<uint4*>(orow + c * 32 + j * 8) =
-                  make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+            stage_store_rows64(stg, packed, obase + c * 64, p.ldo * 2, rows_valid, (p.N - (n0 + c * 32)) * 2);
           }
         }
       }
