@@ -238,3 +238,104 @@ def dispatch_plan(topk_idx: np.ndarray, E: int):
             slot_row[t, j] = fill[e]
             fill[e] += 1
     return counts, offsets, row_token, slot_row
+
+
+# ----------------------------------------------------------------------------
+# backward (the trainer's side of the same definition)
+# ----------------------------------------------------------------------------
+
+def _sigmoid(g):
+    g = np.asarray(g, np.float64)
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-g))
+
+
+def swiglu_backward(x_rows, w13, w2, F, dy, round_ops=True):
+    """Backward of one SwiGLU expert on a block of rows, float64.
+
+    Forward: g = x Wg^T, u = x Wu^T, h = silu(g) * u, y = h W2^T.  With the
+    upstream gradient dy of y:
+        dh = dy W2;  dg = dh * u * silu'(g);  du = dh * silu(g),
+        silu'(g) = s (1 + g (1 - s)),  s = sigmoid(g);
+        dx = [dg, du] W13;  dW2 = dy^T h;  dW13 = [dg, du]^T x.
+    The forward's bf16 rounding of h is a quantisation of the forward
+    numerics, not part of the function being differentiated: its gradient is
+    taken as the identity.  When round_ops, the bf16 operands of the gradient
+    products are rounded as the forward rounds h: dy is taken as given (already
+    bf16), h is the forward's rounded h, and [dg, du] is rounded to bf16.
+    Returns dict(dh, dgu, h, dx, dw13, dw2).
+    """
+    x_rows = np.asarray(x_rows, np.float64)
+    w13 = np.asarray(w13, np.float64)
+    w2 = np.asarray(w2, np.float64)
+    dy = np.asarray(dy, np.float64)
+    g = x_rows @ w13[:F].T
+    u = x_rows @ w13[F:2 * F].T
+    s = _sigmoid(g)
+    si = silu(g)
+    h = si * u
+    if round_ops:
+        h = round_to_bf16(h)
+    dh = dy @ w2
+    dg = dh * u * (s * (1.0 + g * (1.0 - s)))
+    du = dh * si
+    dgu = np.concatenate([dg, du], axis=1)
+    if round_ops:
+        dgu = round_to_bf16(dgu)
+    return dict(dh=dh, dgu=dgu, h=h, dx=dgu @ w13, dw13=dgu.T @ x_rows, dw2=dy.T @ h)
+
+
+def moe_backward(x, w_router, w13, w2, k, F, dout, ws13=None, ws2=None, F_shared=0, round_ops=True):
+    """Gradients of L = sum(dout * out) through the whole MoE layer, float64.
+
+    Forward as ``moe_forward`` (round_h = round_ops).  Backward, per token t and
+    slot j with expert e = idx[t, j], gate w_j and expert output y_j:
+        dgate_j = <dout_t, y_j>;  dy_j = w_j * dout_t  (bf16 operand when round_ops)
+        expert e: ``swiglu_backward`` on its rows;  dx_t += sum_j dx_j
+        router: the selected logits s = L[t, idx_t] give w = softmax(s), so
+            ds_j = w_j (dgate_j - sum_i w_i dgate_i),  dL[t, idx_tj] = ds_j,
+            0 for the experts not selected (the selection is piecewise
+            constant); dx_t += dL_t Wr;  dWr = dL^T x  (dL a bf16 operand when round_ops)
+        shared expert: ``swiglu_backward`` with dy = dout (bf16 operand when round_ops).
+    Returns dict(dx, dw_router, dw13, dw2, dws13, dws2, dgate, dlogits, dy, dgu, dxp, fwd).
+    """
+    x = np.asarray(x, np.float64)
+    dout = np.asarray(dout, np.float64)
+    fwd = moe_forward(x, w_router, w13, w2, k, F, ws13, ws2, F_shared, round_h=round_ops)
+    idx, gates, y = fwd["idx"], fwd["gates"], fwd["y"]
+    T, H = x.shape
+    E = np.asarray(w13).shape[0]
+    rnd = round_to_bf16 if round_ops else (lambda a: a)
+    dgate = np.einsum("th,tjh->tj", dout, y)
+    dy = rnd(gates[:, :, None] * dout[:, None, :])              # [T, k, H]
+    dx = np.zeros((T, H))
+    dxp = np.zeros((T, k, H))
+    dgu = np.zeros((T, k, 2 * F))
+    dw13 = np.zeros(np.asarray(w13).shape)
+    dw2 = np.zeros(np.asarray(w2).shape)
+    for e in range(E):
+        tok, slot = np.nonzero(idx == e)
+        if tok.size == 0:
+            continue
+        b = swiglu_backward(x[tok], w13[e], w2[e], F, dy[tok, slot], round_ops)
+        dxp[tok, slot] = b["dx"]
+        dgu[tok, slot] = b["dgu"]
+        dw13[e] = b["dw13"]
+        dw2[e] = b["dw2"]
+    for j in range(k):
+        dx += dxp[:, j]
+    ds = gates * (dgate - (gates * dgate).sum(axis=1, keepdims=True))
+    dlog = np.zeros((T, E))
+    np.put_along_axis(dlog, idx.astype(np.int64), ds, axis=1)
+    dlog = rnd(dlog)
+    wr = np.asarray(w_router, np.float64)
+    dx_router = dlog @ wr
+    dw_router = dlog.T @ x
+    dws13 = dws2 = dx_shared = None
+    if F_shared:
+        bs = swiglu_backward(x, ws13, ws2, F_shared, rnd(dout), round_ops)
+        dx_shared, dws13, dws2 = bs["dx"], bs["dw13"], bs["dw2"]
+        dx = dx + dx_shared
+    dx = dx + dx_router
+    return dict(dx=dx, dw_router=dw_router, dw13=dw13, dw2=dw2, dws13=dws13, dws2=dws2, dgate=dgate,
+                dlogits=dlog, dy=dy, dgu=dgu, dxp=dxp, dx_router=dx_router, dx_shared=dx_shared, fwd=fwd)

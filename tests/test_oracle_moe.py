@@ -237,3 +237,91 @@ def test_replay_of_own_choice_is_the_plain_forward():
         for j in range(3):
             dense += ((idx[:, j] == e) * c["gates"][:, j])[:, None] * ye
     assert np.allclose(c["out"], dense, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- backward
+
+def _bwd_case(seed=30, T=5, H=6, E=4, k=2, F=3, Fs=2):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((T, H))
+    wr = rng.standard_normal((E, H)) * 0.7
+    w13 = rng.standard_normal((E, 2 * F, H)) * 0.5
+    w2 = rng.standard_normal((E, H, F)) * 0.5
+    ws13 = rng.standard_normal((2 * Fs, H)) * 0.5
+    ws2 = rng.standard_normal((H, Fs)) * 0.5
+    dout = rng.standard_normal((T, H))
+    return x, wr, w13, w2, ws13, ws2, dout
+
+
+def test_moe_backward_central_differences():
+    """Every element of every gradient against a central difference of sum(dout * out),
+    with no bf16 rounding anywhere (the chain rule itself is what is pinned)."""
+    x, wr, w13, w2, ws13, ws2, dout = _bwd_case()
+    k, F, Fs = 2, 3, 2
+    L = moe.router_logits(x, wr)
+    srt = np.sort(L, axis=1)
+    assert np.min(srt[:, 1:] - srt[:, :-1]) > 1e-3          # no selection flips under the perturbation
+    g = moe.moe_backward(x, wr, w13, w2, k, F, dout, ws13, ws2, Fs, round_ops=False)
+
+    def f(x_, wr_, w13_, w2_, ws13_, ws2_):
+        out = moe.moe_forward(x_, wr_, w13_, w2_, k, F, ws13_, ws2_, Fs, round_h=False)["out"]
+        return float(np.sum(dout * out))
+
+    args = [x, wr, w13, w2, ws13, ws2]
+    names = ["dx", "dw_router", "dw13", "dw2", "dws13", "dws2"]
+    eps = 1e-6
+    for a_i, name in enumerate(names):
+        grad = g[name]
+        assert grad.shape == args[a_i].shape, name
+        for i in np.ndindex(args[a_i].shape):
+            ap = [a.copy() for a in args]; am = [a.copy() for a in args]
+            ap[a_i][i] += eps; am[a_i][i] -= eps
+            fd = (f(*ap) - f(*am)) / (2 * eps)
+            assert abs(fd - grad[i]) < 1e-6 * max(1.0, abs(fd)), (name, i, fd, grad[i])
+
+
+def test_moe_backward_structure():
+    x, wr, w13, w2, ws13, ws2, dout = _bwd_case(31, T=9)
+    g = moe.moe_backward(x, wr, w13, w2, 2, 3, dout, ws13, ws2, 2, round_ops=False)
+    fwd = g["fwd"]
+    # dgate is the inner product of the upstream gradient with each slot's expert output
+    assert np.allclose(g["dgate"], np.einsum("th,tjh->tj", dout, fwd["y"]), rtol=1e-14)
+    # the softmax Jacobian over the selected experts: each token's router gradient sums to 0,
+    # and experts not selected get exactly 0
+    assert np.allclose(g["dlogits"].sum(1), 0, atol=1e-14)
+    sel = np.zeros_like(g["dlogits"], bool)
+    np.put_along_axis(sel, fwd["idx"].astype(np.int64), True, axis=1)
+    assert np.all(g["dlogits"][~sel] == 0)
+    # dx is the sum of the expert, shared and router parts
+    assert np.allclose(g["dx"], g["dxp"].sum(1) + g["dx_shared"] + g["dx_router"], rtol=1e-13, atol=1e-13)
+    # an expert no token chose has zero weight gradients
+    x1, wr1 = x.copy(), wr.copy()
+    x1[:, 0] = 5.0
+    wr1[3, 0] = -100.0                                       # expert 3's logit is about -500 for every token
+    g1 = moe.moe_backward(x1, wr1, w13, w2, 2, 3, dout, round_ops=False)
+    assert not (g1["fwd"]["idx"] == 3).any()
+    assert np.all(g1["dw13"][3] == 0) and np.all(g1["dw2"][3] == 0) and np.all(g1["dw_router"][3] == 0)
+
+
+def test_moe_backward_rounded_operands_close_to_exact():
+    x, wr, w13, w2, ws13, ws2, dout = _bwd_case(32, T=40, H=16, E=6, k=3, F=8, Fs=8)
+    a = moe.moe_backward(x, wr, w13, w2, 3, 8, dout, ws13, ws2, 8, round_ops=False)
+    b = moe.moe_backward(x, wr, w13, w2, 3, 8, dout, ws13, ws2, 8, round_ops=True)
+    for name in ("dx", "dw_router", "dw13", "dw2", "dws13", "dws2"):
+        scale = np.abs(a[name]).max()
+        assert np.abs(a[name] - b[name]).max() <= 2e-2 * scale, name
+    assert np.array_equal(round_to_bf16(b["dgu"]), b["dgu"]) and np.array_equal(round_to_bf16(b["dy"]), b["dy"])
+
+
+def test_swiglu_backward_matches_torch_autograd():
+    rng = np.random.default_rng(33)
+    x = torch.from_numpy(rng.standard_normal((7, 5))).requires_grad_(True)
+    w13 = torch.from_numpy(rng.standard_normal((8, 5))).requires_grad_(True)
+    w2 = torch.from_numpy(rng.standard_normal((5, 4))).requires_grad_(True)
+    dy = torch.from_numpy(rng.standard_normal((7, 5)))
+    g, u = x @ w13[:4].T, x @ w13[4:].T
+    ((torch.nn.functional.silu(g) * u) @ w2.T * dy).sum().backward()
+    b = moe.swiglu_backward(x.detach().numpy(), w13.detach().numpy(), w2.detach().numpy(), 4, dy.numpy(),
+                            round_ops=False)
+    for name, t in (("dx", x), ("dw13", w13), ("dw2", w2)):
+        assert np.allclose(b[name], t.grad.numpy(), rtol=1e-12, atol=1e-12), name

@@ -93,7 +93,28 @@ def _pin_ppo_grad(gfn):
         assert abs(fd - gr[t]) < 1e-7
 
 
+def _pin_moe_backward(bwd):
+    rng = np.random.default_rng(8)
+    T, H, E, k, F = 4, 5, 3, 2, 3
+    x = rng.standard_normal((T, H)); wr = rng.standard_normal((E, H)) * 0.7
+    w13 = rng.standard_normal((E, 2 * F, H)) * 0.5; w2 = rng.standard_normal((E, H, F)) * 0.5
+    dout = rng.standard_normal((T, H))
+    g = bwd(x, wr, w13, w2, k, F, dout, round_ops=False)
+
+    def f(args):
+        return float(np.sum(dout * moe.moe_forward(*args, k, F, round_h=False)["out"]))
+
+    base = [x, wr, w13, w2]
+    eps = 1e-6
+    for a_i, name in enumerate(["dx", "dw_router", "dw13", "dw2"]):
+        for i in np.ndindex(base[a_i].shape):
+            ap = [a.copy() for a in base]; am = [a.copy() for a in base]
+            ap[a_i][i] += eps; am[a_i][i] -= eps
+            assert abs((f(ap) - f(am)) / (2 * eps) - g[name][i]) < 1e-6
+
+
 def test_pins_pass_on_the_real_oracle():
+    _pin_moe_backward(moe.moe_backward)
     _pin_head_backward(head.head_backward)
     _pin_ppo_grad(head.ppo_icepop_grad)
     _pin_topk(moe.topk_lowest_index)
@@ -176,7 +197,67 @@ def _ppo_grad_no_mask(lt, lo, lr, A, *a):                # ignored the IcePop ma
     return head.ppo_icepop_grad(lt, lo, lt, A, *a)
 
 
+def _with_swiglu_backward(fake):
+    """moe_backward with its per-expert SwiGLU backward replaced by ``fake``."""
+    def bwd(*a, **kw):
+        real = moe.swiglu_backward
+        moe.swiglu_backward = fake
+        try:
+            return moe.moe_backward(*a, **kw)
+        finally:
+            moe.swiglu_backward = real
+    return bwd
+
+
+def _swiglu_bwd_no_silu_slope(x_rows, w13, w2, F, dy, round_ops=True):   # silu'(g) taken as sigmoid(g)
+    x_rows = np.asarray(x_rows, np.float64); w13 = np.asarray(w13, np.float64)
+    g = x_rows @ w13[:F].T; u = x_rows @ w13[F:2 * F].T
+    s = 1.0 / (1.0 + np.exp(-g))
+    h = g * s * u
+    dh = np.asarray(dy) @ np.asarray(w2)
+    dgu = np.concatenate([dh * u * s, dh * g * s], axis=1)
+    return dict(dh=dh, dgu=dgu, h=h, dx=dgu @ w13, dw13=dgu.T @ x_rows, dw2=np.asarray(dy).T @ h)
+
+
+_REAL_SWIGLU_BACKWARD = moe.swiglu_backward
+
+
+def _swiglu_bwd_gate_up_swapped(x_rows, w13, w2, F, dy, round_ops=True):
+    b = _REAL_SWIGLU_BACKWARD(x_rows, w13, w2, F, dy, round_ops)
+    dgu = np.concatenate([b["dgu"][:, F:], b["dgu"][:, :F]], axis=1)
+    w13 = np.asarray(w13, np.float64)
+    return dict(b, dgu=dgu, dx=dgu @ w13, dw13=dgu.T @ np.asarray(x_rows, np.float64))
+
+
+def _moe_bwd_no_jacobian_centering(x, wr, w13, w2, k, F, dout, **kw):   # ds = w * dgate
+    g = moe.moe_backward(x, wr, w13, w2, k, F, dout, **kw)
+    fwd = g["fwd"]
+    ds = fwd["gates"] * g["dgate"]
+    dlog = np.zeros_like(g["dlogits"])
+    np.put_along_axis(dlog, fwd["idx"].astype(np.int64), ds, axis=1)
+    dx = g["dx"] - g["dx_router"] + dlog @ np.asarray(wr)
+    return dict(g, dx=dx, dw_router=dlog.T @ np.asarray(x))
+
+
+def _moe_bwd_unscaled_dy(x, wr, w13, w2, k, F, dout, **kw):              # forgot the gate in dy
+    E = np.asarray(w13).shape[0]
+    g = moe.moe_backward(x, wr, w13, w2, k, F, dout, **kw)
+    idx = g["fwd"]["idx"]
+    dx = g["dx"] - g["dxp"].sum(1)
+    dw13 = np.zeros_like(g["dw13"]); dw2 = np.zeros_like(g["dw2"])
+    for e in range(E):
+        tok, slot = np.nonzero(idx == e)
+        if tok.size:
+            b = moe.swiglu_backward(np.asarray(x)[tok], w13[e], w2[e], F, np.asarray(dout)[tok], False)
+            np.add.at(dx, tok, b["dx"]); dw13[e] = b["dw13"]; dw2[e] = b["dw2"]
+    return dict(g, dx=dx, dw13=dw13, dw2=dw2)
+
+
 @pytest.mark.parametrize("pin, wrong", [
+    (_pin_moe_backward, _with_swiglu_backward(_swiglu_bwd_no_silu_slope)),
+    (_pin_moe_backward, _with_swiglu_backward(_swiglu_bwd_gate_up_swapped)),
+    (_pin_moe_backward, _moe_bwd_no_jacobian_centering),
+    (_pin_moe_backward, _moe_bwd_unscaled_dy),
     (_pin_head_backward, _hb_sign_flipped),
     (_pin_head_backward, _hb_no_onehot),
     (_pin_head_backward, _hb_unscaled),
