@@ -258,6 +258,68 @@ int lm_head_backward(const void* hidden, const void* w_vocab, const int32_t* tar
                      float* d_wvocab, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * MoE layer backward: moe_combine_backward, then moe_grouped_ffn_backward, then
+ * moe_route_backward.
+ *
+ * The trainer's side of the same definition ("位级一致：前沿训练的差异化关键",
+ * section "端到端零 KLD").  For the upstream gradient dout [T, H] fp32 of the
+ * layer output, with the forward's routing (topk_idx, topk_w, plan), permuted
+ * rows xp and per-slot expert outputs y:
+ *   dgate[t,j] = <dout[t], y[slot_row[t,j]]>;  dy[slot_row[t,j]] = bf16(topk_w[t,j] * dout[t])
+ *   expert e, on its rows:  dh = dy W2_e;  g, u recomputed (the forward's tile
+ *     and K order); dg = (dh*u) * s(1 + g(1 - s)), du = dh * silu(g), s = sigmoid(g),
+ *     [dg | du] rounded to bf16 (the forward's h is taken as silu(g)*u: its bf16
+ *     rounding is not differentiated);  dxp = [dg | du] W13_e;
+ *     dW2_e = dy^T h,  dW13_e = [dg | du]^T xp, over the expert's rows only
+ *   shared expert: the same with dy = bf16(dout) and x
+ *   router: ds_j = w_j (dgate_j - sum_i w_i dgate_i) at column topk_idx[t,j] of
+ *     dlogits [T, E] (bf16, 0 elsewhere);  dx_router = dlogits W_router,
+ *     dW_router = dlogits^T x
+ *   dx[t] = ((sum_j dxp[slot_row[t,j]]) + dx_shared[t]) + dx_router[t]  (slots in rank order)
+ * Every output element is reduced in one fixed order by one CTA (no split
+ * reduction, no atomics): repeated calls give identical bits, and dx rows and
+ * the per-slot rows depend on their own token only (batch-invariant); the
+ * weight gradients are sums over the batch by definition.
+ * ------------------------------------------------------------------------- */
+
+/* Workspace for moe_grouped_ffn_backward and moe_route_backward: status block,
+ * then (each part 256-byte aligned) dh [T*k, F] fp32, [dg | du] [T*k, 2F] bf16,
+ * recomputed h [T*k, F] bf16, the same three for the shared expert ([T, F_shared],
+ * [T, 2*F_shared], [T, F_shared]) and dlogits [T, E] bf16.  After a call those
+ * parts hold that call's intermediate results. */
+size_t invmoe_backward_workspace_size(int T, int H, int E, int k, int F, int F_shared);
+
+/* dout [T, H] fp32, y [T*k, H] fp32 (the forward's per-slot outputs), topk_w
+ * [T, k] fp32, plan from the forward; outputs dy [T*k, H] bf16 (permuted rows, as
+ * xp), dgate [T, k] fp32, dout_bf16 [T, H] bf16 (nullable: the shared expert's
+ * operand).  dgate: lane l of the slot's warp adds elements 4(l + 32i) .. +3 in
+ * ascending order, then a xor butterfly.  Shapes: H % 4 == 0, k <= 32. */
+int moe_combine_backward(const float* dout, const float* y, const float* topk_w, const int32_t* plan,
+                         int T, int H, int E, int k, void* dy, float* dgate, void* dout_bf16, void* stream);
+
+/* xp [T*k, H] bf16, plan, w13 [E, 2F, H] bf16, w2 [E, H, F] bf16, dy [T*k, H] bf16;
+ * outputs dxp [T*k, H] fp32, dw13 [E, 2F, H] fp32 and dw2 [E, H, F] fp32 (both
+ * nullable: not computed).  Shared expert (F_shared > 0): x_shared [T, H] bf16,
+ * ws13 [2*F_shared, H], ws2 [H, F_shared] bf16, dout_bf16 [T, H] bf16; outputs
+ * dx_shared [T, H] fp32, dws13 [2*F_shared, H] and dws2 [H, F_shared] fp32
+ * (nullable).  An expert no token chose gets zero weight gradients.
+ * Shapes: H % 64 == 0, F % 128 == 0, F_shared % 128 == 0, E <= 1024. */
+int moe_grouped_ffn_backward(const void* xp, const int32_t* plan, const void* w13, const void* w2,
+                             const void* dy, int T, int H, int E, int k, int F, float* dxp, float* dw13,
+                             float* dw2, const void* x_shared, const void* ws13, const void* ws2,
+                             const void* dout_bf16, int F_shared, float* dx_shared, float* dws13,
+                             float* dws2, void* workspace, size_t ws_bytes, void* stream);
+
+/* x [T, H] bf16, w_router [E, H] bf16, topk_idx [T, k] int32, topk_w [T, k] fp32,
+ * dgate [T, k] fp32, dxp [T*k, H] fp32, plan, dx_shared [T, H] fp32 (nullable);
+ * outputs dx [T, H] fp32 (the layer input's gradient) and dw_router [E, H] fp32
+ * (nullable).  Shapes: H % 64 == 0, E % 8 == 0, k <= 32. */
+int moe_route_backward(const void* x, const void* w_router, const int32_t* topk_idx, const float* topk_w,
+                       const float* dgate, const float* dxp, const int32_t* plan, const float* dx_shared,
+                       int T, int H, int E, int k, float* dx, float* dw_router, void* workspace,
+                       size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * rl_token_loss -- IcePop-masked clipped policy loss and DIS weights per token
  *
  * "GLM Post-Training Beyond SFT", sections "GRPO 在优化什么" (clipped objective

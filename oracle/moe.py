@@ -285,7 +285,8 @@ def swiglu_backward(x_rows, w13, w2, F, dy, round_ops=True):
     return dict(dh=dh, dgu=dgu, h=h, dx=dgu @ w13, dw13=dgu.T @ x_rows, dw2=dy.T @ h)
 
 
-def moe_backward(x, w_router, w13, w2, k, F, dout, ws13=None, ws2=None, F_shared=0, round_ops=True):
+def moe_backward(x, w_router, w13, w2, k, F, dout, ws13=None, ws2=None, F_shared=0, round_ops=True,
+                 expert_weights=None):
     """Gradients of L = sum(dout * out) through the whole MoE layer, float64.
 
     Forward as ``moe_forward`` (round_h = round_ops).  Backward, per token t and
@@ -297,27 +298,34 @@ def moe_backward(x, w_router, w13, w2, k, F, dout, ws13=None, ws2=None, F_shared
             0 for the experts not selected (the selection is piecewise
             constant); dx_t += dL_t Wr;  dWr = dL^T x  (dL a bf16 operand when round_ops)
         shared expert: ``swiglu_backward`` with dy = dout (bf16 operand when round_ops).
+    ``expert_weights(e) -> (w13_e, w2_e)`` may replace w13 / w2 for large
+    configurations; dw13 / dw2 are then dicts over the experts the batch used.
     Returns dict(dx, dw_router, dw13, dw2, dws13, dws2, dgate, dlogits, dy, dgu, dxp, fwd).
     """
     x = np.asarray(x, np.float64)
     dout = np.asarray(dout, np.float64)
-    fwd = moe_forward(x, w_router, w13, w2, k, F, ws13, ws2, F_shared, round_h=round_ops)
+    fwd = moe_forward(x, w_router, w13, w2, k, F, ws13, ws2, F_shared, round_h=round_ops,
+                      expert_weights=expert_weights)
     idx, gates, y = fwd["idx"], fwd["gates"], fwd["y"]
     T, H = x.shape
-    E = np.asarray(w13).shape[0]
+    E = np.asarray(w_router).shape[0]
     rnd = round_to_bf16 if round_ops else (lambda a: a)
     dgate = np.einsum("th,tjh->tj", dout, y)
     dy = rnd(gates[:, :, None] * dout[:, None, :])              # [T, k, H]
     dx = np.zeros((T, H))
     dxp = np.zeros((T, k, H))
     dgu = np.zeros((T, k, 2 * F))
-    dw13 = np.zeros(np.asarray(w13).shape)
-    dw2 = np.zeros(np.asarray(w2).shape)
+    if expert_weights is None:
+        dw13 = np.zeros(np.asarray(w13).shape)
+        dw2 = np.zeros(np.asarray(w2).shape)
+    else:
+        dw13, dw2 = {}, {}
     for e in range(E):
         tok, slot = np.nonzero(idx == e)
         if tok.size == 0:
             continue
-        b = swiglu_backward(x[tok], w13[e], w2[e], F, dy[tok, slot], round_ops)
+        w13_e, w2_e = (w13[e], w2[e]) if expert_weights is None else expert_weights(e)
+        b = swiglu_backward(x[tok], w13_e, w2_e, F, dy[tok, slot], round_ops)
         dxp[tok, slot] = b["dx"]
         dgu[tok, slot] = b["dgu"]
         dw13[e] = b["dw13"]

@@ -30,6 +30,12 @@ PROTOTYPES = {
     "lm_logprob_kl": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "rl_token_loss": (_i, [_vp, _vp, _vp, _vp, _i, _f, _f, _f, _vp, _vp, _vp, _vp, _vp, _vp]),
     "lm_head_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "invmoe_backward_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "moe_combine_backward": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
+    "moe_grouped_ffn_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp,
+                                      _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_route_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _sz,
+                                _vp]),
     "invmoe_gemm_bf16": (_i, [_vp, _vp, _i, _i, _i, _vp, _i, _vp, _sz, _vp]),
     "invmoe_debug_timeout_probe": (_i, [_vp, _sz, _i, _vp]),
     "invmoe_profile_enable": (_i, [_i]),

@@ -83,6 +83,28 @@ class MoELayer:
         res = self._run(x, self._workspace(x.shape[0]), out_bf16=out_bf16, replay_idx=replay_idx)
         return res if return_all else res["out"]
 
+    def backward(self, x: torch.Tensor, fwd: dict, dout: torch.Tensor, weight_grads: bool = True):
+        """Backward of the layer for one batch, after ``prefill(x, return_all=True)`` returned ``fwd``.
+
+        dout [T, H] fp32 -> dict(dx [T, H], dw_router, dw13, dw2, dws13, dws2) (fp32), computed by the
+        library's combine, grouped-FFN and router backward calls (every reduction in a fixed order,
+        no atomics)."""
+        w = self.w
+        T = x.shape[0]
+        ws = binding.new_workspace(binding.backward_workspace_size(T, w.H, w.E, w.k, w.F, w.F_shared),
+                                   device=x.device)
+        c = binding.moe_combine_backward(dout, fwd["y"], fwd["topk_w"], fwd["plan"], w.E, w.k,
+                                         dout_bf16=w.ws13 is not None)
+        f = binding.moe_grouped_ffn_backward(fwd["xp"], fwd["plan"], w.w13, w.w2, c["dy"], T, w.k, ws,
+                                             dw13=weight_grads, dw2=weight_grads,
+                                             x_shared=x if w.ws13 is not None else None, ws13=w.ws13, ws2=w.ws2,
+                                             dout_bf16=c["dout_bf16"], dws13=weight_grads, dws2=weight_grads)
+        r = binding.moe_route_backward(x, w.w_router, fwd["topk_idx"], fwd["topk_w"], c["dgate"], f["dxp"],
+                                       fwd["plan"], ws, dx_shared=f["dx_shared"], dw_router=weight_grads)
+        binding.check_status(ws)
+        return dict(dx=r["dx"], dw_router=r["dw_router"], dw13=f["dw13"], dw2=f["dw2"], dws13=f["dws13"],
+                    dws2=f["dws2"], dgate=c["dgate"], dy=c["dy"], dxp=f["dxp"], workspace=ws)
+
     def alloc_decode(self, max_batch: int):
         """Preallocate decode buffers for up to ``max_batch`` concurrent requests."""
         w = self.w

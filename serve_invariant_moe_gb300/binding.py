@@ -227,6 +227,86 @@ def lm_head_backward(hidden, w_vocab, target, lse, grad_logp, workspace, dlogits
     return dict(dlogits=dlogits, d_hidden=d_hidden, d_wvocab=d_wvocab)
 
 
+def backward_workspace_size(T, H, E, k, F, F_shared=0) -> int:
+    return int(lib().invmoe_backward_workspace_size(T, H, E, k, F, F_shared))
+
+
+def moe_combine_backward(dout, y, topk_w, plan, E, k, dy=None, dgate=None, dout_bf16=False):
+    """dy [T*k, H] bf16 (permuted rows), dgate [T, k] fp32, optionally dout_bf16 [T, H] bf16."""
+    T, H = dout.shape
+    dev = dout.device
+    _req(dout, torch.float32, "dout")
+    _req(y, torch.float32, "y", (T * k, H))
+    _req(topk_w, torch.float32, "topk_w", (T, k))
+    _req(plan, torch.int32, "plan")
+    dy = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev) if dy is None else dy
+    dgate = torch.empty((T, k), dtype=torch.float32, device=dev) if dgate is None else dgate
+    db = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if dout_bf16 is True else (dout_bf16 or None)
+    check(lib().moe_combine_backward(_p(dout), _p(y), _p(topk_w), _p(plan), T, H, E, k, _p(dy), _p(dgate), _p(db),
+                                     _stream()))
+    return dict(dy=dy, dgate=dgate, dout_bf16=db)
+
+
+def moe_grouped_ffn_backward(xp, plan, w13, w2, dy, T, k, workspace, dxp=None, dw13=True, dw2=True,
+                             x_shared=None, ws13=None, ws2=None, dout_bf16=None, dx_shared=None, dws13=True,
+                             dws2=True):
+    """dxp [T*k, H] fp32, dw13 [E, 2F, H], dw2 [E, H, F] (+ shared: dx_shared, dws13, dws2), all fp32.
+    A weight-gradient argument may be a tensor, True (allocate) or False (skip)."""
+    E, F2, H = w13.shape
+    F = F2 // 2
+    dev = xp.device
+    S = T * k
+    Fs = 0 if ws13 is None else ws13.shape[0] // 2
+    _req(xp, torch.bfloat16, "xp", (S, H))
+    _req(w13, torch.bfloat16, "w13")
+    _req(w2, torch.bfloat16, "w2", (E, H, F))
+    _req(dy, torch.bfloat16, "dy", (S, H))
+    _req(workspace, torch.uint8, "workspace")
+
+    def alloc(v, shape):
+        if v is True:
+            return torch.empty(shape, dtype=torch.float32, device=dev)
+        return None if v is False or v is None else v
+
+    dxp = torch.empty((S, H), dtype=torch.float32, device=dev) if dxp is None else dxp
+    dw13, dw2 = alloc(dw13, (E, 2 * F, H)), alloc(dw2, (E, H, F))
+    if Fs:
+        _req(x_shared, torch.bfloat16, "x_shared", (T, H))
+        _req(dout_bf16, torch.bfloat16, "dout_bf16", (T, H))
+        dx_shared = torch.empty((T, H), dtype=torch.float32, device=dev) if dx_shared is None else dx_shared
+        dws13, dws2 = alloc(dws13, (2 * Fs, H)), alloc(dws2, (H, Fs))
+    else:
+        dx_shared = dws13 = dws2 = None
+    check(lib().moe_grouped_ffn_backward(_p(xp), _p(plan), _p(w13), _p(w2), _p(dy), T, H, E, k, F, _p(dxp), _p(dw13),
+                                         _p(dw2), _p(x_shared), _p(ws13), _p(ws2), _p(dout_bf16), Fs, _p(dx_shared),
+                                         _p(dws13), _p(dws2), _p(workspace), workspace.numel(), _stream()))
+    return dict(dxp=dxp, dw13=dw13, dw2=dw2, dx_shared=dx_shared, dws13=dws13, dws2=dws2)
+
+
+def moe_route_backward(x, w_router, topk_idx, topk_w, dgate, dxp, plan, workspace, dx_shared=None, dx=None,
+                       dw_router=True):
+    """dx [T, H] fp32 (the layer input's gradient) and dw_router [E, H] fp32."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    k = topk_idx.shape[1]
+    dev = x.device
+    _req(x, torch.bfloat16, "x")
+    _req(w_router, torch.bfloat16, "w_router", (E, H))
+    _req(topk_idx, torch.int32, "topk_idx", (T, k))
+    _req(topk_w, torch.float32, "topk_w", (T, k))
+    _req(dgate, torch.float32, "dgate", (T, k))
+    _req(dxp, torch.float32, "dxp", (T * k, H))
+    _req(workspace, torch.uint8, "workspace")
+    dx = torch.empty((T, H), dtype=torch.float32, device=dev) if dx is None else dx
+    if dw_router is True:
+        dw_router = torch.empty((E, H), dtype=torch.float32, device=dev)
+    dw_router = None if dw_router is False else dw_router
+    check(lib().moe_route_backward(_p(x), _p(w_router), _p(topk_idx), _p(topk_w), _p(dgate), _p(dxp), _p(plan),
+                                   _p(dx_shared), T, H, E, k, _p(dx), _p(dw_router), _p(workspace),
+                                   workspace.numel(), _stream()))
+    return dict(dx=dx, dw_router=dw_router)
+
+
 def gemm_bf16(a, b, workspace, variant=0, out=None):
     """Diagnostic: the dense tcgen05 GEMM engine alone, d = a @ b^T in fp32.
 

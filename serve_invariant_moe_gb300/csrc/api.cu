@@ -31,6 +31,27 @@ size_t head_part_bytes(int T, int V) {
 }
 size_t head_ws(int T, int V) { return head_part_bytes(T, V) + align_up(static_cast<size_t>(T) * 4, 256); }
 
+// Backward scratch, in this order after the status block (each part 256-byte aligned):
+//   dh [T*k, F] fp32 | dgu [T*k, 2F] bf16 | h [T*k, F] bf16 |
+//   dh_s [T, Fs] fp32 | dgu_s [T, 2Fs] bf16 | h_s [T, Fs] bf16 | dlog [T, E] bf16
+struct BwdLayout {
+  size_t dh, dgu, h, dh_s, dgu_s, h_s, dlog, end;
+};
+BwdLayout bwd_layout(int T, int E, int k, int F, int Fs) {
+  BwdLayout L;
+  const size_t S = static_cast<size_t>(T) * (k > 0 ? k : 0);
+  size_t o = 0;
+  L.dh = o;    o += align_up(S * F * 4, 256);
+  L.dgu = o;   o += align_up(S * 2 * F * 2, 256);
+  L.h = o;     o += align_up(S * F * 2, 256);
+  L.dh_s = o;  o += align_up(static_cast<size_t>(T) * Fs * 4, 256);
+  L.dgu_s = o; o += align_up(static_cast<size_t>(T) * 2 * Fs * 2, 256);
+  L.h_s = o;   o += align_up(static_cast<size_t>(T) * Fs * 2, 256);
+  L.dlog = o;  o += align_up(static_cast<size_t>(T) * (E > 0 ? E : 0) * 2, 256);
+  L.end = o;
+  return L;
+}
+
 unsigned int* status_word(void* ws) { return static_cast<unsigned int*>(ws); }
 uint8_t* scratch(void* ws) { return static_cast<uint8_t*>(ws) + kStatusBytes; }
 }  // namespace
@@ -134,6 +155,12 @@ size_t invmoe_workspace_size(int T, int H, int E, int k, int F, int F_shared, in
   if (F_shared > 0) need = ffn_ws(T, F_shared) > need ? ffn_ws(T, F_shared) : need;
   if (V > 0) need = head_ws(T, V) > need ? head_ws(T, V) : need;
   return kStatusBytes + need;
+}
+
+size_t invmoe_backward_workspace_size(int T, int H, int E, int k, int F, int F_shared) {
+  (void)H;
+  if (T < 0 || E < 0 || k < 0 || F < 0 || F_shared < 0) return 0;
+  return kStatusBytes + bwd_layout(T, E, k, F, F_shared).end;
 }
 
 int invmoe_check(void* workspace, void* stream) {
@@ -374,6 +401,207 @@ int lm_head_backward(const void* hidden, const void* w_vocab, const int32_t* tar
     if ((rc = gemm_run(w, st))) return rc;
   }
   return INVMOE_OK;
+}
+
+int moe_combine_backward(const float* dout, const float* y, const float* topk_w, const int32_t* plan, int T, int H,
+                         int E, int k, void* dy, float* dgate, void* dout_bf16, void* stream) {
+  REQUIRE(T >= 0 && H > 0 && E > 0 && k > 0 && k <= E && k <= 32, INVMOE_ERR_INVALID_ARG, "bad sizes");
+  REQUIRE(H % 4 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "H=%d is not a multiple of 4", H);
+  if (T == 0) return INVMOE_OK;
+  REQUIRE_PTR(dout); REQUIRE_PTR(y); REQUIRE_PTR(topk_w); REQUIRE_PTR(plan); REQUIRE_PTR(dy); REQUIRE_PTR(dgate);
+  REQUIRE_ALIGNED(dout); REQUIRE_ALIGNED(y);
+  REQUIRE(((uintptr_t)dy & 7u) == 0, INVMOE_ERR_MISALIGNED, "dy is not 8-byte aligned");
+  if (dout_bf16) REQUIRE(((uintptr_t)dout_bf16 & 7u) == 0, INVMOE_ERR_MISALIGNED, "dout_bf16 is not 8-byte aligned");
+  const int32_t* slot_row = plan + 2 * E + 1 + static_cast<long long>(T) * k;
+  return combine_bwd_launch(dout, y, topk_w, slot_row, T, H, k, dy, dgate, dout_bf16,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int moe_grouped_ffn_backward(const void* xp, const int32_t* plan, const void* w13, const void* w2, const void* dy,
+                             int T, int H, int E, int k, int F, float* dxp, float* dw13, float* dw2,
+                             const void* x_shared, const void* ws13, const void* ws2, const void* dout_bf16,
+                             int F_shared, float* dx_shared, float* dws13, float* dws2, void* workspace,
+                             size_t ws_bytes, void* stream) {
+  REQUIRE(T >= 0 && H > 0 && E > 0 && k > 0 && k <= E && F > 0 && F_shared >= 0, INVMOE_ERR_INVALID_ARG,
+          "bad sizes");
+  REQUIRE(E <= 1024, INVMOE_ERR_UNSUPPORTED_SHAPE, "E=%d > 1024", E);
+  REQUIRE(H % 64 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "H=%d is not a multiple of 64", H);
+  REQUIRE(F % 128 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "F=%d is not a multiple of 128", F);
+  REQUIRE(F_shared % 128 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "F_shared=%d is not a multiple of 128", F_shared);
+  REQUIRE_PTR(workspace);
+  const BwdLayout L = bwd_layout(T, E, k, F, F_shared);
+  REQUIRE(ws_bytes >= kStatusBytes + L.end, INVMOE_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
+  REQUIRE_ALIGNED(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    // no token: the weight gradients are sums over nothing
+    int rc = INVMOE_OK;
+    if (dw13) rc = check_cuda(cudaMemsetAsync(dw13, 0, static_cast<size_t>(E) * 2 * F * H * 4, st), "memset");
+    if (!rc && dw2) rc = check_cuda(cudaMemsetAsync(dw2, 0, static_cast<size_t>(E) * H * F * 4, st), "memset");
+    if (!rc && F_shared && dws13)
+      rc = check_cuda(cudaMemsetAsync(dws13, 0, static_cast<size_t>(2) * F_shared * H * 4, st), "memset");
+    if (!rc && F_shared && dws2)
+      rc = check_cuda(cudaMemsetAsync(dws2, 0, static_cast<size_t>(H) * F_shared * 4, st), "memset");
+    return rc;
+  }
+  REQUIRE_PTR(xp); REQUIRE_PTR(plan); REQUIRE_PTR(w13); REQUIRE_PTR(w2); REQUIRE_PTR(dy); REQUIRE_PTR(dxp);
+  REQUIRE_ALIGNED(xp); REQUIRE_ALIGNED(w13); REQUIRE_ALIGNED(w2); REQUIRE_ALIGNED(dy); REQUIRE_ALIGNED(dxp);
+  if (dw13) REQUIRE_ALIGNED(dw13);
+  if (dw2) REQUIRE_ALIGNED(dw2);
+  if (F_shared) {
+    REQUIRE_PTR(x_shared); REQUIRE_PTR(ws13); REQUIRE_PTR(ws2); REQUIRE_PTR(dout_bf16); REQUIRE_PTR(dx_shared);
+    REQUIRE_ALIGNED(x_shared); REQUIRE_ALIGNED(ws13); REQUIRE_ALIGNED(ws2); REQUIRE_ALIGNED(dout_bf16);
+    REQUIRE_ALIGNED(dx_shared);
+    if (dws13) REQUIRE_ALIGNED(dws13);
+    if (dws2) REQUIRE_ALIGNED(dws2);
+  }
+  uint8_t* sc = scratch(workspace);
+  float* dh = reinterpret_cast<float*>(sc + L.dh);
+  void* dgu = sc + L.dgu;
+  void* h = sc + L.h;
+  const long long S = static_cast<long long>(T) * k;
+  const int* counts = plan;
+  const int* offsets = plan + E;
+  unsigned int* status = status_word(workspace);
+  int rc;
+  // dh = dy W2_e (group e's W2 is the stored rows [e*H, (e+1)*H) of w2 viewed as [E*H, F])
+  {
+    GemmCall g{};
+    g.name = "expert_dh";
+    g.variant = GV_F32_BN256_MT2_BMN;
+    g.A = dy; g.a_rows = S; g.B = w2; g.b_rows = F; g.b_outer = static_cast<long long>(E) * H;
+    g.K = H; g.N = F; g.G = E; g.counts = counts; g.offsets = offsets; g.b_group_rows = H;
+    g.out = dh; g.ldo = F; g.status = status;
+    if ((rc = gemm_run(g, st))) return rc;
+  }
+  // gate/up recomputed from xp (the forward's tile and K order), SwiGLU backward in the epilogue
+  {
+    GemmCall g{};
+    g.name = "expert_swiglu_bwd";
+    g.variant = GV_SWIGLU_BWD_BN256_MT2;
+    g.A = xp; g.a_rows = S; g.B = w13; g.b_rows = static_cast<long long>(E) * 2 * F;
+    g.K = H; g.N = F; g.G = E; g.counts = counts; g.offsets = offsets; g.b_group_rows = 2 * F; g.b_up_rows = F;
+    g.out = dgu; g.ldo = 2 * F; g.out2 = h; g.ldo2 = F; g.aux = dh; g.ld_aux = F; g.status = status;
+    if ((rc = gemm_run(g, st))) return rc;
+  }
+  // dxp = [dg, du] W13_e
+  {
+    GemmCall g{};
+    g.name = "expert_dx";
+    g.variant = GV_F32_BN256_MT2_BMN;
+    g.A = dgu; g.a_rows = S; g.B = w13; g.b_rows = H; g.b_outer = static_cast<long long>(E) * 2 * F;
+    g.K = 2 * F; g.N = H; g.G = E; g.counts = counts; g.offsets = offsets; g.b_group_rows = 2 * F;
+    g.out = dxp; g.ldo = H; g.status = status;
+    if ((rc = gemm_run(g, st))) return rc;
+  }
+  // weight gradients over each expert's own rows
+  if (dw2) {
+    GemmCall g{};
+    g.name = "expert_dw2";
+    g.variant = GV_F32_BN256_MT1_KGROUP;
+    g.kgroup = 1;
+    g.A = dy; g.a_rows = H; g.a_outer = S; g.B = h; g.b_rows = F; g.b_outer = S;
+    g.K = 1; g.M = H; g.N = F; g.G = E; g.counts = counts; g.offsets = offsets;
+    g.out = dw2; g.ldo = F; g.status = status;
+    if ((rc = gemm_run(g, st))) return rc;
+  }
+  if (dw13) {
+    GemmCall g{};
+    g.name = "expert_dw13";
+    g.variant = GV_F32_BN256_MT1_KGROUP;
+    g.kgroup = 1;
+    g.A = dgu; g.a_rows = 2 * F; g.a_outer = S; g.B = xp; g.b_rows = H; g.b_outer = S;
+    g.K = 1; g.M = 2 * F; g.N = H; g.G = E; g.counts = counts; g.offsets = offsets;
+    g.out = dw13; g.ldo = H; g.status = status;
+    if ((rc = gemm_run(g, st))) return rc;
+  }
+  if (F_shared) {
+    float* dh_s = reinterpret_cast<float*>(sc + L.dh_s);
+    void* dgu_s = sc + L.dgu_s;
+    void* h_s = sc + L.h_s;
+    GemmCall a{};
+    a.name = "shared_dh";
+    a.variant = GV_PAIR_F32_BMN;
+    a.A = dout_bf16; a.a_rows = T; a.B = ws2; a.b_rows = F_shared; a.K = H; a.N = F_shared; a.M = T;
+    a.out = dh_s; a.ldo = F_shared; a.status = status;
+    if ((rc = gemm_run(a, st))) return rc;
+    GemmCall b{};
+    b.name = "shared_swiglu_bwd";
+    b.variant = GV_PAIR_SWIGLU_BWD;
+    b.A = x_shared; b.a_rows = T; b.B = ws13; b.b_rows = 2 * F_shared; b.b_up_rows = F_shared;
+    b.K = H; b.N = F_shared; b.M = T;
+    b.out = dgu_s; b.ldo = 2 * F_shared; b.out2 = h_s; b.ldo2 = F_shared; b.aux = dh_s; b.ld_aux = F_shared;
+    b.status = status;
+    if ((rc = gemm_run(b, st))) return rc;
+    GemmCall c{};
+    c.name = "shared_dx";
+    c.variant = GV_PAIR_F32_BMN;
+    c.A = dgu_s; c.a_rows = T; c.B = ws13; c.b_rows = H; c.K = 2 * F_shared; c.N = H; c.M = T;
+    c.out = dx_shared; c.ldo = H; c.status = status;
+    if ((rc = gemm_run(c, st))) return rc;
+    if (dws2) {
+      GemmCall d{};
+      d.name = "shared_dw2";
+      d.variant = GV_PAIR_F32_AMN_BMN;
+      d.A = dout_bf16; d.a_rows = H; d.B = h_s; d.b_rows = F_shared; d.K = T; d.N = F_shared; d.M = H;
+      d.out = dws2; d.ldo = F_shared; d.status = status;
+      if ((rc = gemm_run(d, st))) return rc;
+    }
+    if (dws13) {
+      GemmCall e{};
+      e.name = "shared_dw13";
+      e.variant = GV_PAIR_F32_AMN_BMN;
+      e.A = dgu_s; e.a_rows = 2 * F_shared; e.B = x_shared; e.b_rows = H; e.K = T; e.N = H; e.M = 2 * F_shared;
+      e.out = dws13; e.ldo = H; e.status = status;
+      if ((rc = gemm_run(e, st))) return rc;
+    }
+  }
+  return INVMOE_OK;
+}
+
+int moe_route_backward(const void* x, const void* w_router, const int32_t* topk_idx, const float* topk_w,
+                       const float* dgate, const float* dxp, const int32_t* plan, const float* dx_shared, int T,
+                       int H, int E, int k, float* dx, float* dw_router, void* workspace, size_t ws_bytes,
+                       void* stream) {
+  REQUIRE(T >= 0 && H > 0 && E > 0 && k > 0 && k <= E && k <= 32, INVMOE_ERR_INVALID_ARG, "bad sizes");
+  REQUIRE(H % 64 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "H=%d is not a multiple of 64", H);
+  REQUIRE(E % 8 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "E=%d is not a multiple of 8", E);
+  REQUIRE_PTR(workspace);
+  const BwdLayout L = bwd_layout(T, E, k, 0, 0);
+  REQUIRE(ws_bytes >= kStatusBytes + L.end, INVMOE_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
+  REQUIRE_ALIGNED(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    if (dw_router)
+      return check_cuda(cudaMemsetAsync(dw_router, 0, static_cast<size_t>(E) * H * 4, st), "memset");
+    return INVMOE_OK;
+  }
+  REQUIRE_PTR(x); REQUIRE_PTR(w_router); REQUIRE_PTR(topk_idx); REQUIRE_PTR(topk_w); REQUIRE_PTR(dgate);
+  REQUIRE_PTR(dxp); REQUIRE_PTR(plan); REQUIRE_PTR(dx);
+  REQUIRE_ALIGNED(x); REQUIRE_ALIGNED(w_router); REQUIRE_ALIGNED(dxp); REQUIRE_ALIGNED(dx);
+  if (dx_shared) REQUIRE_ALIGNED(dx_shared);
+  if (dw_router) REQUIRE_ALIGNED(dw_router);
+  void* dlog = scratch(workspace) + L.dlog;
+  unsigned int* status = status_word(workspace);
+  int rc = router_bwd_launch(topk_idx, topk_w, dgate, T, E, k, dlog, st);
+  if (rc) return rc;
+  // router part of dx: dlog [T, E] (K = E) times w_router [E, H] read MN-major
+  GemmCall a{};
+  a.name = "router_dx";
+  a.variant = GV_PAIR_F32_BMN;
+  a.A = dlog; a.a_rows = T; a.B = w_router; a.b_rows = H; a.K = E; a.N = H; a.M = T;
+  a.out = dx; a.ldo = H; a.status = status;
+  if ((rc = gemm_run(a, st))) return rc;
+  if (dw_router) {
+    GemmCall b{};
+    b.name = "router_dw";
+    b.variant = GV_PAIR_F32_AMN_BMN;
+    b.A = dlog; b.a_rows = E; b.B = x; b.b_rows = H; b.K = T; b.N = H; b.M = E;
+    b.out = dw_router; b.ldo = H; b.status = status;
+    if ((rc = gemm_run(b, st))) return rc;
+  }
+  const int32_t* slot_row = plan + 2 * E + 1 + static_cast<long long>(T) * k;
+  return unpermute_sum_launch(dxp, slot_row, dx_shared, T, H, k, dx, st);
 }
 
 int rl_token_loss(const float* logp_train, const float* logp_old, const float* logp_rollout, const float* advantage,

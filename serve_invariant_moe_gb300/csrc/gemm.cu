@@ -70,24 +70,33 @@ GemmParams make_params(const GemmCall& c, int nb_cols) {
   p.m_group = c.m_group > 0 ? c.m_group : (1 << 30);
   p.row_lse = c.row_lse;
   p.row_scale = c.row_scale;
+  p.aux = c.aux;
+  p.ld_aux = c.ld_aux;
+  p.out2 = c.out2;
+  p.ldo2 = c.ldo2;
+  p.kgroup = c.kgroup;
   return p;
 }
 
-template <int BN, int MT, int EPI, int STAGES>
+// Single-CTA engine.  K-major operands as [rows, K]; an MN-major operand is
+// stored [outer rows, inner] with the M or N index inner (a_rows / b_rows =
+// inner extent, a_outer / b_outer = stored rows).
+template <int BN, int MT, int EPI, int STAGES, bool A_MN = false, bool B_MN = false, bool KG = false>
 int launch(const GemmCall& c, cudaStream_t st) {
   using S = GemmShape<BN, MT, EPI, STAGES>;
   if (c.G > S::MAX_GROUPS) return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "more than %d groups", S::MAX_GROUPS);
   CUtensorMap ta, tb;
-  int rc = make_tmap(&ta, c.A, c.K, c.a_rows, kBM);
+  int rc = A_MN ? make_tmap(&ta, c.A, c.a_rows, c.a_outer, 64) : make_tmap(&ta, c.A, c.K, c.a_rows, kBM);
   if (rc) return rc;
-  rc = make_tmap(&tb, c.B, c.K, c.b_rows, BN >= 128 ? 128 : BN);
+  rc = B_MN ? make_tmap(&tb, c.B, c.b_rows, c.b_outer, 64)
+            : make_tmap(&tb, c.B, c.K, c.b_rows, BN >= 128 ? 128 : BN);
   if (rc) return rc;
 
   int dev = 0;
   if ((rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice"))) return rc;
   static bool attr_set[64] = {};
   if (dev < 64 && !attr_set[dev]) {
-    rc = check_cuda(cudaFuncSetAttribute(tc_gemm_kernel<BN, MT, EPI, STAGES>,
+    rc = check_cuda(cudaFuncSetAttribute(tc_gemm_kernel<BN, MT, EPI, STAGES, A_MN, B_MN, KG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES),
                     "cudaFuncSetAttribute");
     if (rc) return rc;
@@ -96,16 +105,17 @@ int launch(const GemmCall& c, cudaStream_t st) {
   int sms = 0;
   if ((rc = device_sm_count(&sms))) return rc;
 
-  const GemmParams p = make_params(c, (EPI == EPI_SWIGLU) ? BN / 2 : BN);
+  const GemmParams p = make_params(c, (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) ? BN / 2 : BN);
 
   constexpr long long CH = static_cast<long long>(MT) * kBM;
-  long long max_chunks = (c.G > 0) ? (c.a_rows + CH - 1) / CH + c.G : (c.M + CH - 1) / CH;
+  long long max_chunks = KG ? static_cast<long long>(c.G) * ((c.M + CH - 1) / CH)
+                            : (c.G > 0) ? (c.a_rows + CH - 1) / CH + c.G : (c.M + CH - 1) / CH;
   long long max_units = max_chunks * p.n_blocks;
   if (max_units <= 0) return INVMOE_OK;
   const int grid = static_cast<int>(max_units < sms ? max_units : sms);
   if ((rc = check_cuda(cudaMemsetAsync(p.sched, 0, sizeof(int), st), "cudaMemsetAsync"))) return rc;
   ProfScope prof(c.name ? c.name : "tc_gemm", st);
-  tc_gemm_kernel<BN, MT, EPI, STAGES><<<grid, S::THREADS, S::SMEM_BYTES, st>>>(ta, tb, p);
+  tc_gemm_kernel<BN, MT, EPI, STAGES, A_MN, B_MN, KG><<<grid, S::THREADS, S::SMEM_BYTES, st>>>(ta, tb, p);
   return check_cuda(cudaGetLastError(), "tc_gemm_kernel launch");
 }
 
@@ -134,7 +144,7 @@ int launch_pair(const GemmCall& c, cudaStream_t st) {
   }
   int sms = 0;
   if ((rc = device_sm_count(&sms))) return rc;
-  const GemmParams p = make_params(c, EPI == EPI_SWIGLU ? 128 : 256);
+  const GemmParams p = make_params(c, (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) ? 128 : 256);
   constexpr long long CH = 2LL * kBM;
   long long max_chunks = (c.G > 0) ? (c.a_rows + CH - 1) / CH + c.G : (c.M + CH - 1) / CH;
   long long max_units = max_chunks * p.n_blocks;
@@ -166,7 +176,8 @@ int gemm_run(const GemmCall& c, cudaStream_t st) {
   if (c.a_rows <= 0 || (c.G == 0 && c.M <= 0)) return INVMOE_OK;
   if (c.K <= 0) return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "K=%d", c.K);
   // the MN-major variants take any K (zero-filled tail); every other one needs K % 64 == 0
-  const bool ragged_k_ok = c.variant == GV_PAIR_F32_BMN || c.variant == GV_PAIR_F32_AMN_BMN;
+  const bool ragged_k_ok = c.variant == GV_PAIR_F32_BMN || c.variant == GV_PAIR_F32_AMN_BMN ||
+                           c.variant == GV_F32_BN256_MT1_KGROUP;
   if (!ragged_k_ok && c.K % kBK != 0)
     return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "K=%d is not a multiple of 64", c.K);
   if (c.variant == GV_PAIR_F32_BMN && c.K % 8 != 0)
@@ -184,6 +195,10 @@ int gemm_run(const GemmCall& c, cudaStream_t st) {
     case GV_PAIR_DLOGITS: return launch_pair<EPI_DLOGITS, 6>(c, st);
     case GV_PAIR_F32_BMN: return launch_pair<EPI_F32, 6, false, true>(c, st);
     case GV_PAIR_F32_AMN_BMN: return launch_pair<EPI_F32, 6, true, true>(c, st);
+    case GV_F32_BN256_MT2_BMN: return launch<256, 2, EPI_F32, 3, false, true, false>(c, st);
+    case GV_SWIGLU_BWD_BN256_MT2: return launch<256, 2, EPI_SWIGLU_BWD, 3>(c, st);
+    case GV_F32_BN256_MT1_KGROUP: return launch<256, 1, EPI_F32, 4, true, true, true>(c, st);
+    case GV_PAIR_SWIGLU_BWD: return launch_pair<EPI_SWIGLU_BWD, 6>(c, st);
   }
   return set_error(INVMOE_ERR_INVALID_ARG, "unknown GEMM variant %d", (int)c.variant);
 }

@@ -48,7 +48,11 @@ enum GemmVariant : int {
   GV_PAIR_SWIGLU = 8,      // CTA-pair tile, SwiGLU epilogue
   GV_PAIR_DLOGITS = 9,     // CTA-pair tile, bf16 g * (onehot - softmax) epilogue (head backward)
   GV_PAIR_F32_BMN = 10,    // CTA-pair tile, fp32 out, B MN-major ([K, N]), any K % 8 == 0
-  GV_PAIR_F32_AMN_BMN = 11 // CTA-pair tile, fp32 out, A ([K, M]) and B ([K, N]) MN-major, any K
+  GV_PAIR_F32_AMN_BMN = 11, // CTA-pair tile, fp32 out, A ([K, M]) and B ([K, N]) MN-major, any K
+  GV_F32_BN256_MT2_BMN = 12, // grouped fp32-out, B MN-major: group g's B = stored rows [g*b_group_rows, +K)
+  GV_SWIGLU_BWD_BN256_MT2 = 13, // grouped gate+up recompute with the SwiGLU backward epilogue
+  GV_F32_BN256_MT1_KGROUP = 14, // K-grouped weight gradients: D_g = A_g^T B_g, A and B MN-major
+  GV_PAIR_SWIGLU_BWD = 15  // CTA-pair gate+up recompute with the SwiGLU backward epilogue
 };
 
 struct GemmCall {
@@ -76,6 +80,13 @@ struct GemmCall {
   int m_group;           // dense column-block-major order: row chunks per band (0 = all)
   const float* row_lse;  // GV_PAIR_DLOGITS only
   const float* row_scale;
+  const float* aux;      // SwiGLU backward: dh [rows, N] fp32, row stride ld_aux
+  long long ld_aux;
+  void* out2;            // SwiGLU backward: recomputed h (bf16, nullable), row stride ldo2
+  long long ldo2;
+  int kgroup;            // K-grouped mode (GV_F32_BN256_MT1_KGROUP)
+  long long a_outer;     // MN-major A in the single-CTA engine: stored rows
+  long long b_outer;     // MN-major B in the single-CTA engine: stored rows
 };
 
 int gemm_run(const GemmCall& c, cudaStream_t st);
@@ -100,5 +111,13 @@ int rl_loss_launch(const float* lt, const float* lo, const float* lr, const floa
                    float el, float eh, uint8_t* mask, float* dis, float* loss, float* loss_mean, float* grad,
                    cudaStream_t st);
 int timeout_probe_launch(unsigned int* status, unsigned long long limit_ns, cudaStream_t st);
+
+// ---------------------------------------------------------------- backward
+int combine_bwd_launch(const float* dout, const float* y, const float* topk_w, const int32_t* slot_row, int T,
+                       int H, int k, void* dy, float* dgate, void* dout_bf16, cudaStream_t st);
+int router_bwd_launch(const int32_t* topk_idx, const float* topk_w, const float* dgate, int T, int E, int k,
+                      void* dlog, cudaStream_t st);
+int unpermute_sum_launch(const float* dxp, const int32_t* slot_row, const float* dx_shared, int T, int H, int k,
+                         float* dx, cudaStream_t st);
 
 }  // namespace invmoe

@@ -23,6 +23,13 @@
 // streams its B tile once per K block and multiplies it against up to MT row
 // tiles, so an expert with at most MT*128 tokens reads its weights once.
 //
+// K-grouped mode (weight gradients, dW_g = A_g^T B_g): group g owns the rows
+// [offsets[g], offsets[g]+counts[g]) of two MN-major operands A [rows, M] and
+// B [rows, N]; the reduction runs over the group's rows only, and the block of
+// 64 rows that crosses the group's end has the rows past it zeroed in shared
+// memory before its MMAs (the next group's rows are never multiplied in).  A
+// group with no rows gets an all-zero block.  Output rows g*M .. g*M+M-1.
+//
 // Warp roles (192 threads, one CTA per SM, persistent over units):
 //   warp 0      TMA producer (one lane): A row tiles + B tile per K block into
 //               a STAGES-deep shared-memory ring (128-byte swizzle)
@@ -42,7 +49,7 @@ namespace invmoe {
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 
-enum Epilogue : int { EPI_F32 = 0, EPI_SWIGLU = 1, EPI_LSE = 2, EPI_DLOGITS = 3 };
+enum Epilogue : int { EPI_F32 = 0, EPI_SWIGLU = 1, EPI_LSE = 2, EPI_DLOGITS = 3, EPI_SWIGLU_BWD = 4 };
 
 struct GemmParams {
   int K;                  // reduction length (multiple of 64)
@@ -69,6 +76,13 @@ struct GemmParams {
   // EPI_DLOGITS only (target as above): out = bf16 g[row] * (onehot - exp(z - lse[row]))
   const float* row_lse;   // [rows] log-sum-exp of each row of Z
   const float* row_scale; // [rows] upstream gradient g of each row's logprob
+  // EPI_SWIGLU_BWD only: out = [dg | du] bf16 (ldo = 2N), out2 = h bf16 (ldo2, nullable),
+  // aux = dh fp32 (ld_aux); N = columns of h
+  const float* aux;
+  long long ld_aux;
+  void* out2;
+  long long ldo2;
+  int kgroup;             // 1: K-grouped mode (weight gradients); M = output rows per group
 };
 
 // Epilogue stores.  After tcgen05.ld.32x32b each lane of a warp holds one row
@@ -79,6 +93,29 @@ struct GemmParams {
 // chunk q of row r sits at r*64 + (q ^ ((r >> 1) & 3))*16, so both the
 // row-wise writes and the chunk-wise reads are free of bank conflicts.
 constexpr int kOutStageBytes = 32 * 64;
+
+// The reverse of stage_store_rows64: the warp reads a 32-row x 64-byte segment
+// with four lanes per row (rows past rows_valid and bytes past bytes_valid read
+// as zero) and each lane gets its own row's 16 words.
+__device__ __forceinline__ void stage_load_rows64(uint8_t* stage, const uint8_t* in_row0, long long ld_bytes,
+                                                  int rows_valid, int bytes_valid, uint32_t (&v)[16]) {
+  const int lane = threadIdx.x & 31;
+  const int q = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + (lane >> 2);
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (r < rows_valid && q * 16 < bytes_valid) w = __ldg(reinterpret_cast<const uint4*>(in_row0 + r * ld_bytes + q * 16));
+    *reinterpret_cast<uint4*>(stage + r * 64 + ((q ^ ((r >> 1) & 3)) << 4)) = w;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 w = *reinterpret_cast<const uint4*>(stage + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4));
+    v[4 * c] = w.x; v[4 * c + 1] = w.y; v[4 * c + 2] = w.z; v[4 * c + 3] = w.w;
+  }
+  __syncwarp();
+}
 
 __device__ __forceinline__ void stage_store_rows64(uint8_t* stage, const uint32_t (&v)[16], uint8_t* out_row0,
                                                    long long ld_bytes, int rows_valid, int bytes_valid) {
@@ -127,10 +164,14 @@ struct GemmShape {
 };
 
 struct Unit {
-  int row0;    // first A / D row of the chunk
+  int row0;    // first D row of the chunk (and first A row, except in K-grouped mode)
   int rows;    // valid rows in the chunk (1 .. MT*128)
-  int b_row;   // first B row of the column block (gate rows for SwiGLU)
+  int b_row;   // first B row of the column block (gate rows for SwiGLU), K-major B
   int nb;      // column block
+  int g;       // group
+  int a_m0;    // K-grouped: first M index of the chunk (A is MN-major)
+  int k0;      // K-grouped: first K row of the group
+  int kcount;  // K-grouped: K rows of the group
 };
 
 // Unit order.  Grouped: group by group; inside a group column-block-major, so
@@ -142,7 +183,22 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& p, const in
   constexpr int CH = MT * kBM;
   Unit U;
   int g = 0, nb;
-  if (p.G > 0) {
+  U.a_m0 = 0;
+  U.k0 = 0;
+  U.kcount = p.K;
+  if (p.kgroup) {
+    // group-major, then M chunk, then column block
+    const int mch = (p.M + CH - 1) / CH;
+    g = u / (mch * p.n_blocks);
+    const int local = u - g * mch * p.n_blocks;
+    const int c = local / p.n_blocks;
+    nb = local - c * p.n_blocks;
+    U.a_m0 = c * CH;
+    U.row0 = g * p.M + c * CH;
+    U.rows = min(CH, p.M - c * CH);
+    U.k0 = __ldg(p.offsets + g);
+    U.kcount = __ldg(p.counts + g);
+  } else if (p.G > 0) {
     const int NB = p.n_blocks;
     int lo = 0, hi = p.G;  // NB*s_prefix[lo] <= u < NB*s_prefix[hi]
     while (hi - lo > 1) {
@@ -175,9 +231,10 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmParams& p, const in
     U.row0 = chunk * CH;
     U.rows = min(CH, p.M - U.row0);
   }
-  constexpr int NB_ROWS = (EPI == EPI_SWIGLU) ? BN / 2 : BN;
+  constexpr int NB_ROWS = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) ? BN / 2 : BN;
   U.b_row = g * p.b_group_rows + nb * NB_ROWS;
   U.nb = nb;
+  U.g = g;
   return U;
 }
 
@@ -191,15 +248,73 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// SwiGLU backward for one 32-column chunk of a warp's 32 rows (lane = row):
+//   s = 1 / (1 + exp(-g)),  silu = g / (1 + exp(-g)) (the forward's own expression),
+//   h = silu * u (bit-identical to the forward's h),
+//   dg = (dh * u) * (s * (1 + g * (1 - s))),  du = dh * silu,
+// every operation rounded separately in fp32; dg, du and h are stored as bf16.
+// dh (fp32, 128 B per row) is read through the warp's staging buffer.
+__device__ __forceinline__ void swiglu_bwd_chunk(uint8_t* stg, const uint32_t (&gv)[32], const uint32_t (&uv)[32],
+                                                 const uint8_t* dh_row0, long long ld_dh_bytes, uint8_t* dg_row0,
+                                                 uint8_t* du_row0, long long ld_dgu_bytes, uint8_t* h_row0,
+                                                 long long ld_h_bytes, int rows_valid, int cols_valid) {
+  uint32_t d0[16], d1[16];
+  stage_load_rows64(stg, dh_row0, ld_dh_bytes, rows_valid, cols_valid * 4, d0);
+  stage_load_rows64(stg, dh_row0 + 64, ld_dh_bytes, rows_valid, cols_valid * 4 - 64, d1);
+  uint32_t pg[16], pu[16], ph[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float dgv[2], duv[2], hv[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int col = 2 * j + e;
+      const float g = __uint_as_float(gv[col]);
+      const float u = __uint_as_float(uv[col]);
+      const float d = __uint_as_float(col < 16 ? d0[col & 15] : d1[col & 15]);
+      const float si = silu_f32(g);
+      const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-g)));
+      const float ds = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(g, __fsub_rn(1.0f, sg))));
+      dgv[e] = __fmul_rn(__fmul_rn(d, u), ds);
+      duv[e] = __fmul_rn(d, si);
+      hv[e] = __fmul_rn(si, u);
+    }
+    pg[j] = pack_bf16x2(dgv[0], dgv[1]);
+    pu[j] = pack_bf16x2(duv[0], duv[1]);
+    ph[j] = pack_bf16x2(hv[0], hv[1]);
+  }
+  stage_store_rows64(stg, pg, dg_row0, ld_dgu_bytes, rows_valid, cols_valid * 2);
+  stage_store_rows64(stg, pu, du_row0, ld_dgu_bytes, rows_valid, cols_valid * 2);
+  if (h_row0 != nullptr) stage_store_rows64(stg, ph, h_row0, ld_h_bytes, rows_valid, cols_valid * 2);
+}
+
+// Zero K rows [rem, 64) of `nbox` consecutive MN-major boxes (64 K rows x 128 B
+// each) at `base`: the part of a K-grouped block past its group's last row.
+// All 32 lanes of the calling warp take part.
+__device__ __forceinline__ void zero_k_tail(uint8_t* base, int nbox, int rem) {
+  const int lane = threadIdx.x & 31;
+  const int per_box = (64 - rem) * 8;           // 16-byte chunks per box
+  for (int i = lane; i < nbox * per_box; i += 32) {
+    const int b = i / per_box;
+    const int c = i - b * per_box;
+    *reinterpret_cast<uint4*>(base + b * kMnBoxBytes + rem * 128 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // Work units are handed out dynamically: the producer thread takes the next
 // unit index from a global counter and publishes it through a small shared
 // queue to the MMA thread and the epilogue warps.  Which CTA computes which
 // tile therefore varies from run to run; the arithmetic of every tile does not.
-template <int BN, int MT, int EPI, int STAGES>
+// A_MN / B_MN: operand stored MN-major (see tc_gemm2.cuh).  In this engine an
+// MN-major A occurs only in K-grouped mode (KG); an MN-major B with M-grouped
+// rows takes group g's B from the stored rows [g*b_group_rows, +K).
+template <int BN, int MT, int EPI, int STAGES, bool A_MN = false, bool B_MN = false, bool KG = false>
 __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
   using S = GemmShape<BN, MT, EPI, STAGES>;
+  static_assert(A_MN == KG, "an MN-major A only in K-grouped mode, and K-grouped mode needs it");
+  static_assert(!KG || B_MN, "K-grouped mode reads both operands MN-major");
+  static_assert(!B_MN || (EPI == EPI_F32 && BN >= 64), "MN-major B: fp32 epilogue");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -247,7 +362,9 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
   // Row-chunk prefix over groups (warp 2; G <= 1024): s_prefix[g] = sum_{g'<g} ceil(counts[g'] / (MT*128)).
   constexpr int CH = MT * kBM;
   if (warp == 2) {
-    if (p.G > 0) {
+    if (KG) {
+      if (lane == 0) *s_total = p.G * ((p.M + CH - 1) / CH);
+    } else if (p.G > 0) {
       const int per = (p.G + 31) / 32;
       const int g0 = lane * per;
       int local = 0;
@@ -283,7 +400,6 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int total_chunks = *s_total;
   const int total_units = total_chunks * p.n_blocks;
-  const int num_kb = p.K / kBK;
   WaitCtl wc{s_abort, p.status, p.timeout_ns};
 
   if (warp == 0) {
@@ -310,11 +426,14 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
         const Unit U = decode_unit<MT, EPI, BN>(u, p, s_prefix, total_chunks);
         const int ntile = (U.rows + kBM - 1) / kBM;
         const uint32_t bytes = ntile * S::A_BYTES + S::B_BYTES;
+        const int num_kb = (U.kcount + kBK - 1) / kBK;
+        // MN-major B: the K row the group's B starts at
+        const int b_k0 = KG ? U.k0 : U.g * p.b_group_rows;
         bool ok = true;
         // B row blocks of 128 this unit streams (SwiGLU: gate block, up block)
         constexpr int NBB = BN >= 128 ? BN / 128 : 1;
         int brow[NBB];
-        if (EPI == EPI_SWIGLU) {
+        if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) {
           brow[0] = U.b_row;
           brow[NBB - 1] = U.b_row + p.b_up_rows;
         } else {
@@ -325,9 +444,21 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wc)) { ok = false; break; }
           uint8_t* st = ring + stage * S::STAGE_BYTES;
           mbar_arrive_expect_tx(&full_bar[stage], bytes);
-          for (int t = 0; t < ntile; ++t)
-            tma_load_2d(st + t * S::A_BYTES, &tmA, &full_bar[stage], kb * kBK, U.row0 + t * kBM);
-          if (BN >= 128) {
+          for (int t = 0; t < ntile; ++t) {
+            if (A_MN) {
+              tma_load_2d(st + t * S::A_BYTES, &tmA, &full_bar[stage], U.a_m0 + t * kBM, U.k0 + kb * kBK);
+              tma_load_2d(st + t * S::A_BYTES + kMnBoxBytes, &tmA, &full_bar[stage], U.a_m0 + t * kBM + 64,
+                          U.k0 + kb * kBK);
+            } else {
+              tma_load_2d(st + t * S::A_BYTES, &tmA, &full_bar[stage], kb * kBK, U.row0 + t * kBM);
+            }
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_2d(st + MT * S::A_BYTES + i * kMnBoxBytes, &tmB, &full_bar[stage], U.nb * BN + i * 64,
+                          b_k0 + kb * kBK);
+          } else if (BN >= 128) {
 #pragma unroll
             for (int i = 0; i < NBB; ++i)
               tma_load_2d(st + MT * S::A_BYTES + i * (kBM * kBK * 2), &tmB, &full_bar[stage], kb * kBK,
@@ -347,8 +478,14 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC = idesc_bf16_f32(kBM, BN);
+    // Lane 0 issues; in K-grouped mode the whole warp follows the ring so that
+    // it can zero the rows past a group's end before the block's MMAs.
+    if (KG || lane == 0) {
+      const bool leader = lane == 0;
+      constexpr uint32_t IDESC = idesc_bf16_f32(kBM, BN, A_MN, B_MN);
+      // per K = 16 step: +32 B inside a K-major swizzle row, +2048 B (16 rows) MN-major; encoded >> 4
+      constexpr uint64_t A_STEP = A_MN ? 128u : 2u;
+      constexpr uint64_t B_STEP = B_MN ? 128u : 2u;
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -356,42 +493,65 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
       int qi = 0;
       uint32_t qphase = 0;
       while (true) {
-        if (!mbar_wait(&qfull_bar[qi], qphase, wc)) break;
+        bool okw = mbar_wait(&qfull_bar[qi], qphase, wc);
+        if (KG) okw = __all_sync(0xffffffffu, okw);
+        if (!okw) break;
         const int u = s_queue[qi];
-        mbar_arrive(&qempty_bar[qi]);
+        if (KG) __syncwarp();
+        if (leader) mbar_arrive(&qempty_bar[qi]);
         if (++qi == S::QDEPTH) { qi = 0; qphase ^= 1u; }
         if (u < 0) break;
         const Unit U = decode_unit<MT, EPI, BN>(u, p, s_prefix, total_chunks);
         const int ntile = (U.rows + kBM - 1) / kBM;
-        if (!mbar_wait(&acce_bar[acc], acc_phase ^ 1u, wc)) break;
+        const int num_kb = (U.kcount + kBK - 1) / kBK;
+        okw = mbar_wait(&acce_bar[acc], acc_phase ^ 1u, wc);
+        if (KG) okw = __all_sync(0xffffffffu, okw);
+        if (!okw) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * S::ACC_COLS);
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, wc)) { ok = false; break; }
+          okw = mbar_wait(&full_bar[stage], phase, wc);
+          if (KG) okw = __all_sync(0xffffffffu, okw);
+          if (!okw) { ok = false; break; }
           tc_fence_after();
           uint8_t* st = ring + stage * S::STAGE_BYTES;
-          const uint64_t bdesc = sdesc_k_sw128(smem_u32(st + MT * S::A_BYTES));
-          for (int t = 0; t < ntile; ++t) {
-            const uint64_t adesc = sdesc_k_sw128(smem_u32(st + t * S::A_BYTES));
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              // +32 bytes along K inside the 128-byte swizzle row = +2 in the encoded address
-              umma_bf16(d0 + static_cast<uint32_t>(t * BN), adesc + 2u * kk, bdesc + 2u * kk, IDESC,
-                        (kb | kk) != 0 ? 1u : 0u);
+          if (KG) {
+            const int rem = U.kcount - kb * kBK;
+            if (rem < kBK) {
+              // rows past the group's end belong to the next group (or are the zero fill)
+              zero_k_tail(st, ntile * 2, rem);
+              zero_k_tail(st + MT * S::A_BYTES, BN / 64, rem);
+              fence_proxy_async_shared();
             }
+            __syncwarp();
           }
-          umma_commit(&empty_bar[stage]);
+          if (leader) {
+            const uint64_t bdesc = B_MN ? sdesc_mn_sw128(smem_u32(st + MT * S::A_BYTES))
+                                        : sdesc_k_sw128(smem_u32(st + MT * S::A_BYTES));
+            for (int t = 0; t < ntile; ++t) {
+              const uint64_t adesc = A_MN ? sdesc_mn_sw128(smem_u32(st + t * S::A_BYTES))
+                                          : sdesc_k_sw128(smem_u32(st + t * S::A_BYTES));
+#pragma unroll
+              for (int kk = 0; kk < kBK / 16; ++kk)
+                umma_bf16(d0 + static_cast<uint32_t>(t * BN), adesc + A_STEP * kk, bdesc + B_STEP * kk, IDESC,
+                          (kb | kk) != 0 ? 1u : 0u);
+            }
+            umma_commit(&empty_bar[stage]);
+          }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        umma_commit(&accf_bar[acc]);
+        // (a K-grouped unit whose group has no rows issues no MMA: its epilogue writes zeros)
+        if (leader) umma_commit(&accf_bar[acc]);
         if (++acc == S::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
       }
       // Every MMA this thread issued must finish before TMEM is released.
-      umma_commit(final_bar);
-      WaitCtl drain{nullptr, p.status, p.timeout_ns};
-      mbar_wait(final_bar, 0, drain);
+      if (leader) {
+        umma_commit(final_bar);
+        WaitCtl drain{nullptr, p.status, p.timeout_ns};
+        mbar_wait(final_bar, 0, drain);
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -492,12 +652,41 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
             uint32_t v[32];
             tmem_ld32(tbase + c * 32, v);
             tmem_ld_wait();
+            if (KG && U.kcount == 0) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = 0u;       // a group with no rows: the sum over nothing
+            }
             if (rows_valid > 0) {
               const int bytes_valid = (p.N - (n0 + c * 32)) * 4;
               stage_store_rows64(stg, *reinterpret_cast<uint32_t(*)[16]>(&v[0]), obase + c * 128, p.ldo * 4,
                                  rows_valid, bytes_valid);
               stage_store_rows64(stg, *reinterpret_cast<uint32_t(*)[16]>(&v[16]), obase + c * 128 + 64, p.ldo * 4,
                                  rows_valid, bytes_valid - 64);
+            }
+          }
+        } else if (EPI == EPI_SWIGLU_BWD) {
+          // recomputed gate/up columns [n0, n0+HALF) of h: dg -> out[:, n0..], du -> out[:, N+n0..], h -> out2
+          constexpr int HALF = BN / 2;
+          const int n0 = U.nb * HALF;
+          const int rows_valid = U.rows - (t * kBM + q * 32);
+          const long long r0 = static_cast<long long>(U.row0) + t * kBM + q * 32;
+          uint8_t* stg = ostage + ew * kOutStageBytes;
+#pragma unroll 1
+          for (int c = half; c < HALF / 32; c += NPART) {
+            uint32_t gv[32], uv[32];
+            tmem_ld32(tbase + c * 32, gv);
+            tmem_ld32(tbase + HALF + c * 32, uv);
+            tmem_ld_wait();
+            if (rows_valid > 0) {
+              const int col = n0 + c * 32;
+              __nv_bfloat16* dgu = static_cast<__nv_bfloat16*>(p.out) + r0 * p.ldo;
+              swiglu_bwd_chunk(stg, gv, uv, reinterpret_cast<const uint8_t*>(p.aux + r0 * p.ld_aux + col),
+                               p.ld_aux * 4, reinterpret_cast<uint8_t*>(dgu + col),
+                               reinterpret_cast<uint8_t*>(dgu + p.N + col), p.ldo * 2,
+                               p.out2 != nullptr ? reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.out2) +
+                                                                              r0 * p.ldo2 + col)
+                                                 : nullptr,
+                               p.ldo2 * 2, rows_valid, p.N - col);
             }
           }
         } else {

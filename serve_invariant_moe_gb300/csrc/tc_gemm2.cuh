@@ -198,8 +198,8 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
         if (u < 0) break;
         const Unit U = decode_unit<2, EPI, BN>(u, p, s_prefix, total_chunks);
         const int a_row = U.row0 + static_cast<int>(rank) * kBM;
-        const int b_row = (EPI == EPI_SWIGLU) ? U.b_row + static_cast<int>(rank) * p.b_up_rows
-                                              : U.b_row + static_cast<int>(rank) * kBM;
+        const int b_row = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) ? U.b_row + static_cast<int>(rank) * p.b_up_rows
+                                                                        : U.b_row + static_cast<int>(rank) * kBM;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wc)) { ok = false; break; }
           uint8_t* st = ring + stage * S::STAGE_BYTES;
@@ -397,6 +397,30 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
                                rows_valid, bytes_valid);
             stage_store_rows64(stg, *reinterpret_cast<uint32_t(*)[16]>(&v[16]), obase + c * 128 + 64, p.ldo * 4,
                                rows_valid, bytes_valid - 64);
+          }
+        }
+      } else if (EPI == EPI_SWIGLU_BWD) {
+        constexpr int HALF = BN / 2;
+        const int n0 = U.nb * HALF;
+        const int rows_valid = U.rows - (static_cast<int>(rank) * kBM + q * 32);
+        const long long r0 = static_cast<long long>(U.row0) + rank * kBM + q * 32;
+        uint8_t* stg = ostage + ew * kOutStageBytes;
+#pragma unroll 1
+        for (int c = half; c < HALF / 32; c += 2) {
+          uint32_t gv[32], uv[32];
+          tmem_ld32(tbase + c * 32, gv);
+          tmem_ld32(tbase + HALF + c * 32, uv);
+          tmem_ld_wait();
+          if (rows_valid > 0) {
+            const int col = n0 + c * 32;
+            __nv_bfloat16* dgu = static_cast<__nv_bfloat16*>(p.out) + r0 * p.ldo;
+            swiglu_bwd_chunk(stg, gv, uv, reinterpret_cast<const uint8_t*>(p.aux + r0 * p.ld_aux + col), p.ld_aux * 4,
+                             reinterpret_cast<uint8_t*>(dgu + col), reinterpret_cast<uint8_t*>(dgu + p.N + col),
+                             p.ldo * 2,
+                             p.out2 != nullptr ? reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.out2) +
+                                                                            r0 * p.ldo2 + col)
+                                               : nullptr,
+                             p.ldo2 * 2, rows_valid, p.N - col);
           }
         }
       } else {
