@@ -314,6 +314,8 @@ def run_ours(args):
     nxt = next_rows_timing(st, device) if rank == 0 else None
     if nxt is not None and not args.no_backward:
         nxt.update(head_backward_timing(st, device, peaks))
+        torch.cuda.empty_cache()
+        nxt.update(moe_backward_timing(st, device, peaks))
     moe_names = ["router_gemm", "topk_gate", "dispatch_count", "dispatch_scan", "dispatch_scatter", "gather_rows",
                  "expert_gemm1_swiglu", "expert_gemm2", "shared_gemm1_swiglu", "shared_gemm2", "combine"]
     head_names = ["lm_head_gemm_lse", "lse_merge"]
@@ -450,6 +452,58 @@ def head_backward_timing(st, device, peaks, reps=3):
             out[nm] = dict(ms=round(kms, 4), achieved=round(ach, 1), unit="TFLOP/s",
                            frac=round(ach / peaks["bf16"], 4))
     del dz, dw, dh
+    return out
+
+
+def moe_backward_timing(st, device, peaks, reps=3):
+    """The MoE layer backward on the step's own batch (T = 8192, GLM-scale layer with the shared
+    expert), outside the timed region, from the forward buffers of the last step: combine, grouped
+    FFN (dh, SwiGLU-backward recompute, dx, dW2, dW13; shared expert likewise) and router backward.
+    Per-kernel device time from the library's profiler."""
+    import torch
+    from serve_invariant_moe_gb300 import _lib, binding
+    lib = _lib.lib()
+    mc = st.mc
+    T, H, E, k, F, Fs = mc.T, mc.H, mc.E, mc.k, mc.F, mc.F_shared
+    st.run()
+    d = st.layer._decode
+    fwd = dict(y=d["y"][:T * k], topk_w=d["w"][:T], plan=d["plan"], xp=d["xp"][:T * k], topk_idx=d["idx"][:T])
+    g = torch.Generator().manual_seed(3)
+    dout = torch.randn((T, H), generator=g).to(device)
+
+    def call():
+        return st.layer.backward(st.x, fwd, dout)
+
+    r = call()
+    torch.cuda.synchronize()
+    lib.invmoe_profile_enable(1)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        r = call()
+    e1.record()
+    torch.cuda.synchronize()
+    lib.invmoe_profile_enable(0)
+    kern = _profile_collect(lib)
+    ms = e0.elapsed_time(e1) / reps
+    S = T * k
+    flop = {"expert_dh": 2.0 * S * H * F, "expert_swiglu_bwd": 2.0 * S * 2 * F * H, "expert_dx": 2.0 * S * 2 * F * H,
+            "expert_dw2": 2.0 * S * H * F, "expert_dw13": 2.0 * S * 2 * F * H,
+            "shared_dh": 2.0 * T * H * Fs, "shared_swiglu_bwd": 2.0 * T * 2 * Fs * H, "shared_dx": 2.0 * T * 2 * Fs * H,
+            "shared_dw2": 2.0 * T * H * Fs, "shared_dw13": 2.0 * T * 2 * Fs * H,
+            "router_dx": 2.0 * T * E * H, "router_dw": 2.0 * T * E * H}
+    out = {"moe_backward_ms": round(ms, 3), "moe_backward_tokens_per_s": round(T / (ms / 1e3), 1),
+           "moe_backward_tflops": round(sum(flop.values()) / (ms / 1e3) / 1e12, 1),
+           "moe_backward_weight_grad_bytes": 4 * (E * 3 * F * H + 3 * Fs * H + E * H)}
+    for nm, (tot, c) in kern.items():
+        if c:
+            kms = tot / c
+            ent = dict(ms=round(kms, 4))
+            if nm in flop:
+                ach = flop[nm] / (kms / 1e3) / 1e12
+                ent.update(achieved=round(ach, 1), unit="TFLOP/s", frac=round(ach / peaks["bf16"], 4))
+            out["moe_bwd_" + nm] = ent
+    del r
     return out
 
 
@@ -635,7 +689,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-backward", action="store_true", help="skip the head-backward timing (next rows)")
+    ap.add_argument("--no-backward", action="store_true", help="skip the head and MoE backward timings (next rows)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)
     ap.add_argument("--ref-tokens-per-step", type=int, default=1)
     args = ap.parse_args()

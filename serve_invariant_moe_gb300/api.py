@@ -91,8 +91,10 @@ class MoELayer:
         no atomics)."""
         w = self.w
         T = x.shape[0]
-        ws = binding.new_workspace(binding.backward_workspace_size(T, w.H, w.E, w.k, w.F, w.F_shared),
-                                   device=x.device)
+        need = binding.backward_workspace_size(T, w.H, w.E, w.k, w.F, w.F_shared)
+        if getattr(self, "_bws", None) is None or self._bws.numel() < need:
+            self._bws = binding.new_workspace(need, device=x.device)
+        ws = self._bws
         c = binding.moe_combine_backward(dout, fwd["y"], fwd["topk_w"], fwd["plan"], w.E, w.k,
                                          dout_bf16=w.ws13 is not None)
         f = binding.moe_grouped_ffn_backward(fwd["xp"], fwd["plan"], w.w13, w.w2, c["dy"], T, w.k, ws,
