@@ -34,7 +34,7 @@ WORKLOAD = "glm_scale_moe(T=8192,H=6144,E=256,k=8,F=2048,shared F=2048) + glm_sc
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one full-size launch of
 # the dominant kernel, from a one-pass ncu capture of this step (see profiles/); set to
 # None whenever that kernel's code changes until it is captured again.
-TRAFFIC_BYTES = {"lm_head_gemm_lse": 6.3726e9 + 0.0456e9}
+TRAFFIC_BYTES = {"lm_head_gemm_lse": 6.1679e9 + 0.0433e9}
 
 
 def _peaks():
@@ -640,6 +640,10 @@ def run_profile_case(args):
     lm_head:  vocab-projection GEMM + LSE at T=2048, H=6144, V=32768 (Wv 403 MB, logits 268 MB).
     experts:  the grouped expert GEMMs at T=1024, H=6144, E=32, k=8, F=2048 + shared (weights 2.4 GB);
               256 token-slots per expert on average, as in the T=8192, E=256 layer.
+    moe_backward: one prefill, then one backward of the layer at T=512, H=6144, E=16, k=8, F=2048
+              (no shared expert; 256 token-slots per expert on average; dW13 1.6 GB, dW2 0.8 GB fp32).
+              Single-CTA engine launches in order: router, expert GEMM 1, expert GEMM 2, then
+              expert_dh, expert_swiglu_bwd, expert_dx, expert_dw2, expert_dw13.
     head_backward: one forward for lse, then the head backward twice at T=2048, H=6144, V=32768
               (dlogits 134 MB bf16, d_wvocab 805 MB fp32); the pair-engine launches in order are
               lm_head_gemm_lse, then (lm_head_dlogits, lm_head_dhidden, lm_head_dwvocab) per backward.
@@ -656,6 +660,16 @@ def run_profile_case(args):
         for _ in range(3):
             binding.lm_logprob_kl(hidden.to(dev), wv, target.to(dev), ws)
         binding.check_status(ws)
+    elif args.profile_case == "moe_backward":
+        import dataclasses
+        mc = dataclasses.replace(synth.GLM_MOE, T=512, E=16, F_shared=0)
+        x, wr = synth.moe_activations(mc)
+        w13, w2 = synth.expert_weights(mc, dev)
+        layer = api.MoELayer(api.MoEWeights(wr.to(dev), w13, w2, mc.k))
+        xd = x.to(dev)
+        fwd = layer.prefill(xd, return_all=True)
+        dout = torch.randn((mc.T, mc.H), generator=torch.Generator().manual_seed(3)).to(dev)
+        layer.backward(xd, fwd, dout)
     elif args.profile_case == "head_backward":
         import dataclasses
         hc = dataclasses.replace(synth.GLM_HEAD, T=2048, V=32768)
@@ -683,7 +697,7 @@ def run_profile_case(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile-case", choices=["lm_head", "experts", "head_backward"], default=None)
+    ap.add_argument("--profile-case", choices=["lm_head", "experts", "head_backward", "moe_backward"], default=None)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)

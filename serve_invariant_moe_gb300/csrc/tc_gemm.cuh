@@ -601,6 +601,7 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
             uint32_t v[32];
             tmem_ld32(tbase + c * 32, v);
             tmem_ld_wait();
+            tmem_reg_fence(v);
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const float z = __uint_as_float(v[j]);
@@ -629,6 +630,7 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
             uint32_t v[32];
             tmem_ld32(tbase + c * 32, v);
             tmem_ld_wait();
+            tmem_reg_fence(v);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (n0 + c * 32 + j < p.N) acc8[j & 7] = __fadd_rn(acc8[j & 7], expf(__uint_as_float(v[j]) - m));
@@ -652,6 +654,7 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
             uint32_t v[32];
             tmem_ld32(tbase + c * 32, v);
             tmem_ld_wait();
+            tmem_reg_fence(v);
             if (KG && U.kcount == 0) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = 0u;       // a group with no rows: the sum over nothing
@@ -677,6 +680,8 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
             tmem_ld32(tbase + c * 32, gv);
             tmem_ld32(tbase + HALF + c * 32, uv);
             tmem_ld_wait();
+            tmem_reg_fence(gv);
+            tmem_reg_fence(uv);
             if (rows_valid > 0) {
               const int col = n0 + c * 32;
               __nv_bfloat16* dgu = static_cast<__nv_bfloat16*>(p.out) + r0 * p.ldo;
@@ -705,6 +710,8 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
             tmem_ld32(tbase + c * 32, gv);
             tmem_ld32(tbase + HALF + c * 32, uv);
             tmem_ld_wait();
+            tmem_reg_fence(gv);
+            tmem_reg_fence(uv);
             if (rows_valid > 0) {
               uint32_t packed[16];
 #pragma unroll

@@ -315,6 +315,7 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
             uint32_t v[32];
             tmem_ld32(tbase + c * 32, v);
             tmem_ld_wait();
+            tmem_reg_fence(v);
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const float z = __uint_as_float(v[j]);
@@ -340,6 +341,7 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
             uint32_t v[32];
             tmem_ld32(tbase + c * 32, v);
             tmem_ld_wait();
+            tmem_reg_fence(v);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (n0 + c * 32 + j < p.N) a8[j & 7] = __fadd_rn(a8[j & 7], expf(__uint_as_float(v[j]) - m));
@@ -370,6 +372,7 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
           uint32_t v[32];
           tmem_ld32(tbase + c * 32, v);
           tmem_ld_wait();
+          tmem_reg_fence(v);
           if (rows_valid > 0) {
             uint32_t packed[16];
 #pragma unroll
@@ -391,6 +394,7 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
           uint32_t v[32];
           tmem_ld32(tbase + c * 32, v);
           tmem_ld_wait();
+          tmem_reg_fence(v);
           if (rows_valid > 0) {
             const int bytes_valid = (p.N - (n0 + c * 32)) * 4;
             stage_store_rows64(stg, *reinterpret_cast<uint32_t(*)[16]>(&v[0]), obase + c * 128, p.ldo * 4,
@@ -411,6 +415,8 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
           tmem_ld32(tbase + c * 32, gv);
           tmem_ld32(tbase + HALF + c * 32, uv);
           tmem_ld_wait();
+          tmem_reg_fence(gv);
+          tmem_reg_fence(uv);
           if (rows_valid > 0) {
             const int col = n0 + c * 32;
             __nv_bfloat16* dgu = static_cast<__nv_bfloat16*>(p.out) + r0 * p.ldo;
@@ -439,6 +445,8 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
           tmem_ld32(tbase + c * 32, gv);
           tmem_ld32(tbase + HALF + c * 32, uv);
           tmem_ld_wait();
+          tmem_reg_fence(gv);
+          tmem_reg_fence(uv);
           if (rows_valid > 0) {
             uint32_t packed[16];
 #pragma unroll
