@@ -259,20 +259,24 @@ def run_ours(args):
     out_logp = torch.empty(T, dtype=torch.float32).pin_memory()
     out_k3 = torch.empty(T, dtype=torch.float32).pin_memory()
     out_mask = torch.empty(T, dtype=torch.uint8).pin_memory()
-    x_dev = torch.empty_like(st.x)
-    t_dev = torch.empty_like(st.target)
-    r_dev = torch.empty_like(st.rollout)
+    # inputs of step i+1 are copied on a side stream while step i runs (api.InputStager)
+    from serve_invariant_moe_gb300 import api
+    stager = api.InputStager(dict(x=st.x, target=st.target, rollout=st.rollout))
+    host_in = dict(x=x_pin, target=t_pin, rollout=r_pin)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e2e_steps = max(1, min(args.steps, 10))
     _barrier(ws)
     torch.cuda.synchronize()
     e0.record(stream)
-    for _ in range(e2e_steps):
-        x_dev.copy_(x_pin, non_blocking=True)
-        t_dev.copy_(t_pin, non_blocking=True)
-        r_dev.copy_(r_pin, non_blocking=True)
-        res = st.run(x=x_dev, target=t_dev, rollout=r_dev)
+    stager.copy_stream.wait_event(e0)
+    stager.stage(host_in)
+    for i in range(e2e_steps):
+        inp = stager.next()
+        if i + 1 < e2e_steps:
+            stager.stage(host_in)
+        res = st.run(x=inp["x"], target=inp["target"], rollout=inp["rollout"])
+        stager.release()
         out_logp.copy_(res["logp"], non_blocking=True)
         out_k3.copy_(res["k3"], non_blocking=True)
         out_mask.copy_(res["mask"], non_blocking=True)

@@ -139,6 +139,50 @@ class MoELayer:
         return self._run(x_tokens, d["ws"], bufs, out_bf16=out_bf16)["out"]
 
 
+class InputStager:
+    """Double-buffered host-to-device staging of a step's inputs on a side stream.
+
+    ``stage(host)`` issues the copies of the next batch (pinned host tensors) into
+    the buffer the step before last has finished with; ``next()`` makes the
+    current stream wait for the oldest staged batch and returns its device
+    buffers; ``release()`` marks that batch's buffers free once the work enqueued
+    so far on the current stream is done.  Staging batch i+1 before running
+    batch i overlaps its copies with batch i's kernels.
+    """
+
+    def __init__(self, like: dict):
+        dev = next(iter(like.values())).device
+        self.bufs = [{k: torch.empty_like(v) for k, v in like.items()} for _ in range(2)]
+        self.copy_stream = torch.cuda.Stream(device=dev)
+        self.ready = [torch.cuda.Event() for _ in range(2)]
+        self.free = [torch.cuda.Event() for _ in range(2)]
+        self.used = [False, False]
+        self.fill = 0
+        self.cur = 0
+
+    def stage(self, host: dict):
+        b = self.fill
+        s = self.copy_stream
+        if self.used[b]:
+            s.wait_event(self.free[b])
+        with torch.cuda.stream(s):
+            for k, v in host.items():
+                self.bufs[b][k].copy_(v, non_blocking=True)
+            self.ready[b].record(s)
+        self.fill ^= 1
+
+    def next(self) -> dict:
+        b = self.cur
+        torch.cuda.current_stream().wait_event(self.ready[b])
+        return self.bufs[b]
+
+    def release(self):
+        b = self.cur
+        self.free[b].record(torch.cuda.current_stream())
+        self.used[b] = True
+        self.cur ^= 1
+
+
 class DecodeGraphs:
     """Decode steps captured as CUDA graphs, one per batch-size bucket.
 

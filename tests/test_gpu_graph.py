@@ -59,3 +59,30 @@ def test_decode_graph_buckets_match_eager_decode():
         got = graphs(x).clone()
         torch.cuda.synchronize()
         assert torch.equal(got, ref), b
+
+
+def test_input_stager_double_buffers_in_order():
+    """Copies of batch i+1 overlap the work on batch i; every batch reaches the device intact and
+    no buffer is overwritten while the current stream still reads it."""
+    from serve_invariant_moe_gb300 import api
+    like = dict(x=torch.empty((4096, 1024), dtype=torch.bfloat16, device="cuda"),
+                t=torch.empty(4096, dtype=torch.int32, device="cuda"))
+    stager = api.InputStager(like)
+    g = torch.Generator().manual_seed(5)
+    host = [dict(x=torch.randn((4096, 1024), generator=g).to(torch.bfloat16).pin_memory(),
+                 t=torch.randint(0, 1000, (4096,), generator=g, dtype=torch.int32).pin_memory()) for _ in range(6)]
+    outs = []
+    stager.stage(host[0])
+    for i in range(6):
+        inp = stager.next()
+        if i + 1 < 6:
+            stager.stage(host[i + 1])
+        # some work on the current stream that reads the buffers for a while
+        acc = inp["x"].float()
+        for _ in range(20):
+            acc = acc * 1.0 + 0.0
+        outs.append((acc.to(torch.bfloat16), inp["t"].clone()))
+        stager.release()
+    torch.cuda.synchronize()
+    for i, (x, t) in enumerate(outs):
+        assert torch.equal(x.cpu(), host[i]["x"]) and torch.equal(t.cpu(), host[i]["t"]), i
