@@ -82,6 +82,20 @@ struct WaitCtl {
   uint64_t limit_ns;        // give up after this long
 };
 
+// Non-blocking probe of a barrier phase (no suspend): the fast path of a wait
+// on the critical path of the MMA and TMA issuers.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
 // Bounded wait for the phase with parity `parity` of `bar`.  Returns false if
 // the limit ran out (status recorded, abort flag raised) or if another role of
 // the CTA raised the abort flag.

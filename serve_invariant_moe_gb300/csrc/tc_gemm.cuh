@@ -441,7 +441,10 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
           for (int i = 0; i < NBB; ++i) brow[i] = U.b_row + i * 128;
         }
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wc)) { ok = false; break; }
+          if (!mbar_test(&empty_bar[stage], phase ^ 1u) && !mbar_wait(&empty_bar[stage], phase ^ 1u, wc)) {
+            ok = false;
+            break;
+          }
           uint8_t* st = ring + stage * S::STAGE_BYTES;
           mbar_arrive_expect_tx(&full_bar[stage], bytes);
           for (int t = 0; t < ntile; ++t) {
@@ -486,6 +489,11 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
       // per K = 16 step: +32 B inside a K-major swizzle row, +2048 B (16 rows) MN-major; encoded >> 4
       constexpr uint64_t A_STEP = A_MN ? 128u : 2u;
       constexpr uint64_t B_STEP = B_MN ? 128u : 2u;
+      // stage-0 descriptors; stage s, row tile t add s * STAGE_BYTES + t * A_BYTES to the start
+      // address (encoded >> 4; shared addresses stay below 256 KB, so the 14-bit field never carries)
+      const uint64_t adesc0 = A_MN ? sdesc_mn_sw128(smem_u32(ring)) : sdesc_k_sw128(smem_u32(ring));
+      const uint64_t bdesc0 = B_MN ? sdesc_mn_sw128(smem_u32(ring + MT * S::A_BYTES))
+                                   : sdesc_k_sw128(smem_u32(ring + MT * S::A_BYTES));
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -511,7 +519,7 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * S::ACC_COLS);
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          okw = mbar_wait(&full_bar[stage], phase, wc);
+          okw = mbar_test(&full_bar[stage], phase) || mbar_wait(&full_bar[stage], phase, wc);
           if (KG) okw = __all_sync(0xffffffffu, okw);
           if (!okw) { ok = false; break; }
           tc_fence_after();
@@ -527,11 +535,10 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
             __syncwarp();
           }
           if (leader) {
-            const uint64_t bdesc = B_MN ? sdesc_mn_sw128(smem_u32(st + MT * S::A_BYTES))
-                                        : sdesc_k_sw128(smem_u32(st + MT * S::A_BYTES));
+            const uint64_t so = static_cast<uint64_t>((stage * S::STAGE_BYTES) >> 4);
+            const uint64_t bdesc = bdesc0 + so;
             for (int t = 0; t < ntile; ++t) {
-              const uint64_t adesc = A_MN ? sdesc_mn_sw128(smem_u32(st + t * S::A_BYTES))
-                                          : sdesc_k_sw128(smem_u32(st + t * S::A_BYTES));
+              const uint64_t adesc = adesc0 + so + static_cast<uint64_t>((t * S::A_BYTES) >> 4);
 #pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk)
                 umma_bf16(d0 + static_cast<uint32_t>(t * BN), adesc + A_STEP * kk, bdesc + B_STEP * kk, IDESC,

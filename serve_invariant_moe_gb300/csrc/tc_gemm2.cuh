@@ -201,7 +201,10 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
         const int b_row = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) ? U.b_row + static_cast<int>(rank) * p.b_up_rows
                                                                         : U.b_row + static_cast<int>(rank) * kBM;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wc)) { ok = false; break; }
+          if (!mbar_test(&empty_bar[stage], phase ^ 1u) && !mbar_wait(&empty_bar[stage], phase ^ 1u, wc)) {
+            ok = false;
+            break;
+          }
           uint8_t* st = ring + stage * S::STAGE_BYTES;
           const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * S::STAGE_BYTES);
@@ -236,6 +239,11 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
       // per K = 16 step: +32 B inside a K-major swizzle row, +2048 B (16 rows) MN-major; encoded >> 4
       constexpr uint64_t A_STEP = A_MN ? 128u : 2u;
       constexpr uint64_t B_STEP = B_MN ? 128u : 2u;
+      // stage-0 descriptors; stage s adds s * STAGE_BYTES to the start address (encoded >> 4;
+      // shared addresses stay below 256 KB, so the 14-bit field never carries)
+      const uint64_t adesc0 = A_MN ? sdesc_mn_sw128(smem_u32(ring)) : sdesc_k_sw128(smem_u32(ring));
+      const uint64_t bdesc0 = B_MN ? sdesc_mn_sw128(smem_u32(ring + S::TILE_BYTES))
+                                   : sdesc_k_sw128(smem_u32(ring + S::TILE_BYTES));
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -253,12 +261,11 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * S::ACC_COLS);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, wc)) { ok = false; break; }
+          if (!mbar_test(&full_bar[stage], phase) && !mbar_wait(&full_bar[stage], phase, wc)) { ok = false; break; }
           tc_fence_after();
-          uint8_t* st = ring + stage * S::STAGE_BYTES;
-          const uint64_t adesc = A_MN ? sdesc_mn_sw128(smem_u32(st)) : sdesc_k_sw128(smem_u32(st));
-          const uint64_t bdesc = B_MN ? sdesc_mn_sw128(smem_u32(st + S::TILE_BYTES))
-                                      : sdesc_k_sw128(smem_u32(st + S::TILE_BYTES));
+          const uint64_t so = static_cast<uint64_t>((stage * S::STAGE_BYTES) >> 4);
+          const uint64_t adesc = adesc0 + so;
+          const uint64_t bdesc = bdesc0 + so;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             umma_bf16_pair(d0, adesc + A_STEP * kk, bdesc + B_STEP * kk, IDESC, (kb | kk) != 0 ? 1u : 0u);
