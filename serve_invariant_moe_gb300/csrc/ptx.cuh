@@ -82,25 +82,36 @@ struct WaitCtl {
   uint64_t limit_ns;        // give up after this long
 };
 
-// Non-blocking probe of a barrier phase (no suspend): the fast path of a wait
-// on the critical path of the MMA and TMA issuers.
+// Non-blocking probe of a barrier phase (never suspends): the fast path of
+// every wait.  On the TMA and MMA issue paths the phase is usually complete
+// already, and going straight to a suspending try_wait in a called function
+// there left the tensor pipe idle between K blocks.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
+  if (CLUSTER) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  }
   return done != 0;
 }
 
-// Bounded wait for the phase with parity `parity` of `bar`.  Returns false if
-// the limit ran out (status recorded, abort flag raised) or if another role of
-// the CTA raised the abort flag.
+// The bounded part of a wait (see mbar_wait).
 template <bool CLUSTER = false>
-static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WaitCtl w) {
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, WaitCtl w) {
   if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0; it < (1u << 28); ++it) {
@@ -111,6 +122,15 @@ static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, Wa
   if (w.abort != nullptr) *w.abort = 1;
   atomicOr(w.status, kStatusTimeout);
   return false;
+}
+
+// Bounded wait for the phase with parity `parity` of `bar`: a non-blocking
+// probe first, then suspending try_waits under a time limit.  Returns false if
+// the limit ran out (status recorded, abort flag raised) or if another role of
+// the CTA raised the abort flag.
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WaitCtl w) {
+  return mbar_test<CLUSTER>(bar, parity) || mbar_wait_slow<CLUSTER>(bar, parity, w);
 }
 
 // ---------------------------------------------------------------------- TMA

@@ -441,10 +441,7 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
           for (int i = 0; i < NBB; ++i) brow[i] = U.b_row + i * 128;
         }
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_test(&empty_bar[stage], phase ^ 1u) && !mbar_wait(&empty_bar[stage], phase ^ 1u, wc)) {
-            ok = false;
-            break;
-          }
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wc)) { ok = false; break; }
           uint8_t* st = ring + stage * S::STAGE_BYTES;
           mbar_arrive_expect_tx(&full_bar[stage], bytes);
           for (int t = 0; t < ntile; ++t) {
@@ -519,7 +516,7 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * S::ACC_COLS);
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          okw = mbar_test(&full_bar[stage], phase) || mbar_wait(&full_bar[stage], phase, wc);
+          okw = mbar_wait(&full_bar[stage], phase, wc);
           if (KG) okw = __all_sync(0xffffffffu, okw);
           if (!okw) { ok = false; break; }
           tc_fence_after();

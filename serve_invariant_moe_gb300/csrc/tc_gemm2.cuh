@@ -201,10 +201,7 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
         const int b_row = (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) ? U.b_row + static_cast<int>(rank) * p.b_up_rows
                                                                         : U.b_row + static_cast<int>(rank) * kBM;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_test(&empty_bar[stage], phase ^ 1u) && !mbar_wait(&empty_bar[stage], phase ^ 1u, wc)) {
-            ok = false;
-            break;
-          }
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wc)) { ok = false; break; }
           uint8_t* st = ring + stage * S::STAGE_BYTES;
           const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * S::STAGE_BYTES);
@@ -261,7 +258,7 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
         tc_fence_after();
         const uint32_t d0 = tmem_base + static_cast<uint32_t>(acc * S::ACC_COLS);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_test(&full_bar[stage], phase) && !mbar_wait(&full_bar[stage], phase, wc)) { ok = false; break; }
+          if (!mbar_wait(&full_bar[stage], phase, wc)) { ok = false; break; }
           tc_fence_after();
           const uint64_t so = static_cast<uint64_t>((stage * S::STAGE_BYTES) >> 4);
           const uint64_t adesc = adesc0 + so;
