@@ -194,8 +194,21 @@ def _work_table(mc, hc, counts):
         "gather_rows": ("hbm", S * H * 2 * 2 + S * 4),
         "combine": ("hbm", S * H * 4 + T * H * 4 + T * H * 4 + T * H * 2 + T * k * 8),
         "lse_merge": ("hbm", T * math.ceil(V / 256) * 8 + T * 20),
-        # weight bytes that bound the expert GEMMs (not used for the roofline bound choice)
         "_expert_weight_bytes": ("hbm", active * (2 * F * H + H * F) * 2),
+    }
+
+
+def _gemm_bytes(mc, counts):
+    """Algorithmic DRAM bytes of the expert and shared GEMMs (weights of the experts in use + activations
+    read and written once): with these the roofline time is max(flop / bf16 peak, bytes / HBM peak)."""
+    T, H, E, k, F, Fs = mc.T, mc.H, mc.E, mc.k, mc.F, mc.F_shared
+    S = T * k
+    active = int((counts > 0).sum())
+    return {
+        "expert_gemm1_swiglu": active * 2 * F * H * 2 + S * H * 2 + S * F * 2,
+        "expert_gemm2": active * H * F * 2 + S * F * 2 + S * H * 4,
+        "shared_gemm1_swiglu": 2 * Fs * H * 2 + T * H * 2 + T * Fs * 2,
+        "shared_gemm2": H * Fs * 2 + T * Fs * 2 + T * H * 4,
     }
 
 
@@ -292,6 +305,7 @@ def run_ours(args):
     work = _work_table(st.mc, st.hc, counts)
     peaks = _peaks()
     per_kernel = {}
+    gbytes = _gemm_bytes(st.mc, counts)
     for nm, (msum, c) in kern.items():
         if nm not in work or c == 0:
             continue
@@ -301,6 +315,14 @@ def run_ours(args):
             ach = amount / (avg_ms / 1e3) / 1e12
             per_kernel[nm] = dict(ms=round(avg_ms, 4), launches=c, bound="tensor", achieved=round(ach, 1),
                                   unit="TFLOP/s", frac=round(ach / peaks["bf16"], 4))
+            if nm in gbytes:
+                # memory side of the same kernel: algorithmic bytes over the measured copy bandwidth
+                t_flop = amount / (peaks["bf16"] * 1e12) * 1e3
+                t_byte = gbytes[nm] / (peaks["hbm"] * 1e9) * 1e3
+                per_kernel[nm].update(algorithmic_bytes=gbytes[nm],
+                                      hbm_gbs=round(gbytes[nm] / (avg_ms / 1e3) / 1e9, 1),
+                                      roofline_bound="hbm" if t_byte > t_flop else "tensor",
+                                      roofline_frac=round(max(t_flop, t_byte) / avg_ms, 4))
         else:
             ach = amount / (avg_ms / 1e3) / 1e9
             per_kernel[nm] = dict(ms=round(avg_ms, 4), launches=c, bound="hbm", achieved=round(ach, 1),

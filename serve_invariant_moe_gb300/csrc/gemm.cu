@@ -188,7 +188,6 @@ int gemm_run(const GemmCall& c, cudaStream_t st) {
     case GV_F32_BN128_MT1: return launch<128, 1, EPI_F32, 6>(c, st);
     case GV_F32_BN64_MT1: return launch<64, 1, EPI_F32, 8>(c, st);
     case GV_SWIGLU_BN256_MT2: return launch<256, 2, EPI_SWIGLU, 3>(c, st);
-    case GV_LSE_BN256_MT2: return launch<256, 2, EPI_LSE, 3>(c, st);
     case GV_PAIR_F32: return launch_pair<EPI_F32, 6>(c, st);
     case GV_PAIR_LSE: return launch_pair<EPI_LSE, 6>(c, st);
     case GV_PAIR_SWIGLU: return launch_pair<EPI_SWIGLU, 6>(c, st);

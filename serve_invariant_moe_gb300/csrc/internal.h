@@ -42,7 +42,6 @@ enum GemmVariant : int {
   GV_F32_BN128_MT1 = 2,
   GV_F32_BN64_MT1 = 3,
   GV_SWIGLU_BN256_MT2 = 4, // grouped/dense gate+up with SwiGLU epilogue -> bf16
-  GV_LSE_BN256_MT2 = 5,    // dense vocab projection with per-chunk log-sum-exp partials
   GV_PAIR_F32 = 6,         // CTA-pair 256 x 256 tile, fp32 out
   GV_PAIR_LSE = 7,         // CTA-pair tile, log-sum-exp epilogue
   GV_PAIR_SWIGLU = 8,      // CTA-pair tile, SwiGLU epilogue

@@ -1,6 +1,9 @@
 // tc_gemm.cuh -- the fixed-tile tcgen05 GEMM engine (sm_103a).
 //
-//   D[r, n] = sum_k A[r, k] * B[n, k]      A, B bf16 K-major, D accumulated in fp32 TMEM
+//   D[r, n] = sum_k A[r, k] * B[n, k]      A, B bf16, D accumulated in fp32 TMEM
+//
+// Operands are K-major ([rows, K]) unless a template flag makes one MN-major
+// ([K, rows]; see tc_gemm2.cuh for the layout).
 //
 // Batch invariance ("位级一致：前沿训练的差异化关键", section
 // "为什么比特级一致是一个复杂的问题": one fixed kernel choice for the expert
@@ -30,13 +33,17 @@
 // memory before its MMAs (the next group's rows are never multiplied in).  A
 // group with no rows gets an all-zero block.  Output rows g*M .. g*M+M-1.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over units):
-//   warp 0      TMA producer (one lane): A row tiles + B tile per K block into
-//               a STAGES-deep shared-memory ring (128-byte swizzle)
-//   warp 1      TMEM owner + MMA issuer (one lane): tcgen05.mma kind::f16,
-//               commit frees a ring slot / publishes a finished accumulator
-//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time, convert,
-//               store to global (fp32 rows, or SwiGLU -> bf16)
+// Warp roles (320 threads, one CTA per SM, persistent over units):
+//   warp 0      scheduler + TMA producer (one lane): takes a unit index from a
+//               global counter, publishes it to the other roles through a small
+//               shared queue, and loads the A row tiles + B tile of each K block
+//               into a STAGES-deep shared-memory ring (128-byte swizzle)
+//   warp 1      TMEM owner + MMA issuer (one lane; the whole warp in K-grouped
+//               mode, to zero the block past a group's end): tcgen05.mma
+//               kind::f16, commit frees a ring slot / publishes an accumulator
+//   warps 2..9  epilogue (two warps per TMEM lane quadrant): tcgen05.ld 32 lanes
+//               x 32 columns at a time, convert, stage through shared memory and
+//               store (fp32 rows, SwiGLU -> bf16 h, or the SwiGLU backward)
 #pragma once
 
 #include <cuda_bf16.h>
@@ -158,7 +165,7 @@ struct GemmShape {
   static constexpr int SMEM_BYTES = 1024 /* alignment slack */ + RING_BYTES + OSTAGE_BYTES + BAR_BYTES +
                                     MISC_BYTES + 4 * (MAX_GROUPS + 1);
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
-  static_assert(EPI != EPI_LSE || (MT == 2 && BN == 256), "LSE epilogue: one tile per warp half, 256-column chunks");
+  static_assert(EPI != EPI_LSE && EPI != EPI_DLOGITS, "the LSE and dlogits epilogues run on the CTA-pair engine");
   static_assert(TMEM_NEED <= 512, "TMEM");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
@@ -563,7 +570,6 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
     const int q = warp & 3;                  // TMEM lane quadrant this warp may access
     constexpr int NPART = S::EPI_WARPS / 4;  // warps sharing one lane quadrant
     const int half = ew >> 2;                // which of them this warp is (column chunks c = half mod NPART)
-    const int r_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
     int qi = 0;
@@ -583,69 +589,9 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       for (int t = 0; t < ntile; ++t) {
-        const int row_local = t * kBM + r_in_tile;
-        const bool valid = row_local < U.rows;
-        const long long row = static_cast<long long>(U.row0) + row_local;
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                static_cast<uint32_t>(acc * S::ACC_COLS + t * BN);
-        if (EPI == EPI_LSE) {
-          // Two warps share each TMEM lane quadrant: warp half h takes tile t == h,
-          // so every thread owns one full 256-column row of its tile.
-          if (t != half) continue;
-          const int n0 = U.nb * BN;
-          float* orow = p.out != nullptr ? static_cast<float*>(p.out) + row * p.ldo + n0 : nullptr;
-          const int tg = valid ? __ldg(p.target + row) - n0 : -1;   // target column inside this block
-          // max over the chunk (exact in any order), eight running maxima for ILP
-          float mx[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-          float tv = 0.0f;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tbase + c * 32, v);
-            tmem_ld_wait();
-            tmem_reg_fence(v);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float z = __uint_as_float(v[j]);
-              if (n0 + c * 32 + j < p.N) mx[j & 7] = fmaxf(mx[j & 7], z);
-              if (tg == c * 32 + j) tv = z;
-            }
-            if (valid && orow != nullptr) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                if (n0 + c * 32 + j * 4 < p.N)
-                  *reinterpret_cast<float4*>(orow + c * 32 + j * 4) =
-                      make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-              }
-            }
-          }
-          const float m = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-          // s = sum of exp(z - m) over the chunk: column j of the chunk goes to
-          // accumulator j mod 8 in ascending j; then ((a0+a1)+(a2+a3))+((a4+a5)+(a6+a7))
-          float acc8[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc8[i] = 0.0f;
-#pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tbase + c * 32, v);
-            tmem_ld_wait();
-            tmem_reg_fence(v);
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (n0 + c * 32 + j < p.N) acc8[j & 7] = __fadd_rn(acc8[j & 7], expf(__uint_as_float(v[j]) - m));
-          }
-          const float sum = __fadd_rn(__fadd_rn(__fadd_rn(acc8[0], acc8[1]), __fadd_rn(acc8[2], acc8[3])),
-                                      __fadd_rn(__fadd_rn(acc8[4], acc8[5]), __fadd_rn(acc8[6], acc8[7])));
-          if (valid) {
-            p.part[row * p.nch + U.nb] = make_float2(m, sum);
-            if (tg >= 0 && tg < BN && n0 + tg < p.N) p.tgt_logit[row] = tv;
-          }
-        } else if (EPI == EPI_F32) {
+        if (EPI == EPI_F32) {
           // the warp's 32 rows start at tile row q*32; lane L stores row r of them
           const int n0 = U.nb * BN;
           const int rows_valid = U.rows - (t * kBM + q * 32);
