@@ -286,7 +286,7 @@ def swiglu_backward(x_rows, w13, w2, F, dy, round_ops=True):
 
 
 def moe_backward(x, w_router, w13, w2, k, F, dout, ws13=None, ws2=None, F_shared=0, round_ops=True,
-                 expert_weights=None):
+                 expert_weights=None, replay_idx=None):
     """Gradients of L = sum(dout * out) through the whole MoE layer, float64.
 
     Forward as ``moe_forward`` (round_h = round_ops).  Backward, per token t and
@@ -300,12 +300,15 @@ def moe_backward(x, w_router, w13, w2, k, F, dout, ws13=None, ws2=None, F_shared
         shared expert: ``swiglu_backward`` with dy = dout (bf16 operand when round_ops).
     ``expert_weights(e) -> (w13_e, w2_e)`` may replace w13 / w2 for large
     configurations; dw13 / dw2 are then dicts over the experts the batch used.
+    ``replay_idx`` [T, k] takes the recorded expert choices instead of the top-k
+    (as in ``moe_forward``); the router gradient is then the softmax Jacobian over
+    the replayed experts' logits.
     Returns dict(dx, dw_router, dw13, dw2, dws13, dws2, dgate, dlogits, dy, dgu, dxp, fwd).
     """
     x = np.asarray(x, np.float64)
     dout = np.asarray(dout, np.float64)
     fwd = moe_forward(x, w_router, w13, w2, k, F, ws13, ws2, F_shared, round_h=round_ops,
-                      expert_weights=expert_weights)
+                      expert_weights=expert_weights, replay_idx=replay_idx)
     idx, gates, y = fwd["idx"], fwd["gates"], fwd["y"]
     T, H = x.shape
     E = np.asarray(w_router).shape[0]

@@ -202,3 +202,48 @@ def test_glm_scale_moe_backward_sampled():
     torch.cuda.synchronize()
     for k in ("dx", "dw_router", "dw13", "dw2", "dws13", "dws2"):
         assert torch.equal(b[k], b2[k]), k
+
+
+def test_moe_backward_single_expert_k1_is_the_plain_mlp_backward():
+    """E = 1, k = 1: the gate is exactly 1 and the router gets no gradient (a softmax over one logit),
+    so the layer backward is the SwiGLU MLP backward of the oracle."""
+    from serve_invariant_moe_gb300 import api
+    cfg = dataclasses.replace(synth.GLM_MOE, name="bwd_k1", T=96, H=128, E=8, k=1, F=128, F_shared=0, seed=43)
+    x, _ = synth.moe_activations(cfg)
+    w13, w2 = synth.expert_weights(cfg, "cpu")
+    wr = torch.zeros((8, cfg.H), dtype=torch.bfloat16)
+    wr[3, :] = 1.0                                            # logit of expert 3 = sum(x), far from the others
+    x = (x.abs() + 0.25).to(torch.bfloat16)                  # positive rows: expert 3 wins every token
+    layer = api.MoELayer(api.MoEWeights(wr.cuda(), w13.cuda(), w2.cuda(), 1))
+    g = torch.Generator().manual_seed(4)
+    dout = torch.randn((cfg.T, cfg.H), generator=g)
+    fwd, b = _gpu_backward(layer, x, dout)
+    assert torch.all(fwd["topk_idx"] == 3) and torch.all(fwd["topk_w"] == 1.0)
+    ref = omoe.swiglu_backward(f64(x), f64(w13[3]), f64(w2[3]), cfg.F, omoe.round_to_bf16(dout.double().numpy()))
+    assert torch.all(b["dw_router"] == 0) and torch.all(b["dgate"].abs() >= 0)
+    _close(b["dx"].cpu().numpy(), ref["dx"], "dx")
+    _close(b["dw13"][3].cpu().numpy(), ref["dw13"], "dw13")
+    _close(b["dw2"][3].cpu().numpy(), ref["dw2"], "dw2")
+    others = [e for e in range(8) if e != 3]
+    assert torch.all(b["dw13"][others] == 0) and torch.all(b["dw2"][others] == 0)
+
+
+def test_moe_backward_through_replayed_routing():
+    """Routing replayed from recorded indices: the backward follows the replayed experts and gates
+    (oracle: the same backward with those indices given to its forward)."""
+    from serve_invariant_moe_gb300 import binding
+    cfg = SMALL
+    x, wr, w13, w2, ws13, ws2, dout, layer = _setup(cfg)
+    g = torch.Generator().manual_seed(6)
+    idx = torch.stack([torch.randperm(cfg.E, generator=g)[:cfg.k] for _ in range(x.shape[0])]).to(torch.int32)
+    fwd = layer.prefill(x.cuda(), return_all=True, replay_idx=idx.cuda())
+    b = layer.backward(x.cuda(), fwd, dout.cuda())
+    torch.cuda.synchronize()
+    assert torch.equal(fwd["topk_idx"].cpu(), idx)
+    ref = omoe.moe_backward(f64(x), f64(wr), f64(w13), f64(w2), cfg.k, cfg.F, dout.double().numpy(), f64(ws13),
+                            f64(ws2), cfg.F_shared, replay_idx=idx.numpy())
+    assert np.array_equal(ref["fwd"]["idx"], idx.numpy())
+    _close(b["dgate"].double().cpu().numpy(), ref["dgate"], "dgate")
+    _close(b["dx"].cpu().numpy(), ref["dx"], "dx")
+    _close(b["dw_router"].cpu().numpy(), ref["dw_router"], "dw_router")
+    _close(b["dw13"].cpu().numpy(), ref["dw13"], "dw13")

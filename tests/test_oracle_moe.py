@@ -325,3 +325,29 @@ def test_swiglu_backward_matches_torch_autograd():
                             round_ops=False)
     for name, t in (("dx", x), ("dw13", w13), ("dw2", w2)):
         assert np.allclose(b[name], t.grad.numpy(), rtol=1e-12, atol=1e-12), name
+
+
+def test_moe_backward_replay_of_own_choice_is_the_plain_backward():
+    x, wr, w13, w2, ws13, ws2, dout = _bwd_case(34, T=7)
+    a = moe.moe_backward(x, wr, w13, w2, 2, 3, dout, ws13, ws2, 2, round_ops=False)
+    b = moe.moe_backward(x, wr, w13, w2, 2, 3, dout, ws13, ws2, 2, round_ops=False, replay_idx=a["fwd"]["idx"])
+    for name in ("dx", "dw_router", "dw13", "dw2", "dws13", "dws2"):
+        assert np.array_equal(a[name], b[name]), name
+
+
+def test_moe_backward_with_replayed_experts_central_differences():
+    """Other experts replayed: the router gradient is the softmax Jacobian over the replayed logits."""
+    x, wr, w13, w2, _, _, dout = _bwd_case(35, T=4)
+    idx = np.array([[3, 0], [1, 2], [2, 3], [0, 1]], dtype=np.int32)
+    g = moe.moe_backward(x, wr, w13, w2, 2, 3, dout, round_ops=False, replay_idx=idx)
+
+    def f(x_, wr_):
+        return float(np.sum(dout * moe.moe_forward(x_, wr_, w13, w2, 2, 3, round_h=False, replay_idx=idx)["out"]))
+
+    eps = 1e-6
+    for arr, name in ((x, "dx"), (wr, "dw_router")):
+        for i in np.ndindex(arr.shape):
+            p, m = arr.copy(), arr.copy()
+            p[i] += eps; m[i] -= eps
+            fd = (f(p, wr) - f(m, wr)) / (2 * eps) if name == "dx" else (f(x, p) - f(x, m)) / (2 * eps)
+            assert abs(fd - g[name][i]) < 1e-6 * max(1.0, abs(fd)), (name, i)
