@@ -133,3 +133,16 @@ def test_full_size_head_sampled_tokens():
     assert torch.isfinite(r["logp"]).all() and (r["k3"] >= 0).all()
     # N(0, 0.05) perturbation keeps every sampled token (|d| << ln 2)
     assert torch.all(r["mask"][sample] == 1)
+
+
+def test_head_very_large_vocab():
+    """V = 204800 (800 LSE chunks, 25 per merge lane) with a small hidden size."""
+    T, H, V = 3, 64, 204800
+    g = torch.Generator().manual_seed(21)
+    hidden = torch.randn((T, H), generator=g).to(torch.bfloat16)
+    wv = (torch.randn((V, H), generator=g) * 0.1).to(torch.bfloat16)
+    target = torch.tensor([0, 123457, V - 1], dtype=torch.int32)
+    ref = ohead.head_forward(f64(hidden), f64(wv), target.numpy())
+    r = _run(hidden, wv, target)
+    assert np.abs(r["logp"].double().cpu().numpy() - ref["logp"]).max() <= LOGP_ABS
+    assert np.abs(r["lse"].double().cpu().numpy() - ref["lse"]).max() <= LOGP_ABS
