@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -70,18 +71,21 @@ int check_cuda(cudaError_t e, const char* what) {
 }
 
 int device_sm_count(int* out) {
-  static int cache[64] = {};
+  static std::atomic<int> cache[64] = {};
   int dev = 0;
   int rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
   if (rc) return rc;
-  if (dev < 64 && cache[dev] > 0) {
-    *out = cache[dev];
-    return INVMOE_OK;
+  if (dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) {
+      *out = c;
+      return INVMOE_OK;
+    }
   }
   int n = 0;
   rc = check_cuda(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute");
   if (rc) return rc;
-  if (dev < 64) cache[dev] = n;
+  if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   *out = n;
   return INVMOE_OK;
 }
@@ -92,7 +96,7 @@ struct ProfRec {
   cudaEvent_t a, b;
 };
 std::mutex g_prof_mu;
-bool g_prof_on = false;
+std::atomic<bool> g_prof_on{false};
 std::vector<ProfRec> g_prof_recs;
 std::vector<cudaEvent_t> g_prof_pool;
 
@@ -109,7 +113,7 @@ cudaEvent_t take_event() {
 }  // namespace
 
 ProfScope::ProfScope(const char* name, cudaStream_t st) : idx_(-1), st_(st) {
-  if (!g_prof_on) return;
+  if (!g_prof_on.load(std::memory_order_relaxed)) return;
   std::lock_guard<std::mutex> lk(g_prof_mu);
   ProfRec r{name, take_event(), take_event()};
   if (!r.a || !r.b) return;
@@ -648,7 +652,7 @@ int invmoe_gemm_bf16(const void* a, const void* b, int M, int N, int K, float* d
 
 int invmoe_profile_enable(int on) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
-  g_prof_on = on != 0;
+  g_prof_on.store(on != 0);
   return INVMOE_OK;
 }
 

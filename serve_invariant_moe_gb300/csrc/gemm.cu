@@ -2,6 +2,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -42,6 +43,21 @@ int make_tmap(CUtensorMap* m, const void* base, long long inner, long long rows,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return set_error(INVMOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return INVMOE_OK;
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device (devices 0..63
+// are remembered in `done`; a higher device index sets it on every call).
+int set_smem_attr(const void* kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  int rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc) return rc;
+  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return INVMOE_OK;
+  rc = check_cuda(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
+                  "cudaFuncSetAttribute");
+  if (rc) return rc;
+  if (bit != 0) done.fetch_or(bit, std::memory_order_release);
   return INVMOE_OK;
 }
 
@@ -92,16 +108,10 @@ int launch(const GemmCall& c, cudaStream_t st) {
             : make_tmap(&tb, c.B, c.K, c.b_rows, BN >= 128 ? 128 : BN);
   if (rc) return rc;
 
-  int dev = 0;
-  if ((rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice"))) return rc;
-  static bool attr_set[64] = {};
-  if (dev < 64 && !attr_set[dev]) {
-    rc = check_cuda(cudaFuncSetAttribute(tc_gemm_kernel<BN, MT, EPI, STAGES, A_MN, B_MN, KG>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES),
-                    "cudaFuncSetAttribute");
-    if (rc) return rc;
-    attr_set[dev] = true;
-  }
+  static std::atomic<uint64_t> attr_set{0};
+  if ((rc = set_smem_attr(reinterpret_cast<const void*>(tc_gemm_kernel<BN, MT, EPI, STAGES, A_MN, B_MN, KG>),
+                          S::SMEM_BYTES, attr_set)))
+    return rc;
   int sms = 0;
   if ((rc = device_sm_count(&sms))) return rc;
 
@@ -132,16 +142,10 @@ int launch_pair(const GemmCall& c, cudaStream_t st) {
   if (rc) return rc;
   rc = B_MN ? make_tmap(&tb, c.B, c.b_rows, c.K, 64) : make_tmap(&tb, c.B, c.K, c.b_rows, kBM);
   if (rc) return rc;
-  int dev = 0;
-  if ((rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice"))) return rc;
-  static bool attr_set[64] = {};
-  if (dev < 64 && !attr_set[dev]) {
-    rc = check_cuda(cudaFuncSetAttribute(tc_gemm_pair_kernel<EPI, STAGES, A_MN, B_MN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM_BYTES),
-                    "cudaFuncSetAttribute");
-    if (rc) return rc;
-    attr_set[dev] = true;
-  }
+  static std::atomic<uint64_t> attr_set{0};
+  if ((rc = set_smem_attr(reinterpret_cast<const void*>(tc_gemm_pair_kernel<EPI, STAGES, A_MN, B_MN>),
+                          S::SMEM_BYTES, attr_set)))
+    return rc;
   int sms = 0;
   if ((rc = device_sm_count(&sms))) return rc;
   const GemmParams p = make_params(c, (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) ? 128 : 256);
