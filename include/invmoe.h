@@ -21,9 +21,15 @@
  *   Section "迁移到 NPU 时": a top-k must fix ties, order, NaN handling and the
  *   index dtype.  Section "动作与概率契约": logsumexp needs comparison tests.
  *
+ *   The first page, section "端到端零 KLD": the trainer follows the same
+ *   bit-exact standard.  The trainer-side calls (rl_token_loss's gradient,
+ *   lm_head_backward, moe_*_backward) differentiate the same definition with
+ *   fixed reduction orders and no atomics.
+ *
  * Conventions for every entry point
  *   - Pointers are DEVICE pointers owned by the caller unless stated otherwise.
- *     The library allocates no device memory; it keeps only small host-side
+ *     The library allocates no device memory (moe_route_topk_noalloc uses one
+ *     fixed array built into the library); it keeps only small host-side
  *     caches (SM count, kernel attributes).
  *   - bf16 tensors are passed as void* (raw IEEE bfloat16, row-major).
  *     float is IEEE binary32.  Index tensors are int32.
