@@ -18,7 +18,9 @@
 //     never changes the order of any element's reduction;
 //   * rows of a tile that belong to another group, or lie past the end of A,
 //     are loaded (TMA fills out-of-range rows with zeros) and multiplied, but
-//     never stored: an MMA row depends only on its own A row.
+//     never stored: an MMA row depends only on its own A row;
+//   * a tile with at most 64 valid rows is issued as an M = 64 MMA: its rows get
+//     the same products in the same order (bit-identical to the M = 128 tile).
 //
 // Grouped mode: groups g = 0..G-1 own the A rows [offsets[g], offsets[g]+counts[g])
 // and the B rows [g*b_group_rows, (g+1)*b_group_rows).  A group's rows are cut
@@ -490,6 +492,8 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
     if (KG || lane == 0) {
       const bool leader = lane == 0;
       constexpr uint32_t IDESC = idesc_bf16_f32(kBM, BN, A_MN, B_MN);
+      // a tile with at most 64 valid rows runs as an M = 64 MMA (same per-row products and order)
+      constexpr uint32_t IDESC64 = idesc_bf16_f32(64, BN, A_MN, B_MN);
       // per K = 16 step: +32 B inside a K-major swizzle row, +2048 B (16 rows) MN-major; encoded >> 4
       constexpr uint64_t A_STEP = A_MN ? 128u : 2u;
       constexpr uint64_t B_STEP = B_MN ? 128u : 2u;
@@ -545,8 +549,8 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
               const uint64_t adesc = adesc0 + so + static_cast<uint64_t>((t * S::A_BYTES) >> 4);
 #pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk)
-                umma_bf16(d0 + static_cast<uint32_t>(t * BN), adesc + A_STEP * kk, bdesc + B_STEP * kk, IDESC,
-                          (kb | kk) != 0 ? 1u : 0u);
+                umma_bf16(d0 + static_cast<uint32_t>(t * BN), adesc + A_STEP * kk, bdesc + B_STEP * kk,
+                          U.rows - t * kBM <= 64 ? IDESC64 : IDESC, (kb | kk) != 0 ? 1u : 0u);
             }
             umma_commit(&empty_bar[stage]);
           }
@@ -591,12 +595,17 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
       for (int t = 0; t < ntile; ++t) {
         const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                static_cast<uint32_t>(acc * S::ACC_COLS + t * BN);
+        // The warp's rows in this tile: lane L of quadrant q holds tile row q*32 + L for
+        // an M = 128 accumulator, and row q*16 + L (lanes 0..15) for an M = 64 one.
+        const int tile_rows = U.rows - t * kBM;
+        const bool m64 = tile_rows <= 64;
+        const int wrow = m64 ? q * 16 : q * 32;
+        const int rows_valid = m64 ? max(0, min(16, tile_rows - q * 16)) : tile_rows - q * 32;
         if (EPI == EPI_F32) {
           // the warp's 32 rows start at tile row q*32; lane L stores row r of them
           const int n0 = U.nb * BN;
-          const int rows_valid = U.rows - (t * kBM + q * 32);
           uint8_t* obase = rows_valid > 0 ? reinterpret_cast<uint8_t*>(static_cast<float*>(p.out) +
-                                                (static_cast<long long>(U.row0) + t * kBM + q * 32) * p.ldo + n0)
+                                                (static_cast<long long>(U.row0) + t * kBM + wrow) * p.ldo + n0)
                                           : nullptr;
           uint8_t* stg = ostage + ew * kOutStageBytes;
 #pragma unroll 1
@@ -621,8 +630,7 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
           // recomputed gate/up columns [n0, n0+HALF) of h: dg -> out[:, n0..], du -> out[:, N+n0..], h -> out2
           constexpr int HALF = BN / 2;
           const int n0 = U.nb * HALF;
-          const int rows_valid = U.rows - (t * kBM + q * 32);
-          const long long r0 = static_cast<long long>(U.row0) + t * kBM + q * 32;
+          const long long r0 = static_cast<long long>(U.row0) + t * kBM + wrow;
           uint8_t* stg = ostage + ew * kOutStageBytes;
 #pragma unroll 1
           for (int c = half; c < HALF / 32; c += NPART) {
@@ -647,10 +655,9 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
         } else {
           constexpr int HALF = BN / 2;
           const int n0 = U.nb * HALF;
-          const int rows_valid = U.rows - (t * kBM + q * 32);
           uint8_t* obase = rows_valid > 0
                                ? reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.out) +
-                                                            (static_cast<long long>(U.row0) + t * kBM + q * 32) * p.ldo +
+                                                            (static_cast<long long>(U.row0) + t * kBM + wrow) * p.ldo +
                                                             n0)
                                : nullptr;
           uint8_t* stg = ostage + ew * kOutStageBytes;
