@@ -338,6 +338,8 @@ def run_ours(args):
 
     inv = invariance_check(st, device) if rank == 0 else None
     nxt = next_rows_timing(st, device) if rank == 0 else None
+    if nxt is not None:
+        nxt.update(qwen_layer_timing(device, peaks))
     if nxt is not None and not args.no_backward:
         nxt.update(head_backward_timing(st, device, peaks))
         torch.cuda.empty_cache()
@@ -530,6 +532,52 @@ def moe_backward_timing(st, device, peaks, reps=3):
                 ent.update(achieved=round(ach, 1), unit="TFLOP/s", frac=round(ach / peaks["bf16"], 4))
             out["moe_bwd_" + nm] = ent
     del r
+    return out
+
+
+def qwen_layer_timing(device, peaks, reps=5):
+    """The Qwen-MoE-like layer (T = 4096, H = 2048, E = 128 top-8, F = 768, Zipf(1.1)-skewed routing:
+    per-expert token counts from 0 to about 1500), outside the timed region: whole-layer device time
+    (route, dispatch, grouped SwiGLU experts, combine) and the grouped GEMMs against the bf16 peak and
+    their memory roofline."""
+    import torch
+    from serve_invariant_moe_gb300 import _lib, api, binding, synth
+    lib = _lib.lib()
+    mc = synth.QWEN_MOE
+    x, wr = synth.moe_activations(mc)
+    w13, w2 = synth.expert_weights(mc, device)
+    layer = api.MoELayer(api.MoEWeights(wr.to(device), w13, w2, mc.k))
+    xd = x.to(device)
+    layer.alloc_decode(mc.T)
+    for _ in range(2):
+        layer.decode(xd)
+    torch.cuda.synchronize()
+    lib.invmoe_profile_enable(1)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        layer.decode(xd)
+    e1.record()
+    torch.cuda.synchronize()
+    lib.invmoe_profile_enable(0)
+    kern = _profile_collect(lib)
+    binding.check_status(layer._decode["ws"])
+    ms = e0.elapsed_time(e1) / reps
+    counts = layer._decode["plan"][:mc.E].cpu().numpy()
+    S = mc.T * mc.k
+    out = {"qwen_moe_layer_ms": round(ms, 4), "qwen_moe_layer_tokens_per_s": round(mc.T / (ms / 1e3), 1),
+           "qwen_expert_tokens_max": int(counts.max()), "qwen_experts_empty": int((counts == 0).sum())}
+    flop = {"expert_gemm1_swiglu": 2.0 * S * 2 * mc.F * mc.H, "expert_gemm2": 2.0 * S * mc.H * mc.F}
+    gb = _gemm_bytes(mc, counts)
+    for nm in flop:
+        if nm in kern and kern[nm][1]:
+            kms = kern[nm][0] / kern[nm][1]
+            t_flop = flop[nm] / (peaks["bf16"] * 1e12) * 1e3
+            t_byte = gb[nm] / (peaks["hbm"] * 1e9) * 1e3
+            out["qwen_" + nm] = dict(ms=round(kms, 4), frac=round(t_flop / kms, 4),
+                                     roofline_bound="hbm" if t_byte > t_flop else "tensor",
+                                     roofline_frac=round(max(t_flop, t_byte) / kms, 4))
+    del layer, w13, w2
     return out
 
 
