@@ -116,3 +116,18 @@ def test_mn_major_ragged_k_matches_oracle(ws, variant, M, N, K):
     err = np.abs(d.double().cpu().numpy() - omoe.router_logits(a64, b64))
     bound = dot_bound(a64, b64, K)
     assert (err <= bound).all(), f"max err/bound {(err / bound).max():.3f}"
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2, 3])
+def test_m64_tail_tiles_match_m128_tiles(ws, variant):
+    """A last tile with at most 64 valid rows runs as an M = 64 MMA; the same rows inside a fuller
+    tile run as M = 128.  Both give the same bits (the row-position invariance batch invariance needs)."""
+    from serve_invariant_moe_gb300 import binding
+    K, N = 320, 256
+    a = _rand((600, K), 50)
+    b = _rand((N, K), 51, 0.05).cuda()
+    full = binding.gemm_bf16(a.cuda(), b, ws, variant=variant)          # tiles of 128 rows (tail 88 rows)
+    for M in (129, 140, 192, 256 + 64, 512 + 1):                          # tails of 1, 12, 64, 64 and 1 rows
+        d = binding.gemm_bf16(a[:M].contiguous().cuda(), b, ws, variant=variant)
+        binding.check_status(ws)
+        assert torch.equal(d, full[:M]), M

@@ -61,6 +61,27 @@ def test_invariance_small_layer():
     assert _sweep(SMALL, [1, 2, 3, 7, 31, 32, 33, 127, 128, 129, 255, 257, 1000], 2) > 0
 
 
+def test_invariance_skewed_qwen_like_layer():
+    """The Qwen-MoE-like layer with its own Zipf-skewed traffic around the probe (up to ~1500 tokens on
+    one expert: several row chunks, M = 64 tail tiles, a handful of tokens on others): the probe's bits
+    never change, through prefill and through decode."""
+    cfg = synth.QWEN_MOE
+    layer = _layer(cfg)
+    x_all, _ = synth.moe_activations(cfg)                   # skewed traffic of the workload itself
+    probe = synth.probe_tokens(cfg)
+    ref = layer.prefill(probe.cuda()).clone()
+    for n in (1, 7, 33, 129, 1000, 4000):
+        off = n // 3
+        x = torch.cat([x_all[:off], probe, x_all[off:n]])
+        out = layer.prefill(x.cuda())
+        assert torch.equal(out[off:off + 32], ref), n
+    for B in (1, 5, 64):
+        for i in range(0, 32, 7):
+            xt = torch.cat([x_all[:B - 1], probe[i:i + 1]])
+            o = layer.decode(xt.cuda())
+            assert torch.equal(o[B - 1], ref[i]), (B, i)
+
+
 GLM_SIZES = [1, 2, 3, 7, 31, 32, 33, 127, 128, 129, 255, 256, 257, 511, 1000, 2047, 4096]
 
 
