@@ -296,17 +296,17 @@ __device__ __forceinline__ void swiglu_bwd_chunk(uint8_t* stg, const uint32_t (&
   if (h_row0 != nullptr) stage_store_rows64(stg, ph, h_row0, ld_h_bytes, rows_valid, cols_valid * 2);
 }
 
-// Zero K rows [rem, 64) of `nbox` consecutive MN-major boxes (64 K rows x 128 B
-// each) at `base`: the part of a K-grouped block past its group's last row.
-// All 32 lanes of the calling warp take part.
-__device__ __forceinline__ void zero_k_tail(uint8_t* base, int nbox, int rem) {
+// Zero K rows [rem, end) of `nbox` consecutive MN-major boxes (64 K rows x 128 B
+// each) at `base`: the rows of a K-grouped block's last K = 16 step that lie past
+// its group's last row (end - rem < 16; whole rows, so the swizzle does not
+// matter).  All 32 lanes of the calling warp take part.
+__device__ __forceinline__ void zero_k_tail(uint8_t* base, int nbox, int rem, int end) {
   const int lane = threadIdx.x & 31;
-  const int per_box = (64 - rem) * 8;           // 16-byte chunks per box
-  for (int i = lane; i < nbox * per_box; i += 32) {
-    const int b = i / per_box;
-    const int c = i - b * per_box;
-    *reinterpret_cast<uint4*>(base + b * kMnBoxBytes + rem * 128 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
-  }
+  const int per_box = (end - rem) * 8;          // 16-byte chunks per box
+  uint8_t* p0 = base + rem * 128;
+  for (int b = 0; b < nbox; ++b)
+    for (int c = lane; c < per_box; c += 32)
+      *reinterpret_cast<uint4*>(p0 + b * kMnBoxBytes + c * 16) = make_uint4(0u, 0u, 0u, 0u);
 }
 
 // Work units are handed out dynamically: the producer thread takes the next
@@ -532,13 +532,20 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
           if (!okw) { ok = false; break; }
           tc_fence_after();
           uint8_t* st = ring + stage * S::STAGE_BYTES;
+          // K = 16 steps this block issues: a K-grouped group's last block stops at the
+          // step holding its last row (the skipped steps would add exact zeros)
+          int nkk = kBK / 16;
           if (KG) {
             const int rem = U.kcount - kb * kBK;
             if (rem < kBK) {
-              // rows past the group's end belong to the next group (or are the zero fill)
-              zero_k_tail(st, ntile * 2, rem);
-              zero_k_tail(st + MT * S::A_BYTES, BN / 64, rem);
-              fence_proxy_async_shared();
+              nkk = (rem + 15) >> 4;
+              // rows of that step past the group's end belong to the next group (or are
+              // the zero fill): clear them in both operands
+              if (rem & 15) {
+                zero_k_tail(st, ntile * 2, rem, nkk * 16);
+                zero_k_tail(st + MT * S::A_BYTES, BN / 64, rem, nkk * 16);
+                fence_proxy_async_shared();
+              }
             }
             __syncwarp();
           }
@@ -549,8 +556,9 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
               const uint64_t adesc = adesc0 + so + static_cast<uint64_t>((t * S::A_BYTES) >> 4);
 #pragma unroll
               for (int kk = 0; kk < kBK / 16; ++kk)
-                umma_bf16(d0 + static_cast<uint32_t>(t * BN), adesc + A_STEP * kk, bdesc + B_STEP * kk,
-                          U.rows - t * kBM <= 64 ? IDESC64 : IDESC, (kb | kk) != 0 ? 1u : 0u);
+                if (kk < nkk)
+                  umma_bf16(d0 + static_cast<uint32_t>(t * BN), adesc + A_STEP * kk, bdesc + B_STEP * kk,
+                            U.rows - t * kBM <= 64 ? IDESC64 : IDESC, (kb | kk) != 0 ? 1u : 0u);
             }
             umma_commit(&empty_bar[stage]);
           }
