@@ -46,6 +46,25 @@ int make_tmap(CUtensorMap* m, const void* base, long long inner, long long rows,
   return INVMOE_OK;
 }
 
+// K-grouped fp32 output of G groups, each [M rows, N columns] with row stride
+// ldo floats, group g starting at row g*M: a [G][M][N] map whose box (16
+// columns = 64 B, 32 rows) matches the epilogue's 64-byte-swizzled staging.
+int make_tmap_out_grouped_f32(CUtensorMap* m, void* base, long long N, long long M, long long G, long long ldo) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return set_error(INVMOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if (ldo % 4 != 0 || (reinterpret_cast<uintptr_t>(base) & 15) != 0)
+    return set_error(INVMOE_ERR_INVALID_ARG, "K-grouped output needs a 16-byte aligned base and ldo %% 4 == 0");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(G)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldo) * 4, static_cast<cuuint64_t>(ldo) * 4 * M};
+  cuuint32_t box[3] = {16, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(INVMOE_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (%d)", (int)r);
+  return INVMOE_OK;
+}
+
 // Raise a kernel's dynamic shared-memory limit once per device (devices 0..63
 // are remembered in `done`; a higher device index sets it on every call).
 int set_smem_attr(const void* kernel, int bytes, std::atomic<uint64_t>& done) {
@@ -107,6 +126,10 @@ int launch(const GemmCall& c, cudaStream_t st) {
   rc = B_MN ? make_tmap(&tb, c.B, c.b_rows, c.b_outer, 64)
             : make_tmap(&tb, c.B, c.K, c.b_rows, BN >= 128 ? 128 : BN);
   if (rc) return rc;
+  CUtensorMap to = ta;   // read only in K-grouped mode
+  if (KG && c.G > 0 && c.M > 0 && c.N > 0 &&
+      (rc = make_tmap_out_grouped_f32(&to, c.out, c.N, c.M, c.G, c.ldo)))
+    return rc;
 
   static std::atomic<uint64_t> attr_set{0};
   if ((rc = set_smem_attr(reinterpret_cast<const void*>(tc_gemm_kernel<BN, MT, EPI, STAGES, A_MN, B_MN, KG>),
@@ -125,7 +148,7 @@ int launch(const GemmCall& c, cudaStream_t st) {
   const int grid = static_cast<int>(max_units < sms ? max_units : sms);
   if ((rc = check_cuda(cudaMemsetAsync(p.sched, 0, sizeof(int), st), "cudaMemsetAsync"))) return rc;
   ProfScope prof(c.name ? c.name : "tc_gemm", st);
-  tc_gemm_kernel<BN, MT, EPI, STAGES, A_MN, B_MN, KG><<<grid, S::THREADS, S::SMEM_BYTES, st>>>(ta, tb, p);
+  tc_gemm_kernel<BN, MT, EPI, STAGES, A_MN, B_MN, KG><<<grid, S::THREADS, S::SMEM_BYTES, st>>>(ta, tb, to, p);
   return check_cuda(cudaGetLastError(), "tc_gemm_kernel launch");
 }
 

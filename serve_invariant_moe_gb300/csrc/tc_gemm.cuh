@@ -319,7 +319,7 @@ __device__ __forceinline__ void zero_k_tail(uint8_t* base, int nbox, int rem, in
 template <int BN, int MT, int EPI, int STAGES, bool A_MN = false, bool B_MN = false, bool KG = false>
 __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
   using S = GemmShape<BN, MT, EPI, STAGES>;
   static_assert(A_MN == KG, "an MN-major A only in K-grouped mode, and K-grouped mode needs it");
   static_assert(!KG || B_MN, "K-grouped mode reads both operands MN-major");
@@ -609,13 +609,55 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
         const bool m64 = tile_rows <= 64;
         const int wrow = m64 ? q * 16 : q * 32;
         const int rows_valid = m64 ? max(0, min(16, tile_rows - q * 16)) : tile_rows - q * 32;
-        if (EPI == EPI_F32) {
+        if (KG && !m64) {
+          // K-grouped fp32 D: each 32-row x 16-column piece goes out through the warp's staging
+          // buffer (already in the 64-byte swizzle layout) as one bulk tensor store; the store map
+          // is [G][M][N], so rows past the group's M and columns past N are clipped, not written
+          const int n0 = U.nb * BN;
+          const int m0 = U.a_m0 + t * kBM + wrow;
+          uint8_t* stg = ostage + ew * kOutStageBytes;
+#pragma unroll 1
+          for (int c = half; c < BN / 32; c += NPART) {
+            uint32_t v[32];
+            tmem_ld32(tbase + c * 32, v);
+            tmem_ld_wait();
+            tmem_reg_fence(v);
+            if (U.kcount == 0) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = 0u;       // a group with no rows: the sum over nothing
+            }
+            if (rows_valid > 0) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int col = n0 + c * 32 + 16 * h;
+                if (col >= p.N) break;
+                if (lane == 0) bulk_wait_group_read0();    // the previous piece has left the buffer
+                __syncwarp();
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq)
+                  *reinterpret_cast<uint4*>(stg + lane * 64 + ((qq ^ ((lane >> 1) & 3)) << 4)) =
+                      make_uint4(v[16 * h + 4 * qq], v[16 * h + 4 * qq + 1], v[16 * h + 4 * qq + 2],
+                                 v[16 * h + 4 * qq + 3]);
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                  tma_store_3d(&tmO, stg, col, m0, U.g);
+                  bulk_commit_group();
+                }
+              }
+            }
+          }
+        } else if (EPI == EPI_F32) {
           // the warp's 32 rows start at tile row q*32; lane L stores row r of them
           const int n0 = U.nb * BN;
           uint8_t* obase = rows_valid > 0 ? reinterpret_cast<uint8_t*>(static_cast<float*>(p.out) +
                                                 (static_cast<long long>(U.row0) + t * kBM + wrow) * p.ldo + n0)
                                           : nullptr;
           uint8_t* stg = ostage + ew * kOutStageBytes;
+          if (KG) {
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
+          }
 #pragma unroll 1
           for (int c = half; c < BN / 32; c += NPART) {
             uint32_t v[32];
@@ -695,6 +737,8 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
       mbar_arrive(&acce_bar[acc]);
       if (++acc == S::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
     }
+    // the bulk stores this warp issued complete before the CTA exits
+    if (KG && lane == 0) bulk_wait_group0();
   }
 
   tc_fence_before();
