@@ -119,6 +119,7 @@ GemmParams make_params(const GemmCall& c, int nb_cols) {
 template <int BN, int MT, int EPI, int STAGES, bool A_MN = false, bool B_MN = false, bool KG = false>
 int launch(const GemmCall& c, cudaStream_t st) {
   using S = GemmShape<BN, MT, EPI, STAGES>;
+  if (KG != (c.kgroup != 0)) return set_error(INVMOE_ERR_INVALID_ARG, "K-grouped flag does not match the variant");
   if (c.G > S::MAX_GROUPS) return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "more than %d groups", S::MAX_GROUPS);
   CUtensorMap ta, tb;
   int rc = A_MN ? make_tmap(&ta, c.A, c.a_rows, c.a_outer, 64) : make_tmap(&ta, c.A, c.K, c.a_rows, kBM);
