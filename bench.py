@@ -520,6 +520,21 @@ def moe_backward_timing(st, device, peaks, reps=3):
             "shared_dh": 2.0 * T * H * Fs, "shared_swiglu_bwd": 2.0 * T * 2 * Fs * H, "shared_dx": 2.0 * T * 2 * Fs * H,
             "shared_dw2": 2.0 * T * H * Fs, "shared_dw13": 2.0 * T * 2 * Fs * H,
             "router_dx": 2.0 * T * E * H, "router_dw": 2.0 * T * E * H}
+    # algorithmic DRAM bytes: weights of the experts in use, activations and gradients read and
+    # written once (bf16 activations, fp32 dh / dxp / weight gradients)
+    active = int((d["plan"][:E].cpu() > 0).sum())
+    gbytes = {"expert_dh": active * H * F * 2 + S * H * 2 + S * F * 4,
+              "expert_swiglu_bwd": active * 2 * F * H * 2 + S * H * 2 + S * F * 4 + S * 2 * F * 2 + S * F * 2,
+              "expert_dx": active * 2 * F * H * 2 + S * 2 * F * 2 + S * H * 4,
+              "expert_dw2": S * H * 2 + S * F * 2 + E * H * F * 4,
+              "expert_dw13": S * 2 * F * 2 + S * H * 2 + E * 2 * F * H * 4,
+              "shared_dh": H * Fs * 2 + T * H * 2 + T * Fs * 4,
+              "shared_swiglu_bwd": 2 * Fs * H * 2 + T * H * 2 + T * Fs * 4 + T * 2 * Fs * 2 + T * Fs * 2,
+              "shared_dx": 2 * Fs * H * 2 + T * 2 * Fs * 2 + T * H * 4,
+              "shared_dw2": T * H * 2 + T * Fs * 2 + H * Fs * 4,
+              "shared_dw13": T * 2 * Fs * 2 + T * H * 2 + 2 * Fs * H * 4,
+              "router_dx": T * E * 2 + E * H * 2 + T * H * 4,
+              "router_dw": T * E * 2 + T * H * 2 + E * H * 4}
     out = {"moe_backward_ms": round(ms, 3), "moe_backward_tokens_per_s": round(T / (ms / 1e3), 1),
            "moe_backward_tflops": round(sum(flop.values()) / (ms / 1e3) / 1e12, 1),
            "moe_backward_weight_grad_bytes": 4 * (E * 3 * F * H + 3 * Fs * H + E * H)}
@@ -530,6 +545,12 @@ def moe_backward_timing(st, device, peaks, reps=3):
             if nm in flop:
                 ach = flop[nm] / (kms / 1e3) / 1e12
                 ent.update(achieved=round(ach, 1), unit="TFLOP/s", frac=round(ach / peaks["bf16"], 4))
+                # roofline time of the kernel: max(flop / bf16 peak, bytes / measured copy bandwidth)
+                t_flop = flop[nm] / (peaks["bf16"] * 1e12) * 1e3
+                t_byte = gbytes[nm] / (peaks["hbm"] * 1e9) * 1e3
+                ent.update(algorithmic_bytes=gbytes[nm], hbm_gbs=round(gbytes[nm] / (kms / 1e3) / 1e9, 1),
+                           roofline_bound="hbm" if t_byte > t_flop else "tensor",
+                           roofline_frac=round(max(t_flop, t_byte) / kms, 4))
             out["moe_bwd_" + nm] = ent
     del r
     return out
