@@ -30,10 +30,13 @@
 //
 // K-grouped mode (weight gradients, dW_g = A_g^T B_g): group g owns the rows
 // [offsets[g], offsets[g]+counts[g]) of two MN-major operands A [rows, M] and
-// B [rows, N]; the reduction runs over the group's rows only, and the block of
-// 64 rows that crosses the group's end has the rows past it zeroed in shared
-// memory before its MMAs (the next group's rows are never multiplied in).  A
-// group with no rows gets an all-zero block.  Output rows g*M .. g*M+M-1.
+// B [rows, N]; the reduction runs over the group's rows only.  The block of 64
+// rows that crosses the group's end issues its K = 16 steps only up to the one
+// holding the group's last row (the steps after it would add exact zeros), and
+// that step's rows past the end are zeroed in shared memory before its MMAs, so
+// the next group's rows are never multiplied in.  A group with no rows gets an
+// all-zero block.  Output rows g*M .. g*M+M-1, written by bulk tensor stores
+// through a [G][M][N] map that clips rows past M and columns past N.
 //
 // Warp roles (320 threads, one CTA per SM, persistent over units):
 //   warp 0      scheduler + TMA producer (one lane): takes a unit index from a
@@ -41,7 +44,7 @@
 //               shared queue, and loads the A row tiles + B tile of each K block
 //               into a STAGES-deep shared-memory ring (128-byte swizzle)
 //   warp 1      TMEM owner + MMA issuer (one lane; the whole warp in K-grouped
-//               mode, to zero the block past a group's end): tcgen05.mma
+//               mode, to zero the rows past a group's end): tcgen05.mma
 //               kind::f16, commit frees a ring slot / publishes an accumulator
 //   warps 2..9  epilogue (two warps per TMEM lane quadrant): tcgen05.ld 32 lanes
 //               x 32 columns at a time, convert, stage through shared memory and
