@@ -191,7 +191,7 @@ def _work_table(mc, hc, counts):
         "dispatch_count": ("hbm", T * k * 4),
         "dispatch_scan": ("hbm", 2 * (T // 64) * E * 4),
         "dispatch_scatter": ("hbm", T * k * 4 * 3),
-        "gather_rows": ("hbm", S * H * 2 * 2 + S * 4),
+        "permute_rows": ("hbm", T * H * 2 + S * H * 2 + S * 4),
         "combine": ("hbm", S * H * 4 + T * H * 4 + T * H * 4 + T * H * 2 + T * k * 8),
         "lse_merge": ("hbm", T * math.ceil(V / 256) * 8 + T * 20),
         "_expert_weight_bytes": ("hbm", active * (2 * F * H + H * F) * 2),
@@ -344,7 +344,7 @@ def run_ours(args):
         nxt.update(head_backward_timing(st, device, peaks))
         torch.cuda.empty_cache()
         nxt.update(moe_backward_timing(st, device, peaks))
-    moe_names = ["router_gemm", "topk_gate", "dispatch_count", "dispatch_scan", "dispatch_scatter", "gather_rows",
+    moe_names = ["router_gemm", "topk_gate", "dispatch_count", "dispatch_scan", "dispatch_scatter", "permute_rows",
                  "expert_gemm1_swiglu", "expert_gemm2", "shared_gemm1_swiglu", "shared_gemm2", "combine"]
     head_names = ["lm_head_gemm_lse", "lse_merge"]
     moe_ms = sum(kern[n][0] / kern[n][1] for n in moe_names if n in kern)

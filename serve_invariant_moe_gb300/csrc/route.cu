@@ -1,4 +1,4 @@
-// route.cu -- top-k with lowest-index ties, gates, deterministic dispatch, gather.
+// route.cu -- top-k with lowest-index ties, gates, deterministic dispatch, permute.
 //
 // Sources: "位级一致：前沿训练的差异化关键", section "为什么比特级一致是一个复杂的问题"
 // (a router near-tie flips which expert fires; fix: a deterministic tie
@@ -205,15 +205,44 @@ __global__ void dispatch_scatter_kernel(const int32_t* __restrict__ idx, int T, 
   }
 }
 
-// xp[r, :] = x[row_token[r], :] in 16-byte vectors.
-__global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ row_token, long long R,
-                                   int vec_per_row, uint4* __restrict__ xp) {
-  const long long total = R * vec_per_row;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long r = i / vec_per_row;
-    const int c = static_cast<int>(i - r * vec_per_row);
-    xp[i] = x[static_cast<long long>(row_token[r]) * vec_per_row + c];
+// The permute, token-major: xp[slot_row[t, j], :] = x[t, :] for j < k, in
+// 16-byte vectors.  One warp per token (tokens strided over the grid's warps):
+// each X row is read once and written to its k Xp rows, so X is not re-read
+// from DRAM once the Xp writes have pushed it out of L2.  Lane j (< k) holds
+// slot j's row index; each lane keeps four vectors in flight.
+constexpr int kPermuteThreads = 256;
+__global__ void __launch_bounds__(kPermuteThreads) permute_rows_kernel(const uint4* __restrict__ x,
+                                                                      const int32_t* __restrict__ slot_row,
+                                                                      long long T, int k, int vec_per_row,
+                                                                      uint4* __restrict__ xp) {
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = static_cast<long long>(gridDim.x) * (kPermuteThreads / 32);
+  for (long long t = blockIdx.x * static_cast<long long>(kPermuteThreads / 32) + (threadIdx.x >> 5); t < T;
+       t += nwarps) {
+    const int my_row = lane < k ? __ldg(slot_row + t * k + lane) : 0;
+    const uint4* src = x + t * vec_per_row;
+    // every loop bound below is warp-uniform, so the shuffles always see all 32 lanes
+    int c0 = 0;
+    for (; c0 + 128 <= vec_per_row; c0 += 128) {
+      const int c = c0 + lane;
+      const uint4 v0 = __ldg(src + c), v1 = __ldg(src + c + 32), v2 = __ldg(src + c + 64), v3 = __ldg(src + c + 96);
+      for (int j = 0; j < k; ++j) {
+        uint4* dst = xp + static_cast<long long>(__shfl_sync(0xffffffffu, my_row, j)) * vec_per_row;
+        dst[c] = v0;
+        dst[c + 32] = v1;
+        dst[c + 64] = v2;
+        dst[c + 96] = v3;
+      }
+    }
+    // tail: the row's last vec_per_row % 128 vectors; lanes past the row's end only skip their store
+    for (; c0 < vec_per_row; c0 += 32) {
+      const int cc = c0 + lane;
+      const uint4 v = cc < vec_per_row ? __ldg(src + cc) : make_uint4(0u, 0u, 0u, 0u);
+      for (int j = 0; j < k; ++j) {
+        const long long row = __shfl_sync(0xffffffffu, my_row, j);
+        if (cc < vec_per_row) xp[row * vec_per_row + cc] = v;
+      }
+    }
   }
 }
 
@@ -281,17 +310,17 @@ int dispatch_launch(const int32_t* topk_idx, int T, int E, int k, int H, const v
   if ((rc = check_cuda(cudaGetLastError(), "dispatch_scatter_kernel"))) return rc;
   // permute
   const int vec_per_row = H / 8;
-  const long long total = S * vec_per_row;
   int sms = 0;
   if ((rc = device_sm_count(&sms))) return rc;
-  long long blocks = (total + 255) / 256;
-  const long long cap = static_cast<long long>(sms) * 16;
+  // a warp per token; at most 8 resident blocks of 256 threads per SM
+  long long blocks = (static_cast<long long>(T) + kPermuteThreads / 32 - 1) / (kPermuteThreads / 32);
+  const long long cap = static_cast<long long>(sms) * 8;
   if (blocks > cap) blocks = cap;
-  if (blocks > 0) {
-    ProfScope prof("gather_rows", st);
-    gather_rows_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(static_cast<const uint4*>(x), row_token, S,
-                                                                  vec_per_row, static_cast<uint4*>(xp));
-    if ((rc = check_cuda(cudaGetLastError(), "gather_rows_kernel"))) return rc;
+  if (blocks > 0 && vec_per_row > 0) {
+    ProfScope prof("permute_rows", st);
+    permute_rows_kernel<<<static_cast<int>(blocks), kPermuteThreads, 0, st>>>(
+        static_cast<const uint4*>(x), slot_row, T, k, vec_per_row, static_cast<uint4*>(xp));
+    if ((rc = check_cuda(cudaGetLastError(), "permute_rows_kernel"))) return rc;
   }
   return INVMOE_OK;
 }
