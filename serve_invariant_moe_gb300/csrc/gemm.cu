@@ -127,10 +127,18 @@ int launch(const GemmCall& c, cudaStream_t st) {
   rc = B_MN ? make_tmap(&tb, c.B, c.b_rows, c.b_outer, 64)
             : make_tmap(&tb, c.B, c.K, c.b_rows, BN >= 128 ? 128 : BN);
   if (rc) return rc;
-  CUtensorMap to = ta;   // read only in K-grouped mode
-  if (KG && c.G > 0 && c.M > 0 && c.N > 0 &&
-      (rc = make_tmap_out_grouped_f32(&to, c.out, c.N, c.M, c.G, c.ldo)))
-    return rc;
+  // fp32 D: a store map for the bulk-store epilogue ([G][M][N] in K-grouped mode, [1][rows][N]
+  // otherwise); without one (unaligned output) the epilogue keeps its plain stores
+  CUtensorMap to = ta;
+  bool out_map = false;
+  if (EPI == EPI_F32 && c.N > 0) {
+    const long long rows = KG ? c.M : (c.G > 0 ? c.a_rows : c.M);
+    const long long groups = KG ? c.G : 1;
+    if (rows > 0 && groups > 0 && c.ldo % 4 == 0 && (reinterpret_cast<uintptr_t>(c.out) & 15) == 0) {
+      if ((rc = make_tmap_out_grouped_f32(&to, c.out, c.N, rows, groups, c.ldo))) return rc;
+      out_map = true;
+    }
+  }
 
   static std::atomic<uint64_t> attr_set{0};
   if ((rc = set_smem_attr(reinterpret_cast<const void*>(tc_gemm_kernel<BN, MT, EPI, STAGES, A_MN, B_MN, KG>),
@@ -139,7 +147,8 @@ int launch(const GemmCall& c, cudaStream_t st) {
   int sms = 0;
   if ((rc = device_sm_count(&sms))) return rc;
 
-  const GemmParams p = make_params(c, (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) ? BN / 2 : BN);
+  GemmParams p = make_params(c, (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) ? BN / 2 : BN);
+  p.out_map = out_map ? 1 : 0;
 
   constexpr long long CH = static_cast<long long>(MT) * kBM;
   long long max_chunks = KG ? static_cast<long long>(c.G) * ((c.M + CH - 1) / CH)

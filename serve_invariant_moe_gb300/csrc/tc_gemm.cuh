@@ -95,6 +95,7 @@ struct GemmParams {
   void* out2;
   long long ldo2;
   int kgroup;             // 1: K-grouped mode (weight gradients); M = output rows per group
+  int out_map;            // fp32 D: 1 if the output store map was built (bulk tensor stores)
 };
 
 // Epilogue stores.  After tcgen05.ld.32x32b each lane of a warp holds one row
@@ -612,12 +613,15 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
         const bool m64 = tile_rows <= 64;
         const int wrow = m64 ? q * 16 : q * 32;
         const int rows_valid = m64 ? max(0, min(16, tile_rows - q * 16)) : tile_rows - q * 32;
-        if (KG && !m64) {
-          // K-grouped fp32 D: each 32-row x 16-column piece goes out through the warp's staging
-          // buffer (already in the 64-byte swizzle layout) as one bulk tensor store; the store map
-          // is [G][M][N], so rows past the group's M and columns past N are clipped, not written
+        // fp32 D through bulk tensor stores: each 32-row x 16-column piece goes out through the
+        // warp's staging buffer (already in the 64-byte swizzle layout) as one store.  The map is
+        // [G][M][N] in K-grouped mode (rows past the group's M and columns past N are clipped) and
+        // [1][rows][N] otherwise, where only whole 32-row slabs of one group take this path (a
+        // slab that ends inside the tile would reach the next group's rows).
+        if (EPI == EPI_F32 && p.out_map && !m64 && (KG ? rows_valid > 0 : rows_valid >= 32)) {
           const int n0 = U.nb * BN;
-          const int m0 = U.a_m0 + t * kBM + wrow;
+          const int m0 = KG ? U.a_m0 + t * kBM + wrow : U.row0 + t * kBM + wrow;
+          const int z0 = KG ? U.g : 0;
           uint8_t* stg = ostage + ew * kOutStageBytes;
 #pragma unroll 1
           for (int c = half; c < BN / 32; c += NPART) {
@@ -625,11 +629,11 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
             tmem_ld32(tbase + c * 32, v);
             tmem_ld_wait();
             tmem_reg_fence(v);
-            if (U.kcount == 0) {
+            if (KG && U.kcount == 0) {
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = 0u;       // a group with no rows: the sum over nothing
             }
-            if (rows_valid > 0) {
+            {
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
                 const int col = n0 + c * 32 + 16 * h;
@@ -644,7 +648,7 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
                 fence_proxy_async_shared();
                 __syncwarp();
                 if (lane == 0) {
-                  tma_store_3d(&tmO, stg, col, m0, U.g);
+                  tma_store_3d(&tmO, stg, col, m0, z0);
                   bulk_commit_group();
                 }
               }
@@ -657,8 +661,8 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
                                                 (static_cast<long long>(U.row0) + t * kBM + wrow) * p.ldo + n0)
                                           : nullptr;
           uint8_t* stg = ostage + ew * kOutStageBytes;
-          if (KG) {
-            if (lane == 0) bulk_wait_group_read0();
+          if (p.out_map) {
+            if (lane == 0) bulk_wait_group_read0();   // a bulk store may still read the buffer
             __syncwarp();
           }
 #pragma unroll 1
@@ -741,7 +745,7 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
       if (++acc == S::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
     }
     // the bulk stores this warp issued complete before the CTA exits
-    if (KG && lane == 0) bulk_wait_group0();
+    if (EPI == EPI_F32 && lane == 0) bulk_wait_group0();
   }
 
   tc_fence_before();
