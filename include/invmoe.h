@@ -108,7 +108,8 @@ int invmoe_check(void* workspace, void* stream);
  *                  logits (softmax renormalised over the top-k, fp32, i ascending)
  *   plan         see invmoe_plan_len (deterministic counting sort; no atomics
  *                  decide any position)
- *   xp[r, :]     = x[row_token[r], :]   (bf16 gather, 16-byte vectors)
+ *   xp[r, :]     = x[row_token[r], :]   (bf16 copies, 16-byte vectors; each x row is read once
+ *                                        and written to its k permuted rows)
  *
  * x [T, H] bf16, w_router [E, H] bf16, logits [T, E] fp32, topk_idx [T, k] int32,
  * topk_w [T, k] fp32, plan int32[invmoe_plan_len], xp [T*k, H] bf16.
