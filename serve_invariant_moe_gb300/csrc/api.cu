@@ -482,7 +482,7 @@ int moe_grouped_ffn_backward(const void* xp, const int32_t* plan, const void* w1
   {
     GemmCall g{};
     g.name = "expert_swiglu_bwd";
-    g.variant = GV_SWIGLU_BWD_BN256_MT2;
+    g.variant = GV_PAIR_SWIGLU_BWD;
     g.A = xp; g.a_rows = S; g.B = w13; g.b_rows = static_cast<long long>(E) * 2 * F;
     g.K = H; g.N = F; g.G = E; g.counts = counts; g.offsets = offsets; g.b_group_rows = 2 * F; g.b_up_rows = F;
     g.out = dgu; g.ldo = 2 * F; g.out2 = h; g.ldo2 = F; g.aux = dh; g.ld_aux = F; g.status = status;
