@@ -116,7 +116,12 @@ ProfScope::ProfScope(const char* name, cudaStream_t st) : idx_(-1), st_(st) {
   if (!g_prof_on.load(std::memory_order_relaxed)) return;
   std::lock_guard<std::mutex> lk(g_prof_mu);
   ProfRec r{name, take_event(), take_event()};
-  if (!r.a || !r.b) return;
+  if (!r.a || !r.b) {
+    // keep whichever event was obtained for later use
+    if (r.a) g_prof_pool.push_back(r.a);
+    if (r.b) g_prof_pool.push_back(r.b);
+    return;
+  }
   cudaEventRecord(r.a, st);
   g_prof_recs.push_back(r);
   idx_ = static_cast<long>(g_prof_recs.size()) - 1;
