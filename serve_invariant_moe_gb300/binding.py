@@ -25,6 +25,10 @@ def _req(t, dtype, name, shape=None):
         raise ValueError(f"{name} is required")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    # the library launches on the current device: a pointer into another GPU's memory
+    # must not reach a kernel
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, but the current CUDA device is cuda:{torch.cuda.current_device()}")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -32,6 +36,18 @@ def _req(t, dtype, name, shape=None):
     if shape is not None and tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     return t
+
+
+def _opt(t, dtype, name, shape=None):
+    """_req for an optional tensor (None passes)."""
+    return None if t is None else _req(t, dtype, name, shape)
+
+
+def _req_plan(plan, T, E, k):
+    _req(plan, torch.int32, "plan")
+    if plan.numel() < plan_len(T, E, k):
+        raise ValueError("plan is too small")
+    return plan
 
 
 def plan_len(T, E, k) -> int:
@@ -169,6 +185,10 @@ def lm_logprob_kl(hidden, w_vocab, target, workspace, rollout_logp=None, beta=2.
         _req(rollout_logp, torch.float32, "rollout_logp", (T,))
         k3 = torch.empty(T, dtype=torch.float32, device=dev) if k3 is None else k3
         mask = torch.empty(T, dtype=torch.uint8, device=dev) if mask is None else mask
+        _req(k3, torch.float32, "k3", (T,))
+        _req(mask, torch.uint8, "mask", (T,))
+    _req(logp, torch.float32, "logp", (T,))
+    _req(lse, torch.float32, "lse", (T,))
     _req(workspace, torch.uint8, "workspace")
     check(lib().lm_logprob_kl(_p(hidden), _p(w_vocab), _p(target), _p(rollout_logp), T, H, V, float(beta),
                               _p(logits), _p(logp), _p(lse), _p(k3), _p(mask), _p(workspace), workspace.numel(),
@@ -238,10 +258,13 @@ def moe_combine_backward(dout, y, topk_w, plan, E, k, dy=None, dgate=None, dout_
     _req(dout, torch.float32, "dout")
     _req(y, torch.float32, "y", (T * k, H))
     _req(topk_w, torch.float32, "topk_w", (T, k))
-    _req(plan, torch.int32, "plan")
+    _req_plan(plan, T, E, k)
     dy = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev) if dy is None else dy
     dgate = torch.empty((T, k), dtype=torch.float32, device=dev) if dgate is None else dgate
     db = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if dout_bf16 is True else (dout_bf16 or None)
+    _req(dy, torch.bfloat16, "dy", (T * k, H))
+    _req(dgate, torch.float32, "dgate", (T, k))
+    _opt(db, torch.bfloat16, "dout_bf16", (T, H))
     check(lib().moe_combine_backward(_p(dout), _p(y), _p(topk_w), _p(plan), T, H, E, k, _p(dy), _p(dgate), _p(db),
                                      _stream()))
     return dict(dy=dy, dgate=dgate, dout_bf16=db)
@@ -261,6 +284,7 @@ def moe_grouped_ffn_backward(xp, plan, w13, w2, dy, T, k, workspace, dxp=None, d
     _req(w13, torch.bfloat16, "w13")
     _req(w2, torch.bfloat16, "w2", (E, H, F))
     _req(dy, torch.bfloat16, "dy", (S, H))
+    _req_plan(plan, T, E, k)
     _req(workspace, torch.uint8, "workspace")
 
     def alloc(v, shape):
@@ -270,11 +294,19 @@ def moe_grouped_ffn_backward(xp, plan, w13, w2, dy, T, k, workspace, dxp=None, d
 
     dxp = torch.empty((S, H), dtype=torch.float32, device=dev) if dxp is None else dxp
     dw13, dw2 = alloc(dw13, (E, 2 * F, H)), alloc(dw2, (E, H, F))
+    _req(dxp, torch.float32, "dxp", (S, H))
+    _opt(dw13, torch.float32, "dw13", (E, 2 * F, H))
+    _opt(dw2, torch.float32, "dw2", (E, H, F))
     if Fs:
         _req(x_shared, torch.bfloat16, "x_shared", (T, H))
+        _req(ws13, torch.bfloat16, "ws13", (2 * Fs, H))
+        _req(ws2, torch.bfloat16, "ws2", (H, Fs))
         _req(dout_bf16, torch.bfloat16, "dout_bf16", (T, H))
         dx_shared = torch.empty((T, H), dtype=torch.float32, device=dev) if dx_shared is None else dx_shared
         dws13, dws2 = alloc(dws13, (2 * Fs, H)), alloc(dws2, (H, Fs))
+        _req(dx_shared, torch.float32, "dx_shared", (T, H))
+        _opt(dws13, torch.float32, "dws13", (2 * Fs, H))
+        _opt(dws2, torch.float32, "dws2", (H, Fs))
     else:
         dx_shared = dws13 = dws2 = None
     check(lib().moe_grouped_ffn_backward(_p(xp), _p(plan), _p(w13), _p(w2), _p(dy), T, H, E, k, F, _p(dxp), _p(dw13),
@@ -296,11 +328,15 @@ def moe_route_backward(x, w_router, topk_idx, topk_w, dgate, dxp, plan, workspac
     _req(topk_w, torch.float32, "topk_w", (T, k))
     _req(dgate, torch.float32, "dgate", (T, k))
     _req(dxp, torch.float32, "dxp", (T * k, H))
+    _req_plan(plan, T, E, k)
+    _opt(dx_shared, torch.float32, "dx_shared", (T, H))
     _req(workspace, torch.uint8, "workspace")
     dx = torch.empty((T, H), dtype=torch.float32, device=dev) if dx is None else dx
     if dw_router is True:
         dw_router = torch.empty((E, H), dtype=torch.float32, device=dev)
     dw_router = None if dw_router is False else dw_router
+    _req(dx, torch.float32, "dx", (T, H))
+    _opt(dw_router, torch.float32, "dw_router", (E, H))
     check(lib().moe_route_backward(_p(x), _p(w_router), _p(topk_idx), _p(topk_w), _p(dgate), _p(dxp), _p(plan),
                                    _p(dx_shared), T, H, E, k, _p(dx), _p(dw_router), _p(workspace),
                                    workspace.numel(), _stream()))

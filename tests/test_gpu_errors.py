@@ -45,3 +45,36 @@ def test_host_validation_errors_raise():
     with pytest.raises(InvmoeError) as e:
         binding.moe_route_topk(x, wr, 2, torch.zeros(16, dtype=torch.uint8, device="cuda"))
     assert e.value.code == -3
+
+
+def test_binding_refuses_wrong_caller_buffers():
+    """Caller-provided buffers of the wrong shape or dtype are refused on the host, before any
+    kernel could write past them."""
+    from serve_invariant_moe_gb300 import binding
+    T, H, V, E, k = 64, 128, 512, 8, 2
+    dev = "cuda"
+    ws = binding.new_workspace(binding.workspace_size(T, H, E, k, 128, 0, V), dev)
+    hidden = torch.zeros(T, H, dtype=torch.bfloat16, device=dev)
+    wv = torch.zeros(V, H, dtype=torch.bfloat16, device=dev)
+    target = torch.zeros(T, dtype=torch.int32, device=dev)
+    with pytest.raises(ValueError, match="logp"):
+        binding.lm_logprob_kl(hidden, wv, target, ws, logp=torch.empty(T - 1, device=dev))
+    with pytest.raises(ValueError, match="mask"):
+        binding.lm_logprob_kl(hidden, wv, target, ws, rollout_logp=torch.zeros(T, device=dev),
+                              mask=torch.empty(T, dtype=torch.int32, device=dev))
+    x = torch.zeros(T, H, dtype=torch.bfloat16, device=dev)
+    wr = torch.zeros(E, H, dtype=torch.bfloat16, device=dev)
+    idx = torch.zeros(T, k, dtype=torch.int32, device=dev)
+    w = torch.zeros(T, k, dtype=torch.float32, device=dev)
+    dxp = torch.zeros(T * k, H, dtype=torch.float32, device=dev)
+    small_plan = torch.zeros(binding.plan_len(T, E, k) - 1, dtype=torch.int32, device=dev)
+    with pytest.raises(ValueError, match="plan"):
+        binding.moe_route_backward(x, wr, idx, w, w, dxp, small_plan, ws)
+    plan = torch.zeros(binding.plan_len(T, E, k), dtype=torch.int32, device=dev)
+    with pytest.raises(ValueError, match="dw_router"):
+        binding.moe_route_backward(x, wr, idx, w, w, dxp, plan, ws, dw_router=torch.empty(E, H - 8, device=dev))
+    y = torch.zeros(T * k, H, dtype=torch.float32, device=dev)
+    dout = torch.zeros(T, H, dtype=torch.float32, device=dev)
+    with pytest.raises(ValueError, match="dy"):
+        binding.moe_combine_backward(dout, y, w, plan, E, k, dy=torch.empty(T * k, H, device=dev))
+    torch.cuda.synchronize()
