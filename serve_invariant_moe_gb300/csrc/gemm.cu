@@ -181,7 +181,16 @@ int launch_pair(const GemmCall& c, cudaStream_t st) {
     return rc;
   int sms = 0;
   if ((rc = device_sm_count(&sms))) return rc;
-  const GemmParams p = make_params(c, (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) ? 128 : 256);
+  GemmParams p = make_params(c, (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) ? 128 : 256);
+  // fp32 D: a [1][rows][N] store map for the bulk-store epilogue (none for an unaligned output)
+  CUtensorMap to = ta;
+  if (EPI == EPI_F32 && c.N > 0) {
+    const long long rows = c.G > 0 ? c.a_rows : c.M;
+    if (rows > 0 && c.ldo % 4 == 0 && (reinterpret_cast<uintptr_t>(c.out) & 15) == 0) {
+      if ((rc = make_tmap_out_grouped_f32(&to, c.out, c.N, rows, 1, c.ldo))) return rc;
+      p.out_map = 1;
+    }
+  }
   constexpr long long CH = 2LL * kBM;
   long long max_chunks = (c.G > 0) ? (c.a_rows + CH - 1) / CH + c.G : (c.M + CH - 1) / CH;
   long long max_units = max_chunks * p.n_blocks;
@@ -201,7 +210,7 @@ int launch_pair(const GemmCall& c, cudaStream_t st) {
   cfg.numAttrs = 1;
   if ((rc = check_cuda(cudaMemsetAsync(p.sched, 0, sizeof(int), st), "cudaMemsetAsync"))) return rc;
   ProfScope prof(c.name ? c.name : "tc_gemm_pair", st);
-  rc = check_cuda(cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<EPI, STAGES, A_MN, B_MN>, ta, tb, p),
+  rc = check_cuda(cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<EPI, STAGES, A_MN, B_MN>, ta, tb, to, p),
                   "cudaLaunchKernelEx");
   if (rc) return rc;
   return check_cuda(cudaGetLastError(), "tc_gemm_pair_kernel launch");

@@ -67,7 +67,7 @@ __device__ __forceinline__ uint32_t dlogit_bf16x2(float z0, float z1, bool t0, b
 template <int EPI, int STAGES, bool A_MN = false, bool B_MN = false>
 __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmO, const GemmParams p) {
   using S = PairShape<EPI, STAGES>;
   constexpr int BN = S::BN;
   static_assert(!(B_MN && EPI == EPI_SWIGLU), "SwiGLU reads gate/up row blocks of a K-major B");
@@ -386,6 +386,38 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
             stage_store_rows64(stg, packed, obase + c * 64, p.ldo * 2, rows_valid, (p.N - (n0 + c * 32)) * 2);
           }
         }
+      } else if (EPI == EPI_F32 && p.out_map && U.rows - (static_cast<int>(rank) * kBM + q * 32) >= 32) {
+        // a whole 32-row slab of one group: each 32-row x 16-column piece leaves the warp's
+        // staging buffer (64-byte swizzle layout) as one bulk tensor store through the
+        // [1][rows][N] map, which clips columns past N
+        const int n0 = U.nb * BN;
+        const int m0 = U.row0 + static_cast<int>(rank) * kBM + q * 32;
+        uint8_t* stg = ostage + ew * kOutStageBytes;
+#pragma unroll 1
+        for (int c = half; c < BN / 32; c += 2) {
+          uint32_t v[32];
+          tmem_ld32(tbase + c * 32, v);
+          tmem_ld_wait();
+          tmem_reg_fence(v);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = n0 + c * 32 + 16 * h;
+            if (col >= p.N) break;
+            if (lane == 0) bulk_wait_group_read0();    // the previous piece has left the buffer
+            __syncwarp();
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq)
+              *reinterpret_cast<uint4*>(stg + lane * 64 + ((qq ^ ((lane >> 1) & 3)) << 4)) =
+                  make_uint4(v[16 * h + 4 * qq], v[16 * h + 4 * qq + 1], v[16 * h + 4 * qq + 2],
+                             v[16 * h + 4 * qq + 3]);
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tmO, stg, col, m0, 0);
+              bulk_commit_group();
+            }
+          }
+        }
       } else if (EPI == EPI_F32) {
         const int n0 = U.nb * BN;
         const int rows_valid = U.rows - (static_cast<int>(rank) * kBM + q * 32);
@@ -393,6 +425,10 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
                                               (static_cast<long long>(U.row0) + rank * kBM + q * 32) * p.ldo + n0)
                                         : nullptr;
         uint8_t* stg = ostage + ew * kOutStageBytes;
+        if (p.out_map) {
+          if (lane == 0) bulk_wait_group_read0();    // a bulk store may still read the buffer
+          __syncwarp();
+        }
 #pragma unroll 1
         for (int c = half; c < BN / 32; c += 2) {
           uint32_t v[32];
@@ -468,6 +504,8 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
       mbar_arrive_remote(acce_leader0 + static_cast<uint32_t>(acc * 8));
       if (++acc == S::ACC_STAGES) { acc = 0; acc_phase ^= 1u; }
     }
+    // the bulk stores this warp issued complete before the CTA exits
+    if (EPI == EPI_F32 && lane == 0) bulk_wait_group0();
   }
 
   tc_fence_before();
