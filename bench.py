@@ -340,6 +340,7 @@ def run_ours(args):
     nxt = next_rows_timing(st, device) if rank == 0 else None
     if nxt is not None:
         nxt.update(qwen_layer_timing(device, peaks))
+        nxt.update(tiny_latency(device))
     if nxt is not None and not args.no_backward:
         nxt.update(head_backward_timing(st, device, peaks))
         torch.cuda.empty_cache()
@@ -553,6 +554,40 @@ def moe_backward_timing(st, device, peaks, reps=3):
                            roofline_frac=round(max(t_flop, t_byte) / kms, 4))
             out["moe_bwd_" + nm] = ent
     del r
+    return out
+
+
+def tiny_latency(device, reps=200):
+    """The tiny configuration (T = 64, H = 256, E = 8 top-2, F = 512; head V = 4096), whose calls are
+    launch-bound: microseconds per call of the layer through prefill, decode and a CUDA-graph replay
+    of decode, and of the head, outside the timed region (device time between events around `reps`
+    back-to-back calls)."""
+    import torch
+    from serve_invariant_moe_gb300 import api, binding, synth
+    mc, hc = synth.TINY, synth.TINY_HEAD
+    x, wr = synth.moe_activations(mc)
+    w13, w2 = synth.expert_weights(mc, device)
+    layer = api.MoELayer(api.MoEWeights(wr.to(device), w13, w2, mc.k))
+    xd = x.to(device)
+    graphs = api.DecodeGraphs(layer, buckets=(mc.T,))
+    hidden, wv, target, _, _ = synth.head_inputs(hc, device)
+    hd, td = hidden.to(device), target.to(device)
+    ws = binding.new_workspace(binding.workspace_size(hc.T, hc.H, V=hc.V), device)
+    calls = {"prefill": lambda: layer.prefill(xd), "decode": lambda: layer.decode(xd),
+             "decode_graph": lambda: graphs(xd), "head": lambda: binding.lm_logprob_kl(hd, wv, td, ws)}
+    out = {}
+    for name, fn in calls.items():
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        out[f"tiny_{name}_us"] = round(e0.elapsed_time(e1) / reps * 1e3, 1)
+    binding.check_status(ws)
     return out
 
 
