@@ -142,7 +142,20 @@ __global__ void dispatch_scan_kernel(int32_t* __restrict__ chunk_counts, int NC,
   const int e = threadIdx.x;
   int run = 0;
   if (e < E) {
-    for (int c = 0; c < NC; ++c) {
+    // eight chunks' counts are loaded before any of them is overwritten, so the loads of a
+    // batch are in flight together instead of one dependent round trip per chunk
+    int c = 0;
+    for (; c + 8 <= NC; c += 8) {
+      int v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = chunk_counts[static_cast<long long>(c + i) * E + e];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        chunk_counts[static_cast<long long>(c + i) * E + e] = run;
+        run += v[i];
+      }
+    }
+    for (; c < NC; ++c) {
       const long long i = static_cast<long long>(c) * E + e;
       const int v = chunk_counts[i];
       chunk_counts[i] = run;
