@@ -16,9 +16,9 @@ What the layer computes, from the pages:
 
 The method does not change the mathematics of an MoE layer, only the order of
 its floating-point reductions, so the oracle is the textbook definition written
-out in float64 over bf16-rounded inputs.  Readings where the pages are silent
-(gate function, intermediate precisions, NaN rank) are listed in the design doc and
-restated at each function.
+out in float64 over bf16-rounded inputs.  Where the pages are silent (gate
+function, intermediate precisions, NaN rank) the reading taken is stated at the
+function that depends on it.
 """
 import numpy as np
 
