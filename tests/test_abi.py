@@ -84,3 +84,29 @@ def test_validation_rejects_before_any_launch(lib):
     assert rc == -2
     rc = lib.invmoe_gemm_bf16(null, null, 64, 64, 64, null, 7, ctypes.c_void_p(256), 4096, null)
     assert rc == -1
+
+
+def _declared_arity():
+    """Number of parameters of every function include/invmoe.h declares (comments stripped)."""
+    out = {}
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if not f.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", f)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        for m in re.finditer(r"^\s*(?:const\s+)?(?:int|size_t|char\s*\*|void)\s*\**\s*(\w+)\s*\(([^)]*)\)\s*;",
+                             src, re.M | re.S):
+            params = m.group(2).strip()
+            out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_prototypes_match_the_header_arity():
+    """The ctypes prototypes pass exactly as many arguments as the C declarations take: a
+    drift between the two would hand a kernel wrong pointers."""
+    from serve_invariant_moe_gb300 import _lib
+    arity = _declared_arity()
+    assert set(arity) == set(_lib.PROTOTYPES)
+    for name, (_, args) in _lib.PROTOTYPES.items():
+        assert len(args) == arity[name], (name, len(args), arity[name])
