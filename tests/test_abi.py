@@ -110,3 +110,18 @@ def test_binding_prototypes_match_the_header_arity():
     assert set(arity) == set(_lib.PROTOTYPES)
     for name, (_, args) in _lib.PROTOTYPES.items():
         assert len(args) == arity[name], (name, len(args), arity[name])
+
+
+def test_binding_refuses_host_tensors_before_any_call():
+    """The product path has no CPU fallback: host tensors are refused by the binding."""
+    import torch
+    from serve_invariant_moe_gb300 import binding
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    wr = torch.zeros(8, 64, dtype=torch.bfloat16)
+    ws = torch.zeros(4096, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.moe_route_topk(x, wr, 2, ws)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.rl_token_loss(torch.zeros(4), torch.zeros(4), torch.zeros(4))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.gemm_bf16(x, wr, ws)
