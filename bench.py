@@ -31,10 +31,37 @@ UNIT = "tokens/s"
 WORKLOAD = "glm_scale_moe(T=8192,H=6144,E=256,k=8,F=2048,shared F=2048) + glm_scale_head(V=151552)"
 
 
+# Spec-sheet peaks of one GB300, quoted beside the measured ones (fractions against
+# these are reported as ``frac_spec``): HBM3e ~7.9 TB/s, dense bf16 2.25 PFLOP/s.
+SPEC_HBM_GBS = 7900.0
+SPEC_BF16_TFLOPS = 2250.0
+
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one full-size launch of
-# the dominant kernel, from a one-pass ncu capture of this step (see profiles/); set to
-# None whenever that kernel's code changes until it is captured again.
-TRAFFIC_BYTES = {"lm_head_gemm_lse": 5.8139e9 + 0.0414e9}
+# the dominant kernel, from a one-kernel ncu capture of the vocabulary projection at
+# T = 8192 and V = 151552 / 8, 151552 / 4 and 151552 (``--profile-case lm_head_traffic``),
+# together with the SHA-256 of the sources that define that kernel when it was captured.
+# The figure is reported only while those sources are unchanged; otherwise it is null.
+TRAFFIC = {"lm_head_gemm_lse": dict(bytes=None, sources_sha256=None)}
+TRAFFIC_SOURCES = ["serve_invariant_moe_gb300/csrc/tc_gemm2.cuh", "serve_invariant_moe_gb300/csrc/ptx.cuh",
+                   "serve_invariant_moe_gb300/csrc/gemm.cu", "serve_invariant_moe_gb300/csrc/api.cu"]
+
+
+def kernel_sources_sha256():
+    """SHA-256 over the sources that define the dominant kernel (in TRAFFIC_SOURCES order)."""
+    import hashlib
+    h = hashlib.sha256()
+    for rel in TRAFFIC_SOURCES:
+        with open(os.path.join(_ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_bytes(kernel):
+    """Captured DRAM bytes per launch of `kernel`, or None if not captured for the current sources."""
+    t = TRAFFIC.get(kernel)
+    if not t or t["bytes"] is None or t["sources_sha256"] != kernel_sources_sha256():
+        return None
+    return t["bytes"]
 
 
 def _peaks():
@@ -198,6 +225,13 @@ def _work_table(mc, hc, counts):
     }
 
 
+def _head_bytes(mc, hc):
+    """Algorithmic DRAM bytes of one LM-head launch: the vocabulary weights and the hidden states
+    read once, the LSE partials and the target logits written once."""
+    T, H, V = mc.T, mc.H, hc.V
+    return V * H * 2 + T * H * 2 + T * math.ceil(V / 256) * 8 + T * 4
+
+
 def _gemm_bytes(mc, counts):
     """Algorithmic DRAM bytes of the expert and shared GEMMs (weights of the experts in use + activations
     read and written once): with these the roofline time is max(flop / bf16 peak, bytes / HBM peak)."""
@@ -239,11 +273,10 @@ def run_ours(args):
         st.run()
     torch.cuda.synchronize()
 
-    # ---------------- timed region: device-resident inputs
+    # ---------------- timed region: device-resident inputs, no instrumentation
     clocks = ClockSampler(_smi_id(device))
     clocks.start()
     time.sleep(0.3)
-    lib.invmoe_profile_enable(1)
     stream = torch.cuda.current_stream()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -255,15 +288,27 @@ def run_ours(args):
     ev1.record(stream)
     torch.cuda.synchronize()
     _barrier(ws)
-    lib.invmoe_profile_enable(0)
     ms_total = ev0.elapsed_time(ev1)
     clk = clocks.stop()
-    kern = _profile_collect(lib)
     binding.check_status(st.ws_head)
     binding.check_status(st.layer._decode["ws"])
 
     ms_step = _max_over_ranks(ms_total / args.steps, ws, device)
     value = ws * T / (ms_step / 1e3)
+
+    # ---------------- per-kernel pass: the same K steps again, with the library's CUDA events
+    # recorded around every launch on its stream (kept out of the headline loop above)
+    lib.invmoe_profile_enable(1)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        st.run()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    lib.invmoe_profile_enable(0)
+    ms_profiled = ev0.elapsed_time(ev1) / args.steps
+    kern = _profile_collect(lib)
+    binding.check_status(st.ws_head)
 
     # ---------------- end to end: host inputs in pinned memory, results back to the host
     x_pin = st.x_host.pin_memory()
@@ -278,7 +323,7 @@ def run_ours(args):
     host_in = dict(x=x_pin, target=t_pin, rollout=r_pin)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(1, min(args.steps, 10))
+    e2e_steps = max(1, args.steps)
     _barrier(ws)
     torch.cuda.synchronize()
     e0.record(stream)
@@ -314,26 +359,34 @@ def run_ours(args):
         if kind == "tensor":
             ach = amount / (avg_ms / 1e3) / 1e12
             per_kernel[nm] = dict(ms=round(avg_ms, 4), launches=c, bound="tensor", achieved=round(ach, 1),
-                                  unit="TFLOP/s", frac=round(ach / peaks["bf16"], 4))
+                                  unit="TFLOP/s", frac=round(ach / peaks["bf16"], 4),
+                                  frac_spec=round(ach / SPEC_BF16_TFLOPS, 4))
             if nm in gbytes:
                 # memory side of the same kernel: algorithmic bytes over the measured copy bandwidth
                 t_flop = amount / (peaks["bf16"] * 1e12) * 1e3
                 t_byte = gbytes[nm] / (peaks["hbm"] * 1e9) * 1e3
                 per_kernel[nm].update(algorithmic_bytes=gbytes[nm],
                                       hbm_gbs=round(gbytes[nm] / (avg_ms / 1e3) / 1e9, 1),
+                                      hbm_frac_spec=round(gbytes[nm] / (avg_ms / 1e3) / 1e9 / SPEC_HBM_GBS, 4),
                                       roofline_bound="hbm" if t_byte > t_flop else "tensor",
                                       roofline_frac=round(max(t_flop, t_byte) / avg_ms, 4))
         else:
             ach = amount / (avg_ms / 1e3) / 1e9
             per_kernel[nm] = dict(ms=round(avg_ms, 4), launches=c, bound="hbm", achieved=round(ach, 1),
-                                  unit="GB/s", frac=round(ach / peaks["hbm"], 4))
+                                  unit="GB/s", frac=round(ach / peaks["hbm"], 4),
+                                  frac_spec=round(ach / SPEC_HBM_GBS, 4))
     dom = max(kern.items(), key=lambda kv: kv[1][0])[0] if kern else None
     roof = None
     if dom in per_kernel:
         pk = per_kernel[dom]
         roof = dict(kernel=dom, bound=pk["bound"], achieved=pk["achieved"],
                     peak=peaks["bf16"] if pk["bound"] == "tensor" else peaks["hbm"], unit=pk["unit"],
-                    frac=pk["frac"], traffic=TRAFFIC_BYTES.get(dom), peak_source=peaks["src"] + " (burst)")
+                    frac=pk["frac"], traffic=traffic_bytes(dom), peak_source=peaks["src"] + " (burst)",
+                    peak_spec=SPEC_BF16_TFLOPS if pk["bound"] == "tensor" else SPEC_HBM_GBS,
+                    frac_spec=pk["frac_spec"], timing="CUDA events around each launch, second pass of the K steps")
+        if dom in work and work[dom][0] == "tensor" and roof["traffic"] is not None:
+            roof["algorithmic_bytes"] = _head_bytes(st.mc, st.hc)
+    # launches of this library's kernels in the timed region (K steps of the same sequence)
     launches = sum(c for (_, c) in kern.values())
 
     inv = invariance_check(st, device) if rank == 0 else None
@@ -363,22 +416,50 @@ def run_ours(args):
             "data": "synthetic (seeded), random-init weights",
             "config": {"workload": WORKLOAD, "tokens_per_step_per_gpu": T, "parallelism": f"token-dp{ws}",
                        "l2": "inputs larger than L2 (19.3 GB expert weights, 1.86 GB vocab weights)"},
-            "e2e": {"value": round(ws * T / (e2e_ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
             "moe_layer_tokens_per_s": round(T / (moe_ms / 1e3), 1) if moe_ms else None,
             "head_tokens_per_s": round(T / (head_ms / 1e3), 1) if head_ms else None,
-            "invariance": inv,
-            "next_rows": nxt,
-            "roofline": roof,
             "kernels": per_kernel,
+            "next_rows": nxt,
+            "invariance": inv,
+            "roofline": roof,
             "clocks": clk,
             "cpu_baseline": cpu,
+            "e2e": {"value": round(ws * T / (e2e_ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            # the figures a reader looks for first, last on the line so that a truncated tail keeps them
+            "summary": _summary(per_kernel, nxt, inv, ms_profiled),
         }
         print(json.dumps(line))
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def _summary(per_kernel, nxt, inv, ms_profiled):
+    """Compact digest of the line: per-step time with per-launch events on, the kernels against their
+    roofline, the Qwen-like layer, the tiny configuration's latency and the k3 == 0 evidence."""
+    def pick(nm, *keys):
+        e = per_kernel.get(nm) or {}
+        return {k: e[k] for k in keys if k in e} or None
+    out = {"profiled_ms_per_step": round(ms_profiled, 4),
+           "expert_gemm1_swiglu": pick("expert_gemm1_swiglu", "ms", "frac", "roofline_frac"),
+           "expert_gemm2": pick("expert_gemm2", "ms", "frac", "roofline_frac"),
+           "lm_head_gemm_lse": pick("lm_head_gemm_lse", "ms", "frac"),
+           "router_gemm": pick("router_gemm", "ms", "frac"),
+           "permute_rows": pick("permute_rows", "ms", "frac", "frac_spec"),
+           "combine": pick("combine", "ms", "frac", "frac_spec"),
+           "lse_merge": pick("lse_merge", "ms", "frac", "frac_spec")}
+    if nxt:
+        out["qwen_layer"] = {k: nxt.get(k) for k in ("qwen_moe_layer_ms", "qwen_experts_empty", "qwen_expert_tokens_max")}
+        for nm in ("qwen_expert_gemm1_swiglu", "qwen_expert_gemm2"):
+            if nm in nxt:
+                out["qwen_layer"][nm] = {k: nxt[nm][k] for k in ("frac", "roofline_frac")}
+        out["tiny_us"] = {k[5:-3]: nxt[k] for k in nxt if k.startswith("tiny_") and k.endswith("_us")}
+    if inv:
+        out["invariance"] = {k: inv[k] for k in ("moe_out_values_differing", "logp_differing",
+                                                 "k3_mean_prefill_vs_decode")}
+    return out
 
 
 def invariance_check(st, device):
@@ -768,6 +849,11 @@ def run_profile_case(args):
     """A small launch of one hot kernel for an ncu capture (inputs > L2, a few GB on the device).
 
     lm_head:  vocab-projection GEMM + LSE at T=2048, H=6144, V=32768 (Wv 403 MB, logits 268 MB).
+    lm_head_traffic: the head at T=8192, H=6144 for V = 18944, 37888 and 151552 in turn (one head
+              call each: vocabulary GEMM + LSE partials, then the merge).
+    route_combine: one call of the step's layer shape (T=8192, H=6144, E=256, k=8) with F=128
+              experts and no shared expert: router GEMM, top-k, dispatch, permute, expert GEMMs
+              and combine launch once each.
     experts:  the grouped expert GEMMs at T=1024, H=6144, E=32, k=8, F=2048 + shared (weights 2.4 GB);
               256 token-slots per expert on average, as in the T=8192, E=256 layer.
     moe_backward: one prefill, then one backward of the layer at T=512, H=6144, E=16, k=8, F=2048
@@ -782,7 +868,32 @@ def run_profile_case(args):
     from serve_invariant_moe_gb300 import api, binding, build, synth
     build.build()
     dev = torch.device("cuda:0")
-    if args.profile_case == "lm_head":
+    if args.profile_case == "lm_head_traffic":
+        # the vocabulary projection at the step's T = 8192 (two 4096-row bands, as in the step) for
+        # V = 151552 / 8, 151552 / 4 and 151552: DRAM bytes per launch against V show how the
+        # full-size traffic scales (at most 1.9 GB of weights on the device at a time)
+        import dataclasses
+        for V in (18944, 37888, 151552):
+            hc = dataclasses.replace(synth.GLM_HEAD, T=8192, V=V)
+            hidden, wv, target, _, _ = synth.head_inputs(hc, dev)
+            ws = binding.new_workspace(binding.workspace_size(hc.T, hc.H, V=hc.V), dev)
+            binding.lm_logprob_kl(hidden.to(dev), wv, target.to(dev), ws)
+            binding.check_status(ws)
+            del wv, ws
+            torch.cuda.empty_cache()
+    elif args.profile_case == "route_combine":
+        # the router GEMM, top-k, dispatch, permute and combine of the step's layer shape
+        # (T = 8192, H = 6144, E = 256, k = 8), with experts narrowed to F = 128 so that the
+        # device holds about 4 GB (xp 0.8 GB, Y 1.6 GB, expert weights 1.2 GB); one layer call
+        import dataclasses
+        mc = dataclasses.replace(synth.GLM_MOE, F=128, F_shared=0)
+        x, wr = synth.moe_activations(mc)
+        w13, w2 = synth.expert_weights(mc, dev)
+        layer = api.MoELayer(api.MoEWeights(wr.to(dev), w13, w2, mc.k))
+        hid = torch.empty((mc.T, mc.H), dtype=torch.bfloat16, device=dev)
+        layer.prefill(x.to(dev), out_bf16=hid)
+        binding.check_status(layer._ws)
+    elif args.profile_case == "lm_head":
         import dataclasses
         hc = dataclasses.replace(synth.GLM_HEAD, T=2048, V=32768)
         hidden, wv, target, _, _ = synth.head_inputs(hc, dev)
@@ -827,9 +938,10 @@ def run_profile_case(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile-case", choices=["lm_head", "experts", "head_backward", "moe_backward"], default=None)
+    ap.add_argument("--profile-case", choices=["lm_head", "lm_head_traffic", "route_combine", "experts",
+                                               "head_backward", "moe_backward"], default=None)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

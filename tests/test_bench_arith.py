@@ -51,10 +51,25 @@ def test_gemm_bytes_glm_step():
     assert t_byte > t_flop
 
 
-def test_lm_head_traffic_constant_is_per_launch_dram_bytes():
+def test_lm_head_traffic_is_tied_to_the_kernel_sources():
     b = _bench()
-    # read + write of one full-size launch from a one-pass ncu capture: a few GB, above the
-    # 1.96 GB of algorithmic bytes (Wv + hidden + partials) and far below the 26.9 GB of the
-    # unbanded order
-    t = b.TRAFFIC_BYTES["lm_head_gemm_lse"]
-    assert 1.96e9 < t < 10e9
+    # the captured figure is reported only while the sources it was captured from are unchanged
+    t = b.TRAFFIC["lm_head_gemm_lse"]
+    if t["bytes"] is None:
+        assert b.traffic_bytes("lm_head_gemm_lse") is None
+    else:
+        # read + write of one full-size launch: above the 1.96 GB of algorithmic bytes (Wv, hidden,
+        # partials) and far below the 26.9 GB of an unbanded column order
+        assert 1.96e9 < t["bytes"] < 10e9
+        want = t["bytes"] if t["sources_sha256"] == b.kernel_sources_sha256() else None
+        assert b.traffic_bytes("lm_head_gemm_lse") == want
+    assert b.traffic_bytes("no_such_kernel") is None
+    assert len(b.kernel_sources_sha256()) == 64
+
+
+def test_head_algorithmic_bytes():
+    from serve_invariant_moe_gb300 import synth
+    b = _bench()
+    # Wv 1.862 GB + hidden 100.7 MB + partials 8192 x 592 x 8 B + target logits
+    got = b._head_bytes(synth.GLM_MOE, synth.GLM_HEAD)
+    assert got == 151552 * 6144 * 2 + 8192 * 6144 * 2 + 8192 * 592 * 8 + 8192 * 4
