@@ -104,24 +104,36 @@ def silu(g: np.ndarray) -> np.ndarray:
         return g / (1.0 + np.exp(-g))
 
 
-def swiglu_expert(x_rows: np.ndarray, w13: np.ndarray, w2: np.ndarray, F: int,
-                  round_h: bool = True) -> np.ndarray:
-    """One SwiGLU expert on a block of rows, float64.
+def swiglu_hidden(x_rows: np.ndarray, w13: np.ndarray, F: int, round_h: bool = True) -> np.ndarray:
+    """The first half of one SwiGLU expert on a block of rows, float64.
 
     w13 is [2F, H]: rows 0..F-1 the gate projection, rows F..2F-1 the up
-    projection; w2 is [H, F] (the down projection).
-        g = x Wg^T,  u = x Wu^T,  h = silu(g) * u,  y = h W2^T.
-    The hidden activation h is the bf16 input of the down projection, so it is
-    rounded to bf16 (nearest-even) before the second product when round_h.
+    projection.  g = x Wg^T, u = x Wu^T, h = silu(g) * u.  The hidden activation
+    h is the bf16 input of the down projection, so it is rounded to bf16
+    (nearest-even) when round_h.
     """
     x_rows = np.asarray(x_rows, np.float64)
     w13 = np.asarray(w13, np.float64)
     g = x_rows @ w13[:F].T
     u = x_rows @ w13[F:2 * F].T
     h = silu(g) * u
-    if round_h:
-        h = round_to_bf16(h)
-    return h @ np.asarray(w2, np.float64).T
+    return round_to_bf16(h) if round_h else h
+
+
+def down_projection(h_rows: np.ndarray, w2: np.ndarray) -> np.ndarray:
+    """The second half of one SwiGLU expert: y = h W2^T with w2 [H, F], float64."""
+    return np.asarray(h_rows, np.float64) @ np.asarray(w2, np.float64).T
+
+
+def swiglu_expert(x_rows: np.ndarray, w13: np.ndarray, w2: np.ndarray, F: int,
+                  round_h: bool = True) -> np.ndarray:
+    """One SwiGLU expert on a block of rows, float64: the down projection of the
+    (bf16-rounded when round_h) hidden activation,
+        g = x Wg^T,  u = x Wu^T,  h = silu(g) * u,  y = h W2^T.
+    The two halves are separate functions so that a test can feed either one
+    the GPU path's own intermediate and compare one stage at a time.
+    """
+    return down_projection(swiglu_hidden(x_rows, w13, F, round_h), w2)
 
 
 def expert_outputs(x, topk_idx, w13, w2, F, round_h=True, expert_weights=None):

@@ -108,7 +108,11 @@ def test_full_size_head_sampled_tokens():
     from serve_invariant_moe_gb300 import api
     cfg = synth.GLM_HEAD
     hidden, wv, target, noise, noise_wide = synth.head_inputs(cfg, "cuda")
-    sample = [0, 1, 4095, 8191]
+    # 64 rows: the first row and one seeded row of each 256-row chunk, across both 4096-row bands
+    g = torch.Generator().manual_seed(9)
+    sample = sorted({c * 256 for c in range(cfg.T // 256)}
+                    | {c * 256 + int(torch.randint(1, 256, (1,), generator=g)) for c in range(cfg.T // 256)})
+    assert len(sample) == 64 and sample[-1] >= 4096
     # oracle logits for the sampled tokens, vocabulary in chunks
     hs = f64(hidden[sample])
     z_ref = np.empty((len(sample), cfg.V))

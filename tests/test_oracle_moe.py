@@ -147,6 +147,26 @@ def test_swiglu_expert_structure():
     assert np.allclose(y, h[:, perm], rtol=1e-2)
 
 
+def test_swiglu_stages_compose_and_pin_separately():
+    # the two stages the module-substitution tests feed one at a time
+    rng = np.random.default_rng(18)
+    H, F = 12, 8
+    x = round_to_bf16(rng.standard_normal((7, H)))
+    w13 = round_to_bf16(rng.standard_normal((2 * F, H)) * 0.3)
+    w2 = round_to_bf16(rng.standard_normal((H, F)) * 0.3)
+    h = moe.swiglu_hidden(x, w13, F)
+    assert np.array_equal(moe.swiglu_expert(x, w13, w2, F), moe.down_projection(h, w2))
+    # the hidden stage: silu(gate) * up, with gate and up taken from the right halves of w13
+    g_t = torch.from_numpy(x) @ torch.from_numpy(w13[:F]).T
+    u_t = torch.from_numpy(x) @ torch.from_numpy(w13[F:]).T
+    ref_h = (torch.nn.functional.silu(g_t) * u_t).numpy()
+    assert np.allclose(moe.swiglu_hidden(x, w13, F, round_h=False), ref_h, rtol=1e-13, atol=1e-13)
+    assert np.array_equal(h, round_to_bf16(moe.swiglu_hidden(x, w13, F, round_h=False)))
+    # the down stage: a selection matrix W2 = rows of the identity returns the chosen h columns
+    sel = np.array([3, 0, 7, 1, 1, 5, 2, 6, 4, 0, 3, 7])
+    assert np.array_equal(moe.down_projection(h, np.eye(F)[sel]), h[:, sel])
+
+
 def _tiny_layer(T=24, H=32, E=6, k=2, F=16, seed=9):
     rng = np.random.default_rng(seed)
     x = round_to_bf16(rng.standard_normal((T, H)))
