@@ -207,6 +207,105 @@ int lm_logprob_kl(const void* hidden, const void* w_vocab, const int32_t* target
                   void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Vocabulary-parallel head: lm_logprob_partials on each vocabulary shard, then
+ * lm_logprob_merge over the gathered partials.
+ *
+ * "GLM Post-Training Beyond SFT", section "动作与概率契约": the log-sum-exp over
+ * a vocabulary split across devices needs comparison tests; "位级一致：前沿训练
+ * 的差异化关键", section "为什么比特级一致是一个复杂的问题": a cross-device
+ * reduction must not change its order with the size of the job.  Here the
+ * vocabulary is cut at 256-column chunk boundaries, every shard computes pass 1
+ * of the log-sum-exp for its own chunks with the same tile and K order as
+ * lm_logprob_kl, and pass 2 folds the chunks in the same fixed global order as
+ * lm_logprob_kl -- so any split into shards gives the bits of the unsharded
+ * call.  lm_logprob_kl is exactly these two calls over one shard [0, V).
+ * ------------------------------------------------------------------------- */
+
+/* Pass 1 on the vocabulary shard [v0, v1): for each token t and each chunk
+ * c = v0/256 + j of the shard (columns [256c, 256c + 256) of the whole
+ * vocabulary, clipped to v1):
+ *   partials[2 * (t * ld_part + j)]     = m = max z[t, chunk]
+ *   partials[2 * (t * ld_part + j) + 1] = s = sum exp(z - m)   (the lm_logprob_kl order)
+ * and, for tokens whose target lies in [v0, v1), tgt_logit[t] = z[t, target[t]]
+ * (other tokens' entries are not written).
+ *
+ * hidden [T, H] bf16; w_vocab_shard = rows [v0, v1) of the vocabulary projection,
+ * [v1 - v0, H] bf16; target [T] int32 (ids in the whole vocabulary); logits
+ * (nullable) = the whole [T, V] fp32 logits array, of which columns [v0, v1) are
+ * written; partials (8-byte aligned) as above, ld_part >= the shard's chunk count
+ * (in (m, s) pairs); tgt_logit [T] fp32.  workspace: at least 256 bytes (status).
+ * Shapes: H % 64 == 0, V % 4 == 0, 0 <= v0 < v1 <= V, v0 % 256 == 0, and
+ * v1 % 256 == 0 unless v1 == V. */
+int lm_logprob_partials(const void* hidden, const void* w_vocab_shard, const int32_t* target,
+                        int T, int H, int V, int v0, int v1, float* logits, float* partials,
+                        long long ld_part, float* tgt_logit, void* workspace, size_t ws_bytes,
+                        void* stream);
+
+/* Pass 2 and the per-token outputs (as lm_logprob_kl) from partials laid out in
+ * shards of shard_chunks chunks: the (m, s) pair of global chunk c of token t is at
+ *   partials + 2 * ((c / shard_chunks) * shard_stride + t * ld_part + c % shard_chunks)
+ * and token t's target logit at tgt_logit[(target[t] / 256 / shard_chunks) * tgt_stride + t]
+ * (read from the shard that owns the target; nothing is summed across shards).
+ * One [T, NCH] array (NCH = ceil(V / 256)): shard_chunks = ld_part = NCH,
+ * shard_stride = tgt_stride = 0.  An all-gather of n shards' [T, P] partials into
+ * [n][T][P] and of their [T] target logits into [n][T]: shard_chunks = ld_part = P,
+ * shard_stride = T * P, tgt_stride = T (the last shard may hold fewer than P
+ * chunks; unused entries are not read).  Other arguments and outputs as
+ * lm_logprob_kl. */
+int lm_logprob_merge(const float* partials, long long ld_part, int shard_chunks, long long shard_stride,
+                     const float* tgt_logit, long long tgt_stride, const int32_t* target,
+                     const float* rollout_logp, int T, int V, float beta, float* logp, float* lse,
+                     float* k3, uint8_t* mask, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Expert-parallel layer: the experts split over ranks, each rank owning the
+ * contiguous range [e0, e1) (E_local = e1 - e0 experts).
+ *
+ * Every rank routes its own tokens with the whole router (moe_route_topk).
+ * Its xp rows are sorted by expert, so the rows for the owner of [e0, e1) are
+ * the one slice xp[offsets[e0] : offsets[e1]); an all-to-all (the caller's
+ * collective) delivers to each owner the rows of every source, source-major.
+ * The owner regroups them expert-major (moe_ep_regroup), runs its experts with
+ * moe_grouped_ffn (T = R received rows, k = 1, E = E_local, plan = plan_local,
+ * w13/w2 = its experts' weights), puts the output rows back in the received
+ * order (moe_ep_ungroup) and returns them with the reverse all-to-all; each
+ * source then holds y in its own xp order and combines locally (moe_combine),
+ * adding the shared expert it computed itself (moe_shared_expert).
+ * Rows are only moved between devices, never reduced across them, and an
+ * expert output row depends on its own input row only (one fixed tile, K
+ * ascending), so every output has the bits of the one-device layer
+ * ("位级一致：前沿训练的差异化关键", section "为什么比特级一致是一个复杂的问题").
+ * ------------------------------------------------------------------------- */
+
+/* recv_xp [R, H] bf16: the received rows, source-major (source 0's rows for
+ * local experts 0, 1, ..., then source 1's, ...; within one (source, expert) in
+ * the source's order); recv_counts [n_src, E_local] int32 (device): rows that
+ * source s sent for local expert e.  Outputs: xp_local [R, H] bf16 (expert-major;
+ * within an expert, sources ascending), plan_local int32 [2 * E_local + 1] =
+ * counts[E_local] | offsets[E_local + 1] (the plan moe_grouped_ffn reads), and
+ * row_src [R] int32: the received row each xp_local row was copied from.
+ * If the counts do not add up to R, no access goes out of bounds, the status
+ * word records it and invmoe_check() returns INVMOE_ERR_INVALID_ARG.
+ * workspace: at least 256 bytes (status).  Shapes: H % 8 == 0,
+ * E_local <= 1024, n_src * E_local <= 65535. */
+int moe_ep_regroup(const void* recv_xp, const int32_t* recv_counts, int n_src, int E_local, int R, int H,
+                   void* xp_local, int32_t* plan_local, int32_t* row_src, void* workspace,
+                   size_t ws_bytes, void* stream);
+
+/* y_send[row_src[i], :] = y_local[i, :] for i < R: the expert outputs back in
+ * the received (source-major) order.  y_local, y_send [R, H] fp32, row_src from
+ * moe_ep_regroup.  Shapes: H % 4 == 0. */
+int moe_ep_ungroup(const float* y_local, const int32_t* row_src, int R, int H, float* y_send, void* stream);
+
+/* The shared expert alone (as inside moe_grouped_ffn): y_shared [T, H] fp32 =
+ * SwiGLU(x) with ws13 [2 * F_shared, H], ws2 [H, F_shared] bf16, on the CTA-pair
+ * engine; the bf16 hidden activation lives in the workspace
+ * (invmoe_workspace_size(T, H, 0, 0, 0, F_shared, 0) bytes).
+ * Shapes: H % 64 == 0, F_shared % 128 == 0. */
+int moe_shared_expert(const void* x, const void* ws13, const void* ws2, int T, int H, int F_shared,
+                      float* y_shared, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * moe_route_topk_noalloc -- moe_route_topk for callers that cannot allocate
  *
  * The source pages have no counterpart of this call; it exists for callers that

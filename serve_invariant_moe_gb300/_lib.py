@@ -28,6 +28,13 @@ PROTOTYPES = {
                              _vp, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
     "moe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp]),
     "lm_logprob_kl": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "lm_logprob_partials": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, ctypes.c_longlong, _vp, _vp, _sz,
+                                 _vp]),
+    "lm_logprob_merge": (_i, [_vp, ctypes.c_longlong, _i, ctypes.c_longlong, _vp, ctypes.c_longlong, _vp, _vp, _i,
+                              _i, _f, _vp, _vp, _vp, _vp, _vp]),
+    "moe_ep_regroup": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_ep_ungroup": (_i, [_vp, _vp, _i, _i, _vp, _vp]),
+    "moe_shared_expert": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "rl_token_loss": (_i, [_vp, _vp, _vp, _vp, _i, _f, _f, _f, _vp, _vp, _vp, _vp, _vp, _vp]),
     "lm_head_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp]),
     "invmoe_backward_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),

@@ -196,6 +196,108 @@ def lm_logprob_kl(hidden, w_vocab, target, workspace, rollout_logp=None, beta=2.
     return dict(logits=logits, logp=logp, lse=lse, k3=k3, mask=mask)
 
 
+def lm_logprob_partials(hidden, w_vocab_shard, target, V, v0, workspace, partials, tgt_logit, logits=None):
+    """Pass 1 of the log-sum-exp on the vocabulary shard [v0, v0 + rows of w_vocab_shard).
+
+    partials: fp32 [T, P, 2] (P >= the shard's chunk count), the shard's chunk j of token t at
+    partials[t, j]; tgt_logit [T] fp32 receives z[t, target[t]] where the target is in the shard;
+    logits (optional) is the whole [T, V] fp32 array, of which the shard's columns are written."""
+    T, H = hidden.shape
+    v1 = v0 + w_vocab_shard.shape[0]
+    _req(hidden, torch.bfloat16, "hidden")
+    _req(w_vocab_shard, torch.bfloat16, "w_vocab_shard", (v1 - v0, H))
+    _req(target, torch.int32, "target", (T,))
+    _req(partials, torch.float32, "partials")
+    if partials.dim() != 3 or partials.shape[0] != T or partials.shape[2] != 2:
+        raise ValueError(f"partials must be [T, P, 2], got {tuple(partials.shape)}")
+    _req(tgt_logit, torch.float32, "tgt_logit", (T,))
+    _opt(logits, torch.float32, "logits", (T, V))
+    _req(workspace, torch.uint8, "workspace")
+    check(lib().lm_logprob_partials(_p(hidden), _p(w_vocab_shard), _p(target), T, H, V, v0, v1, _p(logits),
+                                    _p(partials), partials.shape[1], _p(tgt_logit), _p(workspace), workspace.numel(),
+                                    _stream()))
+    return partials
+
+
+def lm_logprob_merge(partials, tgt_logit, target, V, rollout_logp=None, beta=2.0):
+    """Pass 2 and the per-token outputs from partials [T, NCH, 2] with target logits [T] (one array),
+    or from partials [n, T, P, 2] with target logits [n, T] (n gathered shards of P chunks each)."""
+    _req(partials, torch.float32, "partials")
+    if partials.dim() == 3:
+        T, P = partials.shape[0], partials.shape[1]
+        stride, tstride = 0, 0
+        _req(tgt_logit, torch.float32, "tgt_logit", (T,))
+    elif partials.dim() == 4:
+        n, T, P = partials.shape[0], partials.shape[1], partials.shape[2]
+        stride, tstride = T * P, T
+        _req(tgt_logit, torch.float32, "tgt_logit", (n, T))
+    else:
+        raise ValueError("partials must be [T, NCH, 2] or [n, T, P, 2]")
+    if partials.shape[-1] != 2:
+        raise ValueError("partials must end in a (max, sum) pair")
+    dev = partials.device
+    _req(target, torch.int32, "target", (T,))
+    out = dict(logp=torch.empty(T, dtype=torch.float32, device=dev), lse=torch.empty(T, dtype=torch.float32, device=dev),
+               k3=None, mask=None)
+    if rollout_logp is not None:
+        _req(rollout_logp, torch.float32, "rollout_logp", (T,))
+        out["k3"] = torch.empty(T, dtype=torch.float32, device=dev)
+        out["mask"] = torch.empty(T, dtype=torch.uint8, device=dev)
+    check(lib().lm_logprob_merge(_p(partials), P, P, stride, _p(tgt_logit), tstride, _p(target), _p(rollout_logp), T,
+                                 V, float(beta), _p(out["logp"]), _p(out["lse"]), _p(out["k3"]), _p(out["mask"]),
+                                 _stream()))
+    return out
+
+
+def moe_ep_regroup(recv_xp, recv_counts, workspace, xp_local=None, plan_local=None, row_src=None):
+    """Received rows (source-major) -> expert-major rows, the local plan and the row map.
+
+    recv_xp [R, H] bf16, recv_counts [n_src, E_local] int32 (device)."""
+    R, H = recv_xp.shape
+    n_src, E_local = recv_counts.shape
+    dev = recv_xp.device
+    _req(recv_xp, torch.bfloat16, "recv_xp")
+    _req(recv_counts, torch.int32, "recv_counts")
+    xp_local = torch.empty((R, H), dtype=torch.bfloat16, device=dev) if xp_local is None else xp_local
+    plan_local = torch.empty(2 * E_local + 1, dtype=torch.int32, device=dev) if plan_local is None else plan_local
+    row_src = torch.empty(max(R, 1), dtype=torch.int32, device=dev) if row_src is None else row_src
+    _req(xp_local, torch.bfloat16, "xp_local", (R, H))
+    _req(plan_local, torch.int32, "plan_local", (2 * E_local + 1,))
+    _req(row_src, torch.int32, "row_src")
+    if row_src.numel() < R:
+        raise ValueError("row_src is too small")
+    _req(workspace, torch.uint8, "workspace")
+    check(lib().moe_ep_regroup(_p(recv_xp), _p(recv_counts), n_src, E_local, R, H, _p(xp_local), _p(plan_local),
+                               _p(row_src), _p(workspace), workspace.numel(), _stream()))
+    return dict(xp_local=xp_local, plan_local=plan_local, row_src=row_src)
+
+
+def moe_ep_ungroup(y_local, row_src, y_send=None):
+    """y_send[row_src[i]] = y_local[i]: expert outputs back in the received order."""
+    R, H = y_local.shape
+    _req(y_local, torch.float32, "y_local")
+    _req(row_src, torch.int32, "row_src")
+    y_send = torch.empty_like(y_local) if y_send is None else y_send
+    _req(y_send, torch.float32, "y_send", (R, H))
+    check(lib().moe_ep_ungroup(_p(y_local), _p(row_src), R, H, _p(y_send), _stream()))
+    return y_send
+
+
+def moe_shared_expert(x, ws13, ws2, workspace, y_shared=None):
+    """The shared expert alone: y_shared [T, H] fp32 = SwiGLU(x)."""
+    T, H = x.shape
+    Fs = ws13.shape[0] // 2
+    _req(x, torch.bfloat16, "x")
+    _req(ws13, torch.bfloat16, "ws13", (2 * Fs, H))
+    _req(ws2, torch.bfloat16, "ws2", (H, Fs))
+    y_shared = torch.empty((T, H), dtype=torch.float32, device=x.device) if y_shared is None else y_shared
+    _req(y_shared, torch.float32, "y_shared", (T, H))
+    _req(workspace, torch.uint8, "workspace")
+    check(lib().moe_shared_expert(_p(x), _p(ws13), _p(ws2), T, H, Fs, _p(y_shared), _p(workspace), workspace.numel(),
+                                  _stream()))
+    return y_shared
+
+
 def rl_token_loss(logp_train, logp_rollout, advantage, logp_old=None, beta=2.0, eps_low=0.2, eps_high=0.28):
     """IcePop-masked clipped policy loss per token (+ fixed-order mean), IcePop mask, DIS weights."""
     T = logp_train.shape[0]

@@ -133,6 +133,27 @@ ProfScope::~ProfScope() {
   if (idx_ < static_cast<long>(g_prof_recs.size())) cudaEventRecord(g_prof_recs[idx_].b, st_);
 }
 
+// The shared expert: dense SwiGLU over all T tokens on the CTA-pair engine; the
+// bf16 hidden activation [T, F_shared] lives in `hs` (workspace scratch).
+int shared_expert_run(const void* x, const void* ws13, const void* ws2, int T, int H, int F_shared, float* y_shared,
+                      void* hs, unsigned int* status, cudaStream_t st) {
+  GemmCall s1{};
+  s1.name = "shared_gemm1_swiglu";
+  s1.variant = GV_PAIR_SWIGLU;
+  s1.A = x; s1.a_rows = T; s1.B = ws13; s1.b_rows = 2LL * F_shared; s1.K = H;
+  s1.N = F_shared; s1.M = T; s1.G = 0; s1.b_group_rows = 0; s1.b_up_rows = F_shared;
+  s1.out = hs; s1.ldo = F_shared; s1.status = status;
+  int rc = gemm_run(s1, st);
+  if (rc) return rc;
+  GemmCall s2{};
+  s2.name = "shared_gemm2";
+  s2.variant = GV_PAIR_F32;
+  s2.A = hs; s2.a_rows = T; s2.B = ws2; s2.b_rows = H; s2.K = F_shared;
+  s2.N = H; s2.M = T; s2.G = 0;
+  s2.out = y_shared; s2.ldo = H; s2.status = status;
+  return gemm_run(s2, st);
+}
+
 }  // namespace invmoe
 
 using namespace invmoe;
@@ -184,6 +205,9 @@ int invmoe_check(void* workspace, void* stream) {
     if ((rc = check_cuda(cudaStreamSynchronize(st), "cudaStreamSynchronize"))) return rc;
     if (v & kStatusTimeout)
       return set_error(INVMOE_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out (status 0x%x)", v);
+    if (v & kStatusBadCounts)
+      return set_error(INVMOE_ERR_INVALID_ARG,
+                       "expert-parallel regroup: the received row counts do not add up to R (status 0x%x)", v);
     return set_error(INVMOE_ERR_INVALID_ARG,
                      "router replay: an expert index was out of range or repeated within a token (status 0x%x)", v);
   }
@@ -297,23 +321,8 @@ int moe_grouped_ffn(const void* xp, const int32_t* plan, const void* w13, const 
   g2.out = y; g2.ldo = H; g2.status = status;
   if ((rc = gemm_run(g2, st))) return rc;
 
-  if (F_shared > 0) {
-    void* hs = scratch(workspace);
-    GemmCall s1{};
-    s1.name = "shared_gemm1_swiglu";
-    s1.variant = GV_PAIR_SWIGLU;
-    s1.A = x_shared; s1.a_rows = T; s1.B = ws13; s1.b_rows = 2LL * F_shared; s1.K = H;
-    s1.N = F_shared; s1.M = T; s1.G = 0; s1.b_group_rows = 0; s1.b_up_rows = F_shared;
-    s1.out = hs; s1.ldo = F_shared; s1.status = status;
-    if ((rc = gemm_run(s1, st))) return rc;
-    GemmCall s2{};
-    s2.name = "shared_gemm2";
-    s2.variant = GV_PAIR_F32;
-    s2.A = hs; s2.a_rows = T; s2.B = ws2; s2.b_rows = H; s2.K = F_shared;
-    s2.N = H; s2.M = T; s2.G = 0;
-    s2.out = y_shared; s2.ldo = H; s2.status = status;
-    if ((rc = gemm_run(s2, st))) return rc;
-  }
+  if (F_shared > 0)
+    return shared_expert_run(x_shared, ws13, ws2, T, H, F_shared, y_shared, scratch(workspace), status, st);
   return INVMOE_OK;
 }
 
@@ -356,7 +365,106 @@ int lm_logprob_kl(const void* hidden, const void* w_vocab, const int32_t* target
   g.part = part; g.target = target; g.tgt_logit = tgt_logit;
   int rc = gemm_run(g, st);
   if (rc) return rc;
-  return lse_merge_launch(part, tgt_logit, target, rollout_logp, T, V, beta, logp, lse, k3, mask, st);
+  const int NCH = (V + kLseChunk - 1) / kLseChunk;
+  return lse_merge_launch(part, NCH, NCH, 0, tgt_logit, 0, target, rollout_logp, T, V, beta, logp, lse, k3, mask,
+                          st);
+}
+
+int lm_logprob_partials(const void* hidden, const void* w_vocab_shard, const int32_t* target, int T, int H, int V,
+                        int v0, int v1, float* logits, float* partials, long long ld_part, float* tgt_logit,
+                        void* workspace, size_t ws_bytes, void* stream) {
+  REQUIRE(T >= 0 && H > 0 && V > 0, INVMOE_ERR_INVALID_ARG, "bad sizes");
+  REQUIRE(H % 64 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "H=%d is not a multiple of 64", H);
+  REQUIRE(V % 4 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "V=%d is not a multiple of 4", V);
+  REQUIRE(0 <= v0 && v0 < v1 && v1 <= V, INVMOE_ERR_INVALID_ARG, "need 0 <= v0 < v1 <= V (v0=%d, v1=%d, V=%d)", v0,
+          v1, V);
+  REQUIRE(v0 % kLseChunk == 0 && (v1 == V || v1 % kLseChunk == 0), INVMOE_ERR_INVALID_ARG,
+          "a vocabulary shard must start and end on a %d-column chunk boundary (v0=%d, v1=%d)", kLseChunk, v0, v1);
+  const int nch_shard = (v1 - v0 + kLseChunk - 1) / kLseChunk;
+  REQUIRE(ld_part >= nch_shard, INVMOE_ERR_INVALID_ARG, "ld_part=%lld < the shard's %d chunks", ld_part, nch_shard);
+  REQUIRE_PTR(workspace);
+  REQUIRE(ws_bytes >= kStatusBytes, INVMOE_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
+  if (T == 0) return INVMOE_OK;
+  REQUIRE_PTR(hidden); REQUIRE_PTR(w_vocab_shard); REQUIRE_PTR(target); REQUIRE_PTR(partials);
+  REQUIRE_PTR(tgt_logit);
+  REQUIRE_ALIGNED(hidden); REQUIRE_ALIGNED(w_vocab_shard); REQUIRE_ALIGNED(workspace);
+  REQUIRE((reinterpret_cast<uintptr_t>(partials) & 7u) == 0, INVMOE_ERR_MISALIGNED, "partials is not 8-byte aligned");
+  if (logits) REQUIRE_ALIGNED(logits);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  GemmCall g{};
+  g.name = "lm_head_gemm_lse";
+  g.variant = GV_PAIR_LSE;
+  g.A = hidden; g.a_rows = T; g.B = w_vocab_shard; g.b_rows = v1 - v0; g.K = H; g.N = v1 - v0; g.M = T; g.G = 0;
+  // the unsharded call's order: column-block-major in bands of 16 row chunks
+  g.n_major = 1; g.m_group = 16; g.out = logits ? logits + v0 : nullptr; g.ldo = V;
+  g.status = status_word(workspace);
+  g.part = reinterpret_cast<float2*>(partials); g.part_ld = ld_part; g.target_col0 = v0;
+  g.target = target; g.tgt_logit = tgt_logit;
+  return gemm_run(g, st);
+}
+
+int lm_logprob_merge(const float* partials, long long ld_part, int shard_chunks, long long shard_stride,
+                     const float* tgt_logit, long long tgt_stride, const int32_t* target, const float* rollout_logp,
+                     int T, int V, float beta, float* logp, float* lse, float* k3, uint8_t* mask, void* stream) {
+  REQUIRE(T >= 0 && V > 0, INVMOE_ERR_INVALID_ARG, "bad sizes");
+  REQUIRE(beta >= 1.0f, INVMOE_ERR_INVALID_ARG, "beta must be >= 1");
+  REQUIRE(shard_chunks >= 1 && ld_part >= 1 && shard_stride >= 0 && tgt_stride >= 0, INVMOE_ERR_INVALID_ARG,
+          "need shard_chunks >= 1, ld_part >= 1, shard_stride >= 0, tgt_stride >= 0");
+  const int NCH = (V + kLseChunk - 1) / kLseChunk;
+  REQUIRE(ld_part >= (shard_chunks < NCH ? shard_chunks : NCH), INVMOE_ERR_INVALID_ARG,
+          "ld_part=%lld is shorter than a shard's row of chunks", ld_part);
+  REQUIRE(shard_chunks >= NCH || shard_stride >= static_cast<long long>(T) * ld_part, INVMOE_ERR_INVALID_ARG,
+          "shard_stride=%lld overlaps the previous shard's rows", shard_stride);
+  REQUIRE(shard_chunks >= NCH || tgt_stride >= T, INVMOE_ERR_INVALID_ARG,
+          "tgt_stride=%lld overlaps the previous shard's target logits", tgt_stride);
+  if (T == 0) return INVMOE_OK;
+  REQUIRE_PTR(partials); REQUIRE_PTR(tgt_logit); REQUIRE_PTR(target); REQUIRE_PTR(logp);
+  REQUIRE((reinterpret_cast<uintptr_t>(partials) & 7u) == 0, INVMOE_ERR_MISALIGNED, "partials is not 8-byte aligned");
+  return lse_merge_launch(reinterpret_cast<const float2*>(partials), ld_part, shard_chunks, shard_stride, tgt_logit,
+                          tgt_stride, target, rollout_logp, T, V, beta, logp, lse, k3, mask,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int moe_shared_expert(const void* x, const void* ws13, const void* ws2, int T, int H, int F_shared, float* y_shared,
+                      void* workspace, size_t ws_bytes, void* stream) {
+  REQUIRE(T >= 0 && H > 0 && F_shared > 0, INVMOE_ERR_INVALID_ARG, "bad sizes");
+  REQUIRE(H % 64 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "H=%d is not a multiple of 64", H);
+  REQUIRE(F_shared % 128 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "F_shared=%d is not a multiple of 128", F_shared);
+  REQUIRE_PTR(workspace);
+  REQUIRE(ws_bytes >= kStatusBytes + ffn_ws(T, F_shared), INVMOE_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
+  if (T == 0) return INVMOE_OK;
+  REQUIRE_PTR(x); REQUIRE_PTR(ws13); REQUIRE_PTR(ws2); REQUIRE_PTR(y_shared);
+  REQUIRE_ALIGNED(x); REQUIRE_ALIGNED(ws13); REQUIRE_ALIGNED(ws2); REQUIRE_ALIGNED(y_shared);
+  REQUIRE_ALIGNED(workspace);
+  return shared_expert_run(x, ws13, ws2, T, H, F_shared, y_shared, scratch(workspace), status_word(workspace),
+                           static_cast<cudaStream_t>(stream));
+}
+
+int moe_ep_regroup(const void* recv_xp, const int32_t* recv_counts, int n_src, int E_local, int R, int H,
+                   void* xp_local, int32_t* plan_local, int32_t* row_src, void* workspace, size_t ws_bytes,
+                   void* stream) {
+  REQUIRE(n_src >= 1 && E_local >= 1 && R >= 0 && H > 0, INVMOE_ERR_INVALID_ARG, "bad sizes");
+  REQUIRE(E_local <= 1024, INVMOE_ERR_UNSUPPORTED_SHAPE, "E_local=%d > 1024", E_local);
+  REQUIRE(static_cast<long long>(n_src) * E_local <= 65535, INVMOE_ERR_UNSUPPORTED_SHAPE,
+          "n_src * E_local = %lld > 65535", static_cast<long long>(n_src) * E_local);
+  REQUIRE(H % 8 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "H=%d is not a multiple of 8", H);
+  REQUIRE_PTR(recv_counts); REQUIRE_PTR(plan_local); REQUIRE_PTR(workspace);
+  REQUIRE(ws_bytes >= kStatusBytes, INVMOE_ERR_WORKSPACE_TOO_SMALL, "workspace too small");
+  if (R > 0) {
+    REQUIRE_PTR(recv_xp); REQUIRE_PTR(xp_local); REQUIRE_PTR(row_src);
+    REQUIRE_ALIGNED(recv_xp); REQUIRE_ALIGNED(xp_local);
+  }
+  return ep_regroup_launch(recv_xp, recv_counts, n_src, E_local, R, H, xp_local, plan_local, row_src,
+                           status_word(workspace), static_cast<cudaStream_t>(stream));
+}
+
+int moe_ep_ungroup(const float* y_local, const int32_t* row_src, int R, int H, float* y_send, void* stream) {
+  REQUIRE(R >= 0 && H > 0, INVMOE_ERR_INVALID_ARG, "bad sizes");
+  REQUIRE(H % 4 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "H=%d is not a multiple of 4", H);
+  if (R == 0) return INVMOE_OK;
+  REQUIRE_PTR(y_local); REQUIRE_PTR(row_src); REQUIRE_PTR(y_send);
+  REQUIRE_ALIGNED(y_local); REQUIRE_ALIGNED(y_send);
+  return ep_ungroup_launch(y_local, row_src, R, H, y_send, static_cast<cudaStream_t>(stream));
 }
 
 int lm_head_backward(const void* hidden, const void* w_vocab, const int32_t* target, const float* lse,

@@ -78,20 +78,36 @@ __device__ __forceinline__ void lse_fold(float& M, float& S, float m, float s) {
 
 constexpr int kMergeWarps = 4;
 
-__global__ void lse_merge_kernel(const float2* __restrict__ part, const float* __restrict__ tgt_logit,
+// The partials of chunk c of token t sit at
+//   part[(c / shard_chunks) * shard_stride + t * ld_part + c % shard_chunks]
+// and the target logit of token t at tgt_logit[(shard of its target) * tgt_stride + t],
+// which covers one [T, NCH] array (shard_chunks = NCH) and the [shards][T][P]
+// arrays that gathering vocabulary shards of P chunks each produces; the fold
+// order above is the same for every layout.
+__global__ void lse_merge_kernel(const float2* __restrict__ part, long long ld_part, int shard_chunks,
+                                 long long shard_stride, const float* __restrict__ tgt_logit, long long tgt_stride,
                                  const int32_t* __restrict__ target, const float* __restrict__ rollout, int T, int V,
                                  int NCH, float beta, float* __restrict__ logp, float* __restrict__ lse,
                                  float* __restrict__ k3, uint8_t* __restrict__ mask) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   if (t >= T) return;
-  const float2* pt = part + static_cast<long long>(t) * NCH;
   const int P = (NCH + 31) / 32;
+  int c = lane * P;
   const int c1 = min(NCH, (lane + 1) * P);
   float M = -INFINITY, S = 0.0f;
-  for (int c = lane * P; c < c1; ++c) {
-    const float2 ms = pt[c];
-    lse_fold(M, S, ms.x, ms.y);
+  if (c < c1) {
+    int sh = c / shard_chunks;
+    int j = c - sh * shard_chunks;
+    const float2* base = part + sh * shard_stride + static_cast<long long>(t) * ld_part;
+    for (; c < c1; ++c) {
+      const float2 ms = base[j];
+      lse_fold(M, S, ms.x, ms.y);
+      if (++j == shard_chunks) {
+        j = 0;
+        base += shard_stride;
+      }
+    }
   }
 #pragma unroll
   for (int d = 16; d >= 1; d >>= 1) {
@@ -102,7 +118,10 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, const float* _
   if (lane != 0) return;
   const float l = __fadd_rn(M, logf(S));
   const int tg = target[t];
-  const float lp = (tg >= 0 && tg < V) ? __fsub_rn(tgt_logit[t], l) : __uint_as_float(0x7fc00000u);
+  // the target logit comes from the shard that owns the target's chunk
+  const float lp = (tg >= 0 && tg < V)
+                       ? __fsub_rn(tgt_logit[(tg / kLseChunk / shard_chunks) * tgt_stride + t], l)
+                       : __uint_as_float(0x7fc00000u);
   logp[t] = lp;
   if (lse != nullptr) lse[t] = l;
   if (rollout != nullptr) {
@@ -204,14 +223,15 @@ int combine_launch(const float* y, const float* topk_w, const int32_t* slot_row,
   return check_cuda(cudaGetLastError(), "combine_kernel");
 }
 
-int lse_merge_launch(const float2* partials, const float* tgt_logit, const int32_t* target,
-                     const float* rollout_logp, int T, int V, float beta, float* logp, float* lse, float* k3,
-                     uint8_t* mask, cudaStream_t st) {
+int lse_merge_launch(const float2* partials, long long ld_part, int shard_chunks, long long shard_stride,
+                     const float* tgt_logit, long long tgt_stride, const int32_t* target, const float* rollout_logp,
+                     int T, int V, float beta, float* logp, float* lse, float* k3, uint8_t* mask, cudaStream_t st) {
   const int NCH = (V + kLseChunk - 1) / kLseChunk;
   if (T == 0) return INVMOE_OK;
   ProfScope prof("lse_merge", st);
   lse_merge_kernel<<<(T + kMergeWarps - 1) / kMergeWarps, 32 * kMergeWarps, 0, st>>>(
-      partials, tgt_logit, target, rollout_logp, T, V, NCH, beta, logp, lse, k3, mask);
+      partials, ld_part, shard_chunks, shard_stride, tgt_logit, tgt_stride, target, rollout_logp, T, V, NCH, beta,
+      logp, lse, k3, mask);
   return check_cuda(cudaGetLastError(), "lse_merge_kernel");
 }
 

@@ -99,7 +99,8 @@ GemmParams make_params(const GemmCall& c, int nb_cols) {
   p.sched = reinterpret_cast<int*>(reinterpret_cast<char*>(c.status) + 64);
   p.timeout_ns = kTimeoutNs;
   p.part = c.part;
-  p.nch = (c.N + 255) / 256;
+  p.nch = c.part_ld > 0 ? static_cast<int>(c.part_ld) : (c.N + 255) / 256;
+  p.col0 = c.target_col0;
   p.target = c.target;
   p.tgt_logit = c.tgt_logit;
   p.m_group = c.m_group > 0 ? c.m_group : (1 << 30);

@@ -73,9 +73,11 @@ struct GemmCall {
   void* out;
   long long ldo;
   unsigned int* status;
-  float2* part;          // GV_LSE only
-  const int* target;     // GV_LSE only
-  float* tgt_logit;      // GV_LSE only
+  float2* part;          // GV_PAIR_LSE only: partials of the first column block of `row` 0
+  long long part_ld;     // GV_PAIR_LSE: row stride of part in pairs (0 = ceil(N / 256))
+  int target_col0;       // GV_PAIR_LSE: vocabulary column of B's first row (a shard's v0)
+  const int* target;     // GV_PAIR_LSE / GV_PAIR_DLOGITS
+  float* tgt_logit;      // GV_PAIR_LSE only
   int m_group;           // dense column-block-major order: row chunks per band (0 = all)
   const float* row_lse;  // GV_PAIR_DLOGITS only
   const float* row_scale;
@@ -103,13 +105,23 @@ int replay_launch(const float* logits, const int32_t* idx_in, int T, int E, int 
 // ---------------------------------------------------------------- combine / head
 int combine_launch(const float* y, const float* topk_w, const int32_t* slot_row, const float* y_shared,
                    int T, int H, int k, float* out, void* out_bf16, cudaStream_t st);
-int lse_merge_launch(const float2* partials, const float* tgt_logit, const int32_t* target,
-                     const float* rollout_logp, int T, int V, float beta, float* logp, float* lse, float* k3,
-                     uint8_t* mask, cudaStream_t st);
+// Partials of chunk c of token t at partials[(c / shard_chunks) * shard_stride + t * ld_part + c % shard_chunks];
+// the target logit of token t at tgt_logit[(target[t] / 256 / shard_chunks) * tgt_stride + t].
+int lse_merge_launch(const float2* partials, long long ld_part, int shard_chunks, long long shard_stride,
+                     const float* tgt_logit, long long tgt_stride, const int32_t* target, const float* rollout_logp,
+                     int T, int V, float beta, float* logp, float* lse, float* k3, uint8_t* mask, cudaStream_t st);
 int rl_loss_launch(const float* lt, const float* lo, const float* lr, const float* adv, int T, float beta,
                    float el, float eh, uint8_t* mask, float* dis, float* loss, float* loss_mean, float* grad,
                    cudaStream_t st);
 int timeout_probe_launch(unsigned int* status, unsigned long long limit_ns, cudaStream_t st);
+
+int shared_expert_run(const void* x, const void* ws13, const void* ws2, int T, int H, int F_shared, float* y_shared,
+                      void* hs, unsigned int* status, cudaStream_t st);
+
+// ---------------------------------------------------------------- expert parallelism
+int ep_regroup_launch(const void* recv_xp, const int32_t* recv_counts, int n_src, int E_local, int R, int H,
+                      void* xp_local, int32_t* plan_local, int32_t* row_src, unsigned int* status, cudaStream_t st);
+int ep_ungroup_launch(const float* y_local, const int32_t* row_src, int R, int H, float* y_send, cudaStream_t st);
 
 // ---------------------------------------------------------------- backward
 int combine_bwd_launch(const float* dout, const float* y, const float* topk_w, const int32_t* slot_row, int T,

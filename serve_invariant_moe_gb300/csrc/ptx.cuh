@@ -13,6 +13,7 @@ namespace invmoe {
 
 constexpr unsigned int kStatusTimeout = 1u;     // a bounded wait ran out
 constexpr unsigned int kStatusBadIndex = 2u;    // a replayed expert index was out of range or repeated
+constexpr unsigned int kStatusBadCounts = 4u;   // expert-parallel row counts did not add up to the rows given
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

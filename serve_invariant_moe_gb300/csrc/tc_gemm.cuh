@@ -80,9 +80,10 @@ struct GemmParams {
   int* sched;             // unit counter for the dynamic schedule (zero before launch)
   unsigned long long timeout_ns;
   // EPI_LSE only: per (row, column block) log-sum-exp partials and the target logit
-  float2* part;           // [rows, nch] (max, sum exp(z - max)) of each 256-column chunk
-  int nch;                // column blocks = ceil(N / 256)
-  const int* target;      // [rows] target column of each row
+  float2* part;           // (max, sum exp(z - max)) of column block nb of `row` at part[row * nch + nb]
+  int nch;                // row stride of part in pairs (ceil(N / 256) unless the caller sets one)
+  int col0;               // column index of B's first row in the whole vocabulary (vocabulary shards)
+  const int* target;      // [rows] target column of each row (in the whole vocabulary)
   float* tgt_logit;       // [rows] z[row, target[row]] (written by the block holding it)
   int m_group;            // dense column-block-major order: row chunks per band (>= 1)
   // EPI_DLOGITS only (target as above): out = bf16 g[row] * (onehot - exp(z - lse[row]))

@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
         if (half == 0) {
           const int n0 = U.nb * BN;
           float* orow = p.out != nullptr ? static_cast<float*>(p.out) + row * p.ldo + n0 : nullptr;
-          const int tg = valid ? __ldg(p.target + row) - n0 : -1;
+          const int tg = valid ? __ldg(p.target + row) - p.col0 - n0 : -1;
           float mx[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
