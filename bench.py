@@ -673,14 +673,15 @@ def tiny_latency(device, reps=200):
 
 
 def qwen_layer_timing(device, peaks, reps=5):
-    """The Qwen-MoE-like layer (T = 4096, H = 2048, E = 128 top-8, F = 768, Zipf(1.1)-skewed routing:
-    per-expert token counts from 0 to about 1500), outside the timed region: whole-layer device time
+    """The Qwen-MoE-like layer (T = 4096, H = 2048, E = 128 top-8, F = 768, Zipf(1.1)-skewed routing
+    with the 8 least popular experts starved: per-expert token counts from 0 to about 1500), outside
+    the timed region: whole-layer device time
     (route, dispatch, grouped SwiGLU experts, combine) and the grouped GEMMs against the bf16 peak and
     their memory roofline."""
     import torch
     from serve_invariant_moe_gb300 import _lib, api, binding, synth
     lib = _lib.lib()
-    mc = synth.QWEN_MOE
+    mc = synth.QWEN_MOE_EMPTY
     x, wr = synth.moe_activations(mc)
     w13, w2 = synth.expert_weights(mc, device)
     layer = api.MoELayer(api.MoEWeights(wr.to(device), w13, w2, mc.k))

@@ -179,6 +179,22 @@ int moe_combine(const float* y, const float* topk_w, const int32_t* plan, const 
                 int T, int H, int E, int k, float* out, void* out_bf16, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_layer_forward -- the whole layer in one call
+ *
+ * moe_route_topk, then moe_grouped_ffn (with the shared expert on x when
+ * F_shared > 0), then moe_combine, on one stream: exactly those three calls and
+ * their kernels (so the same bits), for callers that serve one small batch at a
+ * time and want one host call per layer.  Arguments, layouts and errors as the
+ * three calls; ws13, ws2 and y_shared are ignored when F_shared == 0; the
+ * workspace is invmoe_workspace_size(T, H, E, k, F, F_shared, 0) bytes.
+ * ------------------------------------------------------------------------- */
+int moe_layer_forward(const void* x, const void* w_router, const void* w13, const void* w2,
+                      const void* ws13, const void* ws2, int T, int H, int E, int k, int F, int F_shared,
+                      float* logits, int32_t* topk_idx, float* topk_w, int32_t* plan, void* xp, void* h,
+                      float* y, float* y_shared, float* out, void* out_bf16, void* workspace,
+                      size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * lm_logprob_kl -- vocab projection, chunked two-pass log-sum-exp, logprob, k3, IcePop
  *
  *   z[t, v] = sum_h hidden[t, h] * w_vocab[v, h]     (fp32 in TMEM, tcgen05 tile 128 x 256 x 64)
@@ -479,6 +495,14 @@ int invmoe_gemm_bf16(const void* a, const void* b, int M, int N, int K, float* d
  * the records and returns the number of rows (negative on error). */
 int invmoe_profile_enable(int on);
 int invmoe_profile_collect(char* names, float* total_ms, int* launches, int max_entries);
+
+/* Programmatic dependent launch (on by default): every kernel of this library is
+ * launched so that it may be scheduled while the previous kernel on its stream is
+ * still finishing; it runs only its set-up (shared memory, TMEM, descriptor
+ * prefetch) before waiting for that kernel to complete, so results are the same
+ * either way.  invmoe_pdl_enable(0) launches them plainly (for timing
+ * comparisons); the setting applies to calls made after it. */
+int invmoe_pdl_enable(int on);
 
 /* Launch a one-CTA kernel that waits on an mbarrier nothing ever completes,
  * with a wait limit of `timeout_us` microseconds (1..2000000).  The kernel

@@ -27,6 +27,8 @@ PROTOTYPES = {
     "moe_grouped_ffn": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp,
                              _vp, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
     "moe_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp]),
+    "moe_layer_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp,
+                               _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "lm_logprob_kl": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "lm_logprob_partials": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, ctypes.c_longlong, _vp, _vp, _sz,
                                  _vp]),
@@ -46,6 +48,7 @@ PROTOTYPES = {
     "invmoe_gemm_bf16": (_i, [_vp, _vp, _i, _i, _i, _vp, _i, _vp, _sz, _vp]),
     "invmoe_debug_timeout_probe": (_i, [_vp, _sz, _i, _vp]),
     "invmoe_profile_enable": (_i, [_i]),
+    "invmoe_pdl_enable": (_i, [_i]),
     "invmoe_profile_collect": (_i, [ctypes.c_char_p, ctypes.POINTER(_f), ctypes.POINTER(_i), _i]),
 }
 

@@ -64,11 +64,14 @@ class MoELayer:
         T = x.shape[0]
         bufs = bufs or {}
         if replay_idx is None:
-            r = binding.moe_route_topk(x, w.w_router, w.k, ws, logits=bufs.get("logits"), topk_idx=bufs.get("idx"),
-                                       topk_w=bufs.get("w"), plan=bufs.get("plan"), xp=bufs.get("xp"))
-        else:
-            r = binding.moe_route_replay(x, w.w_router, replay_idx, ws, logits=bufs.get("logits"),
-                                         topk_w=bufs.get("w"), plan=bufs.get("plan"), xp=bufs.get("xp"))
+            # route, experts and combine in one library call
+            return binding.moe_layer_forward(x, w.w_router, w.w13, w.w2, w.k, ws, ws13=w.ws13, ws2=w.ws2,
+                                             logits=bufs.get("logits"), topk_idx=bufs.get("idx"), topk_w=bufs.get("w"),
+                                             plan=bufs.get("plan"), xp=bufs.get("xp"), h=bufs.get("h"),
+                                             y=bufs.get("y"), y_shared=bufs.get("ys"), out=bufs.get("out"),
+                                             out_bf16=out_bf16)
+        r = binding.moe_route_replay(x, w.w_router, replay_idx, ws, logits=bufs.get("logits"),
+                                     topk_w=bufs.get("w"), plan=bufs.get("plan"), xp=bufs.get("xp"))
         f = binding.moe_grouped_ffn(r["xp"], r["plan"], w.w13, w.w2, T, w.k, ws, h=bufs.get("h"), y=bufs.get("y"),
                                     x_shared=x if w.ws13 is not None else None, ws13=w.ws13, ws2=w.ws2,
                                     y_shared=bufs.get("ys"))
@@ -125,18 +128,39 @@ class MoELayer:
             out=torch.empty((B, w.H), dtype=torch.float32, device=dev),
             ws=binding.new_workspace(binding.workspace_size(B, w.H, w.E, w.k, w.F, w.F_shared, 0), dev),
         )
+        d = self._decode
+        d["device"] = torch.device(dev)
+        p = lambda t: None if t is None else t.data_ptr()   # noqa: E731
+        # moe_layer_forward's arguments; decode() fills in x (0), B (6), out_bf16 (21) and the stream (24)
+        d["args"] = [None, p(w.w_router), p(w.w13), p(w.w2), p(w.ws13), p(w.ws2), B, w.H, w.E, w.k, w.F, w.F_shared,
+                     p(d["logits"]), p(d["idx"]), p(d["w"]), p(d["plan"]), p(d["xp"]), p(d["h"]), p(d["y"]),
+                     p(d["ys"]), p(d["out"]), None, p(d["ws"]), d["ws"].numel(), None]
+        d["fn"] = binding.lib().moe_layer_forward
 
     def decode(self, x_tokens: torch.Tensor, out_bf16: Optional[torch.Tensor] = None) -> torch.Tensor:
         """One token per request: x_tokens [B, H] bf16 -> [B, H] fp32 (a view of the decode buffer);
-        out_bf16 [B, H] (optional) receives the bf16 copy the head reads."""
+        out_bf16 [B, H] (optional) receives the bf16 copy the head reads.
+
+        One library call (moe_layer_forward) on buffers allocated once: the argument list is built in
+        alloc_decode (every buffer's batch-B view starts at the same address), so a call checks the
+        token tensor, sets its pointer, the batch size and the stream, and enters the library."""
         B = x_tokens.shape[0]
         if self._decode is None or self._decode["B"] < B:
             self.alloc_decode(max(B, 1))
         d = self._decode
         w = self.w
-        bufs = dict(logits=d["logits"][:B], idx=d["idx"][:B], w=d["w"][:B], plan=d["plan"], xp=d["xp"],
-                    h=d["h"], y=d["y"], ys=None if d["ys"] is None else d["ys"][:B], out=d["out"][:B])
-        return self._run(x_tokens, d["ws"], bufs, out_bf16=out_bf16)["out"]
+        if (x_tokens.dtype != torch.bfloat16 or x_tokens.device != d["device"] or not x_tokens.is_contiguous()
+                or x_tokens.dim() != 2 or x_tokens.shape[1] != w.H):
+            raise ValueError(f"x_tokens must be a contiguous [B, {w.H}] bf16 tensor on {d['device']}")
+        if out_bf16 is not None:
+            binding._req(out_bf16, torch.bfloat16, "out_bf16", (B, w.H))
+        args = d["args"]
+        args[0] = x_tokens.data_ptr()
+        args[6] = B
+        args[21] = None if out_bf16 is None else out_bf16.data_ptr()
+        args[24] = torch.cuda.current_stream(d["device"]).cuda_stream
+        binding.check(d["fn"](*args))
+        return d["out"][:B]
 
 
 class InputStager:

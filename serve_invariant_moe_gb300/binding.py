@@ -6,6 +6,7 @@ libinvmoe.so and raises on a non-zero status.  No arithmetic of the hot path
 happens here: every step runs in the library's kernels.
 """
 import ctypes
+import math
 
 import torch
 
@@ -148,6 +149,50 @@ def moe_grouped_ffn(xp, plan, w13, w2, T, k, workspace, h=None, y=None,
                                 _p(x_shared), _p(ws13), _p(ws2), Fs, _p(y_shared), _p(workspace),
                                 workspace.numel(), _stream()))
     return dict(h=h, y=y, y_shared=y_shared)
+
+
+def moe_layer_forward(x, w_router, w13, w2, k, workspace, ws13=None, ws2=None, logits=None, topk_idx=None, topk_w=None,
+                      plan=None, xp=None, h=None, y=None, y_shared=None, out=None, out_bf16=None):
+    """The whole layer in one library call (route, grouped SwiGLU experts, combine); missing outputs
+    are allocated.  Returns the same dict as the three calls."""
+    T, H = x.shape
+    E, F2, _ = w13.shape
+    F = F2 // 2
+    Fs = 0 if ws13 is None else ws13.shape[0] // 2
+    S = T * k
+    dev = x.device
+    _req(x, torch.bfloat16, "x")
+    _req(w_router, torch.bfloat16, "w_router", (E, H))
+    _req(w13, torch.bfloat16, "w13", (E, 2 * F, H))
+    _req(w2, torch.bfloat16, "w2", (E, H, F))
+
+    def buf(t, shape, dtype, name, min_numel=None):
+        t = torch.empty(shape, dtype=dtype, device=dev) if t is None else t
+        _req(t, dtype, name)
+        if t.numel() < (min_numel if min_numel is not None else math.prod(shape)):
+            raise ValueError(f"{name} is too small")
+        return t
+    logits = buf(logits, (T, E), torch.float32, "logits")
+    topk_idx = buf(topk_idx, (T, k), torch.int32, "topk_idx")
+    topk_w = buf(topk_w, (T, k), torch.float32, "topk_w")
+    plan = buf(plan, (plan_len(T, E, k),), torch.int32, "plan")
+    xp = buf(xp, (S, H), torch.bfloat16, "xp")
+    h = buf(h, (S, F), torch.bfloat16, "h")
+    y = buf(y, (S, H), torch.float32, "y")
+    out = buf(out, (T, H), torch.float32, "out")
+    if Fs:
+        _req(ws13, torch.bfloat16, "ws13", (2 * Fs, H))
+        _req(ws2, torch.bfloat16, "ws2", (H, Fs))
+        y_shared = buf(y_shared, (T, H), torch.float32, "y_shared")
+    else:
+        y_shared = None
+    _opt(out_bf16, torch.bfloat16, "out_bf16", (T, H))
+    _req(workspace, torch.uint8, "workspace")
+    check(lib().moe_layer_forward(_p(x), _p(w_router), _p(w13), _p(w2), _p(ws13), _p(ws2), T, H, E, k, F, Fs,
+                                  _p(logits), _p(topk_idx), _p(topk_w), _p(plan), _p(xp), _p(h), _p(y), _p(y_shared),
+                                  _p(out), _p(out_bf16), _p(workspace), workspace.numel(), _stream()))
+    return dict(out=out, logits=logits, topk_idx=topk_idx, topk_w=topk_w, plan=plan, xp=xp, h=h, y=y,
+                y_shared=y_shared)
 
 
 def moe_combine(y, topk_w, plan, T, H, E, k, y_shared=None, out=None, out_bf16=None):

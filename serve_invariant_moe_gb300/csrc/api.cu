@@ -70,6 +70,12 @@ int check_cuda(cudaError_t e, const char* what) {
   return set_error(INVMOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+namespace {
+std::atomic<bool> g_pdl_on{true};
+}  // namespace
+
+bool pdl_enabled() { return g_pdl_on.load(std::memory_order_relaxed); }
+
 int device_sm_count(int* out) {
   static std::atomic<int> cache[64] = {};
   int dev = 0;
@@ -324,6 +330,18 @@ int moe_grouped_ffn(const void* xp, const int32_t* plan, const void* w13, const 
   if (F_shared > 0)
     return shared_expert_run(x_shared, ws13, ws2, T, H, F_shared, y_shared, scratch(workspace), status, st);
   return INVMOE_OK;
+}
+
+int moe_layer_forward(const void* x, const void* w_router, const void* w13, const void* w2, const void* ws13,
+                      const void* ws2, int T, int H, int E, int k, int F, int F_shared, float* logits,
+                      int32_t* topk_idx, float* topk_w, int32_t* plan, void* xp, void* h, float* y, float* y_shared,
+                      float* out, void* out_bf16, void* workspace, size_t ws_bytes, void* stream) {
+  int rc = moe_route_topk(x, w_router, T, H, E, k, logits, topk_idx, topk_w, plan, xp, workspace, ws_bytes, stream);
+  if (rc) return rc;
+  rc = moe_grouped_ffn(xp, plan, w13, w2, T, H, E, k, F, h, y, x, ws13, ws2, F_shared, y_shared, workspace, ws_bytes,
+                       stream);
+  if (rc) return rc;
+  return moe_combine(y, topk_w, plan, F_shared > 0 ? y_shared : nullptr, T, H, E, k, out, out_bf16, stream);
 }
 
 int moe_combine(const float* y, const float* topk_w, const int32_t* plan, const float* y_shared, int T, int H, int E,
@@ -761,6 +779,11 @@ int invmoe_gemm_bf16(const void* a, const void* b, int M, int N, int K, float* d
   g.n_major = n_major;
   g.out = d; g.ldo = N; g.status = status_word(workspace);
   return gemm_run(g, static_cast<cudaStream_t>(stream));
+}
+
+int invmoe_pdl_enable(int on) {
+  g_pdl_on.store(on != 0);
+  return INVMOE_OK;
 }
 
 int invmoe_profile_enable(int on) {

@@ -19,6 +19,8 @@ namespace {
 __global__ void combine_kernel(const float4* __restrict__ y, const float* __restrict__ w,
                                const int32_t* __restrict__ slot_row, const float4* __restrict__ y_shared, int T,
                                int H4, int k, float4* __restrict__ out, uint2* __restrict__ out_bf16) {
+  pdl_wait();
+  pdl_trigger();
   const long long total = static_cast<long long>(T) * H4;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -89,6 +91,8 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, long long ld_p
                                  const int32_t* __restrict__ target, const float* __restrict__ rollout, int T, int V,
                                  int NCH, float beta, float* __restrict__ logp, float* __restrict__ lse,
                                  float* __restrict__ k3, uint8_t* __restrict__ mask) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -217,10 +221,11 @@ int combine_launch(const float* y, const float* topk_w, const int32_t* slot_row,
   if (blocks > static_cast<long long>(sms) * 16) blocks = static_cast<long long>(sms) * 16;
   if (blocks == 0) return INVMOE_OK;
   ProfScope prof("combine", st);
-  combine_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(
-      reinterpret_cast<const float4*>(y), topk_w, slot_row, reinterpret_cast<const float4*>(y_shared), T, H4, k,
-      reinterpret_cast<float4*>(out), reinterpret_cast<uint2*>(out_bf16));
-  return check_cuda(cudaGetLastError(), "combine_kernel");
+  return check_cuda(launch_kernel(combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st,
+                                  reinterpret_cast<const float4*>(y), topk_w, slot_row,
+                                  reinterpret_cast<const float4*>(y_shared), T, H4, k, reinterpret_cast<float4*>(out),
+                                  reinterpret_cast<uint2*>(out_bf16)),
+                    "combine_kernel");
 }
 
 int lse_merge_launch(const float2* partials, long long ld_part, int shard_chunks, long long shard_stride,
@@ -229,10 +234,10 @@ int lse_merge_launch(const float2* partials, long long ld_part, int shard_chunks
   const int NCH = (V + kLseChunk - 1) / kLseChunk;
   if (T == 0) return INVMOE_OK;
   ProfScope prof("lse_merge", st);
-  lse_merge_kernel<<<(T + kMergeWarps - 1) / kMergeWarps, 32 * kMergeWarps, 0, st>>>(
-      partials, ld_part, shard_chunks, shard_stride, tgt_logit, tgt_stride, target, rollout_logp, T, V, NCH, beta,
-      logp, lse, k3, mask);
-  return check_cuda(cudaGetLastError(), "lse_merge_kernel");
+  return check_cuda(launch_kernel(lse_merge_kernel, dim3((T + kMergeWarps - 1) / kMergeWarps), dim3(32 * kMergeWarps),
+                                  0, st, partials, ld_part, shard_chunks, shard_stride, tgt_logit, tgt_stride, target,
+                                  rollout_logp, T, V, NCH, beta, logp, lse, k3, mask),
+                    "lse_merge_kernel");
 }
 
 int rl_loss_launch(const float* lt, const float* lo, const float* lr, const float* adv, int T, float beta,

@@ -55,6 +55,8 @@ __global__ void __launch_bounds__(kPlanThreads) ep_plan_kernel(const int32_t* __
                                                                int R, int32_t* __restrict__ plan_local,
                                                                int32_t* __restrict__ row_src,
                                                                unsigned int* __restrict__ status) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ long long red[kPlanThreads / 32];
   const int nflat = n_src * E_local;
   const int b = blockIdx.x;
@@ -101,6 +103,8 @@ __global__ void __launch_bounds__(kPlanThreads) ep_plan_kernel(const int32_t* __
 // xp_local[i, :] = recv[row_src[i], :], 16-byte vectors, one warp per row.
 __global__ void ep_gather_kernel(const uint4* __restrict__ recv, const int32_t* __restrict__ row_src, int R,
                                  int vec_per_row, uint4* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long nw = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x >> 5) + (threadIdx.x >> 5); i < R; i += nw) {
@@ -115,6 +119,8 @@ __global__ void ep_gather_kernel(const uint4* __restrict__ recv, const int32_t* 
 // y_send[row_src[i], :] = y_local[i, :], fp32 rows in 16-byte vectors, one warp per row.
 __global__ void ep_scatter_kernel(const float4* __restrict__ y_local, const int32_t* __restrict__ row_src, int R,
                                   int vec_per_row, float4* __restrict__ y_send) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long nw = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x >> 5) + (threadIdx.x >> 5); i < R; i += nw) {
@@ -141,26 +147,29 @@ int ep_regroup_launch(const void* recv_xp, const int32_t* recv_counts, int n_src
   int rc;
   {
     ProfScope prof("ep_plan", st);
-    ep_plan_kernel<<<n_src * E_local + 1, kPlanThreads, 0, st>>>(recv_counts, n_src, E_local, R, plan_local, row_src,
-                                                                  status);
-    if ((rc = check_cuda(cudaGetLastError(), "ep_plan_kernel"))) return rc;
+    rc = check_cuda(launch_kernel(ep_plan_kernel, dim3(n_src * E_local + 1), dim3(kPlanThreads), 0, st, recv_counts,
+                                  n_src, E_local, R, plan_local, row_src, status),
+                    "ep_plan_kernel");
+    if (rc) return rc;
   }
   if (R == 0) return INVMOE_OK;
   const int blocks = row_grid(R);
   if (blocks <= 0) return set_error(INVMOE_ERR_CUDA, "could not size the regroup grid");
   ProfScope prof("ep_gather_rows", st);
-  ep_gather_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(recv_xp), row_src, R, H / 8,
-                                           static_cast<uint4*>(xp_local));
-  return check_cuda(cudaGetLastError(), "ep_gather_kernel");
+  return check_cuda(launch_kernel(ep_gather_kernel, dim3(blocks), dim3(256), 0, st,
+                                  static_cast<const uint4*>(recv_xp), static_cast<const int32_t*>(row_src), R, H / 8,
+                                  static_cast<uint4*>(xp_local)),
+                    "ep_gather_kernel");
 }
 
 int ep_ungroup_launch(const float* y_local, const int32_t* row_src, int R, int H, float* y_send, cudaStream_t st) {
   const int blocks = row_grid(R);
   if (blocks <= 0) return set_error(INVMOE_ERR_CUDA, "could not size the ungroup grid");
   ProfScope prof("ep_scatter_rows", st);
-  ep_scatter_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(y_local), row_src, R, H / 4,
-                                            reinterpret_cast<float4*>(y_send));
-  return check_cuda(cudaGetLastError(), "ep_scatter_kernel");
+  return check_cuda(launch_kernel(ep_scatter_kernel, dim3(blocks), dim3(256), 0, st,
+                                  reinterpret_cast<const float4*>(y_local), row_src, R, H / 4,
+                                  reinterpret_cast<float4*>(y_send)),
+                    "ep_scatter_kernel");
 }
 
 }  // namespace invmoe

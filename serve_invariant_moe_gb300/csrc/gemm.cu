@@ -157,10 +157,12 @@ int launch(const GemmCall& c, cudaStream_t st) {
   long long max_units = max_chunks * p.n_blocks;
   if (max_units <= 0) return INVMOE_OK;
   const int grid = static_cast<int>(max_units < sms ? max_units : sms);
-  if ((rc = check_cuda(cudaMemsetAsync(p.sched, 0, sizeof(int), st), "cudaMemsetAsync"))) return rc;
+  // the unit counter (p.sched) is zero here: the workspace starts zero-filled and every
+  // launch's last CTA resets it (sched_release)
   ProfScope prof(c.name ? c.name : "tc_gemm", st);
-  tc_gemm_kernel<BN, MT, EPI, STAGES, A_MN, B_MN, KG><<<grid, S::THREADS, S::SMEM_BYTES, st>>>(ta, tb, to, p);
-  return check_cuda(cudaGetLastError(), "tc_gemm_kernel launch");
+  return check_cuda(launch_kernel(tc_gemm_kernel<BN, MT, EPI, STAGES, A_MN, B_MN, KG>, dim3(grid), dim3(S::THREADS),
+                                  S::SMEM_BYTES, st, ta, tb, to, p),
+                    "tc_gemm_kernel launch");
 }
 
 
@@ -197,24 +199,18 @@ int launch_pair(const GemmCall& c, cudaStream_t st) {
   long long max_units = max_chunks * p.n_blocks;
   if (max_units <= 0) return INVMOE_OK;
   const long long pairs = max_units < sms / 2 ? max_units : sms / 2;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
-  cfg.blockDim = dim3(S::THREADS, 1, 1);
-  cfg.dynamicSmemBytes = S::SMEM_BYTES;
-  cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if ((rc = check_cuda(cudaMemsetAsync(p.sched, 0, sizeof(int), st), "cudaMemsetAsync"))) return rc;
+  // the unit counter (p.sched) is zero here: the workspace starts zero-filled and every
+  // launch's last CTA resets it (sched_release)
   ProfScope prof(c.name ? c.name : "tc_gemm_pair", st);
-  rc = check_cuda(cudaLaunchKernelEx(&cfg, tc_gemm_pair_kernel<EPI, STAGES, A_MN, B_MN>, ta, tb, to, p),
-                  "cudaLaunchKernelEx");
-  if (rc) return rc;
-  return check_cuda(cudaGetLastError(), "tc_gemm_pair_kernel launch");
+  return check_cuda(launch_kernel_ex(tc_gemm_pair_kernel<EPI, STAGES, A_MN, B_MN>,
+                                     dim3(static_cast<unsigned>(2 * pairs)), dim3(S::THREADS), S::SMEM_BYTES, st, attr,
+                                     1, ta, tb, to, p),
+                    "tc_gemm_pair_kernel launch");
 }
 
 }  // namespace

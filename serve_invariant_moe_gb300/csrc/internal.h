@@ -35,6 +35,40 @@ int device_sm_count(int* out);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Whether kernels are launched with programmatic dependent launch (on unless switched off
+// with invmoe_pdl_enable(0)).
+bool pdl_enabled();
+
+// Launch `kernel` on `st`; with programmatic dependent launch on, it may be scheduled while
+// the previous kernel on the stream is finishing (every kernel launched this way calls
+// pdl_wait() before touching global memory).  Extra attributes (a cluster shape) may be given.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             const cudaLaunchAttribute* extra, int n_extra, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[4];
+  int n = 0;
+  for (int i = 0; i < n_extra && n < 3; ++i) attr[n++] = extra[i];
+  if (pdl_enabled()) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                          Args... args) {
+  return launch_kernel_ex(kernel, grid, block, smem, st, nullptr, 0, args...);
+}
+
 // ---------------------------------------------------------------- GEMM engine
 enum GemmVariant : int {
   GV_F32_BN256_MT1 = 0,   // dense fp32-out, 4-stage ring, double-buffered TMEM (LM head)
@@ -98,6 +132,7 @@ int route_launch(const float* logits, int T, int E, int k, int H, const void* x,
 
 int dispatch_launch(const int32_t* topk_idx, int T, int E, int k, int H, const void* x, int32_t* plan, void* xp,
                     int32_t* chunk_counts, cudaStream_t st);
+int permute_launch(const void* x, const int32_t* slot_row, int T, int k, int H, void* xp, cudaStream_t st);
 int replay_launch(const float* logits, const int32_t* idx_in, int T, int E, int k, int H, const void* x,
                   int32_t* idx_safe, float* topk_w, int32_t* plan, void* xp, int32_t* chunk_counts,
                   unsigned int* status, cudaStream_t st);

@@ -73,7 +73,8 @@ extern "C" int moe_route_topk_noalloc(const void* x, const void* w_router, int T
   int rc = noalloc_scratch(&scratch);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the status word must start at zero (the schedule counter is zeroed by each GEMM launch)
+  // the status word must start at zero (the schedule counters start at zero in the static array and
+  // every GEMM launch leaves them at zero)
   rc = check_cuda(cudaMemsetAsync(scratch, 0, sizeof(unsigned int), st), "cudaMemsetAsync");
   if (rc) return rc;
   // Same validation and the same kernels as moe_route_topk, on the fixed scratch.

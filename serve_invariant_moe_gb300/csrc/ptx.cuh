@@ -15,6 +15,29 @@ constexpr unsigned int kStatusTimeout = 1u;     // a bounded wait ran out
 constexpr unsigned int kStatusBadIndex = 2u;    // a replayed expert index was out of range or repeated
 constexpr unsigned int kStatusBadCounts = 4u;   // expert-parallel row counts did not add up to the rows given
 
+// Programmatic dependent launch.  A kernel launched with the programmatic-serialization
+// attribute may be scheduled while the previous kernel on its stream is still running;
+// pdl_wait() blocks until that kernel has completed and its memory writes are visible, so
+// every such kernel calls it before its first global-memory access (and before it returns).
+// pdl_trigger() lets the next kernel be scheduled now (its own pdl_wait still waits for
+// this kernel to complete).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// The dynamic-schedule counter of a GEMM launch is left at zero for the next launch: the
+// last CTA of the grid to finish resets it.  A CTA adds itself to the done count only after
+// its producer has taken its last unit index, so no CTA touches the counter after the reset.
+// Both words start at zero (the caller zero-fills the workspace once).
+__device__ __forceinline__ void sched_release(int* sched) {
+  int* done = sched + 1;
+  __threadfence();
+  if (atomicAdd(done, 1) == static_cast<int>(gridDim.x * gridDim.y * gridDim.z) - 1) {
+    atomicExch(sched, 0);
+    atomicExch(done, 0);
+    __threadfence();
+  }
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

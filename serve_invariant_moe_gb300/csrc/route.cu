@@ -5,6 +5,8 @@
 // decision); "GLM Post-Training Beyond SFT", section "迁移到 NPU 时" (a top-k must
 // fix ties, boundary ties, sort order, NaN handling and the index dtype).
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -32,14 +34,12 @@ __device__ __forceinline__ float key_value(uint32_t key) {
 // One warp per token.  Lane l holds experts l, l+32, ... (EPL of them).  Each of
 // the k rounds takes the warp-wide maximum of (key, ~expert): a larger logit
 // wins, an exact tie goes to the lower expert index.  The gate softmax is taken
-// over the k selected logits in rank order, in fp32.
+// over the k selected logits in rank order, in fp32.  Lane j < k returns the
+// j-th ranked expert and its gate.  Both routing kernels below call this one
+// function, so they take the same decisions and compute the same gate bits.
 template <int EPL>
-__global__ void topk_gate_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx,
-                                 float* __restrict__ w) {
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
-  const float* row = logits + static_cast<long long>(t) * E;
+__device__ __forceinline__ void topk_token(const float* __restrict__ row, int E, int k, int lane, int& out_e,
+                                           float& out_w) {
   uint64_t key[EPL];
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
@@ -74,9 +74,140 @@ __global__ void topk_gate_kernel(const float* __restrict__ logits, int T, int E,
   const float ex = (lane < k) ? expf(my_v - v0) : 0.0f;
   float s = 0.0f;
   for (int j = 0; j < k; ++j) s = __fadd_rn(s, __shfl_sync(kFull, ex, j));
+  out_e = my_e;
+  out_w = __fdiv_rn(ex, s);
+}
+
+template <int EPL>
+__global__ void topk_gate_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx,
+                                 float* __restrict__ w) {
+  pdl_wait();
+  pdl_trigger();
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  int e;
+  float wt;
+  topk_token<EPL>(logits + static_cast<long long>(t) * E, E, k, lane, e, wt);
   if (lane < k) {
-    idx[static_cast<long long>(t) * k + lane] = my_e;
-    w[static_cast<long long>(t) * k + lane] = __fdiv_rn(ex, s);
+    idx[static_cast<long long>(t) * k + lane] = e;
+    w[static_cast<long long>(t) * k + lane] = wt;
+  }
+}
+
+// Routing of a small batch in one block of 1024 threads: the top-k and gates of
+// every token, the dispatch plan and (when the copy is small) the permute, in one
+// launch instead of five.  The plan is the same stable counting sort as the
+// multi-kernel path (within an expert, rows in ascending (token, slot) order):
+// warp w counts and then places the (token, slot) pairs of the w-th contiguous
+// range of the batch, so every position is the same integer whichever path
+// computes it.
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallMaxTokens = 256;
+constexpr int kSmallMaxPairs = 4096;
+constexpr long long kSmallPermuteBytes = 512 * 1024;
+
+size_t route_small_smem(int T, int E, int k) {
+  return (2 * static_cast<size_t>(T) * k + 32 * static_cast<size_t>(E) + E + 1 + 32) * sizeof(int);
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(kSmallThreads, 1)
+    route_small_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx,
+                       float* __restrict__ w, int32_t* __restrict__ plan, const uint4* __restrict__ x,
+                       int vec_per_row, uint4* __restrict__ xp, int do_permute) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ int sm[];
+  const int S = T * k;
+  int* s_idx = sm;                 // [S] expert of each pair
+  int* s_pos = s_idx + S;          // [S] permuted row of each pair
+  int* hist = s_pos + S;           // [32][E] per-warp counts, then per-warp running positions
+  int* s_off = hist + 32 * E;      // [E + 1] segment starts
+  int* warp_tot = s_off + E + 1;   // [32]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int32_t* counts = plan;
+  int32_t* offsets = plan + E;
+  int32_t* row_token = plan + 2 * E + 1;
+  int32_t* slot_row = row_token + S;
+  // top-k and gates: warp w takes tokens w, w + 32, ...
+  for (int t = warp; t < T; t += 32) {
+    int e;
+    float wt;
+    topk_token<EPL>(logits + static_cast<long long>(t) * E, E, k, lane, e, wt);
+    if (lane < k) {
+      idx[t * k + lane] = e;
+      w[t * k + lane] = wt;
+      s_idx[t * k + lane] = e;
+    }
+  }
+  for (int i = tid; i < 32 * E; i += kSmallThreads) hist[i] = 0;
+  __syncthreads();
+  // per-warp counts over contiguous ranges of pairs
+  const int per = (S + 31) / 32;
+  const int p0 = min(S, warp * per), p1 = min(S, p0 + per);
+  for (int p = p0 + lane; p < p1; p += 32) atomicAdd(&hist[warp * E + s_idx[p]], 1);
+  __syncthreads();
+  // per expert: exclusive scan over warps (in place) and the expert total
+  int run = 0;
+  if (tid < E) {
+    for (int v = 0; v < 32; ++v) {
+      const int c = hist[v * E + tid];
+      hist[v * E + tid] = run;
+      run += c;
+    }
+    counts[tid] = run;
+  }
+  // exclusive scan of the totals over experts (E <= 1024: one per thread)
+  int incl = run;
+  for (int d = 1; d < 32; d <<= 1) {
+    const int v = __shfl_up_sync(kFull, incl, d);
+    if (lane >= d) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int t = warp_tot[lane];
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(kFull, t, d);
+      if (lane >= d) t += v;
+    }
+    warp_tot[lane] = t;
+  }
+  __syncthreads();
+  const int excl = incl - run + (warp > 0 ? warp_tot[warp - 1] : 0);
+  if (tid < E) {
+    offsets[tid] = excl;
+    s_off[tid] = excl;
+  }
+  if (tid == E - 1) offsets[E] = excl + run;
+  __syncthreads();
+  // placement: each warp walks its range 32 pairs at a time in ascending order
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int pb = p0; pb < p1; pb += 32) {
+    const int p = pb + lane;
+    const int e = (p < p1) ? s_idx[p] : -1;
+    const unsigned m = __match_any_sync(kFull, e);
+    const int rank = __popc(m & lt_mask);
+    if (e >= 0) {
+      const int pos = s_off[e] + hist[warp * E + e] + rank;
+      row_token[pos] = p / k;
+      slot_row[p] = pos;
+      s_pos[p] = pos;
+    }
+    __syncwarp();
+    if (e >= 0 && rank == 0) hist[warp * E + e] += __popc(m);
+    __syncwarp();
+  }
+  if (!do_permute) return;
+  __syncthreads();
+  // permute: xp[slot_row[t, j]] = x[t], one warp per token, 16-byte vectors
+  for (int t = warp; t < T; t += 32) {
+    const uint4* src = x + static_cast<long long>(t) * vec_per_row;
+    for (int c = lane; c < vec_per_row; c += 32) {
+      const uint4 v = __ldg(src + c);
+      for (int j = 0; j < k; ++j) xp[static_cast<long long>(s_pos[t * k + j]) * vec_per_row + c] = v;
+    }
   }
 }
 
@@ -92,6 +223,8 @@ __global__ void topk_gate_kernel(const float* __restrict__ logits, int T, int E,
 __global__ void replay_gate_kernel(const float* __restrict__ logits, const int32_t* __restrict__ idx_in, int T,
                                    int E, int k, int32_t* __restrict__ idx_out, float* __restrict__ w,
                                    unsigned int* __restrict__ status) {
+  pdl_wait();
+  pdl_trigger();
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -123,6 +256,8 @@ __global__ void replay_gate_kernel(const float* __restrict__ logits, const int32
 // Per chunk of kDispatchChunk tokens: how many of its (token, slot) pairs go to each expert.
 __global__ void dispatch_count_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
                                       int32_t* __restrict__ chunk_counts) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -138,6 +273,8 @@ __global__ void dispatch_count_kernel(const int32_t* __restrict__ idx, int T, in
 // totals, and an exclusive scan over experts for the segment offsets.
 __global__ void dispatch_scan_kernel(int32_t* __restrict__ chunk_counts, int NC, int E, int32_t* __restrict__ counts,
                                      int32_t* __restrict__ offsets) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int warp_tot[32];
   const int e = threadIdx.x;
   int run = 0;
@@ -194,6 +331,8 @@ __global__ void dispatch_scan_kernel(int32_t* __restrict__ chunk_counts, int NC,
 __global__ void dispatch_scatter_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
                                         const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
                                         int32_t* __restrict__ row_token, int32_t* __restrict__ slot_row) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int run[];
   const int lane = threadIdx.x;
   for (int e = lane; e < E; e += 32) run[e] = 0;
@@ -228,6 +367,8 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_rows_kernel(const uin
                                                                       const int32_t* __restrict__ slot_row,
                                                                       long long T, int k, int vec_per_row,
                                                                       uint4* __restrict__ xp) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long nwarps = static_cast<long long>(gridDim.x) * (kPermuteThreads / 32);
   for (long long t = blockIdx.x * static_cast<long long>(kPermuteThreads / 32) + (threadIdx.x >> 5); t < T;
@@ -261,22 +402,66 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_rows_kernel(const uin
 
 }  // namespace
 
+namespace {
+
+template <int EPL>
+int route_small_launch_epl(const float* logits, int T, int E, int k, int H, const void* x, int32_t* topk_idx,
+                           float* topk_w, int32_t* plan, void* xp, bool do_permute, cudaStream_t st) {
+  const size_t smem = route_small_smem(T, E, k);
+  static std::atomic<uint64_t> attr_set{0};
+  int dev = 0;
+  int rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc) return rc;
+  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (bit == 0 || !(attr_set.load(std::memory_order_acquire) & bit)) {
+    // the largest shared-memory request of this kernel (E = 1024, 4096 pairs) is 164 KB
+    rc = check_cuda(cudaFuncSetAttribute(route_small_kernel<EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(route_small_smem(kSmallMaxTokens, 1024, 16))),
+                    "cudaFuncSetAttribute");
+    if (rc) return rc;
+    if (bit) attr_set.fetch_or(bit, std::memory_order_release);
+  }
+  ProfScope prof("route_small", st);
+  return check_cuda(launch_kernel(route_small_kernel<EPL>, dim3(1), dim3(kSmallThreads), smem, st, logits, T, E, k,
+                                  topk_idx, topk_w, plan, static_cast<const uint4*>(x), H / 8,
+                                  static_cast<uint4*>(xp), do_permute ? 1 : 0),
+                    "route_small_kernel");
+}
+
+}  // namespace
+
 int route_launch(const float* logits, int T, int E, int k, int H, const void* x, int32_t* topk_idx,
                  float* topk_w, int32_t* plan, void* xp, int32_t* chunk_counts, cudaStream_t st) {
   int rc;
+  if (T <= kSmallMaxTokens && static_cast<long long>(T) * k <= kSmallMaxPairs) {
+    // small batch: one block routes it (same decisions, same plan), and copies the rows too when
+    // they are few; otherwise the grid-wide permute follows
+    const bool fused_permute = static_cast<long long>(T) * k * H * 2 <= kSmallPermuteBytes;
+    const int epl = (E + 31) / 32;
+    if (epl <= 1) rc = route_small_launch_epl<1>(logits, T, E, k, H, x, topk_idx, topk_w, plan, xp, fused_permute, st);
+    else if (epl <= 2) rc = route_small_launch_epl<2>(logits, T, E, k, H, x, topk_idx, topk_w, plan, xp, fused_permute, st);
+    else if (epl <= 4) rc = route_small_launch_epl<4>(logits, T, E, k, H, x, topk_idx, topk_w, plan, xp, fused_permute, st);
+    else if (epl <= 8) rc = route_small_launch_epl<8>(logits, T, E, k, H, x, topk_idx, topk_w, plan, xp, fused_permute, st);
+    else if (epl <= 16) rc = route_small_launch_epl<16>(logits, T, E, k, H, x, topk_idx, topk_w, plan, xp, fused_permute, st);
+    else rc = route_small_launch_epl<32>(logits, T, E, k, H, x, topk_idx, topk_w, plan, xp, fused_permute, st);
+    if (rc || fused_permute) return rc;
+    return permute_launch(x, plan + 2 * E + 1 + static_cast<long long>(T) * k, T, k, H, xp, st);
+  }
   // top-k + gates
   {
     const int threads = 256;
     const long long blocks = (static_cast<long long>(T) * 32 + threads - 1) / threads;
     const int epl = (E + 31) / 32;
     ProfScope prof("topk_gate", st);
-    if (epl <= 1) topk_gate_kernel<1><<<blocks, threads, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
-    else if (epl <= 2) topk_gate_kernel<2><<<blocks, threads, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
-    else if (epl <= 4) topk_gate_kernel<4><<<blocks, threads, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
-    else if (epl <= 8) topk_gate_kernel<8><<<blocks, threads, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
-    else if (epl <= 16) topk_gate_kernel<16><<<blocks, threads, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
-    else topk_gate_kernel<32><<<blocks, threads, 0, st>>>(logits, T, E, k, topk_idx, topk_w);
-    if ((rc = check_cuda(cudaGetLastError(), "topk_gate_kernel"))) return rc;
+    const dim3 g(static_cast<unsigned>(blocks)), b(threads);
+    cudaError_t e;
+    if (epl <= 1) e = launch_kernel(topk_gate_kernel<1>, g, b, 0, st, logits, T, E, k, topk_idx, topk_w);
+    else if (epl <= 2) e = launch_kernel(topk_gate_kernel<2>, g, b, 0, st, logits, T, E, k, topk_idx, topk_w);
+    else if (epl <= 4) e = launch_kernel(topk_gate_kernel<4>, g, b, 0, st, logits, T, E, k, topk_idx, topk_w);
+    else if (epl <= 8) e = launch_kernel(topk_gate_kernel<8>, g, b, 0, st, logits, T, E, k, topk_idx, topk_w);
+    else if (epl <= 16) e = launch_kernel(topk_gate_kernel<16>, g, b, 0, st, logits, T, E, k, topk_idx, topk_w);
+    else e = launch_kernel(topk_gate_kernel<32>, g, b, 0, st, logits, T, E, k, topk_idx, topk_w);
+    if ((rc = check_cuda(e, "topk_gate_kernel"))) return rc;
   }
   return dispatch_launch(topk_idx, T, E, k, H, x, plan, xp, chunk_counts, st);
 }
@@ -289,8 +474,10 @@ int replay_launch(const float* logits, const int32_t* idx_in, int T, int E, int 
     const int threads = 256;
     const long long blocks = (static_cast<long long>(T) * 32 + threads - 1) / threads;
     ProfScope prof("replay_gate", st);
-    replay_gate_kernel<<<blocks, threads, 0, st>>>(logits, idx_in, T, E, k, idx_safe, topk_w, status);
-    if ((rc = check_cuda(cudaGetLastError(), "replay_gate_kernel"))) return rc;
+    rc = check_cuda(launch_kernel(replay_gate_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, st,
+                                  logits, idx_in, T, E, k, idx_safe, topk_w, status),
+                    "replay_gate_kernel");
+    if (rc) return rc;
   }
   return dispatch_launch(idx_safe, T, E, k, H, x, plan, xp, chunk_counts, st);
 }
@@ -307,21 +494,31 @@ int dispatch_launch(const int32_t* topk_idx, int T, int E, int k, int H, const v
   const int NC = (T + kDispatchChunk - 1) / kDispatchChunk;
   {
     ProfScope prof("dispatch_count", st);
-    dispatch_count_kernel<<<NC, 256, E * sizeof(int), st>>>(topk_idx, T, E, k, chunk_counts);
+    rc = check_cuda(launch_kernel(dispatch_count_kernel, dim3(NC), dim3(256), E * sizeof(int), st, topk_idx, T, E,
+                                  k, chunk_counts),
+                    "dispatch_count_kernel");
   }
-  if ((rc = check_cuda(cudaGetLastError(), "dispatch_count_kernel"))) return rc;
+  if (rc) return rc;
   {
     ProfScope prof("dispatch_scan", st);
-    dispatch_scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, NC, E, counts, offsets);
+    rc = check_cuda(launch_kernel(dispatch_scan_kernel, dim3(1), dim3(1024), 0, st, chunk_counts, NC, E, counts,
+                                  offsets),
+                    "dispatch_scan_kernel");
   }
-  if ((rc = check_cuda(cudaGetLastError(), "dispatch_scan_kernel"))) return rc;
+  if (rc) return rc;
   {
     ProfScope prof("dispatch_scatter", st);
-    dispatch_scatter_kernel<<<NC, 32, E * sizeof(int), st>>>(topk_idx, T, E, k, chunk_counts, offsets, row_token,
-                                                             slot_row);
+    rc = check_cuda(launch_kernel(dispatch_scatter_kernel, dim3(NC), dim3(32), E * sizeof(int), st, topk_idx, T, E,
+                                  k, static_cast<const int32_t*>(chunk_counts), static_cast<const int32_t*>(offsets),
+                                  row_token, slot_row),
+                    "dispatch_scatter_kernel");
   }
-  if ((rc = check_cuda(cudaGetLastError(), "dispatch_scatter_kernel"))) return rc;
-  // permute
+  if (rc) return rc;
+  return permute_launch(x, slot_row, T, k, H, xp, st);
+}
+
+int permute_launch(const void* x, const int32_t* slot_row, int T, int k, int H, void* xp, cudaStream_t st) {
+  int rc;
   const int vec_per_row = H / 8;
   int sms = 0;
   if ((rc = device_sm_count(&sms))) return rc;
@@ -331,9 +528,11 @@ int dispatch_launch(const int32_t* topk_idx, int T, int E, int k, int H, const v
   if (blocks > cap) blocks = cap;
   if (blocks > 0 && vec_per_row > 0) {
     ProfScope prof("permute_rows", st);
-    permute_rows_kernel<<<static_cast<int>(blocks), kPermuteThreads, 0, st>>>(
-        static_cast<const uint4*>(x), slot_row, T, k, vec_per_row, static_cast<uint4*>(xp));
-    if ((rc = check_cuda(cudaGetLastError(), "permute_rows_kernel"))) return rc;
+    rc = check_cuda(launch_kernel(permute_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kPermuteThreads), 0,
+                                  st, static_cast<const uint4*>(x), slot_row, static_cast<long long>(T), k, vec_per_row,
+                                  static_cast<uint4*>(xp)),
+                    "permute_rows_kernel");
+    if (rc) return rc;
   }
   return INVMOE_OK;
 }

@@ -372,6 +372,10 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) tmem_alloc(tmem_slot, S::TMEM_COLS);
+  // everything above touches only shared memory, TMEM and the kernel parameters; the
+  // previous kernel on the stream (which wrote this kernel's inputs) is waited for here
+  pdl_wait();
+  pdl_trigger();
 
   // Row-chunk prefix over groups (warp 2; G <= 1024): s_prefix[g] = sum_{g'<g} ceil(counts[g'] / (MT*128)).
   constexpr int CH = MT * kBM;
@@ -755,6 +759,7 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, S::TMEM_COLS);
   }
+  if (threadIdx.x == 0) sched_release(p.sched);
 }
 
 }  // namespace invmoe

@@ -118,6 +118,10 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, S::TMEM_COLS);
+  // everything above touches only shared memory, TMEM and the kernel parameters; the
+  // previous kernel on the stream (which wrote this kernel's inputs) is waited for here
+  pdl_wait();
+  pdl_trigger();
 
   constexpr int CH = 2 * kBM;   // rows per pair unit
   if (warp == 2) {
@@ -515,6 +519,7 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, S::TMEM_COLS);
   }
+  if (threadIdx.x == 0) sched_release(p.sched);
 }
 
 }  // namespace invmoe

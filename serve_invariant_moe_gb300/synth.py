@@ -35,6 +35,7 @@ class MoEConfig:
     zipf_s: float = 0.0             # >0: skew expert popularity p_e ~ rank^-s
     zipf_alpha: float = 0.0         # logit offset scale c_e = alpha * log p_e
     zipf_m: float = 4.0             # size of the shared input direction
+    zipf_starve: int = 0            # the n least popular experts get a further -8 logit offset (no tokens)
     seed: int = 0
 
 
@@ -52,17 +53,21 @@ class HeadConfig:
 
 # The workloads.  The Zipf offset scale of the Qwen-MoE-like layer (0.27) was
 # chosen once, by bisection on this seed's draw, so that the busiest expert gets
-# about 1500 of the 4096 tokens (the least popular gets about 80: with logit
-# noise of this size a log-rank offset cannot also empty the tail; empty
-# experts are exercised by the ragged test layers instead).
+# about 1500 of the 4096 tokens.  The 32768 (token, slot) pairs average 256 per
+# expert, so a busiest expert near 1500 leaves the least popular about 80 under a
+# log-rank offset (a Zipf(1.1) profile scaled to a head of 1500 would hold only
+# about 6400 pairs); the variant below also starves the 8 least popular experts,
+# so that its counts run from 0 to about 1500.
 TINY = MoEConfig("tiny", T=64, H=256, E=8, k=2, F=512, dup_router_rows=True, seed=0)
 TINY_HEAD = HeadConfig("tiny_head", T=64, H=256, V=4096, seed=0)
 QWEN_MOE = MoEConfig("qwen_moe_like", T=4096, H=2048, E=128, k=8, F=768,
                      zipf_s=1.1, zipf_alpha=0.27, seed=1)
+QWEN_MOE_EMPTY = MoEConfig("qwen_moe_like_empty", T=4096, H=2048, E=128, k=8, F=768,
+                           zipf_s=1.1, zipf_alpha=0.27, zipf_starve=8, seed=1)
 GLM_MOE = MoEConfig("glm_scale_moe", T=8192, H=6144, E=256, k=8, F=2048, F_shared=2048, seed=2)
 GLM_HEAD = HeadConfig("glm_scale_head", T=8192, H=6144, V=151552, seed=4)
 
-CONFIGS = {c.name: c for c in (TINY, TINY_HEAD, QWEN_MOE, GLM_MOE, GLM_HEAD)}
+CONFIGS = {c.name: c for c in (TINY, TINY_HEAD, QWEN_MOE, QWEN_MOE_EMPTY, GLM_MOE, GLM_HEAD)}
 
 
 def _gen(seed: int, device="cpu") -> torch.Generator:
@@ -81,14 +86,18 @@ def to_bf16(t: torch.Tensor) -> torch.Tensor:
     return t.to(torch.bfloat16)
 
 
-def zipf_offsets(E: int, s: float, alpha: float, gen) -> torch.Tensor:
-    """c_e = alpha * log p_e with p_e ~ rank(e)^-s over a seeded permutation of experts."""
+def zipf_offsets(E: int, s: float, alpha: float, gen, starve: int = 0) -> torch.Tensor:
+    """c_e = alpha * log p_e with p_e ~ rank(e)^-s over a seeded permutation of experts; the
+    `starve` experts of the lowest popularity get a further -8 (far below the logit noise)."""
     perm = torch.randperm(E, generator=gen)
     rank = torch.empty(E, dtype=torch.float64)
     rank[perm] = torch.arange(1, E + 1, dtype=torch.float64)
     logp = -s * torch.log(rank)
     logp = logp - torch.logsumexp(logp, 0)
-    return (alpha * logp).to(torch.float32)
+    c = alpha * logp
+    if starve > 0:
+        c = c - 8.0 * (rank > E - starve).to(torch.float64)
+    return c.to(torch.float32)
 
 
 def moe_activations(cfg: MoEConfig, T: int = None, seed_offset: int = 0):
@@ -107,7 +116,7 @@ def moe_activations(cfg: MoEConfig, T: int = None, seed_offset: int = 0):
     if cfg.zipf_s > 0:
         u = torch.randn(cfg.H, generator=gw, dtype=torch.float32)
         u = u / u.norm()
-        c = zipf_offsets(cfg.E, cfg.zipf_s, cfg.zipf_alpha, gw)
+        c = zipf_offsets(cfg.E, cfg.zipf_s, cfg.zipf_alpha, gw, cfg.zipf_starve)
         wr = wr + (c / cfg.zipf_m)[:, None] * u[None, :]
         x = x + cfg.zipf_m * u[None, :]
     x = to_bf16(x)

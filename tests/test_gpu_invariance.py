@@ -61,11 +61,12 @@ def test_invariance_small_layer():
     assert _sweep(SMALL, [1, 2, 3, 7, 31, 32, 33, 127, 128, 129, 255, 257, 1000], 2) > 0
 
 
-def test_invariance_skewed_qwen_like_layer():
+@pytest.mark.parametrize("name", ["qwen_moe_like", "qwen_moe_like_empty"])
+def test_invariance_skewed_qwen_like_layer(name):
     """The Qwen-MoE-like layer with its own Zipf-skewed traffic around the probe (up to ~1500 tokens on
-    one expert: several row chunks, M = 64 tail tiles, a handful of tokens on others): the probe's bits
-    never change, through prefill and through decode."""
-    cfg = synth.QWEN_MOE
+    one expert: several row chunks, M = 64 tail tiles, a handful of tokens on others, and in the second
+    variant experts with none): the probe's bits never change, through prefill and through decode."""
+    cfg = synth.CONFIGS[name]
     layer = _layer(cfg)
     x_all, _ = synth.moe_activations(cfg)                   # skewed traffic of the workload itself
     probe = synth.probe_tokens(cfg)

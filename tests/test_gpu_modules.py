@@ -157,7 +157,7 @@ def test_stages_small_layers_every_expert(cfg):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["qwen_moe_like", "glm_scale_moe"])
+@pytest.mark.parametrize("name", ["qwen_moe_like", "qwen_moe_like_empty", "glm_scale_moe"])
 def test_stages_full_size_tile_paths(name):
     cfg = synth.CONFIGS[name]
     x, w13, w2, ws13, ws2, res = _run_layer(cfg, "cuda")
@@ -167,8 +167,10 @@ def test_stages_full_size_tile_paths(name):
     assert "busiest" in picks and "second_row_chunk" in picks
     assert "last_tile_65_127" in picks or not any(65 <= c % 128 <= 127 for c in counts)
     assert "last_tile_m64" in picks or not any(1 <= c % 128 <= 64 and c > 128 for c in counts)
-    if name == "qwen_moe_like":
+    if name.startswith("qwen_moe_like"):
         assert counts[picks["busiest"]] > 1200      # the ~1500-row expert of the Zipf head
+    if cfg.zipf_starve:
+        assert (counts == 0).sum() == cfg.zipf_starve   # empty experts at full size
     for kind, e in picks.items():
         _check_expert_stages(e, res, w13[e], w2[e], cfg.F, f"{name} {kind} (n={counts[e]})")
     _check_combine(res, cfg.T, cfg.k, cfg.H, name)

@@ -154,7 +154,7 @@ def _sampled_oracle(x, wr, w13_dev, w2_dev, cfg, tokens, idx_gpu, L_gpu, ws13=No
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["qwen_moe_like", "glm_scale_moe"])
+@pytest.mark.parametrize("name", ["qwen_moe_like", "qwen_moe_like_empty", "glm_scale_moe"])
 def test_full_size_layer_sampled_tokens(name):
     from serve_invariant_moe_gb300 import api
     cfg = synth.CONFIGS[name]
@@ -166,6 +166,8 @@ def test_full_size_layer_sampled_tokens(name):
     torch.cuda.synchronize()
     counts = res["plan"][:cfg.E].cpu().numpy()
     assert counts.sum() == cfg.T * cfg.k
+    if cfg.zipf_starve:
+        assert (counts == 0).sum() == cfg.zipf_starve and 1200 <= counts.max() <= 1800
     # whole-batch properties: logits in bound, top-k exact on the kernel's logits, plan bit-exact
     _check_route(res, x, wr, cfg)
     g = torch.Generator().manual_seed(5)

@@ -233,13 +233,16 @@ def test_combine_is_gate_weighted_sum():
     assert np.array_equal(moe.combine(y[:, :1], np.ones((4, 1))), y[:, 0])
 
 
-def test_skewed_layer_has_busy_experts():
-    cfg = synth.QWEN_MOE
+@pytest.mark.parametrize("name", ["qwen_moe_like", "qwen_moe_like_empty"])
+def test_skewed_layer_has_busy_experts(name):
+    cfg = synth.CONFIGS[name]
     x, wr = synth.moe_activations(cfg)
     idx = moe.topk_lowest_index(moe.router_logits(moe.to_f64(x), moe.to_f64(wr)), cfg.k)
     counts = np.bincount(idx.ravel(), minlength=cfg.E)
     assert 1200 <= counts.max() <= 1800
     assert counts.sum() == cfg.T * cfg.k
+    # the starved variant: per-expert counts from 0 to about 1500
+    assert (counts == 0).sum() == cfg.zipf_starve
 
 
 def test_replay_of_own_choice_is_the_plain_forward():
