@@ -25,9 +25,9 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // The dynamic-schedule counter of a GEMM launch is left at zero for the next launch: the
-// last CTA of the grid to finish resets it.  A CTA adds itself to the done count only after
-// its producer has taken its last unit index, so no CTA touches the counter after the reset.
-// Both words start at zero (the caller zero-fills the workspace once).
+// last CTA to be done taking units resets it.  A CTA's producer thread adds the CTA to the
+// done count only after its last access to the counter, so no CTA touches the counter after
+// the reset.  Both words start at zero (the caller zero-fills the workspace once).
 __device__ __forceinline__ void sched_release(int* sched) {
   int* done = sched + 1;
   __threadfence();

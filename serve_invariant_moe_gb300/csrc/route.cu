@@ -107,34 +107,48 @@ constexpr int kSmallMaxTokens = 256;
 constexpr int kSmallMaxPairs = 4096;
 constexpr long long kSmallPermuteBytes = 512 * 1024;
 
-size_t route_small_smem(int T, int E, int k) {
-  return (2 * static_cast<size_t>(T) * k + 32 * static_cast<size_t>(E) + E + 1 + 32) * sizeof(int);
+// Shared memory of route_small_kernel: the plan's scratch (ints), then, when they fit, the
+// logits [T, E] and the rows of x [T, H] staged with one round trip each at the start.
+constexpr size_t kSmallSmemMax = 227 * 1024;
+size_t route_small_plan_smem(int T, int E, int k) {
+  return align_up((2 * static_cast<size_t>(T) * k + 32 * static_cast<size_t>(E) + E + 1 + 32) * sizeof(int), 16);
 }
 
 template <int EPL>
 __global__ void __launch_bounds__(kSmallThreads, 1)
     route_small_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx,
                        float* __restrict__ w, int32_t* __restrict__ plan, const uint4* __restrict__ x,
-                       int vec_per_row, uint4* __restrict__ xp, int do_permute) {
+                       int vec_per_row, uint4* __restrict__ xp, int do_permute, int stage_logits, int stage_x) {
   pdl_wait();
   pdl_trigger();
-  extern __shared__ int sm[];
+  extern __shared__ __align__(16) int sm[];
   const int S = T * k;
   int* s_idx = sm;                 // [S] expert of each pair
   int* s_pos = s_idx + S;          // [S] permuted row of each pair
   int* hist = s_pos + S;           // [32][E] per-warp counts, then per-warp running positions
   int* s_off = hist + 32 * E;      // [E + 1] segment starts
   int* warp_tot = s_off + E + 1;   // [32]
+  uint8_t* extra = reinterpret_cast<uint8_t*>(sm) + ((2 * S + 32 * E + E + 1 + 32) * sizeof(int) + 15) / 16 * 16;
+  float* s_logits = reinterpret_cast<float*>(extra);                                    // [T, E] if staged
+  uint4* s_x = reinterpret_cast<uint4*>(extra + (stage_logits ? ((T * E * 4 + 15) / 16) * 16 : 0));  // [T, H]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int32_t* counts = plan;
   int32_t* offsets = plan + E;
   int32_t* row_token = plan + 2 * E + 1;
   int32_t* slot_row = row_token + S;
+  // the loads that do not depend on the routing are all issued first
+  if (stage_x)
+    for (int i = tid; i < T * vec_per_row; i += kSmallThreads) s_x[i] = __ldg(x + i);
+  if (stage_logits) {
+    for (int i = tid; i < T * E; i += kSmallThreads) s_logits[i] = __ldg(logits + i);
+    __syncthreads();
+  }
+  const float* lrow0 = stage_logits ? s_logits : logits;
   // top-k and gates: warp w takes tokens w, w + 32, ...
   for (int t = warp; t < T; t += 32) {
     int e;
     float wt;
-    topk_token<EPL>(logits + static_cast<long long>(t) * E, E, k, lane, e, wt);
+    topk_token<EPL>(lrow0 + static_cast<long long>(t) * E, E, k, lane, e, wt);
     if (lane < k) {
       idx[t * k + lane] = e;
       w[t * k + lane] = wt;
@@ -203,9 +217,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   __syncthreads();
   // permute: xp[slot_row[t, j]] = x[t], one warp per token, 16-byte vectors
   for (int t = warp; t < T; t += 32) {
-    const uint4* src = x + static_cast<long long>(t) * vec_per_row;
+    const uint4* src = (stage_x ? s_x : x) + static_cast<long long>(t) * vec_per_row;
     for (int c = lane; c < vec_per_row; c += 32) {
-      const uint4 v = __ldg(src + c);
+      const uint4 v = stage_x ? src[c] : __ldg(src + c);
       for (int j = 0; j < k; ++j) xp[static_cast<long long>(s_pos[t * k + j]) * vec_per_row + c] = v;
     }
   }
@@ -407,7 +421,14 @@ namespace {
 template <int EPL>
 int route_small_launch_epl(const float* logits, int T, int E, int k, int H, const void* x, int32_t* topk_idx,
                            float* topk_w, int32_t* plan, void* xp, bool do_permute, cudaStream_t st) {
-  const size_t smem = route_small_smem(T, E, k);
+  // stage the logits and the rows of x in shared memory when they fit
+  size_t smem = route_small_plan_smem(T, E, k);
+  const size_t lbytes = align_up(static_cast<size_t>(T) * E * 4, 16);
+  const size_t xbytes = static_cast<size_t>(T) * H * 2;
+  const bool stage_logits = smem + lbytes <= kSmallSmemMax && lbytes <= 64 * 1024;
+  if (stage_logits) smem += lbytes;
+  const bool stage_x = do_permute && smem + xbytes <= kSmallSmemMax && xbytes <= 64 * 1024;
+  if (stage_x) smem += xbytes;
   static std::atomic<uint64_t> attr_set{0};
   int dev = 0;
   int rc = check_cuda(cudaGetDevice(&dev), "cudaGetDevice");
@@ -416,7 +437,7 @@ int route_small_launch_epl(const float* logits, int T, int E, int k, int H, cons
   if (bit == 0 || !(attr_set.load(std::memory_order_acquire) & bit)) {
     // the largest shared-memory request of this kernel (E = 1024, 4096 pairs) is 164 KB
     rc = check_cuda(cudaFuncSetAttribute(route_small_kernel<EPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(route_small_smem(kSmallMaxTokens, 1024, 16))),
+                                         static_cast<int>(kSmallSmemMax)),
                     "cudaFuncSetAttribute");
     if (rc) return rc;
     if (bit) attr_set.fetch_or(bit, std::memory_order_release);
@@ -424,7 +445,8 @@ int route_small_launch_epl(const float* logits, int T, int E, int k, int H, cons
   ProfScope prof("route_small", st);
   return check_cuda(launch_kernel(route_small_kernel<EPL>, dim3(1), dim3(kSmallThreads), smem, st, logits, T, E, k,
                                   topk_idx, topk_w, plan, static_cast<const uint4*>(x), H / 8,
-                                  static_cast<uint4*>(xp), do_permute ? 1 : 0),
+                                  static_cast<uint4*>(xp), do_permute ? 1 : 0, stage_logits ? 1 : 0,
+                                  stage_x ? 1 : 0),
                     "route_small_kernel");
 }
 

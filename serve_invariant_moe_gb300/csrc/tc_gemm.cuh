@@ -433,8 +433,12 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
       // the unit index is taken only when its loads are about to be issued: units
       // with neighbouring indices (the row chunks of one expert's column block,
       // which share the weight tile) then start close together and share it in L2
+      // the first unit of every CTA is its block index (no counter round trip on the way in);
+      // later ones come from the counter, offset past those
+      bool first = true;
       while (true) {
-        int u = atomicAdd(p.sched, 1);
+        int u = first ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x) + atomicAdd(p.sched, 1);
+        first = false;
         if (u >= total_units) u = -1;
         if (!mbar_wait(&qempty_bar[qi], qphase ^ 1u, wc)) break;
         s_queue[qi] = u;
@@ -489,6 +493,8 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
         }
         if (!ok) break;
       }
+      // this CTA takes no more units: once every CTA is past this point the counter is reset
+      sched_release(p.sched);
       // Let every copy this thread issued land before the CTA can exit.
       WaitCtl drain{nullptr, p.status, p.timeout_ns};
       for (int s = 0; s < STAGES; ++s)
@@ -759,7 +765,6 @@ __global__ void __launch_bounds__(GemmShape<BN, MT, EPI, STAGES>::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, S::TMEM_COLS);
   }
-  if (threadIdx.x == 0) sched_release(p.sched);
 }
 
 }  // namespace invmoe

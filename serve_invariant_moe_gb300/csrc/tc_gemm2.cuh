@@ -183,10 +183,15 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
       uint32_t qphase = 0;
       const uint32_t q_peer0 = mapa_shared(smem_u32(const_cast<int*>(s_queue)), peer);
       const uint32_t qfull_peer0 = mapa_shared(smem_u32(&qfull_bar[0]), peer);
+      // the leader's first unit is its pair index (no counter round trip on the way in); later
+      // ones come from the counter, offset past those
+      bool first = true;
       while (ok) {
         int u;
         if (rank == 0) {
-          u = atomicAdd(p.sched, 1);
+          const int pairs = static_cast<int>(gridDim.x) / 2;
+          u = first ? static_cast<int>(blockIdx.x) / 2 : pairs + atomicAdd(p.sched, 1);
+          first = false;
           if (u >= total_units) u = -1;
           if (!mbar_wait<true>(&qempty_bar[qi], qphase ^ 1u, wc)) { ok = false; break; }
           s_queue[qi] = u;
@@ -226,6 +231,9 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
         }
       }
       if (!ok) st_shared_remote_u32(peer_abort, 1u);
+      // this CTA takes no more units (the follower's last one came from the leader after the
+      // leader's last counter access): once every CTA is past this point the counter is reset
+      sched_release(p.sched);
       // The leader's full barrier counts both CTAs' copies; it may only drain its own.
       if (rank == 0) {
         WaitCtl drain{nullptr, p.status, p.timeout_ns};
@@ -519,7 +527,6 @@ __global__ void __launch_bounds__(PairShape<EPI, STAGES>::THREADS, 1)
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, S::TMEM_COLS);
   }
-  if (threadIdx.x == 0) sched_release(p.sched);
 }
 
 }  // namespace invmoe
