@@ -337,6 +337,9 @@ int moe_shared_expert(const void* x, const void* ws13, const void* ws2, int T, i
  *   - No cudaMalloc, cudaFree or other allocating call is made.
  *   - The first call on each device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
+ *     The address is kept for the life of the process: it does not survive a
+ *     cudaDeviceReset() (or anything else that replaces the device's primary
+ *     context), after which this call must not be used in that process.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents (the status word is cleared at the start of every call): calls
  *     that overlap on the GPU (other streams, other host threads) race.
@@ -503,6 +506,16 @@ int invmoe_profile_collect(char* names, float* total_ms, int* launches, int max_
  * either way.  invmoe_pdl_enable(0) launches them plainly (for timing
  * comparisons); the setting applies to calls made after it. */
 int invmoe_pdl_enable(int on);
+
+/* Engine of moe_grouped_ffn's two routed-expert GEMMs (calls made after it):
+ * 0 puts each expert's tokens on the MMA's M side in 128-row tiles (64 for a
+ * last tile of at most 64 rows); 1 puts its weight rows on the M side and its
+ * tokens on the N side (any multiple of 16 tokens, up to 320 per unit, on a CTA
+ * pair); 2 (default) takes 1 for the gate/up GEMM when the batch averages at
+ * most 32 token slots per expert (decode-sized batches) and 0 otherwise.  Both
+ * walk every element's reduction in the same order and give the same bits
+ * (tested), so the choice never changes an output. */
+int invmoe_expert_engine(int which);
 
 /* Launch a one-CTA kernel that waits on an mbarrier nothing ever completes,
  * with a wait limit of `timeout_us` microseconds (1..2000000).  The kernel

@@ -8,6 +8,7 @@
 #include "internal.h"
 #include "tc_gemm.cuh"
 #include "tc_gemm2.cuh"
+#include "tc_gemm_tok.cuh"
 
 namespace invmoe {
 
@@ -213,6 +214,43 @@ int launch_pair(const GemmCall& c, cudaStream_t st) {
                     "tc_gemm_pair_kernel launch");
 }
 
+// Token-column engine (grouped only): clusters of 2, grid = 2 x min(units, SMs / 2).
+// Weights [G * b_group_rows, K] in 64-row boxes, tokens [rows, K] in 32-row boxes.
+template <int EPI, int STAGES>
+int launch_tok(const GemmCall& c, cudaStream_t st) {
+  using S = TokShape<EPI, STAGES>;
+  if (c.G <= 0) return set_error(INVMOE_ERR_INVALID_ARG, "the token-column engine is grouped only");
+  if (c.G > S::MAX_GROUPS) return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "more than %d groups", S::MAX_GROUPS);
+  const int wb_cols = EPI == EPI_SWIGLU ? 128 : 256;
+  if (c.N % wb_cols != 0)
+    return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "N=%d is not a multiple of %d", c.N, wb_cols);
+  CUtensorMap tw, tx;
+  int rc = make_tmap(&tw, c.B, c.K, c.b_rows, 64);
+  if (rc) return rc;
+  if ((rc = make_tmap(&tx, c.A, c.K, c.a_rows, kTokBoxRows))) return rc;
+  static std::atomic<uint64_t> attr_set{0};
+  if ((rc = set_smem_attr(reinterpret_cast<const void*>(tc_gemm_tok_kernel<EPI, STAGES>), S::SMEM_BYTES, attr_set)))
+    return rc;
+  int sms = 0;
+  if ((rc = device_sm_count(&sms))) return rc;
+  GemmParams p = make_params(c, wb_cols);
+  const long long max_chunks = (c.a_rows + kTokChunk - 1) / kTokChunk + c.G;
+  const long long max_units = max_chunks * p.n_blocks;
+  if (max_units <= 0) return INVMOE_OK;
+  const long long pairs = max_units < sms / 2 ? max_units : sms / 2;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // the unit counter (p.sched) is zero here: the workspace starts zero-filled and every
+  // launch's last producer resets it (sched_release)
+  ProfScope prof(c.name ? c.name : "tc_gemm_tok", st);
+  return check_cuda(launch_kernel_ex(tc_gemm_tok_kernel<EPI, STAGES>, dim3(static_cast<unsigned>(2 * pairs)),
+                                     dim3(S::THREADS), S::SMEM_BYTES, st, attr, 1, tw, tx, p),
+                    "tc_gemm_tok_kernel launch");
+}
+
 }  // namespace
 
 int gemm_run(const GemmCall& c, cudaStream_t st) {
@@ -241,6 +279,8 @@ int gemm_run(const GemmCall& c, cudaStream_t st) {
     case GV_SWIGLU_BWD_BN256_MT2: return launch<256, 2, EPI_SWIGLU_BWD, 3>(c, st);
     case GV_F32_BN256_MT1_KGROUP: return launch<256, 1, EPI_F32, 4, true, true, true>(c, st);
     case GV_PAIR_SWIGLU_BWD: return launch_pair<EPI_SWIGLU_BWD, 6>(c, st);
+    case GV_TOK_SWIGLU: return launch_tok<EPI_SWIGLU, 5>(c, st);
+    case GV_TOK_F32: return launch_tok<EPI_F32, 5>(c, st);
   }
   return set_error(INVMOE_ERR_INVALID_ARG, "unknown GEMM variant %d", (int)c.variant);
 }

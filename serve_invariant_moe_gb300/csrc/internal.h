@@ -85,8 +85,14 @@ enum GemmVariant : int {
   GV_F32_BN256_MT2_BMN = 12, // grouped fp32-out, B MN-major: group g's B = stored rows [g*b_group_rows, +K)
   GV_SWIGLU_BWD_BN256_MT2 = 13, // grouped gate+up recompute with the SwiGLU backward epilogue
   GV_F32_BN256_MT1_KGROUP = 14, // K-grouped weight gradients: D_g = A_g^T B_g, A and B MN-major
-  GV_PAIR_SWIGLU_BWD = 15  // CTA-pair gate+up recompute with the SwiGLU backward epilogue
+  GV_PAIR_SWIGLU_BWD = 15, // CTA-pair gate+up recompute with the SwiGLU backward epilogue
+  GV_TOK_SWIGLU = 16,      // grouped gate+up, tokens on the MMA's N side (CTA pair), SwiGLU -> bf16
+  GV_TOK_F32 = 17          // grouped, tokens on the MMA's N side (CTA pair), fp32 out
 };
+
+// Which engine runs the forward grouped expert GEMMs: 0 = tokens on the MMA's M side in row
+// tiles (tc_gemm.cuh), 1 = tokens on the N side (tc_gemm_tok.cuh), 2 = chosen per call (default).
+int expert_engine();
 
 struct GemmCall {
   const char* name;    // kernel label for the profiler

@@ -29,7 +29,10 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
 // Device address of g_noalloc_scratch, looked up once per device with that
 // device current.  In host code the symbol itself is only a host-side handle,
-// so it must never be passed to a kernel directly.
+// so it must never be passed to a kernel directly.  The cached address belongs
+// to the device's primary context at the time of the lookup; a device reset
+// replaces that context (and the module holding the array), so the entry point
+// is not for use after one (the header says so).
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[64] = {};
 

@@ -1,0 +1,447 @@
+// tc_gemm_tok.cuh -- grouped expert GEMMs with the tokens on the MMA's N side (sm_103a).
+//
+// The expert GEMMs of the layer multiply each expert's token rows by that
+// expert's weights.  The row-tile engines (tc_gemm.cuh, tc_gemm2.cuh) put the
+// tokens on the MMA's M side, in tiles of 128 (or 64) rows: an expert with 269
+// tokens then runs as a 256-row unit and a 13-row unit, and the 13-row unit
+// streams the whole weight tile again for 5 % of the work.  This engine puts the
+// weights on the M side and the tokens on the N side, where the MMA takes any
+// multiple of 16 up to 256 (and a second MMA extends it to kTokChunk columns):
+//   D^T[w, t] = sum_k W[w, k] * X[t, k]       (W: an expert's weight rows, X: its tokens)
+// on a CTA pair (cta_group::2, M = 256 weight rows, 128 per CTA).  One unit is
+// (expert, token chunk of at most kTokChunk tokens, weight block); an expert
+// with up to kTokChunk tokens is one chunk, so its weights stream exactly once.
+//
+// Per-element arithmetic is that of the row-tile engines: the same bf16
+// products, K ascending in 64-wide blocks of four K = 16 steps, fp32
+// accumulation in TMEM, no split-K (swapping the operands' roles, the tile
+// position and the N of the MMA change no bit of an element; the tests compare
+// this engine's outputs with the row-tile engines' bit for bit).
+//
+//   * CTA r loads its 128 weight rows of the block (SwiGLU: gate rows
+//     [f0 + 64r, +64) and the matching up rows, so both halves of a SwiGLU pair
+//     sit in the same CTA's TMEM) and its half of the token rows: MMA 1 covers
+//     tokens [0, N1) with CTA r holding [r*N1/2, (r+1)*N1/2), MMA 2 (when the
+//     chunk has more than 256 tokens) tokens [256, 256 + N2) split the same way;
+//     token boxes are 32 rows, rows past the chunk are loaded and never stored.
+//   * TMEM: lane = weight row, column j = token j of the chunk (MMA 2 writes
+//     columns 256.. ); one accumulator of up to kTokChunk columns.
+//   * Epilogues transpose through shared memory: SwiGLU pairs the warp holding
+//     gate lanes with the warp holding the matching up lanes (named barriers),
+//     forms h = silu(g) * u in fp32 -> bf16 and stores 64-byte row segments of h;
+//     the fp32 epilogue stores 128-byte row segments of Y.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "tc_gemm.cuh"
+
+namespace invmoe {
+
+constexpr int kTokChunk = 320;     // most tokens (TMEM columns) of one unit
+constexpr int kTokBoxRows = 32;    // token rows per TMA box
+
+template <int EPI, int STAGES>
+struct TokShape {
+  static constexpr int A_BYTES = kBM * kBK * 2;                   // 16 KB: 128 weight rows x 64 K
+  static constexpr int B_ROWS = 128 + 32;                         // token rows per CTA: MMA 1 + MMA 2
+  static constexpr int B_BYTES = B_ROWS * kBK * 2;                // 20 KB
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;           // 36 KB (1 KB multiple)
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int EPI_THREADS = 32 * EPI_WARPS;
+  static constexpr int THREADS = 64 + EPI_THREADS;
+  static constexpr int QDEPTH = 4;
+  static constexpr int MAX_GROUPS = 1024;
+  static constexpr int XCHG_BYTES = EPI == EPI_SWIGLU ? 4 * 32 * 32 * 4 : 0;   // one 32 x 32 fp32 block per warp pair
+  static constexpr int OSTAGE_BYTES = EPI_WARPS * 2048;
+  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 + 1 + 2 * QDEPTH + 8);   // + the SwiGLU exchange pairs
+  static constexpr int MISC_BYTES = 16 + 4 * QDEPTH;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + XCHG_BYTES + OSTAGE_BYTES + BAR_BYTES + MISC_BYTES +
+                                    4 * (MAX_GROUPS + 1);
+  static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+  static_assert(EPI == EPI_SWIGLU || EPI == EPI_F32, "epilogue");
+};
+
+struct TokUnit {
+  int g;      // group (expert)
+  int wb;     // weight block
+  int tok0;   // first token row of the chunk (row of X and of the output)
+  int nv;     // tokens in the chunk (1 .. kTokChunk)
+};
+
+// Chunks of group g: ceil(n / kTokChunk), near-equal sizes.  Units are ordered
+// group by group, chunk-major inside a group, so consecutive units share the
+// chunk's token rows in L2.
+__device__ __forceinline__ TokUnit decode_tok_unit(int u, const GemmParams& p, const int* s_prefix) {
+  const int NB = p.n_blocks;
+  int lo = 0, hi = p.G;  // NB*s_prefix[lo] <= u < NB*s_prefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (NB * s_prefix[mid] <= u) lo = mid; else hi = mid;
+  }
+  TokUnit U;
+  U.g = lo;
+  const int nch = s_prefix[lo + 1] - s_prefix[lo];
+  const int local = u - NB * s_prefix[lo];
+  const int c = local / NB;
+  U.wb = local - c * NB;
+  const int n = __ldg(p.counts + lo);
+  const int s0 = static_cast<int>(static_cast<long long>(n) * c / nch);
+  const int s1 = static_cast<int>(static_cast<long long>(n) * (c + 1) / nch);
+  U.tok0 = __ldg(p.offsets + lo) + s0;
+  U.nv = s1 - s0;
+  return U;
+}
+
+template <int EPI, int STAGES>
+__global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
+    tc_gemm_tok_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       const GemmParams p) {
+  using S = TokShape<EPI, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint8_t* xchg = smem + STAGES * S::STAGE_BYTES;
+  uint8_t* ostage = xchg + S::XCHG_BYTES;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(ostage + S::OSTAGE_BYTES);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* accf_bar = empty_bar + STAGES;
+  uint64_t* acce_bar = accf_bar + 1;
+  uint64_t* final_bar = acce_bar + 1;
+  uint64_t* qfull_bar = final_bar + 1;
+  uint64_t* qempty_bar = qfull_bar + S::QDEPTH;
+  uint64_t* xfull_bar = qempty_bar + S::QDEPTH;      // [4] SwiGLU exchange: up block written
+  uint64_t* xempty_bar = xfull_bar + 4;              // [4] SwiGLU exchange: up block read
+  uint32_t* misc = reinterpret_cast<uint32_t*>(xempty_bar + 4);
+  uint32_t* tmem_slot = misc;
+  volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 1);
+  int* s_total = reinterpret_cast<int*>(misc + 2);
+  volatile int* s_queue = reinterpret_cast<volatile int*>(misc + 4);    // [QDEPTH]
+  int* s_prefix = reinterpret_cast<int*>(misc + 4 + S::QDEPTH);         // [G+1]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();          // 0 = leader (issues the MMAs), 1 = follower
+  const uint32_t peer = rank ^ 1u;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(accf_bar, 1);
+    mbar_init(acce_bar, 2 * S::EPI_THREADS);
+    mbar_init(final_bar, 1);
+    for (int qq = 0; qq < S::QDEPTH; ++qq) {
+      mbar_init(&qfull_bar[qq], 1);
+      // consumers of a queue slot: per CTA its epilogue threads, plus the
+      // leader's MMA thread and the follower's producer thread
+      mbar_init(&qempty_bar[qq], 2 + 2 * S::EPI_THREADS);
+    }
+    for (int x = 0; x < 4; ++x) {
+      mbar_init(&xfull_bar[x], 32);
+      mbar_init(&xempty_bar[x], 32);
+    }
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, S::TMEM_COLS);
+  // everything above touches only shared memory, TMEM and the kernel parameters; the
+  // previous kernel on the stream (which wrote this kernel's inputs) is waited for here
+  pdl_wait();
+  pdl_trigger();
+
+  // chunk prefix over groups (warp 2; G <= 1024): s_prefix[g] = sum_{g'<g} ceil(counts[g'] / kTokChunk)
+  if (warp == 2) {
+    const int per = (p.G + 31) / 32;
+    const int g0 = lane * per;
+    int local = 0;
+    for (int i = 0; i < per; ++i) {
+      const int g = g0 + i;
+      if (g < p.G) local += (__ldg(p.counts + g) + kTokChunk - 1) / kTokChunk;
+    }
+    int incl = local;
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - local;
+    for (int i = 0; i < per; ++i) {
+      const int g = g0 + i;
+      if (g < p.G) {
+        s_prefix[g] = run;
+        run += (__ldg(p.counts + g) + kTokChunk - 1) / kTokChunk;
+      }
+    }
+    if (lane == 31) {
+      s_prefix[p.G] = incl;
+      *s_total = incl;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();     // both CTAs' barriers initialised and TMEM allocated
+  tc_fence_after();
+
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_units = *s_total * p.n_blocks;
+  const int num_kb = (p.K + kBK - 1) / kBK;
+  WaitCtl wc{s_abort, p.status, p.timeout_ns};
+  const uint32_t peer_abort = mapa_shared(smem_u32(const_cast<int*>(s_abort)), peer);
+  const uint32_t qempty_leader0 = mapa_shared(smem_u32(&qempty_bar[0]), 0);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int filled_phase[STAGES];
+#pragma unroll
+      for (int s = 0; s < STAGES; ++s) filled_phase[s] = -1;
+      bool ok = true;
+      int qi = 0;
+      uint32_t qphase = 0;
+      const uint32_t q_peer0 = mapa_shared(smem_u32(const_cast<int*>(s_queue)), peer);
+      const uint32_t qfull_peer0 = mapa_shared(smem_u32(&qfull_bar[0]), peer);
+      // the leader's first unit is its pair index; later ones come from the counter, offset past those
+      bool first = true;
+      while (ok) {
+        int u;
+        if (rank == 0) {
+          const int pairs = static_cast<int>(gridDim.x) / 2;
+          u = first ? static_cast<int>(blockIdx.x) / 2 : pairs + atomicAdd(p.sched, 1);
+          first = false;
+          if (u >= total_units) u = -1;
+          if (!mbar_wait<true>(&qempty_bar[qi], qphase ^ 1u, wc)) { ok = false; break; }
+          s_queue[qi] = u;
+          mbar_arrive(&qfull_bar[qi]);
+          st_shared_remote_u32(q_peer0 + 4u * qi, static_cast<uint32_t>(u));
+          mbar_arrive_remote(qfull_peer0 + 8u * qi);
+        } else {
+          if (!mbar_wait<true>(&qfull_bar[qi], qphase, wc)) { ok = false; break; }
+          u = s_queue[qi];
+          mbar_arrive_remote(qempty_leader0 + 8u * qi);
+        }
+        if (++qi == S::QDEPTH) { qi = 0; qphase ^= 1u; }
+        if (u < 0) break;
+        const TokUnit U = decode_tok_unit(u, p, s_prefix);
+        const int nmma = (U.nv + 15) & ~15;
+        const int n1 = nmma < 256 ? nmma : 256;
+        const int r1 = n1 / 2, r2 = (nmma - n1) / 2;
+        const int nb1 = (r1 + kTokBoxRows - 1) / kTokBoxRows;
+        const uint32_t bytes = S::A_BYTES + (nb1 + (r2 > 0 ? 1 : 0)) * (kTokBoxRows * kBK * 2);
+        // this CTA's weight rows: SwiGLU gate [f0 + 64r, +64) and up [F + f0 + 64r, +64); fp32 [128 wb' + 128r, +128)
+        const int wrow0 = (EPI == EPI_SWIGLU) ? U.g * p.b_group_rows + U.wb * 128 + 64 * static_cast<int>(rank)
+                                              : U.g * p.b_group_rows + U.wb * 256 + 128 * static_cast<int>(rank);
+        const int wrow1 = (EPI == EPI_SWIGLU) ? wrow0 + p.b_up_rows : wrow0 + 64;
+        const int t1 = U.tok0 + static_cast<int>(rank) * r1;
+        const int t2 = U.tok0 + n1 + static_cast<int>(rank) * r2;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wc)) { ok = false; break; }
+          uint8_t* st = ring + stage * S::STAGE_BYTES;
+          const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * bytes);
+          tma_load_2d_pair(st, &tmW, fb, kb * kBK, wrow0);
+          tma_load_2d_pair(st + S::A_BYTES / 2, &tmW, fb, kb * kBK, wrow1);
+          uint8_t* bst = st + S::A_BYTES;
+          for (int i = 0; i < nb1; ++i)
+            tma_load_2d_pair(bst + i * (kTokBoxRows * kBK * 2), &tmX, fb, kb * kBK, t1 + i * kTokBoxRows);
+          if (r2 > 0) tma_load_2d_pair(bst + 128 * kBK * 2, &tmX, fb, kb * kBK, t2);
+          filled_phase[stage] = static_cast<int>(phase);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) st_shared_remote_u32(peer_abort, 1u);
+      // this CTA takes no more units: once every CTA is past this point the counter is reset
+      sched_release(p.sched);
+      // The leader's full barrier counts both CTAs' copies; it may only drain its own.
+      if (rank == 0) {
+        WaitCtl drain{nullptr, p.status, p.timeout_ns};
+        for (int s = 0; s < STAGES; ++s)
+          if (filled_phase[s] >= 0) mbar_wait(&full_bar[s], static_cast<uint32_t>(filled_phase[s]), drain);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader only)
+    if (lane == 0 && rank == 0) {
+      const uint64_t adesc0 = sdesc_k_sw128(smem_u32(ring));
+      const uint64_t bdesc0 = sdesc_k_sw128(smem_u32(ring + S::A_BYTES));
+      constexpr uint64_t B2_OFF = (128 * kBK * 2) >> 4;      // MMA 2's token rows start at row 128
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      int qi = 0;
+      uint32_t qphase = 0;
+      while (ok) {
+        if (!mbar_wait(&qfull_bar[qi], qphase, wc)) { ok = false; break; }
+        const int u = s_queue[qi];
+        mbar_arrive(&qempty_bar[qi]);
+        if (++qi == S::QDEPTH) { qi = 0; qphase ^= 1u; }
+        if (u < 0) break;
+        const TokUnit U = decode_tok_unit(u, p, s_prefix);
+        const int nmma = (U.nv + 15) & ~15;
+        const int n1 = nmma < 256 ? nmma : 256;
+        const int n2 = nmma - n1;
+        const uint32_t idesc1 = idesc_bf16_f32(2 * kBM, n1);
+        const uint32_t idesc2 = idesc_bf16_f32(2 * kBM, n2 > 0 ? n2 : 16);
+        if (!mbar_wait<true>(acce_bar, acc_phase ^ 1u, wc)) { ok = false; break; }
+        tc_fence_after();
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, wc)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t so = static_cast<uint64_t>((stage * S::STAGE_BYTES) >> 4);
+          const uint64_t adesc = adesc0 + so;
+          const uint64_t bdesc = bdesc0 + so;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16_pair(tmem_base, adesc + 2u * kk, bdesc + 2u * kk, idesc1, (kb | kk) != 0 ? 1u : 0u);
+          if (n2 > 0) {
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              umma_bf16_pair(tmem_base + 256u, adesc + 2u * kk, bdesc + B2_OFF + 2u * kk, idesc2,
+                             (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit_pair(&empty_bar[stage], 0x3);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit_pair(accf_bar, 0x3);
+        acc_phase ^= 1u;
+      }
+      if (!ok) st_shared_remote_u32(peer_abort, 1u);
+      umma_commit_pair(final_bar, 0x1);
+      WaitCtl drain{nullptr, p.status, p.timeout_ns};
+      mbar_wait(final_bar, 0, drain);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int ew = warp - 2;
+    const int q = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int half = ew >> 2;               // column chunks c = half, half + 2, ...
+    const uint32_t acce_leader0 = mapa_shared(smem_u32(acce_bar), 0);
+    uint8_t* stg = ostage + ew * 2048;
+    // SwiGLU: the warp on gate lanes 32q' (q' = 0, 1) and the warp on the matching up lanes
+    // 32(q' + 2) of the same half exchange the up values through `xchg`, handed over by the
+    // pair's two mbarriers (bounded waits, like every other wait of the kernel)
+    const int pair_id = (q & 1) + 2 * half;
+    float* xb = reinterpret_cast<float*>(xchg + pair_id * 4096);
+    uint32_t xphase = 0;
+    bool xok = true;
+    uint32_t acc_phase = 0;
+    int qi = 0;
+    uint32_t qphase = 0;
+    while (true) {
+      const bool okq = mbar_wait<true>(&qfull_bar[qi], qphase, wc);
+      if (!__all_sync(0xffffffffu, okq)) break;
+      const int u = s_queue[qi];
+      mbar_arrive_remote(qempty_leader0 + 8u * qi);
+      if (++qi == S::QDEPTH) { qi = 0; qphase ^= 1u; }
+      if (u < 0) break;
+      const TokUnit U = decode_tok_unit(u, p, s_prefix);
+      const bool ok = mbar_wait(accf_bar, acc_phase, wc);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      acc_phase ^= 1u;
+      tc_fence_after();
+      const int nchunk = (U.nv + 31) / 32;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      if (EPI == EPI_SWIGLU) {
+        const bool up_warp = q >= 2;
+        // h columns [f0, f0 + 32) of this warp pair
+        const int f0 = U.wb * 128 + 64 * static_cast<int>(rank) + 32 * (q & 1);
+#pragma unroll 1
+        for (int c = half; c < nchunk; c += 2) {
+          uint32_t v[32];
+          tmem_ld32(tbase + c * 32, v);
+          tmem_ld_wait();
+          tmem_reg_fence(v);
+          if (up_warp) {
+            // the gate warp has read the previous block
+            xok = __all_sync(0xffffffffu, mbar_wait(&xempty_bar[pair_id], xphase ^ 1u, wc));
+            if (!xok) break;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) xb[j * 32 + lane] = __uint_as_float(v[j]);
+            mbar_arrive(&xfull_bar[pair_id]);
+            xphase ^= 1u;
+          } else {
+            xok = __all_sync(0xffffffffu, mbar_wait(&xfull_bar[pair_id], xphase, wc));
+            if (!xok) break;
+            float uu[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) uu[j] = xb[j * 32 + lane];
+            mbar_arrive(&xempty_bar[pair_id]);
+            xphase ^= 1u;
+            // h[token j, f0 + lane] = silu(g) * u, fp32, rounded to bf16 (the row-tile engines' arithmetic)
+            __nv_bfloat16* hs = reinterpret_cast<__nv_bfloat16*>(stg);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              hs[j * 32 + lane] = __float2bfloat16_rn(__fmul_rn(silu_f32(__uint_as_float(v[j])), uu[j]));
+            __syncwarp();
+            const int rows_valid = U.nv - c * 32;
+            const int qq = lane & 3;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = 8 * i + (lane >> 2);
+              const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 64 + qq * 16);
+              if (r < rows_valid)
+                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                          static_cast<long long>(U.tok0 + c * 32 + r) * p.ldo + f0 + qq * 8) = w;
+            }
+            __syncwarp();
+          }
+        }
+      } else {
+        // fp32 Y[token, h0 + lane] for the warp's 32 rows of this CTA's 128 weight rows
+        const int h0 = U.wb * 256 + 128 * static_cast<int>(rank) + 32 * q;
+        float* ys = reinterpret_cast<float*>(stg);
+#pragma unroll 1
+        for (int c = half; c < nchunk; c += 2) {
+          uint32_t v[32];
+          tmem_ld32(tbase + c * 32, v);
+          tmem_ld_wait();
+          tmem_reg_fence(v);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) ys[j * 32 + lane] = __uint_as_float(v[16 * hh + j]);
+            __syncwarp();
+            const int rows_valid = U.nv - c * 32 - 16 * hh;
+            const int ch = lane & 7;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int r = 4 * i + (lane >> 3);
+              const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 128 + ch * 16);
+              if (r < rows_valid)
+                *reinterpret_cast<uint4*>(static_cast<float*>(p.out) +
+                                          static_cast<long long>(U.tok0 + c * 32 + 16 * hh + r) * p.ldo + h0 +
+                                          ch * 4) = w;
+            }
+            __syncwarp();
+          }
+        }
+      }
+      if (!xok) break;
+      tc_fence_before();
+      // release the accumulator on the leader (counts both CTAs' epilogue threads)
+      mbar_arrive_remote(acce_leader0);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();     // no remote arrive or multicast commit can still target this CTA
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, S::TMEM_COLS);
+  }
+}
+
+}  // namespace invmoe

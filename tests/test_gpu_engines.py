@@ -1,0 +1,84 @@
+"""The two engines of the grouped expert GEMMs give the same bits.
+
+moe_grouped_ffn runs the routed experts' two GEMMs either with each expert's tokens on the MMA's
+M side in 128-row tiles (the row-tile engine) or with its weights on the M side and its tokens on
+the N side (the token-column engine; by default it runs the gate/up GEMM of decode-sized
+batches).  Every element is the same K-ascending chain of
+bf16 products accumulated in fp32 either way ("位级一致：前沿训练的差异化关键", section
+"为什么比特级一致是一个复杂的问题": one fixed reduction order per element whatever the token
+count), so h, Y and the layer output must match bit for bit: on layers with empty experts, experts
+with one token, experts split into several token chunks, and at full size."""
+import dataclasses
+
+import pytest
+import torch
+
+from serve_invariant_moe_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _build():
+    from serve_invariant_moe_gb300 import build
+    build.build()
+
+
+def _bits(t):
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+
+
+def _both_engines(cfg, expert_device="cpu"):
+    from serve_invariant_moe_gb300 import _lib, api
+    lib = _lib.lib()
+    x, wr = synth.moe_activations(cfg)
+    w13, w2 = synth.expert_weights(cfg, expert_device)
+    ws13, ws2 = synth.shared_expert_weights(cfg, expert_device)
+    c = lambda t: None if t is None else t.cuda()   # noqa: E731
+    layer = api.MoELayer(api.MoEWeights(wr.cuda(), c(w13), c(w2), cfg.k, c(ws13), c(ws2)))
+    S = cfg.T * cfg.k
+    out = {}
+    try:
+        for eng in (0, 1):
+            assert lib.invmoe_expert_engine(eng) == 0
+            r = layer.prefill(x.cuda(), return_all=True)
+            torch.cuda.synchronize()
+            out[eng] = dict(h=r["h"][:S].clone(), y=r["y"][:S].clone(), out=r["out"].clone(),
+                            counts=r["plan"][:cfg.E].cpu())
+    finally:
+        lib.invmoe_expert_engine(2)
+    return out
+
+
+SMALL = [
+    # a heavy expert (several token chunks of the token-column engine), empty and one-token experts
+    dataclasses.replace(synth.TINY, name="heavy_and_empty", T=900, H=256, E=16, k=2, F=256,
+                        dup_router_rows=False, zipf_s=1.1, zipf_alpha=2.5, seed=61),
+    # H = 384 is not a multiple of 256: the down projection falls back to the row tiles
+    dataclasses.replace(synth.TINY, name="h384_shared", T=190, H=384, E=12, k=4, F=384, F_shared=256,
+                        dup_router_rows=False, seed=62),
+    # one token in all
+    dataclasses.replace(synth.TINY, name="one_token", T=1, H=512, E=8, k=8, F=128, dup_router_rows=False, seed=63),
+    # every expert just above and below a chunk boundary
+    dataclasses.replace(synth.TINY, name="near_chunk_edges", T=1300, H=256, E=8, k=2, F=512,
+                        dup_router_rows=False, seed=64),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+def test_engines_bit_identical_small(cfg):
+    r = _both_engines(cfg)
+    counts = r[1]["counts"]
+    if cfg.name == "heavy_and_empty":
+        assert counts.max() > 640 and (counts == 0).any()     # three or more chunks; empty experts
+    for key in ("h", "y", "out"):
+        assert torch.equal(_bits(r[0][key]), _bits(r[1][key])), f"{cfg.name}: {key} differs between the engines"
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["glm_scale_moe", "qwen_moe_like_empty"])
+def test_engines_bit_identical_full_size(name):
+    cfg = synth.CONFIGS[name]
+    r = _both_engines(cfg, expert_device="cuda")
+    for key in ("h", "y", "out"):
+        assert torch.equal(_bits(r[0][key]), _bits(r[1][key])), f"{name}: {key} differs between the engines"
