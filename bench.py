@@ -856,6 +856,8 @@ def run_profile_case(args):
     route_combine: one call of the step's layer shape (T=8192, H=6144, E=256, k=8) with F=128
               experts and no shared expert: router GEMM, top-k, dispatch, permute, expert GEMMs
               and combine launch once each.
+    tiny_decode: 20 decode calls of the tiny layer (T=64, H=256, E=8 top-2, F=512), five kernels each:
+              router GEMM, one-block routing, token-column gate/up GEMM, down GEMM, combine.
     experts:  the grouped expert GEMMs at T=1024, H=6144, E=32, k=8, F=2048 + shared (weights 2.4 GB);
               256 token-slots per expert on average, as in the T=8192, E=256 layer.
     moe_backward: one prefill, then one backward of the layer at T=512, H=6144, E=16, k=8, F=2048
@@ -895,6 +897,16 @@ def run_profile_case(args):
         hid = torch.empty((mc.T, mc.H), dtype=torch.bfloat16, device=dev)
         layer.prefill(x.to(dev), out_bf16=hid)
         binding.check_status(layer._ws)
+    elif args.profile_case == "tiny_decode":
+        # the launch-bound tiny layer (T = 64, H = 256, E = 8 top-2, F = 512): 20 decode calls
+        mc = synth.TINY
+        x, wr = synth.moe_activations(mc)
+        w13, w2 = synth.expert_weights(mc, dev)
+        layer = api.MoELayer(api.MoEWeights(wr.to(dev), w13, w2, mc.k))
+        xd = x.to(dev)
+        for _ in range(20):
+            layer.decode(xd)
+        binding.check_status(layer._decode["ws"])
     elif args.profile_case == "lm_head":
         import dataclasses
         hc = dataclasses.replace(synth.GLM_HEAD, T=2048, V=32768)
@@ -941,7 +953,7 @@ def run_profile_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile-case", choices=["lm_head", "lm_head_traffic", "route_combine", "experts",
-                                               "head_backward", "moe_backward"], default=None)
+                                               "head_backward", "moe_backward", "tiny_decode"], default=None)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
