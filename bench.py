@@ -452,7 +452,8 @@ def _summary(per_kernel, nxt, inv, ms_profiled):
            "combine": pick("combine", "ms", "frac", "frac_spec"),
            "lse_merge": pick("lse_merge", "ms", "frac", "frac_spec")}
     if nxt:
-        out["qwen_layer"] = {k: nxt.get(k) for k in ("qwen_moe_layer_ms", "qwen_experts_empty", "qwen_expert_tokens_max")}
+        out["qwen_layer"] = {k: nxt.get(k) for k in ("qwen_moe_layer_ms", "qwen_experts_empty",
+                                                     "qwen_expert_tokens_max")}
         for nm in ("qwen_expert_gemm1_swiglu", "qwen_expert_gemm2"):
             if nm in nxt:
                 out["qwen_layer"][nm] = {k: nxt[nm][k] for k in ("frac", "roofline_frac")}

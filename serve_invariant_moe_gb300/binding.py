@@ -282,8 +282,8 @@ def lm_logprob_merge(partials, tgt_logit, target, V, rollout_logp=None, beta=2.0
         raise ValueError("partials must end in a (max, sum) pair")
     dev = partials.device
     _req(target, torch.int32, "target", (T,))
-    out = dict(logp=torch.empty(T, dtype=torch.float32, device=dev), lse=torch.empty(T, dtype=torch.float32, device=dev),
-               k3=None, mask=None)
+    out = dict(logp=torch.empty(T, dtype=torch.float32, device=dev),
+               lse=torch.empty(T, dtype=torch.float32, device=dev), k3=None, mask=None)
     if rollout_logp is not None:
         _req(rollout_logp, torch.float32, "rollout_logp", (T,))
         out["k3"] = torch.empty(T, dtype=torch.float32, device=dev)

@@ -146,12 +146,21 @@ class ExpertParallelMoE:
         if self.E_local * coll.world != self.E:
             raise ValueError("the local experts times the ranks must be all experts")
 
+    def _ws(self, key, nbytes, device):
+        """A zero-filled workspace of at least nbytes, kept across calls."""
+        cache = self.__dict__.setdefault("_ws_cache", {})
+        w = cache.get(key)
+        if w is None or w.numel() < nbytes:
+            w = binding.new_workspace(nbytes, device)
+            cache[key] = w
+        return w
+
     def forward(self, x: torch.Tensor, out_bf16: Optional[torch.Tensor] = None) -> torch.Tensor:
         """x [T, H] bf16 (this rank's tokens) -> out [T, H] fp32, the bits of the one-device layer."""
         T, H = x.shape
         k, E, F = self.k, self.E, self.w13.shape[1] // 2
         Fs = 0 if self.ws13 is None else self.ws13.shape[0] // 2
-        ws = _ep_workspace(T, H, E, self.E_local, k, F, Fs, 0, x.device)
+        ws = self._ws("route", binding.workspace_size(T, H, E, k, F, Fs, 0), x.device)
         r = ep_route(self.w_router, k, x, ws)
         send_counts = ep_send_counts(r["plan"][:E], self.coll.world)
         recv_counts = self.coll.exchange_counts(send_counts)
@@ -159,7 +168,7 @@ class ExpertParallelMoE:
         recv_splits = recv_counts.sum(1).tolist()
         recv_xp = self.coll.exchange_rows(r["xp"][:T * k], send_splits, recv_splits)
         R = recv_xp.shape[0]
-        ws_e = _ep_workspace(0, H, E, self.E_local, k, F, 0, R, x.device)
+        ws_e = self._ws("experts", binding.workspace_size(R, H, self.E_local, 1, F, 0, 0), x.device)
         y_send = ep_experts(recv_xp, recv_counts, self.w13, self.w2, ws_e)
         y_back = self.coll.exchange_rows(y_send, recv_splits, send_splits)
         return ep_combine(r, y_back, x, H, E, k, self.ws13, self.ws2, ws, out_bf16)
