@@ -197,3 +197,41 @@ def test_shared_expert_alone_matches_the_fused_call():
     ys = binding.moe_shared_expert(x, ws13, ws2, ws)
     torch.cuda.synchronize()
     assert torch.equal(_bits(ys), _bits(ref["y_shared"]))
+
+
+def test_sharded_classes_over_nccl_with_one_rank():
+    """The torch.distributed path itself (ExpertParallelMoE, VocabParallelHead, Collectives) on a
+    one-rank NCCL group: every collective runs for real (with one rank it moves the data to itself),
+    and the outputs are the unsharded calls' bits."""
+    import socket
+
+    import torch.distributed as dist
+    from serve_invariant_moe_gb300 import api, sharded
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1)
+    try:
+        coll = sharded.Collectives()
+        cfg = EP_CASES[0][0]
+        x, wr, w13, w2, ws13, ws2 = _moe_inputs(cfg)
+        ref = api.MoELayer(api.MoEWeights(wr, w13, w2, cfg.k, ws13, ws2)).prefill(x)
+        ep = sharded.ExpertParallelMoE(wr, w13, w2, cfg.k, coll, ws13, ws2)
+        got = ep.forward(x)
+        torch.cuda.synchronize()
+        assert torch.equal(_bits(got), _bits(ref))
+        T, H, V = 70, 128, 3000
+        g = torch.Generator().manual_seed(91)
+        hidden = torch.randn((T, H), generator=g).to(torch.bfloat16).cuda()
+        wv = (torch.randn((V, H), generator=g) * 0.05).to(torch.bfloat16).cuda()
+        target = torch.randint(0, V, (T,), generator=g, dtype=torch.int32).cuda()
+        rollout = (torch.randn(T, generator=g) * 0.5 - math.log(V)).cuda()
+        href = api.head_logprob_kl(hidden, wv, target, rollout_logp=rollout)
+        vp = sharded.VocabParallelHead(wv, V, coll)
+        hgot = vp.forward(hidden, target, rollout)
+        torch.cuda.synchronize()
+        for key in ("logp", "lse", "k3", "mask"):
+            assert torch.equal(_bits(hgot[key]), _bits(href[key])), key
+    finally:
+        dist.destroy_process_group()
