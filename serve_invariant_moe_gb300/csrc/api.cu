@@ -176,7 +176,7 @@ using namespace invmoe;
 
 extern "C" {
 
-int invmoe_version(void) { return 120; }
+int invmoe_version(void) { return 110; }
 
 const char* invmoe_last_error(void) { return g_last_error; }
 
