@@ -512,7 +512,8 @@ int invmoe_pdl_enable(int on);
  * last tile of at most 64 rows); 1 puts its weight rows on the M side and its
  * tokens on the N side (any multiple of 16 tokens, up to 320 per unit, on a CTA
  * pair); 2 (default) takes 1 for the gate/up GEMM when the batch averages at
- * most 32 token slots per expert (decode-sized batches) and 0 otherwise.  Both
+ * least 64 token slots per expert, holds at most 64 slots in all, or H <= 1024,
+ * and 0 otherwise (and 0 for the down projection).  Both
  * walk every element's reduction in the same order and give the same bits
  * (tested), so the choice never changes an output. */
 int invmoe_expert_engine(int which);

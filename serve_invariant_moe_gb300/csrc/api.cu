@@ -313,13 +313,17 @@ int moe_grouped_ffn(const void* xp, const int32_t* plan, const void* w13, const 
   unsigned int* status = status_word(workspace);
 
   // Engines (same bits either way): tokens on the MMA's M side in row tiles, or on its N side.
-  // Measured on GB300 the row tiles are faster once experts hold more than a few dozen
-  // tokens (GLM-scale layer 2.74 vs 3.04 ms for the gate/up GEMM, 1.49 vs 1.69 ms for the down
-  // projection); for decode-sized batches the token columns spread each expert's weights over
-  // twice as many SMs and the gate/up GEMM is faster (tiny layer 15.8 vs 20.6 us), while the
-  // down projection is not (14.3 vs 12.2 us).  The automatic choice follows that.
+  // Measured on GB300 (gate/up GEMM, token columns vs row tiles): GLM-scale layer, 256 tokens per
+  // expert on average, 2.55 vs 2.72 ms (the token columns stream each expert's weights once where
+  // the row tiles stream them again for an expert's last few rows); Qwen-like layer 0.221 vs
+  // 0.226 ms; decode batches of 1 and 8 on the GLM-scale layer 84 vs 113 us and 504 vs 523 us;
+  // tiny layer (H = 256) 14.5 vs 20.4 us.  In between (1 to 16 tokens per expert on the
+  // GLM-scale layer, 32 to 512 requests) both stream every weight and the row tiles, with more
+  // weight bytes in flight per SM, are 2-7 % faster.  The down projection is faster in row
+  // tiles in every measured case but a batch of one (GLM-scale layer 1.48 vs 1.50 ms, Qwen-like
+  // 0.131 vs 0.153 ms, tiny 12.1 vs 14.1 us).  The automatic choice follows that.
   const int eng = expert_engine();
-  const bool tok1 = eng == 1 || (eng == 2 && S <= 32LL * E);
+  const bool tok1 = eng == 1 || (eng == 2 && (S >= 64LL * E || S <= 64 || H <= 1024));
   const bool tok2 = eng == 1 && H % 256 == 0;
   GemmCall g1{};
   g1.name = "expert_gemm1_swiglu";

@@ -47,6 +47,26 @@ int make_tmap(CUtensorMap* m, const void* base, long long inner, long long rows,
   return INVMOE_OK;
 }
 
+// SwiGLU weights [E][2F][K] bf16 as a rank-5 tensor (K, 16 rows, gate/up, F/16 row
+// groups, E) whose box (64, 16, 2, 4, 1) holds 4 groups of 16 gate rows each
+// followed by the matching 16 up rows.
+int make_tmap_gate_up(CUtensorMap* m, const void* base, long long K, long long F, long long E) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return set_error(INVMOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if (F % 64 != 0) return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "F=%lld is not a multiple of 64", F);
+  const cuuint64_t row = static_cast<cuuint64_t>(K) * 2;
+  cuuint64_t dims[5] = {static_cast<cuuint64_t>(K), 16, 2, static_cast<cuuint64_t>(F / 16),
+                        static_cast<cuuint64_t>(E)};
+  cuuint64_t strides[4] = {row, row * F, row * 16, row * 2 * F};
+  cuuint32_t box[5] = {static_cast<cuuint32_t>(kBK), 16, 2, 4, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(INVMOE_ERR_CUDA, "cuTensorMapEncodeTiled (gate/up) failed (%d)", (int)r);
+  return INVMOE_OK;
+}
+
 // K-grouped fp32 output of G groups, each [M rows, N columns] with row stride
 // ldo floats, group g starting at row g*M: a [G][M][N] map whose box (16
 // columns = 64 B, 32 rows) matches the epilogue's 64-byte-swizzled staging.
@@ -224,10 +244,12 @@ int launch_tok(const GemmCall& c, cudaStream_t st) {
   const int wb_cols = EPI == EPI_SWIGLU ? 128 : 256;
   if (c.N % wb_cols != 0)
     return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "N=%d is not a multiple of %d", c.N, wb_cols);
-  CUtensorMap tw, tx;
-  int rc = make_tmap(&tw, c.B, c.K, c.b_rows, 64);
+  CUtensorMap tw, tx, txb;
+  int rc = EPI == EPI_SWIGLU ? make_tmap_gate_up(&tw, c.B, c.K, c.b_up_rows, c.b_rows / c.b_group_rows)
+                             : make_tmap(&tw, c.B, c.K, c.b_rows, 128);
   if (rc) return rc;
   if ((rc = make_tmap(&tx, c.A, c.K, c.a_rows, kTokBoxRows))) return rc;
+  if ((rc = make_tmap(&txb, c.A, c.K, c.a_rows, kTokBigRows))) return rc;
   static std::atomic<uint64_t> attr_set{0};
   if ((rc = set_smem_attr(reinterpret_cast<const void*>(tc_gemm_tok_kernel<EPI, STAGES>), S::SMEM_BYTES, attr_set)))
     return rc;
@@ -247,7 +269,7 @@ int launch_tok(const GemmCall& c, cudaStream_t st) {
   // launch's last producer resets it (sched_release)
   ProfScope prof(c.name ? c.name : "tc_gemm_tok", st);
   return check_cuda(launch_kernel_ex(tc_gemm_tok_kernel<EPI, STAGES>, dim3(static_cast<unsigned>(2 * pairs)),
-                                     dim3(S::THREADS), S::SMEM_BYTES, st, attr, 1, tw, tx, p),
+                                     dim3(S::THREADS), S::SMEM_BYTES, st, attr, 1, tw, tx, txb, p),
                     "tc_gemm_tok_kernel launch");
 }
 

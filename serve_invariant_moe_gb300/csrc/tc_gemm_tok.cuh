@@ -18,18 +18,26 @@
 // position and the N of the MMA change no bit of an element; the tests compare
 // this engine's outputs with the row-tile engines' bit for bit).
 //
-//   * CTA r loads its 128 weight rows of the block (SwiGLU: gate rows
-//     [f0 + 64r, +64) and the matching up rows, so both halves of a SwiGLU pair
-//     sit in the same CTA's TMEM) and its half of the token rows: MMA 1 covers
-//     tokens [0, N1) with CTA r holding [r*N1/2, (r+1)*N1/2), MMA 2 (when the
-//     chunk has more than 256 tokens) tokens [256, 256 + N2) split the same way;
-//     token boxes are 32 rows, rows past the chunk are loaded and never stored.
-//   * TMEM: lane = weight row, column j = token j of the chunk (MMA 2 writes
-//     columns 256.. ); one accumulator of up to kTokChunk columns.
-//   * Epilogues transpose through shared memory: SwiGLU pairs the warp holding
-//     gate lanes with the warp holding the matching up lanes (named barriers),
-//     forms h = silu(g) * u in fp32 -> bf16 and stores 64-byte row segments of h;
-//     the fp32 epilogue stores 128-byte row segments of Y.
+//   * CTA r loads its 128 weight rows of the block and its half of the token
+//     rows: MMA 1 covers tokens [0, N1) with CTA r holding [r*N1/2, (r+1)*N1/2),
+//     MMA 2 (when the chunk has more than 256 tokens) tokens [256, 256 + N2)
+//     split the same way; token boxes are 32 rows, rows past the chunk are
+//     loaded and never stored.  SwiGLU: the CTA's h columns are
+//     [f0, f0 + 64), f0 = 128 * block + 64 * r, and its weight rows arrive in
+//     16-row boxes, gate and up alternating: tile rows 32i + [0, 16) are the gate
+//     rows of h columns f0 + 16i + [0, 16), tile rows 32i + [16, 32) the matching
+//     up rows, so the warp on TMEM lanes 32i holds both halves of its 16 SwiGLU
+//     pairs and exchanges them with one shuffle.
+//   * TMEM: lane = weight row, one column per token.  Consecutive units of a CTA
+//     alternate between two placements: slot 0 puts MMA 1 at column 0 and MMA 2
+//     at column 256 (columns [0, 320)), slot 1 puts MMA 1 at column 256 and
+//     MMA 2 at column 192 (columns [192, 512)).  Two consecutive units share
+//     only columns [192, 320): the epilogue drains its chunks there first and
+//     releases them, and the next unit's MMAs run while it drains the rest.
+//   * Epilogues read 32 token columns per tcgen05.ld (two loads per wait) and
+//     store through a per-warp staging tile: SwiGLU forms h = silu(g) * u in
+//     fp32 -> bf16 and stores 32-byte row segments of h; the fp32 epilogue
+//     stores 128-byte row segments of Y.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -40,8 +48,20 @@
 
 namespace invmoe {
 
+// TMA load of rank 5 into this CTA's shared memory, completion counted on an
+// mbarrier that may live in the peer CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_5d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster_addr, int c0,
+                                                 int c1, int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+
 constexpr int kTokChunk = 320;     // most tokens (TMEM columns) of one unit
-constexpr int kTokBoxRows = 32;    // token rows per TMA box
+constexpr int kTokBoxRows = 32;    // token rows per small TMA box
+constexpr int kTokBigRows = 128;   // token rows per large TMA box (a CTA's whole MMA-1 share)
 
 template <int EPI, int STAGES>
 struct TokShape {
@@ -55,11 +75,10 @@ struct TokShape {
   static constexpr int THREADS = 64 + EPI_THREADS;
   static constexpr int QDEPTH = 4;
   static constexpr int MAX_GROUPS = 1024;
-  static constexpr int XCHG_BYTES = EPI == EPI_SWIGLU ? 4 * 32 * 32 * 4 : 0;   // one 32 x 32 fp32 block per warp pair
   static constexpr int OSTAGE_BYTES = EPI_WARPS * 2048;
-  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 2 + 1 + 2 * QDEPTH + 8);   // + the SwiGLU exchange pairs
+  static constexpr int BAR_BYTES = 8 * (2 * STAGES + 6 + 1 + 2 * QDEPTH);
   static constexpr int MISC_BYTES = 16 + 4 * QDEPTH;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + XCHG_BYTES + OSTAGE_BYTES + BAR_BYTES + MISC_BYTES +
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + OSTAGE_BYTES + BAR_BYTES + MISC_BYTES +
                                     4 * (MAX_GROUPS + 1);
   static_assert(STAGE_BYTES % 1024 == 0, "stage alignment");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
@@ -97,26 +116,46 @@ __device__ __forceinline__ TokUnit decode_tok_unit(int u, const GemmParams& p, c
   return U;
 }
 
+// TMEM placement of a unit in column slot `slot` (0 or 1; consecutive units of a
+// CTA alternate): MMA 1 (tokens [0, 256)) and MMA 2 (tokens [256, kTokChunk)).
+__device__ __forceinline__ uint32_t tok_col1(int slot) { return slot ? 256u : 0u; }
+__device__ __forceinline__ uint32_t tok_col2(int slot) { return slot ? 192u : 256u; }
+// TMEM column of the 32-token chunk c (tokens [32c, 32c + 32) of the unit)
+__device__ __forceinline__ uint32_t tok_chunk_col(int slot, int c) {
+  return c < 8 ? tok_col1(slot) + 32u * c : tok_col2(slot) + 32u * (c - 8);
+}
+// The epilogue drains a unit's nchunk chunks in two phases: phase 0 the chunks
+// whose columns lie in [192, 320) (the only columns the next unit, in the other
+// slot, may write), phase 1 the rest.  Length of a phase and its k-th chunk:
+__device__ __forceinline__ int tok_phase_len(int slot, int ph, int nchunk) {
+  if (slot == 0) return ph == 0 ? max(0, nchunk - 6) : min(nchunk, 6);
+  return ph == 0 ? min(nchunk, 2) + max(0, nchunk - 8) : max(0, min(nchunk, 8) - 2);
+}
+__device__ __forceinline__ int tok_phase_chunk(int slot, int ph, int nchunk, int k) {
+  if (slot == 0) return ph == 0 ? 6 + k : k;
+  if (ph == 1) return 2 + k;
+  const int a = min(nchunk, 2);
+  return k < a ? k : 8 + (k - a);
+}
+
 template <int EPI, int STAGES>
 __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
     tc_gemm_tok_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                       const GemmParams p) {
+                       const __grid_constant__ CUtensorMap tmXb, const GemmParams p) {
   using S = TokShape<EPI, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint8_t* xchg = smem + STAGES * S::STAGE_BYTES;
-  uint8_t* ostage = xchg + S::XCHG_BYTES;
+  uint8_t* ostage = smem + STAGES * S::STAGE_BYTES;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(ostage + S::OSTAGE_BYTES);
   uint64_t* empty_bar = full_bar + STAGES;
-  uint64_t* accf_bar = empty_bar + STAGES;
-  uint64_t* acce_bar = accf_bar + 1;
-  uint64_t* final_bar = acce_bar + 1;
+  uint64_t* accf_bar = empty_bar + STAGES;           // [2] per column slot: the unit's MMAs are done
+  uint64_t* accmid_bar = accf_bar + 2;               // [2] columns [192, 320) of the slot drained
+  uint64_t* accall_bar = accmid_bar + 2;             // [2] every column of the slot drained
+  uint64_t* final_bar = accall_bar + 2;
   uint64_t* qfull_bar = final_bar + 1;
   uint64_t* qempty_bar = qfull_bar + S::QDEPTH;
-  uint64_t* xfull_bar = qempty_bar + S::QDEPTH;      // [4] SwiGLU exchange: up block written
-  uint64_t* xempty_bar = xfull_bar + 4;              // [4] SwiGLU exchange: up block read
-  uint32_t* misc = reinterpret_cast<uint32_t*>(xempty_bar + 4);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(qempty_bar + S::QDEPTH);
   uint32_t* tmem_slot = misc;
   volatile int* s_abort = reinterpret_cast<volatile int*>(misc + 1);
   int* s_total = reinterpret_cast<int*>(misc + 2);
@@ -133,8 +172,11 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(accf_bar, 1);
-    mbar_init(acce_bar, 2 * S::EPI_THREADS);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&accf_bar[x], 1);
+      mbar_init(&accmid_bar[x], 2 * S::EPI_THREADS);
+      mbar_init(&accall_bar[x], 2 * S::EPI_THREADS);
+    }
     mbar_init(final_bar, 1);
     for (int qq = 0; qq < S::QDEPTH; ++qq) {
       mbar_init(&qfull_bar[qq], 1);
@@ -142,16 +184,13 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
       // leader's MMA thread and the follower's producer thread
       mbar_init(&qempty_bar[qq], 2 + 2 * S::EPI_THREADS);
     }
-    for (int x = 0; x < 4; ++x) {
-      mbar_init(&xfull_bar[x], 32);
-      mbar_init(&xempty_bar[x], 32);
-    }
     *s_abort = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmXb);
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, S::TMEM_COLS);
   // everything above touches only shared memory, TMEM and the kernel parameters; the
@@ -236,12 +275,16 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
         const int nmma = (U.nv + 15) & ~15;
         const int n1 = nmma < 256 ? nmma : 256;
         const int r1 = n1 / 2, r2 = (nmma - n1) / 2;
+        // MMA 1's token rows of this CTA: up to two small boxes, else one large box (rows past
+        // the chunk are read from L2 and never stored); MMA 2's: one small box
         const int nb1 = (r1 + kTokBoxRows - 1) / kTokBoxRows;
-        const uint32_t bytes = S::A_BYTES + (nb1 + (r2 > 0 ? 1 : 0)) * (kTokBoxRows * kBK * 2);
-        // this CTA's weight rows: SwiGLU gate [f0 + 64r, +64) and up [F + f0 + 64r, +64); fp32 [128 wb' + 128r, +128)
-        const int wrow0 = (EPI == EPI_SWIGLU) ? U.g * p.b_group_rows + U.wb * 128 + 64 * static_cast<int>(rank)
-                                              : U.g * p.b_group_rows + U.wb * 256 + 128 * static_cast<int>(rank);
-        const int wrow1 = (EPI == EPI_SWIGLU) ? wrow0 + p.b_up_rows : wrow0 + 64;
+        const bool big1 = nb1 > 2;
+        const uint32_t bytes = S::A_BYTES + (big1 ? kTokBigRows : nb1 * kTokBoxRows) * (kBK * 2) +
+                               (r2 > 0 ? kTokBoxRows * kBK * 2 : 0);
+        // this CTA's weight rows: SwiGLU h columns [f0, f0 + 64), f0 = 128 wb + 64r (gate rows f0.., up
+        // rows F + f0..); fp32 rows [256 wb + 128r, +128)
+        const int f0 = U.wb * 128 + 64 * static_cast<int>(rank);
+        const int wrow = U.g * p.b_group_rows + U.wb * 256 + 128 * static_cast<int>(rank);
         const int t1 = U.tok0 + static_cast<int>(rank) * r1;
         const int t2 = U.tok0 + n1 + static_cast<int>(rank) * r2;
         for (int kb = 0; kb < num_kb; ++kb) {
@@ -249,11 +292,20 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
           uint8_t* st = ring + stage * S::STAGE_BYTES;
           const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * bytes);
-          tma_load_2d_pair(st, &tmW, fb, kb * kBK, wrow0);
-          tma_load_2d_pair(st + S::A_BYTES / 2, &tmW, fb, kb * kBK, wrow1);
+          if (EPI == EPI_SWIGLU) {
+            // one box of 4 row groups x (16 gate rows, the matching 16 up rows): tile rows
+            // 32i + [0, 16) are gate rows f0 + 16i + [0, 16), 32i + [16, 32) the up rows
+            tma_load_5d_pair(st, &tmW, fb, kb * kBK, 0, 0, f0 / 16, U.g);
+          } else {
+            tma_load_2d_pair(st, &tmW, fb, kb * kBK, wrow);
+          }
           uint8_t* bst = st + S::A_BYTES;
-          for (int i = 0; i < nb1; ++i)
-            tma_load_2d_pair(bst + i * (kTokBoxRows * kBK * 2), &tmX, fb, kb * kBK, t1 + i * kTokBoxRows);
+          if (big1) {
+            tma_load_2d_pair(bst, &tmXb, fb, kb * kBK, t1);
+          } else {
+            for (int i = 0; i < nb1; ++i)
+              tma_load_2d_pair(bst + i * (kTokBoxRows * kBK * 2), &tmX, fb, kb * kBK, t1 + i * kTokBoxRows);
+          }
           if (r2 > 0) tma_load_2d_pair(bst + 128 * kBK * 2, &tmX, fb, kb * kBK, t2);
           filled_phase[stage] = static_cast<int>(phase);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -277,7 +329,7 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
       constexpr uint64_t B2_OFF = (128 * kBK * 2) >> 4;      // MMA 2's token rows start at row 128
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t acc_phase = 0;
+      uint32_t nunit = 0;        // units this pair has run: column slot nunit & 1
       bool ok = true;
       int qi = 0;
       uint32_t qphase = 0;
@@ -293,8 +345,17 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
         const int n2 = nmma - n1;
         const uint32_t idesc1 = idesc_bf16_f32(2 * kBM, n1);
         const uint32_t idesc2 = idesc_bf16_f32(2 * kBM, n2 > 0 ? n2 : 16);
-        if (!mbar_wait<true>(acce_bar, acc_phase ^ 1u, wc)) { ok = false; break; }
+        const int slot = static_cast<int>(nunit & 1u);
+        // the slot's previous unit fully drained; the previous unit (other slot) drained its
+        // columns in [192, 320), the only ones the two slots share
+        if (!mbar_wait<true>(&accall_bar[slot], ((nunit >> 1) & 1u) ^ 1u, wc)) { ok = false; break; }
+        if (nunit > 0 && !mbar_wait<true>(&accmid_bar[slot ^ 1], ((nunit - 1) >> 1) & 1u, wc)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
+        const uint32_t d1 = tmem_base + tok_col1(slot);
+        const uint32_t d2 = tmem_base + tok_col2(slot);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, wc)) { ok = false; break; }
           tc_fence_after();
@@ -303,19 +364,18 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
           const uint64_t bdesc = bdesc0 + so;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_bf16_pair(tmem_base, adesc + 2u * kk, bdesc + 2u * kk, idesc1, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16_pair(d1, adesc + 2u * kk, bdesc + 2u * kk, idesc1, (kb | kk) != 0 ? 1u : 0u);
           if (n2 > 0) {
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
-              umma_bf16_pair(tmem_base + 256u, adesc + 2u * kk, bdesc + B2_OFF + 2u * kk, idesc2,
-                             (kb | kk) != 0 ? 1u : 0u);
+              umma_bf16_pair(d2, adesc + 2u * kk, bdesc + B2_OFF + 2u * kk, idesc2, (kb | kk) != 0 ? 1u : 0u);
           }
           umma_commit_pair(&empty_bar[stage], 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        umma_commit_pair(accf_bar, 0x3);
-        acc_phase ^= 1u;
+        umma_commit_pair(&accf_bar[slot], 0x3);
+        ++nunit;
       }
       if (!ok) st_shared_remote_u32(peer_abort, 1u);
       umma_commit_pair(final_bar, 0x1);
@@ -326,17 +386,12 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int ew = warp - 2;
     const int q = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int half = ew >> 2;               // column chunks c = half, half + 2, ...
-    const uint32_t acce_leader0 = mapa_shared(smem_u32(acce_bar), 0);
+    const int half = ew >> 2;               // every other chunk of each phase, starting at `half`
+    const uint32_t accmid_leader0 = mapa_shared(smem_u32(accmid_bar), 0);
+    const uint32_t accall_leader0 = mapa_shared(smem_u32(accall_bar), 0);
     uint8_t* stg = ostage + ew * 2048;
-    // SwiGLU: the warp on gate lanes 32q' (q' = 0, 1) and the warp on the matching up lanes
-    // 32(q' + 2) of the same half exchange the up values through `xchg`, handed over by the
-    // pair's two mbarriers (bounded waits, like every other wait of the kernel)
-    const int pair_id = (q & 1) + 2 * half;
-    float* xb = reinterpret_cast<float*>(xchg + pair_id * 4096);
-    uint32_t xphase = 0;
-    bool xok = true;
-    uint32_t acc_phase = 0;
+    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    uint32_t nunit = 0;
     int qi = 0;
     uint32_t qphase = 0;
     while (true) {
@@ -347,79 +402,60 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
       if (++qi == S::QDEPTH) { qi = 0; qphase ^= 1u; }
       if (u < 0) break;
       const TokUnit U = decode_tok_unit(u, p, s_prefix);
-      const bool ok = mbar_wait(accf_bar, acc_phase, wc);
+      const int slot = static_cast<int>(nunit & 1u);
+      const bool ok = mbar_wait(&accf_bar[slot], (nunit >> 1) & 1u, wc);
       if (!__all_sync(0xffffffffu, ok)) break;
-      acc_phase ^= 1u;
+      ++nunit;
       tc_fence_after();
       const int nchunk = (U.nv + 31) / 32;
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-      if (EPI == EPI_SWIGLU) {
-        const bool up_warp = q >= 2;
-        // h columns [f0, f0 + 32) of this warp pair
-        const int f0 = U.wb * 128 + 64 * static_cast<int>(rank) + 32 * (q & 1);
-#pragma unroll 1
-        for (int c = half; c < nchunk; c += 2) {
-          uint32_t v[32];
-          tmem_ld32(tbase + c * 32, v);
-          tmem_ld_wait();
-          tmem_reg_fence(v);
-          if (up_warp) {
-            // the gate warp has read the previous block
-            xok = __all_sync(0xffffffffu, mbar_wait(&xempty_bar[pair_id], xphase ^ 1u, wc));
-            if (!xok) break;
+
+      // one 32-token chunk c held in v (this thread's lane, 32 consecutive columns)
+      auto store_chunk = [&](int c, const uint32_t (&v)[32]) {
+        const int rows_valid = U.nv - c * 32;
+        if (EPI == EPI_SWIGLU) {
+          // lanes 0-15 hold gate rows, lanes 16-31 the matching up rows of h columns
+          // [fq, fq + 16): a lane computes h for its column and 16 of the 32 tokens
+          // (lanes 0-15 tokens 0-15, lanes 16-31 tokens 16-31) after one exchange
+          const int fq = U.wb * 128 + 64 * static_cast<int>(rank) + 16 * q;
+          const bool upper = lane >= 16;
+          const int tb = upper ? 16 : 0;
+          __nv_bfloat16* hs = reinterpret_cast<__nv_bfloat16*>(stg);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) xb[j * 32 + lane] = __uint_as_float(v[j]);
-            mbar_arrive(&xfull_bar[pair_id]);
-            xphase ^= 1u;
-          } else {
-            xok = __all_sync(0xffffffffu, mbar_wait(&xfull_bar[pair_id], xphase, wc));
-            if (!xok) break;
-            float uu[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) uu[j] = xb[j * 32 + lane];
-            mbar_arrive(&xempty_bar[pair_id]);
-            xphase ^= 1u;
-            // h[token j, f0 + lane] = silu(g) * u, fp32, rounded to bf16 (the row-tile engines' arithmetic)
-            __nv_bfloat16* hs = reinterpret_cast<__nv_bfloat16*>(stg);
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              hs[j * 32 + lane] = __float2bfloat16_rn(__fmul_rn(silu_f32(__uint_as_float(v[j])), uu[j]));
-            __syncwarp();
-            const int rows_valid = U.nv - c * 32;
-            const int qq = lane & 3;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int r = 8 * i + (lane >> 2);
-              const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 64 + qq * 16);
-              if (r < rows_valid)
-                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                          static_cast<long long>(U.tok0 + c * 32 + r) * p.ldo + f0 + qq * 8) = w;
-            }
-            __syncwarp();
+          for (int j = 0; j < 16; ++j) {
+            const uint32_t send = upper ? v[j] : v[16 + j];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, 16);
+            const float g = __uint_as_float(upper ? recv : v[j]);
+            const float uu = __uint_as_float(upper ? v[16 + j] : recv);
+            // staging row r (token) at byte 32r, rows 16-31 one row further on (no bank conflict)
+            hs[(tb + j) * 16 + tb + (lane & 15)] = __float2bfloat16_rn(__fmul_rn(silu_f32(g), uu));
           }
-        }
-      } else {
-        // fp32 Y[token, h0 + lane] for the warp's 32 rows of this CTA's 128 weight rows
-        const int h0 = U.wb * 256 + 128 * static_cast<int>(rank) + 32 * q;
-        float* ys = reinterpret_cast<float*>(stg);
-#pragma unroll 1
-        for (int c = half; c < nchunk; c += 2) {
-          uint32_t v[32];
-          tmem_ld32(tbase + c * 32, v);
-          tmem_ld_wait();
-          tmem_reg_fence(v);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int m = lane + 32 * i;
+            const int r = m >> 1;
+            const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 32 + (r >= 16 ? 32 : 0) + (m & 1) * 16);
+            if (r < rows_valid)
+              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                        static_cast<long long>(U.tok0 + c * 32 + r) * p.ldo + fq + (m & 1) * 8) = w;
+          }
+          __syncwarp();
+        } else {
+          // fp32 Y[token, h0 + lane] for the warp's 32 rows of this CTA's 128 weight rows
+          const int h0 = U.wb * 256 + 128 * static_cast<int>(rank) + 32 * q;
+          float* ys = reinterpret_cast<float*>(stg);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) ys[j * 32 + lane] = __uint_as_float(v[16 * hh + j]);
             __syncwarp();
-            const int rows_valid = U.nv - c * 32 - 16 * hh;
+            const int rv = rows_valid - 16 * hh;
             const int ch = lane & 7;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int r = 4 * i + (lane >> 3);
               const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 128 + ch * 16);
-              if (r < rows_valid)
+              if (r < rv)
                 *reinterpret_cast<uint4*>(static_cast<float*>(p.out) +
                                           static_cast<long long>(U.tok0 + c * 32 + 16 * hh + r) * p.ldo + h0 +
                                           ch * 4) = w;
@@ -427,11 +463,31 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
             __syncwarp();
           }
         }
+      };
+
+#pragma unroll 1
+      for (int ph = 0; ph < 2; ++ph) {
+        const int len = tok_phase_len(slot, ph, nchunk);
+        // two chunks per TMEM round trip: k and k + 2 (the second load repeats the first
+        // when k + 2 is past the phase, and is not stored)
+#pragma unroll 1
+        for (int k = half; k < len; k += 4) {
+          const int ca = tok_phase_chunk(slot, ph, nchunk, k);
+          const bool two = k + 2 < len;
+          const int cb = two ? tok_phase_chunk(slot, ph, nchunk, k + 2) : ca;
+          uint32_t va[32], vb[32];
+          tmem_ld32(tbase + tok_chunk_col(slot, ca), va);
+          tmem_ld32(tbase + tok_chunk_col(slot, cb), vb);
+          tmem_ld_wait();
+          tmem_reg_fence(va);
+          tmem_reg_fence(vb);
+          store_chunk(ca, va);
+          if (two) store_chunk(cb, vb);
+        }
+        tc_fence_before();
+        // phase 0: the next unit (other slot) may write columns [192, 320); phase 1: the slot is free
+        mbar_arrive_remote((ph == 0 ? accmid_leader0 : accall_leader0) + 8u * slot);
       }
-      if (!xok) break;
-      tc_fence_before();
-      // release the accumulator on the leader (counts both CTAs' epilogue threads)
-      mbar_arrive_remote(acce_leader0);
     }
   }
 

@@ -2,8 +2,8 @@
 
 moe_grouped_ffn runs the routed experts' two GEMMs either with each expert's tokens on the MMA's
 M side in 128-row tiles (the row-tile engine) or with its weights on the M side and its tokens on
-the N side (the token-column engine; by default it runs the gate/up GEMM of decode-sized
-batches).  Every element is the same K-ascending chain of
+the N side (the token-column engine; by default it runs the gate/up GEMM of prefill-sized
+batches, of batches of at most 64 token slots and of layers with H <= 1024).  Every element is the same K-ascending chain of
 bf16 products accumulated in fp32 either way ("位级一致：前沿训练的差异化关键", section
 "为什么比特级一致是一个复杂的问题": one fixed reduction order per element whatever the token
 count), so h, Y and the layer output must match bit for bit: on layers with empty experts, experts
