@@ -861,6 +861,8 @@ def run_profile_case(args):
               router GEMM, one-block routing, token-column gate/up GEMM, down GEMM, combine.
     experts:  the grouped expert GEMMs at T=1024, H=6144, E=32, k=8, F=2048 + shared (weights 2.4 GB);
               256 token-slots per expert on average, as in the T=8192, E=256 layer.
+    qwen_layer: three prefill calls of the Qwen-MoE-like layer with its starved experts (T=4096,
+              H=2048, E=128, k=8, F=768; expert weights 1.2 GB, counts 0..1518).
     moe_backward: one prefill, then one backward of the layer at T=512, H=6144, E=16, k=8, F=2048
               (no shared expert; 256 token-slots per expert on average; dW13 1.6 GB, dW2 0.8 GB fp32).
               Single-CTA engine launches in order: router, expert GEMM 1, expert GEMM 2, then
@@ -908,6 +910,14 @@ def run_profile_case(args):
         for _ in range(20):
             layer.decode(xd)
         binding.check_status(layer._decode["ws"])
+    elif args.profile_case == "qwen_layer":
+        mc = synth.QWEN_MOE_EMPTY
+        x, wr = synth.moe_activations(mc)
+        w13, w2 = synth.expert_weights(mc, dev)
+        layer = api.MoELayer(api.MoEWeights(wr.to(dev), w13, w2, mc.k))
+        for _ in range(3):
+            layer.prefill(x.to(dev))
+        binding.check_status(layer._ws)
     elif args.profile_case == "lm_head":
         import dataclasses
         hc = dataclasses.replace(synth.GLM_HEAD, T=2048, V=32768)
@@ -954,7 +964,7 @@ def run_profile_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile-case", choices=["lm_head", "lm_head_traffic", "route_combine", "experts",
-                                               "head_backward", "moe_backward", "tiny_decode"], default=None)
+                                               "head_backward", "moe_backward", "tiny_decode", "qwen_layer"], default=None)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)

@@ -33,7 +33,9 @@
 //     at column 256 (columns [0, 320)), slot 1 puts MMA 1 at column 256 and
 //     MMA 2 at column 192 (columns [192, 512)).  Two consecutive units share
 //     only columns [192, 320): the epilogue drains its chunks there first and
-//     releases them, and the next unit's MMAs run while it drains the rest.
+//     releases them, and the next unit's MMAs run while it drains the rest;
+//     when neither unit has a second MMA they share no column at all and the
+//     next unit's MMAs do not wait.
 //   * Epilogues read 32 token columns per tcgen05.ld (two loads per wait) and
 //     store through a per-warp staging tile: SwiGLU forms h = silu(g) * u in
 //     fp32 -> bf16 and stores 32-byte row segments of h; the fp32 epilogue
@@ -330,6 +332,7 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t nunit = 0;        // units this pair has run: column slot nunit & 1
+      int prev_n2 = 0;           // width of the previous unit's second MMA (0: none)
       bool ok = true;
       int qi = 0;
       uint32_t qphase = 0;
@@ -347,12 +350,16 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
         const uint32_t idesc2 = idesc_bf16_f32(2 * kBM, n2 > 0 ? n2 : 16);
         const int slot = static_cast<int>(nunit & 1u);
         // the slot's previous unit fully drained; the previous unit (other slot) drained its
-        // columns in [192, 320), the only ones the two slots share
+        // columns in [192, 320), the only ones the two slots share.  When neither unit has a
+        // second MMA, the previous one's columns (all its chunks, read in either phase) and this
+        // one's are disjoint ([0, 256) and [256, 512)), and the MMAs start at once.
         if (!mbar_wait<true>(&accall_bar[slot], ((nunit >> 1) & 1u) ^ 1u, wc)) { ok = false; break; }
-        if (nunit > 0 && !mbar_wait<true>(&accmid_bar[slot ^ 1], ((nunit - 1) >> 1) & 1u, wc)) {
+        if (nunit > 0 && (n2 > 0 || prev_n2 > 0) &&
+            !mbar_wait<true>(&accmid_bar[slot ^ 1], ((nunit - 1) >> 1) & 1u, wc)) {
           ok = false;
           break;
         }
+        prev_n2 = n2;
         tc_fence_after();
         const uint32_t d1 = tmem_base + tok_col1(slot);
         const uint32_t d2 = tmem_base + tok_col2(slot);
