@@ -176,15 +176,15 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&accf_bar[x], 1);
-      mbar_init(&accmid_bar[x], 2 * S::EPI_THREADS);
-      mbar_init(&accall_bar[x], 2 * S::EPI_THREADS);
+      mbar_init(&accmid_bar[x], 2 * S::EPI_WARPS);    // one arrive per epilogue warp of each CTA
+      mbar_init(&accall_bar[x], 2 * S::EPI_WARPS);
     }
     mbar_init(final_bar, 1);
     for (int qq = 0; qq < S::QDEPTH; ++qq) {
       mbar_init(&qfull_bar[qq], 1);
-      // consumers of a queue slot: per CTA its epilogue threads, plus the
+      // consumers of a queue slot: per CTA its epilogue warps, plus the
       // leader's MMA thread and the follower's producer thread
-      mbar_init(&qempty_bar[qq], 2 + 2 * S::EPI_THREADS);
+      mbar_init(&qempty_bar[qq], 2 + 2 * S::EPI_WARPS);
     }
     *s_abort = 0;
     fence_barrier_init();
@@ -405,7 +405,8 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
       const bool okq = mbar_wait<true>(&qfull_bar[qi], qphase, wc);
       if (!__all_sync(0xffffffffu, okq)) break;
       const int u = s_queue[qi];
-      mbar_arrive_remote(qempty_leader0 + 8u * qi);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(qempty_leader0 + 8u * qi);
       if (++qi == S::QDEPTH) { qi = 0; qphase ^= 1u; }
       if (u < 0) break;
       const TokUnit U = decode_tok_unit(u, p, s_prefix);
@@ -472,9 +473,21 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
         }
       };
 
+      // A warp releases a phase's columns (one arrive per warp on the leader: phase 0 lets the
+      // next unit, in the other slot, write columns [192, 320); phase 1 frees the slot) as soon
+      // as its last TMEM loads of the phase have completed, before it forms and stores them.
+      const uint32_t rel0 = accmid_leader0 + 8u * slot;
+      const uint32_t rel1 = accall_leader0 + 8u * slot;
+      auto release = [&](uint32_t bar) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(bar);
+      };
 #pragma unroll 1
       for (int ph = 0; ph < 2; ++ph) {
         const int len = tok_phase_len(slot, ph, nchunk);
+        const uint32_t rel = ph == 0 ? rel0 : rel1;
+        if (half >= len) release(rel);
         // two chunks per TMEM round trip: k and k + 2 (the second load repeats the first
         // when k + 2 is past the phase, and is not stored)
 #pragma unroll 1
@@ -488,12 +501,10 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
           tmem_ld_wait();
           tmem_reg_fence(va);
           tmem_reg_fence(vb);
+          if (k + 4 >= len) release(rel);
           store_chunk(ca, va);
           if (two) store_chunk(cb, vb);
         }
-        tc_fence_before();
-        // phase 0: the next unit (other slot) may write columns [192, 320); phase 1: the slot is free
-        mbar_arrive_remote((ph == 0 ? accmid_leader0 : accall_leader0) + 8u * slot);
       }
     }
   }
