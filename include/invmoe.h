@@ -182,11 +182,19 @@ int moe_combine(const float* y, const float* topk_w, const int32_t* plan, const 
  * moe_layer_forward -- the whole layer in one call
  *
  * moe_route_topk, then moe_grouped_ffn (with the shared expert on x when
- * F_shared > 0), then moe_combine, on one stream: exactly those three calls and
- * their kernels (so the same bits), for callers that serve one small batch at a
- * time and want one host call per layer.  Arguments, layouts and errors as the
- * three calls; ws13, ws2 and y_shared are ignored when F_shared == 0; the
- * workspace is invmoe_workspace_size(T, H, E, k, F, F_shared, 0) bytes.
+ * F_shared > 0), then moe_combine: exactly those three calls' kernels (so the
+ * same bits), for callers that serve one small batch at a time and want one
+ * host call per layer.  Arguments, layouts and errors as the three calls;
+ * ws13, ws2 and y_shared are ignored when F_shared == 0; the workspace is
+ * invmoe_workspace_size(T, H, E, k, F, F_shared, 0) bytes.
+ * With a shared expert, at most 1024 tokens (see invmoe_shared_overlap) and a
+ * workspace of that size, the shared expert's two GEMMs run on a stream of the
+ * library's own (one per device, created on the first such call that is not
+ * made during a graph capture) while the routing and the routed experts run on
+ * `stream`; `stream` waits for that stream (an event) before the combine, so on
+ * return the call is ordered on `stream` as if it had run there alone, and a
+ * graph captured from `stream` holds both branches.  Such calls from several
+ * host threads are serialised by a lock around their launches.
  * ------------------------------------------------------------------------- */
 int moe_layer_forward(const void* x, const void* w_router, const void* w13, const void* w2,
                       const void* ws13, const void* ws2, int T, int H, int E, int k, int F, int F_shared,
@@ -506,6 +514,12 @@ int invmoe_profile_collect(char* names, float* total_ms, int* launches, int max_
  * either way.  invmoe_pdl_enable(0) launches them plainly (for timing
  * comparisons); the setting applies to calls made after it. */
 int invmoe_pdl_enable(int on);
+
+/* Where moe_layer_forward runs the shared expert (calls made after it): 0 on
+ * `stream` after the routed experts, 1 on the library's side stream beside the
+ * routing and the routed experts, 2 (default) the side stream for batches of at
+ * most 1024 tokens.  The kernels and their results are the same either way. */
+int invmoe_shared_overlap(int mode);
 
 /* Engine of moe_grouped_ffn's two routed-expert GEMMs (calls made after it):
  * 0 puts each expert's tokens on the MMA's M side in 128-row tiles (64 for a

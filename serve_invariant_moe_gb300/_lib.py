@@ -50,6 +50,7 @@ PROTOTYPES = {
     "invmoe_profile_enable": (_i, [_i]),
     "invmoe_pdl_enable": (_i, [_i]),
     "invmoe_expert_engine": (_i, [_i]),
+    "invmoe_shared_overlap": (_i, [_i]),
     "invmoe_profile_collect": (_i, [ctypes.c_char_p, ctypes.POINTER(_f), ctypes.POINTER(_i), _i]),
 }
 

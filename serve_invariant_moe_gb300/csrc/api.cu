@@ -73,6 +73,49 @@ int check_cuda(cudaError_t e, const char* what) {
 namespace {
 std::atomic<bool> g_pdl_on{true};
 std::atomic<int> g_expert_engine{2};
+std::atomic<int> g_shared_overlap{2};
+
+// A stream of the library's own per device, and two events, on which moe_layer_forward runs
+// the shared expert beside the routing and the routed experts.  Created on first use, never
+// while the caller's stream is being captured into a graph; kept for the life of the process.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool ready = false;
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+// With g_side_mu held: this device's side stream, or null when there is none to use.
+SideStream* side_stream_locked(cudaStream_t st) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  SideStream& ss = g_side[dev];
+  if (ss.ready) return &ss;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    ss.s = nullptr;
+    return nullptr;
+  }
+  if (cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    if (ss.fork) cudaEventDestroy(ss.fork);
+    cudaStreamDestroy(ss.s);
+    ss = SideStream{};
+    return nullptr;
+  }
+  ss.ready = true;
+  return &ss;
+}
 }  // namespace
 
 bool pdl_enabled() { return g_pdl_on.load(std::memory_order_relaxed); }
@@ -143,14 +186,25 @@ ProfScope::~ProfScope() {
 
 // The shared expert: dense SwiGLU over all T tokens on the CTA-pair engine; the
 // bf16 hidden activation [T, F_shared] lives in `hs` (workspace scratch).
+// Router GEMM tiles: 128 columns wide, or 64 when that still fits the whole GEMM in one wave of
+// the SMs (decode-sized batches: E = 256 then streams its router weights through 4 SMs instead of
+// 2).  The tile width changes no bit of a logit.
+GemmVariant router_variant(int T, int E) {
+  if (E <= 64) return GV_F32_BN64_MT1;
+  int sms = 0;
+  if (device_sm_count(&sms) != INVMOE_OK) return GV_F32_BN128_MT1;
+  const long long units64 = ((static_cast<long long>(T) + 127) / 128) * ((E + 63) / 64);
+  return units64 <= sms ? GV_F32_BN64_MT1 : GV_F32_BN128_MT1;
+}
+
 int shared_expert_run(const void* x, const void* ws13, const void* ws2, int T, int H, int F_shared, float* y_shared,
-                      void* hs, unsigned int* status, cudaStream_t st) {
+                      void* hs, unsigned int* status, cudaStream_t st, int* sched) {
   GemmCall s1{};
   s1.name = "shared_gemm1_swiglu";
   s1.variant = GV_PAIR_SWIGLU;
   s1.A = x; s1.a_rows = T; s1.B = ws13; s1.b_rows = 2LL * F_shared; s1.K = H;
   s1.N = F_shared; s1.M = T; s1.G = 0; s1.b_group_rows = 0; s1.b_up_rows = F_shared;
-  s1.out = hs; s1.ldo = F_shared; s1.status = status;
+  s1.out = hs; s1.ldo = F_shared; s1.status = status; s1.sched = sched;
   int rc = gemm_run(s1, st);
   if (rc) return rc;
   GemmCall s2{};
@@ -158,7 +212,7 @@ int shared_expert_run(const void* x, const void* ws13, const void* ws2, int T, i
   s2.variant = GV_PAIR_F32;
   s2.A = hs; s2.a_rows = T; s2.B = ws2; s2.b_rows = H; s2.K = F_shared;
   s2.N = H; s2.M = T; s2.G = 0;
-  s2.out = y_shared; s2.ldo = H; s2.status = status;
+  s2.out = y_shared; s2.ldo = H; s2.status = status; s2.sched = sched;
   return gemm_run(s2, st);
 }
 
@@ -190,7 +244,11 @@ size_t invmoe_workspace_size(int T, int H, int E, int k, int F, int F_shared, in
   if (T < 0) return 0;
   size_t need = 0;
   if (E > 0 && k > 0) need = replay_ws(T, E, k) > need ? replay_ws(T, E, k) : need;
-  if (F_shared > 0) need = ffn_ws(T, F_shared) > need ? ffn_ws(T, F_shared) : need;
+  if (F_shared > 0) {
+    // moe_layer_forward keeps the routing scratch and the shared expert's h apart (they run at once)
+    const size_t w = ffn_ws(T, F_shared) + (E > 0 ? route_ws(T, E) : 0);
+    need = w > need ? w : need;
+  }
   if (V > 0) need = head_ws(T, V) > need ? head_ws(T, V) : need;
   return kStatusBytes + need;
 }
@@ -243,8 +301,7 @@ int moe_route_topk(const void* x, const void* w_router, int T, int H, int E, int
 
   GemmCall g{};
   g.name = "router_gemm";
-  // narrow tiles so that even E = 256 spreads over twice as many SMs as a 256-wide tile
-  g.variant = E <= 64 ? GV_F32_BN64_MT1 : GV_F32_BN128_MT1;
+  g.variant = router_variant(T, E);
   g.A = x; g.a_rows = T; g.B = w_router; g.b_rows = E; g.K = H; g.N = E; g.M = T; g.G = 0;
   g.out = logits; g.ldo = E; g.status = status_word(workspace);
   // the fp32 epilogue stores 4 columns at a time; E % 4 != 0 would need a scalar tail
@@ -276,7 +333,7 @@ int moe_route_replay(const void* x, const void* w_router, const int32_t* topk_id
   REQUIRE_ALIGNED(workspace);
   GemmCall g{};
   g.name = "router_gemm";
-  g.variant = E <= 64 ? GV_F32_BN64_MT1 : GV_F32_BN128_MT1;
+  g.variant = router_variant(T, E);
   g.A = x; g.a_rows = T; g.B = w_router; g.b_rows = E; g.K = H; g.N = E; g.M = T; g.G = 0;
   g.out = logits; g.ldo = E; g.status = status_word(workspace);
   int rc = gemm_run(g, st);
@@ -351,12 +408,55 @@ int moe_layer_forward(const void* x, const void* w_router, const void* w13, cons
                       const void* ws2, int T, int H, int E, int k, int F, int F_shared, float* logits,
                       int32_t* topk_idx, float* topk_w, int32_t* plan, void* xp, void* h, float* y, float* y_shared,
                       float* out, void* out_bf16, void* workspace, size_t ws_bytes, void* stream) {
-  int rc = moe_route_topk(x, w_router, T, H, E, k, logits, topk_idx, topk_w, plan, xp, workspace, ws_bytes, stream);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The shared expert depends on x alone: with a large enough workspace it runs on the library's
+  // side stream (its h after the routing scratch, its own unit counter) while the routing and the
+  // routed experts run on `stream`; the combine waits for both.  Same kernels, same bits.
+  const int mode = g_shared_overlap.load(std::memory_order_relaxed);
+  const bool overlap = F_shared > 0 && T > 0 && E > 0 && (mode == 1 || (mode == 2 && T <= kSharedOverlapMaxT)) &&
+                       workspace != nullptr && ws_bytes >= kStatusBytes + route_ws(T, E) + ffn_ws(T, F_shared);
+  if (!overlap) {
+    int rc = moe_route_topk(x, w_router, T, H, E, k, logits, topk_idx, topk_w, plan, xp, workspace, ws_bytes, stream);
+    if (rc) return rc;
+    rc = moe_grouped_ffn(xp, plan, w13, w2, T, H, E, k, F, h, y, x, ws13, ws2, F_shared, y_shared, workspace,
+                         ws_bytes, stream);
+    if (rc) return rc;
+    return moe_combine(y, topk_w, plan, F_shared > 0 ? y_shared : nullptr, T, H, E, k, out, out_bf16, stream);
+  }
+  // everything the shared expert needs is checked before the fork, so no early return leaves it open
+  REQUIRE(H > 0 && H % 64 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "H=%d is not a multiple of 64", H);
+  REQUIRE(F_shared % 64 == 0, INVMOE_ERR_UNSUPPORTED_SHAPE, "F_shared=%d is not a multiple of 64", F_shared);
+  REQUIRE_PTR(x); REQUIRE_PTR(ws13); REQUIRE_PTR(ws2); REQUIRE_PTR(y_shared);
+  REQUIRE_ALIGNED(x); REQUIRE_ALIGNED(ws13); REQUIRE_ALIGNED(ws2); REQUIRE_ALIGNED(y_shared);
+  REQUIRE_ALIGNED(workspace);
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream* ss = side_stream_locked(st);
+  if (!ss) {
+    int rc = moe_route_topk(x, w_router, T, H, E, k, logits, topk_idx, topk_w, plan, xp, workspace, ws_bytes, stream);
+    if (rc) return rc;
+    rc = moe_grouped_ffn(xp, plan, w13, w2, T, H, E, k, F, h, y, x, ws13, ws2, F_shared, y_shared, workspace,
+                         ws_bytes, stream);
+    if (rc) return rc;
+    return moe_combine(y, topk_w, plan, y_shared, T, H, E, k, out, out_bf16, stream);
+  }
+  int rc = check_cuda(cudaEventRecord(ss->fork, st), "cudaEventRecord (fork)");
   if (rc) return rc;
-  rc = moe_grouped_ffn(xp, plan, w13, w2, T, H, E, k, F, h, y, x, ws13, ws2, F_shared, y_shared, workspace, ws_bytes,
-                       stream);
+  if ((rc = check_cuda(cudaStreamWaitEvent(ss->s, ss->fork, 0), "cudaStreamWaitEvent (fork)"))) return rc;
+  unsigned int* status = status_word(workspace);
+  int* side_sched = reinterpret_cast<int*>(reinterpret_cast<char*>(status) + 128);
+  const int rc_side = shared_expert_run(x, ws13, ws2, T, H, F_shared, y_shared, scratch(workspace) + route_ws(T, E),
+                                        status, ss->s, side_sched);
+  rc = moe_route_topk(x, w_router, T, H, E, k, logits, topk_idx, topk_w, plan, xp, workspace, ws_bytes, stream);
+  if (!rc)
+    rc = moe_grouped_ffn(xp, plan, w13, w2, T, H, E, k, F, h, y, nullptr, nullptr, nullptr, 0, nullptr, workspace,
+                         ws_bytes, stream);
+  // the join is made whatever failed, so that `stream` (and a graph being captured) stays whole
+  int rc_join = check_cuda(cudaEventRecord(ss->join, ss->s), "cudaEventRecord (join)");
+  if (!rc_join) rc_join = check_cuda(cudaStreamWaitEvent(st, ss->join, 0), "cudaStreamWaitEvent (join)");
+  if (rc_side) return rc_side;
   if (rc) return rc;
-  return moe_combine(y, topk_w, plan, F_shared > 0 ? y_shared : nullptr, T, H, E, k, out, out_bf16, stream);
+  if (rc_join) return rc_join;
+  return moe_combine(y, topk_w, plan, y_shared, T, H, E, k, out, out_bf16, stream);
 }
 
 int moe_combine(const float* y, const float* topk_w, const int32_t* plan, const float* y_shared, int T, int H, int E,
@@ -800,6 +900,12 @@ int invmoe_expert_engine(int which) {
   REQUIRE(which >= 0 && which <= 2, INVMOE_ERR_INVALID_ARG,
           "engine must be 0 (row tiles), 1 (token columns) or 2 (automatic)");
   g_expert_engine.store(which);
+  return INVMOE_OK;
+}
+
+int invmoe_shared_overlap(int mode) {
+  if (mode < 0 || mode > 2) return set_error(INVMOE_ERR_INVALID_ARG, "mode must be 0, 1 or 2");
+  g_shared_overlap.store(mode);
   return INVMOE_OK;
 }
 

@@ -117,7 +117,7 @@ GemmParams make_params(const GemmCall& c, int nb_cols) {
   p.ldo = c.ldo;
   p.status = c.status;
   // the dynamic-schedule counter lives in the workspace's status block, after the status word
-  p.sched = reinterpret_cast<int*>(reinterpret_cast<char*>(c.status) + 64);
+  p.sched = c.sched ? c.sched : reinterpret_cast<int*>(reinterpret_cast<char*>(c.status) + 64);
   p.timeout_ns = kTimeoutNs;
   p.part = c.part;
   p.nch = c.part_ld > 0 ? static_cast<int>(c.part_ld) : (c.N + 255) / 256;

@@ -14,6 +14,8 @@ constexpr unsigned long long kTimeoutNs = 1000000000ull;
 
 // Fixed chunk sizes (part of the numerical definition; never derived from T).
 constexpr int kDispatchChunk = 64;   // tokens per dispatch-count chunk
+constexpr int kSharedOverlapMaxT = 1024;   // moe_layer_forward's automatic choice: the shared expert
+                                           // runs on the side stream for batches up to this size
 constexpr int kLseChunk = 256;       // vocabulary columns per log-sum-exp partial
 
 // Workspace: [0, 256) status block, then per-call scratch.
@@ -113,6 +115,9 @@ struct GemmCall {
   void* out;
   long long ldo;
   unsigned int* status;
+  int* sched;            // unit counter and done count (two ints, zero between launches); null = the
+                         // status block's first pair (byte 64); launches that may run at the same
+                         // time need different pairs
   float2* part;          // GV_PAIR_LSE only: partials of the first column block of `row` 0
   long long part_ld;     // GV_PAIR_LSE: row stride of part in pairs (0 = ceil(N / 256))
   int target_col0;       // GV_PAIR_LSE: vocabulary column of B's first row (a shard's v0)
@@ -157,7 +162,7 @@ int rl_loss_launch(const float* lt, const float* lo, const float* lr, const floa
 int timeout_probe_launch(unsigned int* status, unsigned long long limit_ns, cudaStream_t st);
 
 int shared_expert_run(const void* x, const void* ws13, const void* ws2, int T, int H, int F_shared, float* y_shared,
-                      void* hs, unsigned int* status, cudaStream_t st);
+                      void* hs, unsigned int* status, cudaStream_t st, int* sched = nullptr);
 
 // ---------------------------------------------------------------- expert parallelism
 int ep_regroup_launch(const void* recv_xp, const int32_t* recv_counts, int n_src, int E_local, int R, int H,

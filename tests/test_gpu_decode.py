@@ -104,3 +104,30 @@ def test_decode_rejects_a_bad_token_tensor():
         layer.decode(x[:4, :128].contiguous())
     with pytest.raises(ValueError):
         layer.decode(x[:4].cpu())
+
+
+def test_shared_expert_on_the_side_stream_changes_no_bit():
+    """moe_layer_forward runs the shared expert on the library's side stream beside the routing and
+    the routed experts (invmoe_shared_overlap 1, and 2 for batches up to 1024 tokens) or after them
+    on the caller's stream (0): the same kernels, so the same bits, and a workspace of the size
+    invmoe_workspace_size gives keeps the routing scratch and the shared expert's h apart."""
+    from serve_invariant_moe_gb300 import _lib
+    cfg = CFGS[0]
+    x, layer = _layer(cfg)
+    lib = _lib.lib()
+    try:
+        for T in (1, 37, cfg.T):
+            outs = []
+            for mode in (0, 1, 2, 0):
+                assert lib.invmoe_shared_overlap(mode) == 0
+                r = layer.prefill(x[:T], return_all=True)
+                torch.cuda.synchronize()
+                outs.append((r["out"].clone(), r["y_shared"][:T].clone()))
+            for o, ys in outs[1:]:
+                assert torch.equal(o.view(torch.int32), outs[0][0].view(torch.int32)), T
+                assert torch.equal(ys.view(torch.int32), outs[0][1].view(torch.int32)), T
+            d = layer.decode(x[:T]).clone()
+            assert torch.equal(d.view(torch.int32), outs[0][0].view(torch.int32)), T
+    finally:
+        lib.invmoe_shared_overlap(2)
+    assert lib.invmoe_shared_overlap(3) != 0
