@@ -527,7 +527,8 @@ int invmoe_shared_overlap(int mode);
  * tokens on the N side (any multiple of 16 tokens, up to 320 per unit, on a CTA
  * pair); 2 (default) takes 1 for the gate/up GEMM when the batch averages at
  * least 64 token slots per expert, holds at most 64 slots in all, or H <= 1024,
- * and 0 otherwise (and 0 for the down projection).  Both
+ * and 0 otherwise; for the down projection 1 when the batch holds at most 8 slots
+ * and H > 1024 (one decode token of a wide layer), else 0.  Both
  * walk every element's reduction in the same order and give the same bits
  * (tested), so the choice never changes an output. */
 int invmoe_expert_engine(int which);

@@ -236,9 +236,9 @@ int launch_pair(const GemmCall& c, cudaStream_t st) {
 
 // Token-column engine (grouped only): clusters of 2, grid = 2 x min(units, SMs / 2).
 // Weights [G * b_group_rows, K] in 64-row boxes, tokens [rows, K] in 32-row boxes.
-template <int EPI, int STAGES>
+template <int EPI, int STAGES, int CHUNK>
 int launch_tok(const GemmCall& c, cudaStream_t st) {
-  using S = TokShape<EPI, STAGES>;
+  using S = TokShape<EPI, STAGES, CHUNK>;
   if (c.G <= 0) return set_error(INVMOE_ERR_INVALID_ARG, "the token-column engine is grouped only");
   if (c.G > S::MAX_GROUPS) return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "more than %d groups", S::MAX_GROUPS);
   const int wb_cols = EPI == EPI_SWIGLU ? 128 : 256;
@@ -251,12 +251,12 @@ int launch_tok(const GemmCall& c, cudaStream_t st) {
   if ((rc = make_tmap(&tx, c.A, c.K, c.a_rows, kTokBoxRows))) return rc;
   if ((rc = make_tmap(&txb, c.A, c.K, c.a_rows, kTokBigRows))) return rc;
   static std::atomic<uint64_t> attr_set{0};
-  if ((rc = set_smem_attr(reinterpret_cast<const void*>(tc_gemm_tok_kernel<EPI, STAGES>), S::SMEM_BYTES, attr_set)))
+  if ((rc = set_smem_attr(reinterpret_cast<const void*>(tc_gemm_tok_kernel<EPI, STAGES, CHUNK>), S::SMEM_BYTES, attr_set)))
     return rc;
   int sms = 0;
   if ((rc = device_sm_count(&sms))) return rc;
   GemmParams p = make_params(c, wb_cols);
-  const long long max_chunks = (c.a_rows + kTokChunk - 1) / kTokChunk + c.G;
+  const long long max_chunks = (c.a_rows + CHUNK - 1) / CHUNK + c.G;
   const long long max_units = max_chunks * p.n_blocks;
   if (max_units <= 0) return INVMOE_OK;
   const long long pairs = max_units < sms / 2 ? max_units : sms / 2;
@@ -268,7 +268,7 @@ int launch_tok(const GemmCall& c, cudaStream_t st) {
   // the unit counter (p.sched) is zero here: the workspace starts zero-filled and every
   // launch's last producer resets it (sched_release)
   ProfScope prof(c.name ? c.name : "tc_gemm_tok", st);
-  return check_cuda(launch_kernel_ex(tc_gemm_tok_kernel<EPI, STAGES>, dim3(static_cast<unsigned>(2 * pairs)),
+  return check_cuda(launch_kernel_ex(tc_gemm_tok_kernel<EPI, STAGES, CHUNK>, dim3(static_cast<unsigned>(2 * pairs)),
                                      dim3(S::THREADS), S::SMEM_BYTES, st, attr, 1, tw, tx, txb, p),
                     "tc_gemm_tok_kernel launch");
 }
@@ -301,8 +301,11 @@ int gemm_run(const GemmCall& c, cudaStream_t st) {
     case GV_SWIGLU_BWD_BN256_MT2: return launch<256, 2, EPI_SWIGLU_BWD, 3>(c, st);
     case GV_F32_BN256_MT1_KGROUP: return launch<256, 1, EPI_F32, 4, true, true, true>(c, st);
     case GV_PAIR_SWIGLU_BWD: return launch_pair<EPI_SWIGLU_BWD, 6>(c, st);
-    case GV_TOK_SWIGLU: return launch_tok<EPI_SWIGLU, 5>(c, st);
-    case GV_TOK_F32: return launch_tok<EPI_F32, 5>(c, st);
+    // at most 64 token slots in all (decode): 64-token units, a 32-row token tile, a ring twice as deep
+    case GV_TOK_SWIGLU:
+      return c.a_rows <= 64 ? launch_tok<EPI_SWIGLU, 10, 64>(c, st) : launch_tok<EPI_SWIGLU, 5, kTokChunk>(c, st);
+    case GV_TOK_F32:
+      return c.a_rows <= 64 ? launch_tok<EPI_F32, 10, 64>(c, st) : launch_tok<EPI_F32, 5, kTokChunk>(c, st);
   }
   return set_error(INVMOE_ERR_INVALID_ARG, "unknown GEMM variant %d", (int)c.variant);
 }

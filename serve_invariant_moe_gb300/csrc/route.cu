@@ -380,18 +380,24 @@ constexpr int kPermuteThreads = 256;
 __global__ void __launch_bounds__(kPermuteThreads) permute_rows_kernel(const uint4* __restrict__ x,
                                                                       const int32_t* __restrict__ slot_row,
                                                                       long long T, int k, int vec_per_row,
+                                                                      int seg_vec, int nseg,
                                                                       uint4* __restrict__ xp) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long nwarps = static_cast<long long>(gridDim.x) * (kPermuteThreads / 32);
-  for (long long t = blockIdx.x * static_cast<long long>(kPermuteThreads / 32) + (threadIdx.x >> 5); t < T;
-       t += nwarps) {
+  // a warp copies segment `seg` (vectors [seg * seg_vec, +seg_vec) of the row) of token t to its
+  // k rows of xp; one segment per token for large batches, 2 KB segments for small ones
+  for (long long item = blockIdx.x * static_cast<long long>(kPermuteThreads / 32) + (threadIdx.x >> 5);
+       item < T * nseg; item += nwarps) {
+    const long long t = item / nseg;
+    const int seg = static_cast<int>(item - t * nseg);
+    const int c_end = min(vec_per_row, (seg + 1) * seg_vec);
     const int my_row = lane < k ? __ldg(slot_row + t * k + lane) : 0;
     const uint4* src = x + t * vec_per_row;
     // every loop bound below is warp-uniform, so the shuffles always see all 32 lanes
-    int c0 = 0;
-    for (; c0 + 128 <= vec_per_row; c0 += 128) {
+    int c0 = seg * seg_vec;
+    for (; c0 + 128 <= c_end; c0 += 128) {
       const int c = c0 + lane;
       const uint4 v0 = __ldg(src + c), v1 = __ldg(src + c + 32), v2 = __ldg(src + c + 64), v3 = __ldg(src + c + 96);
       for (int j = 0; j < k; ++j) {
@@ -402,13 +408,13 @@ __global__ void __launch_bounds__(kPermuteThreads) permute_rows_kernel(const uin
         dst[c + 96] = v3;
       }
     }
-    // tail: the row's last vec_per_row % 128 vectors; lanes past the row's end only skip their store
-    for (; c0 < vec_per_row; c0 += 32) {
+    // tail: the segment's last (c_end - c0) < 128 vectors; lanes past its end only skip their store
+    for (; c0 < c_end; c0 += 32) {
       const int cc = c0 + lane;
-      const uint4 v = cc < vec_per_row ? __ldg(src + cc) : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 v = cc < c_end ? __ldg(src + cc) : make_uint4(0u, 0u, 0u, 0u);
       for (int j = 0; j < k; ++j) {
         const long long row = __shfl_sync(0xffffffffu, my_row, j);
-        if (cc < vec_per_row) xp[row * vec_per_row + cc] = v;
+        if (cc < c_end) xp[row * vec_per_row + cc] = v;
       }
     }
   }
@@ -544,15 +550,20 @@ int permute_launch(const void* x, const int32_t* slot_row, int T, int k, int H, 
   const int vec_per_row = H / 8;
   int sms = 0;
   if ((rc = device_sm_count(&sms))) return rc;
-  // a warp per token; at most 8 resident blocks of 256 threads per SM
-  long long blocks = (static_cast<long long>(T) + kPermuteThreads / 32 - 1) / (kPermuteThreads / 32);
+  // a warp per token; with fewer tokens than about four per SM, a warp per 2 KB segment of a
+  // token's row (128 vectors), so that small batches are not copied by a handful of warps
+  const int seg_vec = static_cast<long long>(T) < 4LL * sms ? 128 : (vec_per_row > 0 ? vec_per_row : 1);
+  const int nseg = vec_per_row > 0 ? (vec_per_row + seg_vec - 1) / seg_vec : 1;
+  const long long items = static_cast<long long>(T) * nseg;
+  // at most 8 resident blocks of 256 threads per SM
+  long long blocks = (items + kPermuteThreads / 32 - 1) / (kPermuteThreads / 32);
   const long long cap = static_cast<long long>(sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks > 0 && vec_per_row > 0) {
     ProfScope prof("permute_rows", st);
     rc = check_cuda(launch_kernel(permute_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kPermuteThreads), 0,
                                   st, static_cast<const uint4*>(x), slot_row, static_cast<long long>(T), k, vec_per_row,
-                                  static_cast<uint4*>(xp)),
+                                  seg_vec, nseg, static_cast<uint4*>(xp)),
                     "permute_rows_kernel");
     if (rc) return rc;
   }

@@ -65,10 +65,15 @@ constexpr int kTokChunk = 320;     // most tokens (TMEM columns) of one unit
 constexpr int kTokBoxRows = 32;    // token rows per small TMA box
 constexpr int kTokBigRows = 128;   // token rows per large TMA box (a CTA's whole MMA-1 share)
 
-template <int EPI, int STAGES>
+// CHUNK: most tokens of one unit.  kTokChunk for any batch; 64 when the whole batch holds at most
+// 64 token slots (decode), where a CTA's token tile is one 32-row box and the stages are small
+// enough for twice the ring depth.
+template <int EPI, int STAGES, int CHUNK = kTokChunk>
 struct TokShape {
+  static_assert(CHUNK == kTokChunk || CHUNK == 64, "unit size");
   static constexpr int A_BYTES = kBM * kBK * 2;                   // 16 KB: 128 weight rows x 64 K
-  static constexpr int B_ROWS = 128 + 32;                         // token rows per CTA: MMA 1 + MMA 2
+  // token rows per CTA: MMA 1 (half of up to 256) + MMA 2 (half of up to 64), or half of 64
+  static constexpr int B_ROWS = CHUNK == kTokChunk ? 128 + 32 : 32;
   static constexpr int B_BYTES = B_ROWS * kBK * 2;                // 20 KB
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;           // 36 KB (1 KB multiple)
   static constexpr int TMEM_COLS = 512;
@@ -91,10 +96,10 @@ struct TokUnit {
   int g;      // group (expert)
   int wb;     // weight block
   int tok0;   // first token row of the chunk (row of X and of the output)
-  int nv;     // tokens in the chunk (1 .. kTokChunk)
+  int nv;     // tokens in the chunk (1 .. CHUNK)
 };
 
-// Chunks of group g: ceil(n / kTokChunk), near-equal sizes.  Units are ordered
+// Chunks of group g: ceil(n / CHUNK), near-equal sizes (the kernel's prefix holds the counts).  Units are ordered
 // group by group, chunk-major inside a group, so consecutive units share the
 // chunk's token rows in L2.
 __device__ __forceinline__ TokUnit decode_tok_unit(int u, const GemmParams& p, const int* s_prefix) {
@@ -140,11 +145,11 @@ __device__ __forceinline__ int tok_phase_chunk(int slot, int ph, int nchunk, int
   return k < a ? k : 8 + (k - a);
 }
 
-template <int EPI, int STAGES>
-__global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
+template <int EPI, int STAGES, int CHUNK>
+__global__ void __launch_bounds__(TokShape<EPI, STAGES, CHUNK>::THREADS, 1)
     tc_gemm_tok_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmXb, const GemmParams p) {
-  using S = TokShape<EPI, STAGES>;
+  using S = TokShape<EPI, STAGES, CHUNK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
@@ -200,14 +205,14 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
   pdl_wait();
   pdl_trigger();
 
-  // chunk prefix over groups (warp 2; G <= 1024): s_prefix[g] = sum_{g'<g} ceil(counts[g'] / kTokChunk)
+  // chunk prefix over groups (warp 2; G <= 1024): s_prefix[g] = sum_{g'<g} ceil(counts[g'] / CHUNK)
   if (warp == 2) {
     const int per = (p.G + 31) / 32;
     const int g0 = lane * per;
     int local = 0;
     for (int i = 0; i < per; ++i) {
       const int g = g0 + i;
-      if (g < p.G) local += (__ldg(p.counts + g) + kTokChunk - 1) / kTokChunk;
+      if (g < p.G) local += (__ldg(p.counts + g) + CHUNK - 1) / CHUNK;
     }
     int incl = local;
     for (int d = 1; d < 32; d <<= 1) {
@@ -219,7 +224,7 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
       const int g = g0 + i;
       if (g < p.G) {
         s_prefix[g] = run;
-        run += (__ldg(p.counts + g) + kTokChunk - 1) / kTokChunk;
+        run += (__ldg(p.counts + g) + CHUNK - 1) / CHUNK;
       }
     }
     if (lane == 31) {
@@ -280,7 +285,7 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES>::THREADS, 1)
         // MMA 1's token rows of this CTA: up to two small boxes, else one large box (rows past
         // the chunk are read from L2 and never stored); MMA 2's: one small box
         const int nb1 = (r1 + kTokBoxRows - 1) / kTokBoxRows;
-        const bool big1 = nb1 > 2;
+        const bool big1 = S::B_ROWS >= kTokBigRows && nb1 > 2;
         const uint32_t bytes = S::A_BYTES + (big1 ? kTokBigRows : nb1 * kTokBoxRows) * (kBK * 2) +
                                (r2 > 0 ? kTokBoxRows * kBK * 2 : 0);
         // this CTA's weight rows: SwiGLU h columns [f0, f0 + 64), f0 = 128 wb + 64r (gate rows f0.., up
