@@ -395,6 +395,7 @@ def run_ours(args):
     if nxt is not None:
         nxt.update(qwen_layer_timing(device, peaks))
         nxt.update(tiny_latency(device))
+        nxt.update(glm_decode_latency(st))
     if nxt is not None and not args.no_backward:
         nxt.update(head_backward_timing(st, device, peaks))
         torch.cuda.empty_cache()
@@ -439,7 +440,8 @@ def run_ours(args):
 
 def _summary(per_kernel, nxt, inv, ms_profiled):
     """Compact digest of the line: per-step time with per-launch events on, the kernels against their
-    roofline, the Qwen-like layer, the tiny configuration's latency and the k3 == 0 evidence."""
+    roofline, the Qwen-like layer, the tiny configuration's and the GLM-scale layer's decode latency and
+    the k3 == 0 evidence."""
     def pick(nm, *keys):
         e = per_kernel.get(nm) or {}
         return {k: e[k] for k in keys if k in e} or None
@@ -458,6 +460,7 @@ def _summary(per_kernel, nxt, inv, ms_profiled):
             if nm in nxt:
                 out["qwen_layer"][nm] = {k: nxt[nm][k] for k in ("frac", "roofline_frac")}
         out["tiny_us"] = {k[5:-3]: nxt[k] for k in nxt if k.startswith("tiny_") and k.endswith("_us")}
+        out["glm_decode_us"] = {k[11:-3]: nxt[k] for k in nxt if k.startswith("glm_decode_") and k.endswith("_us")}
     if inv:
         out["invariance"] = {k: inv[k] for k in ("moe_out_values_differing", "logp_differing",
                                                  "k3_mean_prefill_vs_decode")}
@@ -637,6 +640,27 @@ def moe_backward_timing(st, device, peaks, reps=3):
                            roofline_frac=round(max(t_flop, t_byte) / kms, 4))
             out["moe_bwd_" + nm] = ent
     del r
+    return out
+
+
+def glm_decode_latency(st, reps=50):
+    """Decode latency of the step's own GLM-scale layer (with its shared expert): microseconds per
+    MoELayer.decode call for 1, 8 and 64 concurrent requests (one token each), outside the timed
+    region (device time between events around `reps` back-to-back calls)."""
+    import torch
+    out = {}
+    for B in (1, 8, 64):
+        xb = st.x[:B]
+        for _ in range(5):
+            st.layer.decode(xb)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            st.layer.decode(xb)
+        e1.record()
+        torch.cuda.synchronize()
+        out[f"glm_decode_B{B}_us"] = round(e0.elapsed_time(e1) / reps * 1e3, 1)
     return out
 
 
