@@ -528,7 +528,8 @@ int invmoe_shared_overlap(int mode);
  * pair); 2 (default) takes 1 for the gate/up GEMM when the batch averages at
  * least 64 token slots per expert, holds at most 64 slots in all, or H <= 1024,
  * and 0 otherwise; for the down projection 1 when the batch holds at most 8 slots
- * and H > 1024 (one decode token of a wide layer), else 0.  Both
+ * and H > 1024 (one decode token of a wide layer) or averages at least 64 slots
+ * per expert with F >= 2048, else 0.  Both
  * walk every element's reduction in the same order and give the same bits
  * (tested), so the choice never changes an output. */
 int invmoe_expert_engine(int which);

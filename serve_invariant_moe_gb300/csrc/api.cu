@@ -376,13 +376,14 @@ int moe_grouped_ffn(const void* xp, const int32_t* plan, const void* w13, const 
   // 0.226 ms; decode batches of 1 and 8 on the GLM-scale layer 84 vs 113 us and 504 vs 523 us;
   // tiny layer (H = 256) 14.5 vs 20.4 us.  In between (1 to 16 tokens per expert on the
   // GLM-scale layer, 32 to 512 requests) both stream every weight and the row tiles, with more
-  // weight bytes in flight per SM, are 2-7 % faster.  The down projection is faster in row
-  // tiles in every measured case but a GLM-scale batch of one (48 vs 57 us; GLM-scale layer 1.48
-  // vs 1.50 ms, Qwen-like 0.131 vs 0.153 ms, tiny 12.1 vs 14.1 us, 8 GLM-scale requests 250 vs
-  // 232 us).  The automatic choice follows that.
+  // weight bytes in flight per SM, are 2-7 % faster.  The down projection runs in token columns
+  // for a GLM-scale batch of one (48 vs 57 us) and for prefill-sized batches whose reduction is at
+  // least 32 K blocks long (GLM-scale layer, F = 2048: 1.43 vs 1.48 ms); with short reductions its
+  // epilogue weighs more than the tails it removes (Qwen-like layer, F = 768: 0.149 vs 0.131 ms;
+  // tiny 14.1 vs 12.1 us; 8 GLM-scale requests 250 vs 232 us).  The automatic choice follows that.
   const int eng = expert_engine();
   const bool tok1 = eng == 1 || (eng == 2 && (S >= 64LL * E || S <= 64 || H <= 1024));
-  const bool tok2 = H % 256 == 0 && (eng == 1 || (eng == 2 && S <= 8 && H > 1024));
+  const bool tok2 = H % 256 == 0 && (eng == 1 || (eng == 2 && ((S <= 8 && H > 1024) || (S >= 64LL * E && F >= 2048))));
   GemmCall g1{};
   g1.name = "expert_gemm1_swiglu";
   g1.variant = tok1 ? GV_TOK_SWIGLU : GV_SWIGLU_BN256_MT2;
