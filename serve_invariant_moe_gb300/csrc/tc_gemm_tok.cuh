@@ -21,13 +21,20 @@
 //   * CTA r loads its 128 weight rows of the block and its half of the token
 //     rows: MMA 1 covers tokens [0, N1) with CTA r holding [r*N1/2, (r+1)*N1/2),
 //     MMA 2 (when the chunk has more than 256 tokens) tokens [256, 256 + N2)
-//     split the same way; token boxes are 32 rows, rows past the chunk are
-//     loaded and never stored.  SwiGLU: the CTA's h columns are
-//     [f0, f0 + 64), f0 = 128 * block + 64 * r, and its weight rows arrive in
-//     16-row boxes, gate and up alternating: tile rows 32i + [0, 16) are the gate
-//     rows of h columns f0 + 16i + [0, 16), tile rows 32i + [16, 32) the matching
+//     split the same way.  One stage is one TMA box of weights (SwiGLU: a
+//     rank-5 box, below; fp32: 128 rows), one or two 32-row token boxes or one
+//     128-row box for MMA 1, and one 32-row box for MMA 2: at this size the
+//     producer thread's copy issue, not the bytes, set the pace, so a stage
+//     takes as few copies as it can (rows past the chunk are read from L2 and
+//     never stored).  SwiGLU: the CTA's h columns are [f0, f0 + 64),
+//     f0 = 128 * block + 64 * r, and its weight rows arrive as 4 groups of 16
+//     gate rows and the matching 16 up rows: tile rows 32i + [0, 16) are the
+//     gate rows of h columns f0 + 16i + [0, 16), tile rows 32i + [16, 32) the
 //     up rows, so the warp on TMEM lanes 32i holds both halves of its 16 SwiGLU
 //     pairs and exchanges them with one shuffle.
+//   * A batch of at most 64 token slots (decode) runs the same kernel with units
+//     of at most 64 tokens: a 32-row token tile per CTA, 20 KB stages, a ring
+//     twice as deep.
 //   * TMEM: lane = weight row, one column per token.  Consecutive units of a CTA
 //     alternate between two placements: slot 0 puts MMA 1 at column 0 and MMA 2
 //     at column 256 (columns [0, 320)), slot 1 puts MMA 1 at column 256 and
@@ -36,10 +43,11 @@
 //     releases them, and the next unit's MMAs run while it drains the rest;
 //     when neither unit has a second MMA they share no column at all and the
 //     next unit's MMAs do not wait.
-//   * Epilogues read 32 token columns per tcgen05.ld (two loads per wait) and
-//     store through a per-warp staging tile: SwiGLU forms h = silu(g) * u in
-//     fp32 -> bf16 and stores 32-byte row segments of h; the fp32 epilogue
-//     stores 128-byte row segments of Y.
+//   * Epilogues read 32 token columns per tcgen05.ld (two loads per wait),
+//     release a phase's columns (one arrive per warp) as soon as its last loads
+//     complete, and store through a per-warp staging tile: SwiGLU forms
+//     h = silu(g) * u in fp32 -> bf16 and stores 32-byte row segments of h; the
+//     fp32 epilogue stores 128-byte row segments of Y.
 #pragma once
 
 #include <cuda_bf16.h>

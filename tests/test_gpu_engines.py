@@ -62,6 +62,12 @@ SMALL = [
     # every expert just above and below a chunk boundary
     dataclasses.replace(synth.TINY, name="near_chunk_edges", T=1300, H=256, E=8, k=2, F=512,
                         dup_router_rows=False, seed=64),
+    # at most 64 slots in all (the decode form: 64-token units, a 32-row token tile per CTA):
+    # one expert holding all 64, and 8 slots per token spread over 16 experts
+    dataclasses.replace(synth.TINY, name="decode_form_one_full_unit", T=64, H=512, E=4, k=1, F=256,
+                        dup_router_rows=False, zipf_s=1.1, zipf_alpha=5.0, seed=65),
+    dataclasses.replace(synth.TINY, name="decode_form_mixed", T=8, H=2048, E=16, k=8, F=256, F_shared=128,
+                        dup_router_rows=False, seed=66),
 ]
 
 
@@ -71,6 +77,8 @@ def test_engines_bit_identical_small(cfg):
     counts = r[1]["counts"]
     if cfg.name == "heavy_and_empty":
         assert counts.max() > 640 and (counts == 0).any()     # three or more chunks; empty experts
+    if cfg.name == "decode_form_one_full_unit":
+        assert counts.max() == 64                              # one expert fills a whole 64-token unit
     for key in ("h", "y", "out"):
         assert torch.equal(_bits(r[0][key]), _bits(r[1][key])), f"{cfg.name}: {key} differs between the engines"
 
