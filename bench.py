@@ -807,7 +807,7 @@ def _oracle_sample(x, wr, expert, ws13, ws2, wv, target, rollout, mc, tokens):
     return logp, ohead.k3(logp, rollout[tokens])
 
 
-def cpu_baseline(st, samples=16):
+def cpu_baseline(st, samples=32):
     """Time the float64 oracle on `samples` tokens of the same step (bounded, ~10-30 s)."""
     from oracle import moe as omoe
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
@@ -995,7 +995,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip the head and MoE backward timings (next rows)")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=16)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=32)
     ap.add_argument("--ref-tokens-per-step", type=int, default=1)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
