@@ -82,8 +82,19 @@ class MoELayer:
     def prefill(self, x: torch.Tensor, out_bf16: Optional[torch.Tensor] = None, return_all=False,
                 replay_idx: Optional[torch.Tensor] = None):
         """x [T, H] bf16 -> out [T, H] fp32 (optionally also a bf16 copy).  With replay_idx [T, k]
-        int32 the recorded expert choices are used instead of the router's own top-k."""
-        res = self._run(x, self._workspace(x.shape[0]), out_bf16=out_bf16, replay_idx=replay_idx)
+        int32 the recorded expert choices are used instead of the router's own top-k.
+
+        A small batch (at most 1024 tokens) whose intermediates are not returned runs on the
+        layer's preallocated decode buffers (only `out` is allocated per call): for such batches
+        the host's allocations, not the kernels, set the call's latency."""
+        T = x.shape[0]
+        if not return_all and replay_idx is None and 0 < T <= 1024:
+            if self._decode is None or self._decode["B"] < T:
+                self.alloc_decode(max(T, 1))
+            d = self._decode
+            bufs = {k: d[k] for k in ("logits", "idx", "w", "plan", "xp", "h", "y", "ys")}
+            return self._run(x, d["ws"], bufs, out_bf16=out_bf16)["out"]
+        res = self._run(x, self._workspace(T), out_bf16=out_bf16, replay_idx=replay_idx)
         return res if return_all else res["out"]
 
     def backward(self, x: torch.Tensor, fwd: dict, dout: torch.Tensor, weight_grads: bool = True):
