@@ -68,6 +68,9 @@ SMALL = [
                         dup_router_rows=False, zipf_s=1.1, zipf_alpha=5.0, seed=65),
     dataclasses.replace(synth.TINY, name="decode_form_mixed", T=8, H=2048, E=16, k=8, F=256, F_shared=128,
                         dup_router_rows=False, seed=66),
+    # up to 1024 slots run the decode form too: experts of more than 64 tokens take several units
+    dataclasses.replace(synth.TINY, name="decode_form_multi_unit", T=480, H=1024, E=8, k=2, F=256,
+                        dup_router_rows=False, zipf_s=1.1, zipf_alpha=1.5, seed=67),
 ]
 
 
@@ -79,6 +82,8 @@ def test_engines_bit_identical_small(cfg):
         assert counts.max() > 640 and (counts == 0).any()     # three or more chunks; empty experts
     if cfg.name == "decode_form_one_full_unit":
         assert counts.max() == 64                              # one expert fills a whole 64-token unit
+    if cfg.name == "decode_form_multi_unit":
+        assert counts.max() > 128                              # three or more 64-token units
     for key in ("h", "y", "out"):
         assert torch.equal(_bits(r[0][key]), _bits(r[1][key])), f"{cfg.name}: {key} differs between the engines"
 

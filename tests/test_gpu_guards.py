@@ -52,6 +52,9 @@ CFGS = [
     dataclasses.replace(synth.TINY, name="one_token", T=1, H=512, E=8, k=8, F=128, dup_router_rows=False, seed=73),
     dataclasses.replace(synth.TINY, name="ragged_rows", T=333, H=512, E=24, k=4, F=384, dup_router_rows=False,
                         seed=74),
+    # the decode form with experts of more than 64 tokens (several 64-token units each)
+    dataclasses.replace(synth.TINY, name="decode_form_multi_unit", T=300, H=512, E=8, k=2, F=256,
+                        dup_router_rows=False, seed=76),
 ]
 
 
