@@ -526,7 +526,8 @@ int invmoe_shared_overlap(int mode);
  * last tile of at most 64 rows); 1 puts its weight rows on the M side and its
  * tokens on the N side (any multiple of 16 tokens, up to 320 per unit, on a CTA
  * pair); 2 (default) takes 1 for the gate/up GEMM when the batch averages at
- * least 64 token slots per expert, holds at most 1024 slots in all, or H <= 1024,
+ * least 64 token slots per expert, holds at most 1024 slots in all or at most 16
+ * per expert, or H <= 1024,
  * and 0 otherwise; for the down projection 1 when the batch holds at most 8 slots
  * and H > 1024 (one decode token of a wide layer) or averages at least 64 slots
  * per expert with F >= 2048, else 0.  Both

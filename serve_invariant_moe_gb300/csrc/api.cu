@@ -373,18 +373,18 @@ int moe_grouped_ffn(const void* xp, const int32_t* plan, const void* w13, const 
   // Measured on GB300 (gate/up GEMM, token columns vs row tiles): GLM-scale layer, 256 tokens per
   // expert on average, 2.55 vs 2.72 ms (the token columns stream each expert's weights once where
   // the row tiles stream them again for an expert's last few rows); Qwen-like layer 0.221 vs
-  // 0.226 ms; decode batches of up to 1024 token slots, which run the token columns' decode form
-  // (64-token units, a ring twice as deep): GLM-scale 1 request 79 vs 113 us, 16 to 128 requests
-  // 5-10 % faster, Qwen-like 8 to 128 requests 16-18 % faster; tiny layer (H = 256) 15 vs 20 us.
-  // Between 1024 slots and 64 slots per expert (GLM-scale, 256 to 512 requests) both stream every
-  // weight and the row tiles, with more weight bytes in flight per SM, are about 6 % faster.  The
+  // 0.226 ms; decode batches of up to 1024 token slots or 16 per expert, which run the token
+  // columns' decode form (64-token units, a ring twice as deep): GLM-scale 1 request 79 vs 113 us,
+  // 16 to 512 requests 4-10 % faster, Qwen-like 8 to 256 requests 3-18 % faster; tiny layer
+  // (H = 256) 15 vs 20 us.  From 32 to 64 slots per expert the row tiles are as fast or faster
+  // (Qwen-like 512 requests 149 vs 149 us, 1024 requests 157 vs 185 us).  The
   // down projection runs in token columns for a GLM-scale batch of one (48 vs 57 us) and for
   // prefill-sized batches whose reduction is at least 32 K blocks long (GLM-scale layer, F = 2048:
   // 1.43 vs 1.48 ms); with short reductions its epilogue weighs more than the tails it removes
   // (Qwen-like layer, F = 768: 0.149 vs 0.131 ms; tiny 14.1 vs 12.1 us; 8 GLM-scale requests 250 vs
   // 232 us).  The automatic choice follows that.
   const int eng = expert_engine();
-  const bool tok1 = eng == 1 || (eng == 2 && (S >= 64LL * E || S <= 1024 || H <= 1024));
+  const bool tok1 = eng == 1 || (eng == 2 && (S >= 64LL * E || S <= 1024 || S <= 16LL * E || H <= 1024));
   const bool tok2 = H % 256 == 0 && (eng == 1 || (eng == 2 && ((S <= 8 && H > 1024) || (S >= 64LL * E && F >= 2048))));
   GemmCall g1{};
   g1.name = "expert_gemm1_swiglu";

@@ -301,12 +301,14 @@ int gemm_run(const GemmCall& c, cudaStream_t st) {
     case GV_SWIGLU_BWD_BN256_MT2: return launch<256, 2, EPI_SWIGLU_BWD, 3>(c, st);
     case GV_F32_BN256_MT1_KGROUP: return launch<256, 1, EPI_F32, 4, true, true, true>(c, st);
     case GV_PAIR_SWIGLU_BWD: return launch_pair<EPI_SWIGLU_BWD, 6>(c, st);
-    // at most 1024 token slots in all (decode batches): 64-token units (an expert with more tokens
-    // takes several), a 32-row token tile, a ring twice as deep
+    // decode batches (at most 1024 token slots, or at most 16 per expert on average): 64-token
+    // units (an expert with more tokens takes several), a 32-row token tile, a ring twice as deep
     case GV_TOK_SWIGLU:
-      return c.a_rows <= 1024 ? launch_tok<EPI_SWIGLU, 10, 64>(c, st) : launch_tok<EPI_SWIGLU, 5, kTokChunk>(c, st);
+      return c.a_rows <= 1024 || c.a_rows <= 16LL * c.G ? launch_tok<EPI_SWIGLU, 10, 64>(c, st)
+                                                         : launch_tok<EPI_SWIGLU, 5, kTokChunk>(c, st);
     case GV_TOK_F32:
-      return c.a_rows <= 1024 ? launch_tok<EPI_F32, 10, 64>(c, st) : launch_tok<EPI_F32, 5, kTokChunk>(c, st);
+      return c.a_rows <= 1024 || c.a_rows <= 16LL * c.G ? launch_tok<EPI_F32, 10, 64>(c, st)
+                                                         : launch_tok<EPI_F32, 5, kTokChunk>(c, st);
   }
   return set_error(INVMOE_ERR_INVALID_ARG, "unknown GEMM variant %d", (int)c.variant);
 }

@@ -32,9 +32,9 @@
 //     gate rows of h columns f0 + 16i + [0, 16), tile rows 32i + [16, 32) the
 //     up rows, so the warp on TMEM lanes 32i holds both halves of its 16 SwiGLU
 //     pairs and exchanges them with one shuffle.
-//   * A batch of at most 1024 token slots (decode) runs the same kernel with
-//     units of at most 64 tokens (an expert with more takes several): a 32-row
-//     token tile per CTA, 20 KB stages, a ring twice as deep.
+//   * A batch of at most 1024 token slots or 16 per expert (decode) runs the
+//     same kernel with units of at most 64 tokens (an expert with more takes
+//     several): a 32-row token tile per CTA, 20 KB stages, a ring twice as deep.
 //   * TMEM: lane = weight row, one column per token.  Consecutive units of a CTA
 //     alternate between two placements: slot 0 puts MMA 1 at column 0 and MMA 2
 //     at column 256 (columns [0, 320)), slot 1 puts MMA 1 at column 256 and
@@ -74,8 +74,8 @@ constexpr int kTokBoxRows = 32;    // token rows per small TMA box
 constexpr int kTokBigRows = 128;   // token rows per large TMA box (a CTA's whole MMA-1 share)
 
 // CHUNK: most tokens of one unit.  kTokChunk for prefill-sized batches; 64 for batches of at most
-// 1024 token slots (decode), where a CTA's token tile is one 32-row box and the stages are small
-// enough for twice the ring depth.
+// 1024 token slots or 16 per expert (decode), where a CTA's token tile is one 32-row box and the
+// stages are small enough for twice the ring depth.
 template <int EPI, int STAGES, int CHUNK = kTokChunk>
 struct TokShape {
   static_assert(CHUNK == kTokChunk || CHUNK == 64, "unit size");
