@@ -224,6 +224,10 @@ int moe_layer_forward(const void* x, const void* w_router, const void* w13, cons
  * are then never written to memory), logp [T] fp32, lse/k3 [T] fp32 and mask [T]
  * uint8 (nullable).
  * Shapes: H % 64 == 0, V % 4 == 0, beta >= 1.
+ * With fewer than 64 tokens and a workspace of invmoe_workspace_size(T, H, ...,
+ * V) bytes, the hidden rows are first copied into the workspace, padded to 64
+ * rows (faster tiles; the rows past T are never stored, the results are the
+ * same); a workspace large enough for the partials alone also works.
  * ------------------------------------------------------------------------- */
 int lm_logprob_kl(const void* hidden, const void* w_vocab, const int32_t* target,
                   const float* rollout_logp, int T, int H, int V, float beta,
