@@ -461,6 +461,7 @@ def _summary(per_kernel, nxt, inv, ms_profiled):
                 out["qwen_layer"][nm] = {k: nxt[nm][k] for k in ("frac", "roofline_frac")}
         out["tiny_us"] = {k[5:-3]: nxt[k] for k in nxt if k.startswith("tiny_") and k.endswith("_us")}
         out["glm_decode_us"] = {k[11:-3]: nxt[k] for k in nxt if k.startswith("glm_decode_") and k.endswith("_us")}
+        out["glm_head_decode_us"] = {k[9:-3]: nxt[k] for k in nxt if k.startswith("glm_head_") and k.endswith("_us")}
     if inv:
         out["invariance"] = {k: inv[k] for k in ("moe_out_values_differing", "logp_differing",
                                                  "k3_mean_prefill_vs_decode")}
@@ -644,23 +645,31 @@ def moe_backward_timing(st, device, peaks, reps=3):
 
 
 def glm_decode_latency(st, reps=50):
-    """Decode latency of the step's own GLM-scale layer (with its shared expert): microseconds per
-    MoELayer.decode call for 1, 8 and 64 concurrent requests (one token each), outside the timed
-    region (device time between events around `reps` back-to-back calls)."""
+    """Decode latency of the step's own GLM-scale layer (with its shared expert) and head: microseconds
+    per MoELayer.decode call and per head call (vocabulary GEMM + LSE + logprob, V = 151552) for 1, 8
+    and 64 concurrent requests (one token each), outside the timed region (device time between events
+    around `reps` back-to-back calls)."""
     import torch
+    from serve_invariant_moe_gb300 import binding
     out = {}
     for B in (1, 8, 64):
-        xb = st.x[:B]
-        for _ in range(5):
-            st.layer.decode(xb)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(reps):
-            st.layer.decode(xb)
-        e1.record()
-        torch.cuda.synchronize()
-        out[f"glm_decode_B{B}_us"] = round(e0.elapsed_time(e1) / reps * 1e3, 1)
+        xb, hb, tb = st.x[:B], st.hidden[:B], st.target[:B]
+        ws = binding.new_workspace(binding.workspace_size(B, st.mc.H, V=st.hc.V), st.x.device)
+        calls = (("layer", lambda: st.layer.decode(xb)),
+                 ("head", lambda: st.binding.lm_logprob_kl(hb, st.wv, tb, ws)))
+        for name, fn in calls:
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            key = f"glm_decode_B{B}_us" if name == "layer" else f"glm_head_B{B}_us"
+            out[key] = round(e0.elapsed_time(e1) / reps * 1e3, 1)
+        binding.check_status(ws)
     return out
 
 
