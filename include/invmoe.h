@@ -528,15 +528,14 @@ int invmoe_shared_overlap(int mode);
 /* Engine of moe_grouped_ffn's two routed-expert GEMMs (calls made after it):
  * 0 puts each expert's tokens on the MMA's M side in 128-row tiles (64 for a
  * last tile of at most 64 rows); 1 puts its weight rows on the M side and its
- * tokens on the N side (any multiple of 16 tokens, up to 320 per unit, on a CTA
- * pair); 2 (default) takes 1 for the gate/up GEMM when the batch averages at
- * least 64 token slots per expert, holds at most 1024 slots in all or at most 16
- * per expert, or H <= 1024,
- * and 0 otherwise; for the down projection 1 when the batch holds at most 8 slots
- * and H > 1024 (one decode token of a wide layer) or averages at least 64 slots
- * per expert with F >= 2048, else 0.  Both
- * walk every element's reduction in the same order and give the same bits
- * (tested), so the choice never changes an output. */
+ * tokens on the N side (any multiple of 16 tokens, on a CTA pair, in units of
+ * at most 64 tokens for batches of at most 1024 slots or 16 per expert, 128 for
+ * at most 64 per expert, else 320); 2 (default) takes 1 for the gate/up GEMM,
+ * and for the down projection 1 when the batch holds at most 8 slots and
+ * H > 1024 (one decode token of a wide layer) or, with F >= 2048, averages at
+ * most 64 or at least 256 slots per expert, else 0.  Both walk every element's
+ * reduction in the same order and give the same bits (tested), so the choice
+ * never changes an output. */
 int invmoe_expert_engine(int which);
 
 /* Launch a one-CTA kernel that waits on an mbarrier nothing ever completes,

@@ -382,22 +382,23 @@ int moe_grouped_ffn(const void* xp, const int32_t* plan, const void* w13, const 
   unsigned int* status = status_word(workspace);
 
   // Engines (same bits either way): tokens on the MMA's M side in row tiles, or on its N side.
-  // Measured on GB300 (gate/up GEMM, token columns vs row tiles): GLM-scale layer, 256 tokens per
-  // expert on average, 2.55 vs 2.72 ms (the token columns stream each expert's weights once where
-  // the row tiles stream them again for an expert's last few rows); Qwen-like layer 0.221 vs
-  // 0.226 ms; decode batches of up to 1024 token slots or 16 per expert, which run the token
-  // columns' decode form (64-token units, a ring twice as deep): GLM-scale 1 request 79 vs 113 us,
-  // 16 to 512 requests 4-10 % faster, Qwen-like 8 to 256 requests 3-18 % faster; tiny layer
-  // (H = 256) 15 vs 20 us.  From 32 to 64 slots per expert the row tiles are as fast or faster
-  // (Qwen-like 512 requests 149 vs 149 us, 1024 requests 157 vs 185 us).  The
-  // down projection runs in token columns for a GLM-scale batch of one (48 vs 57 us) and for
-  // prefill-sized batches whose reduction is at least 32 K blocks long (GLM-scale layer, F = 2048:
-  // 1.43 vs 1.48 ms); with short reductions its epilogue weighs more than the tails it removes
-  // (Qwen-like layer, F = 768: 0.149 vs 0.131 ms; tiny 14.1 vs 12.1 us; 8 GLM-scale requests 250 vs
-  // 232 us).  The automatic choice follows that.
+  // Measured on GB300 (same process, best of two; gate/up and down GEMM, token columns in the unit
+  // size the batch takes vs row tiles), by token slots per expert on average:
+  //   GLM-scale layer (H = 6144, F = 2048):   16: 1873 / 971 vs 1983 / 978 us;  32: 1902 / 990 vs
+  //     2006 / 998;  64: 1976 / 1021 vs 1990 / 1029;  128: 2157 / 1192 vs 2113 / 1118;
+  //     192: 2249 / 1291 vs 2267 / 1249;  256: 2595 / 1522 vs 2969 / 1610 (the row tiles stream an
+  //     expert's weights again for its last few rows beyond 256);
+  //   Qwen-like layer (H = 2048, F = 768, Zipf-skewed):  16: 138 / 85 vs 146 / 72;  32: 141 / 87 vs
+  //     149 / 76;  64: 151 / 99 vs 158 / 80;  128: 170 / 113 vs 173 / 93;  256: 208 / 153 vs 225 / 131;
+  //   one GLM-scale token 79 / 48 vs 113 / 57 us; tiny layer (H = 256) 15 / 14 vs 20 / 12 us.
+  // So the gate/up GEMM always runs in token columns, and the down projection (whose fp32 epilogue
+  // weighs more) in token columns for one wide decode token and, with a reduction of at least 32 K
+  // blocks (F >= 2048), up to 64 slots per expert and from 256.
   const int eng = expert_engine();
-  const bool tok1 = eng == 1 || (eng == 2 && (S >= 64LL * E || S <= 1024 || S <= 16LL * E || H <= 1024));
-  const bool tok2 = H % 256 == 0 && (eng == 1 || (eng == 2 && ((S <= 8 && H > 1024) || (S >= 64LL * E && F >= 2048))));
+  const bool tok1 = eng != 0;
+  const bool tok2 = H % 256 == 0 &&
+                    (eng == 1 || (eng == 2 && ((S <= 8 && H > 1024) ||
+                                               (F >= 2048 && (S <= 64LL * E || S >= 256LL * E)))));
   GemmCall g1{};
   g1.name = "expert_gemm1_swiglu";
   g1.variant = tok1 ? GV_TOK_SWIGLU : GV_SWIGLU_BN256_MT2;

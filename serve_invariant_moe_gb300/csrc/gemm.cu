@@ -235,7 +235,7 @@ int launch_pair(const GemmCall& c, cudaStream_t st) {
 }
 
 // Token-column engine (grouped only): clusters of 2, grid = 2 x min(units, SMs / 2).
-// Weights [G * b_group_rows, K] in 64-row boxes, tokens [rows, K] in 32-row boxes.
+// Weights [G * b_group_rows, K] in 64-row boxes, tokens [rows, K] in 32-, 64-, 128- or 160-row boxes.
 template <int EPI, int STAGES, int CHUNK>
 int launch_tok(const GemmCall& c, cudaStream_t st) {
   using S = TokShape<EPI, STAGES, CHUNK>;
@@ -244,12 +244,17 @@ int launch_tok(const GemmCall& c, cudaStream_t st) {
   const int wb_cols = EPI == EPI_SWIGLU ? 128 : 256;
   if (c.N % wb_cols != 0)
     return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "N=%d is not a multiple of %d", c.N, wb_cols);
-  CUtensorMap tw, tx, txb;
+  CUtensorMap tw, tx, txm, txb, txt;
   int rc = EPI == EPI_SWIGLU ? make_tmap_gate_up(&tw, c.B, c.K, c.b_up_rows, c.b_rows / c.b_group_rows)
                              : make_tmap(&tw, c.B, c.K, c.b_rows, 128);
   if (rc) return rc;
   if ((rc = make_tmap(&tx, c.A, c.K, c.a_rows, kTokBoxRows))) return rc;
-  if ((rc = make_tmap(&txb, c.A, c.K, c.a_rows, kTokBigRows))) return rc;
+  txm = txb = txt = tx;         // the 64-token form loads 32-row boxes only, the 128-token form 32 or 64
+  if (CHUNK >= 128 && (rc = make_tmap(&txm, c.A, c.K, c.a_rows, kTokMidRows))) return rc;
+  if (CHUNK == kTokChunk) {
+    if ((rc = make_tmap(&txb, c.A, c.K, c.a_rows, kTokBigRows))) return rc;
+    if ((rc = make_tmap(&txt, c.A, c.K, c.a_rows, kTokTwoRows))) return rc;
+  }
   static std::atomic<uint64_t> attr_set{0};
   if ((rc = set_smem_attr(reinterpret_cast<const void*>(tc_gemm_tok_kernel<EPI, STAGES, CHUNK>), S::SMEM_BYTES, attr_set)))
     return rc;
@@ -269,7 +274,7 @@ int launch_tok(const GemmCall& c, cudaStream_t st) {
   // launch's last producer resets it (sched_release)
   ProfScope prof(c.name ? c.name : "tc_gemm_tok", st);
   return check_cuda(launch_kernel_ex(tc_gemm_tok_kernel<EPI, STAGES, CHUNK>, dim3(static_cast<unsigned>(2 * pairs)),
-                                     dim3(S::THREADS), S::SMEM_BYTES, st, attr, 1, tw, tx, txb, p),
+                                     dim3(S::THREADS), S::SMEM_BYTES, st, attr, 1, tw, tx, txm, txb, txt, p),
                     "tc_gemm_tok_kernel launch");
 }
 
@@ -301,14 +306,17 @@ int gemm_run(const GemmCall& c, cudaStream_t st) {
     case GV_SWIGLU_BWD_BN256_MT2: return launch<256, 2, EPI_SWIGLU_BWD, 3>(c, st);
     case GV_F32_BN256_MT1_KGROUP: return launch<256, 1, EPI_F32, 4, true, true, true>(c, st);
     case GV_PAIR_SWIGLU_BWD: return launch_pair<EPI_SWIGLU_BWD, 6>(c, st);
-    // decode batches (at most 1024 token slots, or at most 16 per expert on average): 64-token
-    // units (an expert with more tokens takes several), a 32-row token tile, a ring twice as deep
+    // units by batch size (an expert with more tokens than a unit takes several): decode batches
+    // (at most 1024 token slots, or at most 16 per expert on average) 64 tokens, a 32-row token
+    // tile, a ring twice as deep; at most 64 slots per expert 128 tokens, a 64-row tile, 8 stages
     case GV_TOK_SWIGLU:
-      return c.a_rows <= 1024 || c.a_rows <= 16LL * c.G ? launch_tok<EPI_SWIGLU, 10, 64>(c, st)
-                                                         : launch_tok<EPI_SWIGLU, 5, kTokChunk>(c, st);
+      if (c.a_rows <= 1024 || c.a_rows <= 16LL * c.G) return launch_tok<EPI_SWIGLU, 10, 64>(c, st);
+      if (c.a_rows <= 64LL * c.G) return launch_tok<EPI_SWIGLU, 8, 128>(c, st);
+      return launch_tok<EPI_SWIGLU, 5, kTokChunk>(c, st);
     case GV_TOK_F32:
-      return c.a_rows <= 1024 || c.a_rows <= 16LL * c.G ? launch_tok<EPI_F32, 10, 64>(c, st)
-                                                         : launch_tok<EPI_F32, 5, kTokChunk>(c, st);
+      if (c.a_rows <= 1024 || c.a_rows <= 16LL * c.G) return launch_tok<EPI_F32, 10, 64>(c, st);
+      if (c.a_rows <= 64LL * c.G) return launch_tok<EPI_F32, 8, 128>(c, st);
+      return launch_tok<EPI_F32, 5, kTokChunk>(c, st);
   }
   return set_error(INVMOE_ERR_INVALID_ARG, "unknown GEMM variant %d", (int)c.variant);
 }

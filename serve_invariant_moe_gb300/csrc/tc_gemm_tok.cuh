@@ -19,22 +19,26 @@
 // this engine's outputs with the row-tile engines' bit for bit).
 //
 //   * CTA r loads its 128 weight rows of the block and its half of the token
-//     rows: MMA 1 covers tokens [0, N1) with CTA r holding [r*N1/2, (r+1)*N1/2),
-//     MMA 2 (when the chunk has more than 256 tokens) tokens [256, 256 + N2)
-//     split the same way.  One stage is one TMA box of weights (SwiGLU: a
-//     rank-5 box, below; fp32: 128 rows), one or two 32-row token boxes or one
-//     128-row box for MMA 1, and one 32-row box for MMA 2: at this size the
-//     producer thread's copy issue, not the bytes, set the pace, so a stage
-//     takes as few copies as it can (rows past the chunk are read from L2 and
-//     never stored).  SwiGLU: the CTA's h columns are [f0, f0 + 64),
+//     rows, each as one TMA box per stage (at this size the producer thread's
+//     copy issue, not the bytes, sets the pace; rows past the chunk are read
+//     from L2 and never stored).  A chunk of at most 256 tokens is one MMA of
+//     N1 columns, CTA r holding tokens [r*N1/2, (r+1)*N1/2) in a 32-, 64- or
+//     128-row box.  A longer chunk adds a second MMA of N2 columns, and CTA 0
+//     holds tokens [0, 128 + N2/2), CTA 1 the next 128 + N2/2, each in one
+//     160-row box whose rows [0, 128) feed MMA 1 and rows [128, 128 + N2/2)
+//     MMA 2; the epilogue maps the columns back to tokens (MMA 1 column j >= 128
+//     is token j + N2/2, MMA 2 column j is token 128 + j below N2/2, else
+//     256 + j).  SwiGLU: the CTA's h columns are [f0, f0 + 64),
 //     f0 = 128 * block + 64 * r, and its weight rows arrive as 4 groups of 16
 //     gate rows and the matching 16 up rows: tile rows 32i + [0, 16) are the
 //     gate rows of h columns f0 + 16i + [0, 16), tile rows 32i + [16, 32) the
 //     up rows, so the warp on TMEM lanes 32i holds both halves of its 16 SwiGLU
 //     pairs and exchanges them with one shuffle.
-//   * A batch of at most 1024 token slots or 16 per expert (decode) runs the
-//     same kernel with units of at most 64 tokens (an expert with more takes
-//     several): a 32-row token tile per CTA, 20 KB stages, a ring twice as deep.
+//   * Smaller batches run the same kernel with smaller units (an expert with
+//     more tokens takes several): at most 1024 token slots or 16 per expert
+//     (decode), units of at most 64 tokens, a 32-row token tile per CTA, 20 KB
+//     stages and a ring twice as deep; at most 64 slots per expert, units of at
+//     most 128 tokens, a 64-row tile, 24 KB stages, 8 of them.
 //   * TMEM: lane = weight row, one column per token.  Consecutive units of a CTA
 //     alternate between two placements: slot 0 puts MMA 1 at column 0 and MMA 2
 //     at column 256 (columns [0, 320)), slot 1 puts MMA 1 at column 256 and
@@ -70,20 +74,22 @@ __device__ __forceinline__ void tma_load_5d_pair(void* dst, const CUtensorMap* m
 }
 
 constexpr int kTokChunk = 320;     // most tokens (TMEM columns) of one unit
-constexpr int kTokBoxRows = 32;    // token rows per small TMA box
-constexpr int kTokBigRows = 128;   // token rows per large TMA box (a CTA's whole MMA-1 share)
+constexpr int kTokBoxRows = 32;    // token rows per TMA box: 32, 64 or 128 (a CTA's share of one MMA) ...
+constexpr int kTokMidRows = 64;
+constexpr int kTokBigRows = 128;
+constexpr int kTokTwoRows = 160;   // ... or 160 (its share of both MMAs of a chunk of more than 256 tokens)
 
 // CHUNK: most tokens of one unit.  kTokChunk for prefill-sized batches; 64 for batches of at most
-// 1024 token slots or 16 per expert (decode), where a CTA's token tile is one 32-row box and the
-// stages are small enough for twice the ring depth.
+// 1024 token slots or 16 per expert (decode) and 128 for at most 64 per expert, where a CTA's
+// token tile is one 32- or 64-row box and the stages are small enough for a deeper ring.
 template <int EPI, int STAGES, int CHUNK = kTokChunk>
 struct TokShape {
-  static_assert(CHUNK == kTokChunk || CHUNK == 64, "unit size");
+  static_assert(CHUNK == kTokChunk || CHUNK == 64 || CHUNK == 128, "unit size");
   static constexpr int A_BYTES = kBM * kBK * 2;                   // 16 KB: 128 weight rows x 64 K
-  // token rows per CTA: MMA 1 (half of up to 256) + MMA 2 (half of up to 64), or half of 64
-  static constexpr int B_ROWS = CHUNK == kTokChunk ? 128 + 32 : 32;
-  static constexpr int B_BYTES = B_ROWS * kBK * 2;                // 20 KB
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;           // 36 KB (1 KB multiple)
+  // token rows per CTA: MMA 1 (half of up to 256) + MMA 2 (half of up to 64), or half of the unit
+  static constexpr int B_ROWS = CHUNK == kTokChunk ? 128 + 32 : CHUNK / 2;
+  static constexpr int B_BYTES = B_ROWS * kBK * 2;                // 20 KB (4 or 8 KB)
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;           // 36 KB (20 or 24 KB; 1 KB multiples)
   static constexpr int TMEM_COLS = 512;
   static constexpr int EPI_WARPS = 8;
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
@@ -156,7 +162,8 @@ __device__ __forceinline__ int tok_phase_chunk(int slot, int ph, int nchunk, int
 template <int EPI, int STAGES, int CHUNK>
 __global__ void __launch_bounds__(TokShape<EPI, STAGES, CHUNK>::THREADS, 1)
     tc_gemm_tok_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                       const __grid_constant__ CUtensorMap tmXb, const GemmParams p) {
+                       const __grid_constant__ CUtensorMap tmXm, const __grid_constant__ CUtensorMap tmXb,
+                       const __grid_constant__ CUtensorMap tmXt, const GemmParams p) {
   using S = TokShape<EPI, STAGES, CHUNK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -205,7 +212,11 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES, CHUNK>::THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
-    tma_prefetch_desc(&tmXb);
+    if (CHUNK >= 128) tma_prefetch_desc(&tmXm);
+    if (CHUNK == kTokChunk) {
+      tma_prefetch_desc(&tmXb);
+      tma_prefetch_desc(&tmXt);
+    }
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, S::TMEM_COLS);
   // everything above touches only shared memory, TMEM and the kernel parameters; the
@@ -290,18 +301,25 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES, CHUNK>::THREADS, 1)
         const int nmma = (U.nv + 15) & ~15;
         const int n1 = nmma < 256 ? nmma : 256;
         const int r1 = n1 / 2, r2 = (nmma - n1) / 2;
-        // MMA 1's token rows of this CTA: up to two small boxes, else one large box (rows past
-        // the chunk are read from L2 and never stored); MMA 2's: one small box
-        const int nb1 = (r1 + kTokBoxRows - 1) / kTokBoxRows;
-        const bool big1 = S::B_ROWS >= kTokBigRows && nb1 > 2;
-        const uint32_t bytes = S::A_BYTES + (big1 ? kTokBigRows : nb1 * kTokBoxRows) * (kBK * 2) +
-                               (r2 > 0 ? kTokBoxRows * kBK * 2 : 0);
+        // this CTA's token rows, one box: its share of MMA 1 alone in the smallest box that
+        // holds it, or its shares of both MMAs in one 160-row box (CTA 0 tokens [0, 128 + r2),
+        // CTA 1 the next 128 + r2)
+        int box_rows = kTokBoxRows;
+        const CUtensorMap* tmT = &tmX;
+        if (CHUNK == kTokChunk) {
+          if (r2 > 0) { box_rows = kTokTwoRows; tmT = &tmXt; }
+          else if (r1 > kTokMidRows) { box_rows = kTokBigRows; tmT = &tmXb; }
+          else if (r1 > kTokBoxRows) { box_rows = kTokMidRows; tmT = &tmXm; }
+        } else if (CHUNK == 128 && r1 > kTokBoxRows) {
+          box_rows = kTokMidRows;
+          tmT = &tmXm;
+        }
+        const uint32_t bytes = S::A_BYTES + box_rows * (kBK * 2);
         // this CTA's weight rows: SwiGLU h columns [f0, f0 + 64), f0 = 128 wb + 64r (gate rows f0.., up
         // rows F + f0..); fp32 rows [256 wb + 128r, +128)
         const int f0 = U.wb * 128 + 64 * static_cast<int>(rank);
         const int wrow = U.g * p.b_group_rows + U.wb * 256 + 128 * static_cast<int>(rank);
-        const int t1 = U.tok0 + static_cast<int>(rank) * r1;
-        const int t2 = U.tok0 + n1 + static_cast<int>(rank) * r2;
+        const int t1 = U.tok0 + static_cast<int>(rank) * (r1 + r2);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wc)) { ok = false; break; }
           uint8_t* st = ring + stage * S::STAGE_BYTES;
@@ -314,14 +332,7 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES, CHUNK>::THREADS, 1)
           } else {
             tma_load_2d_pair(st, &tmW, fb, kb * kBK, wrow);
           }
-          uint8_t* bst = st + S::A_BYTES;
-          if (big1) {
-            tma_load_2d_pair(bst, &tmXb, fb, kb * kBK, t1);
-          } else {
-            for (int i = 0; i < nb1; ++i)
-              tma_load_2d_pair(bst + i * (kTokBoxRows * kBK * 2), &tmX, fb, kb * kBK, t1 + i * kTokBoxRows);
-          }
-          if (r2 > 0) tma_load_2d_pair(bst + 128 * kBK * 2, &tmX, fb, kb * kBK, t2);
+          tma_load_2d_pair(st + S::A_BYTES, tmT, fb, kb * kBK, t1);
           filled_phase[stage] = static_cast<int>(phase);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -429,10 +440,18 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES, CHUNK>::THREADS, 1)
       ++nunit;
       tc_fence_after();
       const int nchunk = (U.nv + 31) / 32;
+      // half of the second MMA's width (0: none); the token of row r of chunk c (columns
+      // 32c + r of MMA 1 for c < 8, 32(c - 8) + r of MMA 2 after; the loader's split above)
+      const int h2 = max(0, ((U.nv + 15) & ~15) - 256) / 2;
+      auto tok_of = [&](int c, int r) -> int {
+        const int j = 32 * (c & 7) + r;
+        if (h2 == 0) return 32 * c + r;
+        if (c < 8) return j < 128 ? j : j + h2;
+        return j < h2 ? 128 + j : 256 + j;
+      };
 
       // one 32-token chunk c held in v (this thread's lane, 32 consecutive columns)
       auto store_chunk = [&](int c, const uint32_t (&v)[32]) {
-        const int rows_valid = U.nv - c * 32;
         if (EPI == EPI_SWIGLU) {
           // lanes 0-15 hold gate rows, lanes 16-31 the matching up rows of h columns
           // [fq, fq + 16): a lane computes h for its column and 16 of the 32 tokens
@@ -456,9 +475,10 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES, CHUNK>::THREADS, 1)
             const int m = lane + 32 * i;
             const int r = m >> 1;
             const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 32 + (r >= 16 ? 32 : 0) + (m & 1) * 16);
-            if (r < rows_valid)
+            const int t = tok_of(c, r);
+            if (t < U.nv)
               *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                        static_cast<long long>(U.tok0 + c * 32 + r) * p.ldo + fq + (m & 1) * 8) = w;
+                                        static_cast<long long>(U.tok0 + t) * p.ldo + fq + (m & 1) * 8) = w;
           }
           __syncwarp();
         } else {
@@ -470,16 +490,15 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES, CHUNK>::THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j) ys[j * 32 + lane] = __uint_as_float(v[16 * hh + j]);
             __syncwarp();
-            const int rv = rows_valid - 16 * hh;
             const int ch = lane & 7;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int r = 4 * i + (lane >> 3);
               const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 128 + ch * 16);
-              if (r < rv)
+              const int t = tok_of(c, 16 * hh + r);
+              if (t < U.nv)
                 *reinterpret_cast<uint4*>(static_cast<float*>(p.out) +
-                                          static_cast<long long>(U.tok0 + c * 32 + 16 * hh + r) * p.ldo + h0 +
-                                          ch * 4) = w;
+                                          static_cast<long long>(U.tok0 + t) * p.ldo + h0 + ch * 4) = w;
             }
             __syncwarp();
           }

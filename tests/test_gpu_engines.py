@@ -2,8 +2,8 @@
 
 moe_grouped_ffn runs the routed experts' two GEMMs either with each expert's tokens on the MMA's
 M side in 128-row tiles (the row-tile engine) or with its weights on the M side and its tokens on
-the N side (the token-column engine; by default it runs the gate/up GEMM of prefill-sized
-batches, of batches of at most 64 token slots and of layers with H <= 1024).  Every element is the same K-ascending chain of
+the N side (the token-column engine, in 64-, 128- or 320-token units by batch size; by default it
+runs every gate/up GEMM and some down projections).  Every element is the same K-ascending chain of
 bf16 products accumulated in fp32 either way ("位级一致：前沿训练的差异化关键", section
 "为什么比特级一致是一个复杂的问题": one fixed reduction order per element whatever the token
 count), so h, Y and the layer output must match bit for bit: on layers with empty experts, experts
@@ -71,6 +71,10 @@ SMALL = [
     # up to 1024 slots run the decode form too: experts of more than 64 tokens take several units
     dataclasses.replace(synth.TINY, name="decode_form_multi_unit", T=480, H=1024, E=8, k=2, F=256,
                         dup_router_rows=False, zipf_s=1.1, zipf_alpha=1.5, seed=67),
+    # at most 64 slots per expert on average (128-token units, a 32- or 64-row token tile per CTA):
+    # empty experts, experts of up to 32, 33-64 and 65-128 tokens, and experts of several units
+    dataclasses.replace(synth.TINY, name="unit128_form", T=600, H=512, E=64, k=4, F=256,
+                        dup_router_rows=False, zipf_s=1.1, zipf_alpha=0.4, seed=69),
 ]
 
 
@@ -84,14 +88,24 @@ def test_engines_bit_identical_small(cfg):
         assert counts.max() == 64                              # one expert fills a whole 64-token unit
     if cfg.name == "decode_form_multi_unit":
         assert counts.max() > 128                              # three or more 64-token units
+    if cfg.name == "unit128_form":
+        S, E = cfg.T * cfg.k, cfg.E
+        assert 16 * E < S <= 64 * E                            # the batch takes the 128-token units
+        assert (counts == 0).any() and ((counts > 32) & (counts <= 64)).any()
+        assert ((counts > 64) & (counts <= 128)).any() and counts.max() > 256
     for key in ("h", "y", "out"):
         assert torch.equal(_bits(r[0][key]), _bits(r[1][key])), f"{cfg.name}: {key} differs between the engines"
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["glm_scale_moe", "qwen_moe_like_empty"])
-def test_engines_bit_identical_full_size(name):
+@pytest.mark.parametrize("name,T", [("glm_scale_moe", None), ("qwen_moe_like_empty", None),
+                                    ("glm_scale_moe", 1024), ("qwen_moe_like_empty", 1024)])
+def test_engines_bit_identical_full_size(name, T):
+    # at the configurations' own batch sizes the token columns run 320-token units; at 1024 tokens
+    # (32 and 64 slots per expert) 128-token units
     cfg = synth.CONFIGS[name]
+    if T is not None:
+        cfg = dataclasses.replace(cfg, T=T)
     r = _both_engines(cfg, expert_device="cuda")
     for key in ("h", "y", "out"):
         assert torch.equal(_bits(r[0][key]), _bits(r[1][key])), f"{name}: {key} differs between the engines"

@@ -4,8 +4,8 @@ Every output buffer is filled with a NaN bit pattern that no kernel computes (fi
 finite results), with guard rows past the region a call may write.  After the call, the region it
 owns must hold no poison (every element written) and the guard rows must hold nothing else (no
 store past the end).  Covered: the routing's permuted rows, both engines of the grouped expert GEMMs
-(the token-column engine's 64-token decode form, several-chunk experts and empty experts
-included), and the decode buffers, of which a call on fewer requests than they were sized for owns
+(the token-column engine's 64- and 128-token unit forms, several-chunk experts and empty
+experts included), and the decode buffers, of which a call on fewer requests than they were sized for owns
 only the leading rows."""
 import dataclasses
 
@@ -55,6 +55,10 @@ CFGS = [
     # the decode form with experts of more than 64 tokens (several 64-token units each)
     dataclasses.replace(synth.TINY, name="decode_form_multi_unit", T=300, H=512, E=8, k=2, F=256,
                         dup_router_rows=False, seed=76),
+    # the 128-token units (at most 64 slots per expert on average), skewed: empty experts, experts
+    # of 33-64 and 65-128 tokens, experts of several units
+    dataclasses.replace(synth.TINY, name="unit128_form", T=600, H=512, E=64, k=4, F=256,
+                        dup_router_rows=False, zipf_s=1.1, zipf_alpha=0.4, seed=69),
 ]
 
 
