@@ -109,3 +109,53 @@ def test_engines_bit_identical_full_size(name, T):
     r = _both_engines(cfg, expert_device="cuda")
     for key in ("h", "y", "out"):
         assert torch.equal(_bits(r[0][key]), _bits(r[1][key])), f"{name}: {key} differs between the engines"
+
+
+# Per-expert token counts fixed through router replay (k = 1), one list per unit form of the token
+# columns: every chunk width where a CTA's token rows change box or split.
+#   320-token units (more than 64 slots per expert on average): chunks of 257-320 tokens take a
+#   second MMA of 16, 32, 48 or 64 columns and one 160-row box per CTA; 321 splits into two chunks.
+#   128-token units (at most 64 per expert): a CTA's share of up to 32 rows in a 32-row box, of 33-64
+#   rows in a 64-row box; experts of more than 128 tokens split into near-equal chunks.
+#   64-token units (at most 1024 slots): one 32-row box; experts of more than 64 tokens split.
+EXACT_COUNTS = {
+    "units320": (16, [0, 1, 15, 16, 17, 255, 256, 257, 272, 273, 288, 289, 304, 305, 320, 321]),
+    "units128": (64, [0, 1, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257] + [0] * 50),
+    "units64": (16, [0, 1, 15, 16, 17, 31, 32, 33, 63, 64, 65, 129, 0, 0, 0, 0]),
+}
+
+
+@pytest.mark.parametrize("form", sorted(EXACT_COUNTS))
+def test_engines_bit_identical_exact_chunk_widths(form):
+    from serve_invariant_moe_gb300 import _lib, api
+    lib = _lib.lib()
+    E, counts = EXACT_COUNTS[form]
+    T = sum(counts)
+    # the batch takes the intended unit form (same thresholds as the library's dispatch)
+    if form == "units320":
+        assert T > 64 * E
+    elif form == "units128":
+        assert 16 * E < T <= 64 * E and T > 1024
+    else:
+        assert T <= 1024
+    cfg = dataclasses.replace(synth.TINY, name=f"exact_{form}", T=T, H=256, E=E, k=1, F=256,
+                              dup_router_rows=False, seed=80)
+    x, wr = synth.moe_activations(cfg)
+    w13, w2 = synth.expert_weights(cfg, "cuda")
+    experts = torch.repeat_interleave(torch.arange(E), torch.tensor(counts))
+    perm = torch.randperm(T, generator=torch.Generator().manual_seed(81))
+    replay = experts[perm].to(torch.int32).view(T, 1).cuda()
+    layer = api.MoELayer(api.MoEWeights(wr.cuda(), w13, w2, 1))
+    out = {}
+    try:
+        for eng in (0, 1):
+            assert lib.invmoe_expert_engine(eng) == 0
+            r = layer.prefill(x.cuda(), return_all=True, replay_idx=replay)
+            torch.cuda.synchronize()
+            out[eng] = dict(h=r["h"][:T].clone(), y=r["y"][:T].clone(), out=r["out"].clone(),
+                            counts=r["plan"][:E].cpu())
+    finally:
+        lib.invmoe_expert_engine(2)
+    assert out[1]["counts"].tolist() == counts
+    for key in ("h", "y", "out"):
+        assert torch.equal(_bits(out[0][key]), _bits(out[1][key])), f"{form}: {key} differs between the engines"

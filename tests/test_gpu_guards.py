@@ -109,3 +109,35 @@ def test_decode_on_fewer_requests_writes_only_their_rows():
         torch.cuda.synchronize()
         for key, rows in (("xp", B * cfg.k), ("h", B * cfg.k), ("y", B * cfg.k), ("ys", B), ("out", B)):
             _check(f"{key} (B={B})", d[key], rows)
+
+
+def test_expert_gemms_write_exactly_their_rows_at_exact_chunk_widths():
+    # per-expert counts fixed through router replay (k = 1): chunks of 257-320 tokens (a second MMA
+    # of each width, one 160-row token box per CTA of the pair) and a 321-token expert split in two
+    from serve_invariant_moe_gb300 import _lib, binding
+    lib = _lib.lib()
+    counts = [0, 1, 15, 16, 17, 255, 256, 257, 272, 273, 288, 289, 304, 305, 320, 321]
+    E, T = len(counts), sum(counts)
+    cfg = dataclasses.replace(synth.TINY, name="guard_exact", T=T, H=256, E=E, k=1, F=256,
+                              dup_router_rows=False, seed=77)
+    x, wr = synth.moe_activations(cfg)
+    w13, w2 = synth.expert_weights(cfg, "cuda")
+    experts = torch.repeat_interleave(torch.arange(E), torch.tensor(counts))
+    perm = torch.randperm(T, generator=torch.Generator().manual_seed(78))
+    replay = experts[perm].to(torch.int32).view(T, 1).cuda()
+    ws = binding.new_workspace(binding.workspace_size(T, cfg.H, E, 1, cfg.F, 0, 0))
+    r = binding.moe_route_replay(x.cuda(), wr.cuda(), replay, ws)
+    torch.cuda.synchronize()
+    assert r["plan"][:E].cpu().tolist() == counts
+    try:
+        for eng in (0, 1):
+            assert lib.invmoe_expert_engine(eng) == 0
+            h = _poisoned(T + GUARD, cfg.F, torch.bfloat16)
+            y = _poisoned(T + GUARD, cfg.H, torch.float32)
+            binding.moe_grouped_ffn(r["xp"], r["plan"], w13, w2, T, 1, ws, h=h, y=y)
+            torch.cuda.synchronize()
+            binding.check_status(ws)
+            _check(f"h (engine {eng})", h, T)
+            _check(f"y (engine {eng})", y, T)
+    finally:
+        lib.invmoe_expert_engine(2)
