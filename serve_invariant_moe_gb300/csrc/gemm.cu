@@ -308,13 +308,14 @@ int gemm_run(const GemmCall& c, cudaStream_t st) {
     case GV_PAIR_SWIGLU_BWD: return launch_pair<EPI_SWIGLU_BWD, 6>(c, st);
     // units by batch size (an expert with more tokens than a unit takes several): decode batches
     // (at most 1024 token slots, or at most 16 per expert on average) 64 tokens, a 32-row token
-    // tile, a ring twice as deep; at most 64 slots per expert 128 tokens, a 64-row tile, 8 stages
+    // tile, 5 stages of two K blocks; at most 64 slots per expert 128 tokens, a 64-row tile,
+    // 4 stages of two K blocks (SwiGLU) or 8 of one (fp32)
     case GV_TOK_SWIGLU:
-      if (c.a_rows <= 1024 || c.a_rows <= 16LL * c.G) return launch_tok<EPI_SWIGLU, 10, 64>(c, st);
-      if (c.a_rows <= 64LL * c.G) return launch_tok<EPI_SWIGLU, 8, 128>(c, st);
+      if (c.a_rows <= 1024 || c.a_rows <= 16LL * c.G) return launch_tok<EPI_SWIGLU, 5, 64>(c, st);
+      if (c.a_rows <= 64LL * c.G) return launch_tok<EPI_SWIGLU, 4, 128>(c, st);
       return launch_tok<EPI_SWIGLU, 5, kTokChunk>(c, st);
     case GV_TOK_F32:
-      if (c.a_rows <= 1024 || c.a_rows <= 16LL * c.G) return launch_tok<EPI_F32, 10, 64>(c, st);
+      if (c.a_rows <= 1024 || c.a_rows <= 16LL * c.G) return launch_tok<EPI_F32, 5, 64>(c, st);
       if (c.a_rows <= 64LL * c.G) return launch_tok<EPI_F32, 8, 128>(c, st);
       return launch_tok<EPI_F32, 5, kTokChunk>(c, st);
   }

@@ -37,8 +37,9 @@
 //   * Smaller batches run the same kernel with smaller units (an expert with
 //     more tokens takes several): at most 1024 token slots or 16 per expert
 //     (decode), units of at most 64 tokens, a 32-row token tile per CTA, 20 KB
-//     stages and a ring twice as deep; at most 64 slots per expert, units of at
-//     most 128 tokens, a 64-row tile, 24 KB stages, 8 of them.
+//     per K block and a ring of 5 stages of two K blocks each; at most 64 slots
+//     per expert, units of at most 128 tokens, a 64-row tile, 24 KB per K block
+//     (SwiGLU: 4 stages of two K blocks; fp32: 8 stages of one).
 //   * TMEM: lane = weight row, one column per token.  Consecutive units of a CTA
 //     alternate between two placements: slot 0 puts MMA 1 at column 0 and MMA 2
 //     at column 256 (columns [0, 320)), slot 1 puts MMA 1 at column 256 and
@@ -98,7 +99,11 @@ struct TokShape {
   // token rows per CTA: MMA 1 (half of up to 256) + MMA 2 (half of up to 64), or half of the unit
   static constexpr int B_ROWS = CHUNK == kTokChunk ? 128 + 32 : CHUNK / 2;
   static constexpr int B_BYTES = B_ROWS * kBK * 2;                // 20 KB (4 or 8 KB)
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;           // 36 KB (20 or 24 KB; 1 KB multiples)
+  // 64-wide K blocks per ring stage: two for the 64-token units and the 128-token SwiGLU units
+  // (measured faster there; one stage then holds both blocks' weights and tokens, one after the other)
+  static constexpr int KSUB = (CHUNK == 64 || (CHUNK == 128 && EPI == EPI_SWIGLU)) ? 2 : 1;
+  static constexpr int SUB_BYTES = A_BYTES + B_BYTES;             // 36 KB (20 or 24 KB; 1 KB multiples)
+  static constexpr int STAGE_BYTES = KSUB * SUB_BYTES;
   static constexpr int TMEM_COLS = 512;
   static constexpr int EPI_WARPS = 8;
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
@@ -267,7 +272,8 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES, CHUNK>::THREADS, 1)
 
   const uint32_t tmem_base = *tmem_slot;
   const int total_units = *s_total * p.n_blocks;
-  const int num_kb = (p.K + kBK - 1) / kBK;
+  const int num_kb = (p.K + kBK - 1) / kBK;                      // 64-wide K blocks
+  const int num_st = (num_kb + S::KSUB - 1) / S::KSUB;             // ring stages per unit
   WaitCtl wc{s_abort, p.status, p.timeout_ns};
   const uint32_t peer_abort = mapa_shared(smem_u32(const_cast<int*>(s_abort)), peer);
   const uint32_t qempty_leader0 = mapa_shared(smem_u32(&qempty_bar[0]), 0);
@@ -329,19 +335,24 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES, CHUNK>::THREADS, 1)
         const int f0 = U.wb * 128 + 64 * static_cast<int>(rank);
         const int wrow = U.g * p.b_group_rows + U.wb * 256 + 128 * static_cast<int>(rank);
         const int t1 = U.tok0 + static_cast<int>(rank) * (r1 + r2);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int ks = 0; ks < num_st; ++ks) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, wc)) { ok = false; break; }
           uint8_t* st = ring + stage * S::STAGE_BYTES;
           const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
-          if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * bytes);
-          if (EPI == EPI_SWIGLU) {
-            // one box of 4 row groups x (16 gate rows, the matching 16 up rows): tile rows
-            // 32i + [0, 16) are gate rows f0 + 16i + [0, 16), 32i + [16, 32) the up rows
-            tma_load_5d_pair(st, &tmW, fb, kb * kBK, 0, 0, f0 / 16, U.g);
-          } else {
-            tma_load_2d_pair(st, &tmW, fb, kb * kBK, wrow);
+          const int nsub = min(S::KSUB, num_kb - ks * S::KSUB);    // K blocks in this stage
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * nsub * bytes);
+          for (int j = 0; j < nsub; ++j) {
+            uint8_t* sj = st + j * S::SUB_BYTES;
+            const int kx = (ks * S::KSUB + j) * kBK;
+            if (EPI == EPI_SWIGLU) {
+              // one box of 4 row groups x (16 gate rows, the matching 16 up rows): tile rows
+              // 32i + [0, 16) are gate rows f0 + 16i + [0, 16), 32i + [16, 32) the up rows
+              tma_load_5d_pair(sj, &tmW, fb, kx, 0, 0, f0 / 16, U.g);
+            } else {
+              tma_load_2d_pair(sj, &tmW, fb, kx, wrow);
+            }
+            tma_load_2d_pair(sj + S::A_BYTES, tmT, fb, kx, t1);
           }
-          tma_load_2d_pair(st + S::A_BYTES, tmT, fb, kb * kBK, t1);
           filled_phase[stage] = static_cast<int>(phase);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -396,19 +407,23 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES, CHUNK>::THREADS, 1)
         tc_fence_after();
         const uint32_t d1 = tmem_base + tok_col1(slot);
         const uint32_t d2 = tmem_base + tok_col2(slot);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int ks = 0; ks < num_st; ++ks) {
           if (!mbar_wait(&full_bar[stage], phase, wc)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t so = static_cast<uint64_t>((stage * S::STAGE_BYTES) >> 4);
-          const uint64_t adesc = adesc0 + so;
-          const uint64_t bdesc = bdesc0 + so;
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_bf16_pair(d1, adesc + 2u * kk, bdesc + 2u * kk, idesc1, (kb | kk) != 0 ? 1u : 0u);
-          if (n2 > 0) {
+          const int nsub = min(S::KSUB, num_kb - ks * S::KSUB);
+          for (int j = 0; j < nsub; ++j) {
+            const int kb = ks * S::KSUB + j;         // K blocks in ascending order, as one chain
+            const uint64_t so = static_cast<uint64_t>((stage * S::STAGE_BYTES + j * S::SUB_BYTES) >> 4);
+            const uint64_t adesc = adesc0 + so;
+            const uint64_t bdesc = bdesc0 + so;
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
-              umma_bf16_pair(d2, adesc + 2u * kk, bdesc + B2_OFF + 2u * kk, idesc2, (kb | kk) != 0 ? 1u : 0u);
+              umma_bf16_pair(d1, adesc + 2u * kk, bdesc + 2u * kk, idesc1, (kb | kk) != 0 ? 1u : 0u);
+            if (n2 > 0) {
+#pragma unroll
+              for (int kk = 0; kk < kBK / 16; ++kk)
+                umma_bf16_pair(d2, adesc + 2u * kk, bdesc + B2_OFF + 2u * kk, idesc2, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           umma_commit_pair(&empty_bar[stage], 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }

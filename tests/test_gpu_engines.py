@@ -75,6 +75,12 @@ SMALL = [
     # empty experts, experts of up to 32, 33-64 and 65-128 tokens, and experts of several units
     dataclasses.replace(synth.TINY, name="unit128_form", T=600, H=512, E=64, k=4, F=256,
                         dup_router_rows=False, zipf_s=1.1, zipf_alpha=0.4, seed=69),
+    # H = 448: seven 64-wide K blocks, so the forms whose ring stages hold two K blocks (64-token
+    # units; 128-token SwiGLU units) end on a stage with one
+    dataclasses.replace(synth.TINY, name="odd_k_blocks_units64", T=200, H=448, E=16, k=4, F=256,
+                        dup_router_rows=False, seed=70),
+    dataclasses.replace(synth.TINY, name="odd_k_blocks_units128", T=600, H=448, E=64, k=4, F=256,
+                        dup_router_rows=False, zipf_s=1.1, zipf_alpha=0.4, seed=69),
 ]
 
 

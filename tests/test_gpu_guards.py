@@ -59,6 +59,9 @@ CFGS = [
     # of 33-64 and 65-128 tokens, experts of several units
     dataclasses.replace(synth.TINY, name="unit128_form", T=600, H=512, E=64, k=4, F=256,
                         dup_router_rows=False, zipf_s=1.1, zipf_alpha=0.4, seed=69),
+    # seven K blocks (H = 448) in the forms whose stages hold two
+    dataclasses.replace(synth.TINY, name="odd_k_blocks_units64", T=200, H=448, E=16, k=4, F=256,
+                        dup_router_rows=False, seed=79),
 ]
 
 
