@@ -987,8 +987,10 @@ def run_profile_case(args):
         w13, w2 = synth.expert_weights(mc, dev)
         ws13, ws2 = synth.shared_expert_weights(mc, dev)
         layer = api.MoELayer(api.MoEWeights(wr.to(dev), w13, w2, mc.k, ws13, ws2))
+        # return_all: the layer's own workspace and buffers (a 1024-token call would otherwise take the
+        # small-batch path on the preallocated decode buffers)
         for _ in range(3):
-            layer.prefill(x.to(dev))
+            layer.prefill(x.to(dev), return_all=True)
         binding.check_status(layer._ws)
     torch.cuda.synchronize()
     print(json.dumps({"profile_case": args.profile_case, "ok": True}))
