@@ -79,6 +79,7 @@ __device__ __forceinline__ void lse_fold(float& M, float& S, float m, float s) {
 }
 
 constexpr int kMergeWarps = 4;
+constexpr int kMergeBatch = 4;   // partials a lane loads before folding them
 
 // The partials of chunk c of token t sit at
 //   part[(c / shard_chunks) * shard_stride + t * ld_part + c % shard_chunks]
@@ -104,13 +105,23 @@ __global__ void lse_merge_kernel(const float2* __restrict__ part, long long ld_p
     int sh = c / shard_chunks;
     int j = c - sh * shard_chunks;
     const float2* base = part + sh * shard_stride + static_cast<long long>(t) * ld_part;
-    for (; c < c1; ++c) {
-      const float2 ms = base[j];
-      lse_fold(M, S, ms.x, ms.y);
-      if (++j == shard_chunks) {
-        j = 0;
-        base += shard_stride;
+    // the lane's partials in batches of kMergeBatch: a batch's loads are all issued before its
+    // first fold (the folds keep their ascending order)
+    for (; c < c1; c += kMergeBatch) {
+      float2 v[kMergeBatch];
+#pragma unroll
+      for (int i = 0; i < kMergeBatch; ++i) {
+        if (c + i < c1) {
+          v[i] = base[j];
+          if (++j == shard_chunks) {
+            j = 0;
+            base += shard_stride;
+          }
+        }
       }
+#pragma unroll
+      for (int i = 0; i < kMergeBatch; ++i)
+        if (c + i < c1) lse_fold(M, S, v[i].x, v[i].y);
     }
   }
 #pragma unroll

@@ -32,41 +32,41 @@ __device__ __forceinline__ float key_value(uint32_t key) {
 }
 
 // One warp per token.  Lane l holds experts l, l+32, ... (EPL of them).  Each of
-// the k rounds takes the warp-wide maximum of (key, ~expert): a larger logit
-// wins, an exact tie goes to the lower expert index.  The gate softmax is taken
-// over the k selected logits in rank order, in fp32.  Lane j < k returns the
-// j-th ranked expert and its gate.  Both routing kernels below call this one
-// function, so they take the same decisions and compute the same gate bits.
+// the k rounds takes the warp-wide maximum of the order keys still in play
+// (redux.sync max), then the lowest expert index holding that key (redux.sync
+// min): a larger logit wins, an exact tie goes to the lower expert index, and a
+// NaN (key 0) is taken only after every number, lowest index first.  The gate
+// softmax is taken over the k selected logits in rank order, in fp32.  Lane j < k
+// returns the j-th ranked expert and its gate.  Both routing kernels below call
+// this one function, so they take the same decisions and compute the same gate bits.
 template <int EPL>
 __device__ __forceinline__ void topk_token(const float* __restrict__ row, int E, int k, int lane, int& out_e,
                                            float& out_w) {
-  uint64_t key[EPL];
+  uint32_t key[EPL];
+  uint32_t live = 0u;   // bit i: expert i*32 + lane exists and has not been taken yet
 #pragma unroll
   for (int i = 0; i < EPL; ++i) {
     const int e = i * 32 + lane;
-    key[i] = (e < E) ? ((static_cast<uint64_t>(order_key(row[e])) << 32) | static_cast<uint32_t>(~e)) : 0ull;
-    // a NaN logit keeps key 0 in its high half but a non-zero low half, so it
-    // still outranks an absent entry (key 0) and ties among NaNs go by index
+    key[i] = (e < E) ? order_key(row[e]) : 0u;
+    if (e < E) live |= 1u << i;
   }
   int my_e = 0;
   float my_v = 0.0f;
   for (int j = 0; j < k; ++j) {
-    uint64_t best = 0ull;
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) best = key[i] > best ? key[i] : best;
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) {
-      const uint64_t o = __shfl_xor_sync(kFull, best, d);
-      best = o > best ? o : best;
-    }
-    const int e = static_cast<int>(~static_cast<uint32_t>(best));
-    const float v = key_value(static_cast<uint32_t>(best >> 32));
+    uint32_t best = 0u;
 #pragma unroll
     for (int i = 0; i < EPL; ++i)
-      if (i * 32 + lane == e) key[i] = 0ull;
+      if (((live >> i) & 1u) && key[i] > best) best = key[i];
+    const uint32_t gbest = __reduce_max_sync(kFull, best);
+    uint32_t cand = 0xffffffffu;
+#pragma unroll
+    for (int i = EPL - 1; i >= 0; --i)
+      if (((live >> i) & 1u) && key[i] == gbest) cand = static_cast<uint32_t>(i * 32 + lane);
+    const int e = static_cast<int>(__reduce_min_sync(kFull, cand));
+    if ((e & 31) == lane) live &= ~(1u << (e >> 5));
     if (lane == j) {
       my_e = e;
-      my_v = v;
+      my_v = key_value(gbest);
     }
   }
   // gates: w_j = exp(v_j - v_0) / sum_{i<k} exp(v_i - v_0), the sum in rank order
@@ -78,9 +78,14 @@ __device__ __forceinline__ void topk_token(const float* __restrict__ row, int E,
   out_w = __fdiv_rn(ex, s);
 }
 
+// Blocks of kTopkThreads; up to E = 256 at most 32 registers a thread, so that a whole batch of
+// 8192 tokens (one warp each) is resident at once (64 warps per SM on 152 SMs) instead of a
+// second wave of a few blocks.
+constexpr int kTopkThreads = 256;
 template <int EPL>
-__global__ void topk_gate_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx,
-                                 float* __restrict__ w) {
+__global__ void __launch_bounds__(kTopkThreads, EPL <= 8 ? 8 : 1)
+    topk_gate_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ idx,
+                     float* __restrict__ w) {
   pdl_wait();
   pdl_trigger();
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -283,16 +288,56 @@ __global__ void dispatch_count_kernel(const int32_t* __restrict__ idx, int T, in
   for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[static_cast<long long>(c) * E + e] = hist[e];
 }
 
-// One block: per expert an exclusive scan over chunks (in place), the expert
-// totals, and an exclusive scan over experts for the segment offsets.
-__global__ void dispatch_scan_kernel(int32_t* __restrict__ chunk_counts, int NC, int E, int32_t* __restrict__ counts,
-                                     int32_t* __restrict__ offsets) {
+// One block of 1024 threads: per expert an exclusive scan over chunks (in place),
+// the expert totals, and an exclusive scan over experts for the segment offsets.
+// When every thread's share fits in registers, Q = 1024 / E threads (at most 4)
+// share an expert's chunks: thread (q, e) loads its whole range [q*per, +per) at
+// once, the Q range totals meet in shared memory, and each thread writes its
+// range's exclusive counts from the total of the ranges before it.  Integer sums,
+// so the plan is the same whichever way it is computed.
+constexpr int kScanRegs = 32;
+__global__ void __launch_bounds__(1024, 1)
+    dispatch_scan_kernel(int32_t* __restrict__ chunk_counts, int NC, int E, int32_t* __restrict__ counts,
+                         int32_t* __restrict__ offsets) {
   pdl_wait();
   pdl_trigger();
   __shared__ int warp_tot[32];
+  __shared__ int part[1024];
   const int e = threadIdx.x;
+  const int Q = E <= 256 ? 4 : (E <= 512 ? 2 : 1);
+  const int per = (NC + Q - 1) / Q;
   int run = 0;
-  if (e < E) {
+  if (per <= kScanRegs) {
+    const int q = e / E, ee = e - q * E;
+    const int c0 = q * per;
+    const int n = q < Q ? max(0, min(per, NC - c0)) : 0;
+    int32_t* col = chunk_counts + static_cast<long long>(c0) * E + ee;
+    int v[kScanRegs];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < kScanRegs; ++i)
+      if (i < n) v[i] = col[static_cast<long long>(i) * E];
+#pragma unroll
+    for (int i = 0; i < kScanRegs; ++i)
+      if (i < n) sum += v[i];
+    part[e] = sum;
+    __syncthreads();
+    if (q < Q) {
+      int base = 0;
+      for (int qq = 0; qq < q; ++qq) base += part[qq * E + ee];
+#pragma unroll
+      for (int i = 0; i < kScanRegs; ++i) {
+        if (i < n) {
+          col[static_cast<long long>(i) * E] = base;
+          base += v[i];
+        }
+      }
+    }
+    if (e < E) {
+      for (int qq = 0; qq < Q; ++qq) run += part[qq * E + e];
+      counts[e] = run;
+    }
+  } else if (e < E) {
     // eight chunks' counts are loaded before any of them is overwritten, so the loads of a
     // batch are in flight together instead of one dependent round trip per chunk
     int c = 0;
@@ -339,29 +384,37 @@ __global__ void dispatch_scan_kernel(int32_t* __restrict__ chunk_counts, int NC,
 
 // One warp per chunk: walk the chunk's pairs p = t*k + j in ascending order, 32 at
 // a time.  Lanes holding the same expert are ranked by lane (match_any), and a
-// per-expert running count in shared memory carries the rank across batches, so
+// per-expert running position in shared memory carries the rank across batches, so
 // each expert's rows come out in ascending token order (a token never picks the
-// same expert twice).
+// same expert twice).  The chunk's expert indices and each expert's first position
+// for the chunk (segment offset + the chunk's exclusive count) are staged in shared
+// memory first, with all their loads in flight together, so the walk itself makes
+// no dependent global round trip.
 __global__ void dispatch_scatter_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
                                         const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ offsets,
                                         int32_t* __restrict__ row_token, int32_t* __restrict__ slot_row) {
   pdl_wait();
   pdl_trigger();
-  extern __shared__ int run[];
+  extern __shared__ int sm_scatter[];
+  int* run = sm_scatter;            // [E] next position of each expert's rows from this chunk
+  int* s_e = sm_scatter + E;        // [kDispatchChunk * k] the chunk's expert indices
   const int lane = threadIdx.x;
-  for (int e = lane; e < E; e += 32) run[e] = 0;
-  __syncwarp();
   const int c = blockIdx.x;
   const long long p0 = static_cast<long long>(c) * kDispatchChunk * k;
   const long long p1 = min(static_cast<long long>(T), static_cast<long long>(c + 1) * kDispatchChunk) * k;
+  const int np = static_cast<int>(p1 - p0);
+  for (int e = lane; e < E; e += 32) run[e] = offsets[e] + chunk_base[static_cast<long long>(c) * E + e];
+  for (int i = lane; i < np; i += 32) s_e[i] = idx[p0 + i];
+  __syncwarp();
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (long long pb = p0; pb < p1; pb += 32) {
-    const long long p = pb + lane;
-    const int e = (p < p1) ? idx[p] : -1;
+  for (int ib = 0; ib < np; ib += 32) {
+    const int i = ib + lane;
+    const int e = (i < np) ? s_e[i] : -1;
     const unsigned m = __match_any_sync(kFull, e);
     const int rank = __popc(m & lt_mask);
     if (e >= 0) {
-      const int pos = offsets[e] + chunk_base[static_cast<long long>(c) * E + e] + run[e] + rank;
+      const int pos = run[e] + rank;
+      const long long p = p0 + i;
       row_token[pos] = static_cast<int32_t>(p / k);
       slot_row[p] = pos;
     }
@@ -477,7 +530,7 @@ int route_launch(const float* logits, int T, int E, int k, int H, const void* x,
   }
   // top-k + gates
   {
-    const int threads = 256;
+    const int threads = kTopkThreads;
     const long long blocks = (static_cast<long long>(T) * 32 + threads - 1) / threads;
     const int epl = (E + 31) / 32;
     ProfScope prof("topk_gate", st);
@@ -536,7 +589,9 @@ int dispatch_launch(const int32_t* topk_idx, int T, int E, int k, int H, const v
   if (rc) return rc;
   {
     ProfScope prof("dispatch_scatter", st);
-    rc = check_cuda(launch_kernel(dispatch_scatter_kernel, dim3(NC), dim3(32), E * sizeof(int), st, topk_idx, T, E,
+    rc = check_cuda(launch_kernel(dispatch_scatter_kernel, dim3(NC), dim3(32),
+                                  (static_cast<size_t>(E) + static_cast<size_t>(kDispatchChunk) * k) * sizeof(int), st,
+                                  topk_idx, T, E,
                                   k, static_cast<const int32_t*>(chunk_counts), static_cast<const int32_t*>(offsets),
                                   row_token, slot_row),
                     "dispatch_scatter_kernel");
