@@ -195,10 +195,12 @@ ProfScope::~ProfScope() {
 
 // The shared expert: dense SwiGLU over all T tokens on the CTA-pair engine; the
 // bf16 hidden activation [T, F_shared] lives in `hs` (workspace scratch).
-// Router GEMM tiles: 128 columns wide, or 64 when that still fits the whole GEMM in one wave of
-// the SMs (decode-sized batches: E = 256 then streams its router weights through 4 SMs instead of
-// 2).  The tile width changes no bit of a logit.
+// Router GEMM tiles: at most 64 tokens take the small-M kernel (one 64-expert tile per CTA, four
+// K blocks per copy); otherwise 128 columns wide, or 64 when that still fits the whole GEMM in one
+// wave of the SMs.  Neither the tile width nor the kernel changes a bit of a logit (the same M = 64
+// MMA steps in the same K order for a tile of at most 64 tokens).
 GemmVariant router_variant(int T, int E) {
+  if (T <= 64) return GV_F32_SMALL64;
   if (E <= 64) return GV_F32_BN64_MT1;
   int sms = 0;
   if (device_sm_count(&sms) != INVMOE_OK) return GV_F32_BN128_MT1;

@@ -9,6 +9,7 @@
 #include "tc_gemm.cuh"
 #include "tc_gemm2.cuh"
 #include "tc_gemm_tok.cuh"
+#include "tc_gemm_small.cuh"
 
 namespace invmoe {
 
@@ -44,6 +45,25 @@ int make_tmap(CUtensorMap* m, const void* base, long long inner, long long rows,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return set_error(INVMOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return INVMOE_OK;
+}
+
+// Row-major bf16 [rows, inner] matrix as a rank-3 tensor (64 elements, rows, inner / 64 blocks):
+// one box = 64 elements x box_rows rows x kblocks consecutive 64-column blocks of the row.
+int make_tmap_kblocks(CUtensorMap* m, const void* base, long long inner, long long rows, int box_rows, int kblocks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return set_error(INVMOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if (inner % kBK != 0) return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "K=%lld is not a multiple of 64", inner);
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kBK), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(inner / kBK)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 2, static_cast<cuuint64_t>(kBK) * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows),
+                       static_cast<cuuint32_t>(kblocks)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_error(INVMOE_ERR_CUDA, "cuTensorMapEncodeTiled (K blocks) failed (%d)", (int)r);
   return INVMOE_OK;
 }
 
@@ -278,6 +298,23 @@ int launch_tok(const GemmCall& c, cudaStream_t st) {
                     "tc_gemm_tok_kernel launch");
 }
 
+// At most 64 rows of A, dense, fp32 out: one 64-column tile per CTA (tc_gemm_small.cuh).
+int launch_small(const GemmCall& c, cudaStream_t st) {
+  if (c.G != 0 || c.M > 64 || c.N % 4 != 0 || c.ldo % 4 != 0 || (reinterpret_cast<uintptr_t>(c.out) & 15) != 0)
+    return set_error(INVMOE_ERR_INVALID_ARG, "the small-M GEMM takes a dense A of at most 64 rows and an aligned output");
+  CUtensorMap ta, tb;
+  int rc = make_tmap_kblocks(&ta, c.A, c.K, c.a_rows, 64, kSmallKsub);
+  if (rc) return rc;
+  if ((rc = make_tmap_kblocks(&tb, c.B, c.K, c.b_rows, 64, kSmallKsub))) return rc;
+  static std::atomic<uint64_t> attr_set{0};
+  if ((rc = set_smem_attr(reinterpret_cast<const void*>(tc_gemm_small_kernel), kSmallSmemBytes, attr_set))) return rc;
+  const int grid = (c.N + 63) / 64;
+  ProfScope prof(c.name ? c.name : "tc_gemm_small", st);
+  return check_cuda(launch_kernel(tc_gemm_small_kernel, dim3(grid), dim3(kSmallThreads), kSmallSmemBytes, st, ta, tb,
+                                  c.M, c.N, c.K, static_cast<float*>(c.out), c.ldo, c.status, kTimeoutNs),
+                    "tc_gemm_small_kernel launch");
+}
+
 }  // namespace
 
 int gemm_run(const GemmCall& c, cudaStream_t st) {
@@ -314,6 +351,7 @@ int gemm_run(const GemmCall& c, cudaStream_t st) {
       if (c.a_rows <= 1024 || c.a_rows <= 16LL * c.G) return launch_tok<EPI_SWIGLU, 5, 64>(c, st);
       if (c.a_rows <= 64LL * c.G) return launch_tok<EPI_SWIGLU, 4, 128>(c, st);
       return launch_tok<EPI_SWIGLU, 5, kTokChunk>(c, st);
+    case GV_F32_SMALL64: return launch_small(c, st);
     case GV_TOK_F32:
       if (c.a_rows <= 1024 || c.a_rows <= 16LL * c.G) return launch_tok<EPI_F32, 5, 64>(c, st);
       if (c.a_rows <= 64LL * c.G) return launch_tok<EPI_F32, 8, 128>(c, st);

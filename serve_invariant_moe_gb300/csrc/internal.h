@@ -89,7 +89,8 @@ enum GemmVariant : int {
   GV_F32_BN256_MT1_KGROUP = 14, // K-grouped weight gradients: D_g = A_g^T B_g, A and B MN-major
   GV_PAIR_SWIGLU_BWD = 15, // CTA-pair gate+up recompute with the SwiGLU backward epilogue
   GV_TOK_SWIGLU = 16,      // grouped gate+up, tokens on the MMA's N side (CTA pair), SwiGLU -> bf16
-  GV_TOK_F32 = 17          // grouped, tokens on the MMA's N side (CTA pair), fp32 out
+  GV_TOK_F32 = 17,         // grouped, tokens on the MMA's N side (CTA pair), fp32 out
+  GV_F32_SMALL64 = 18      // dense fp32-out, at most 64 rows of A, one 64-column tile per CTA, 4 K blocks per copy
 };
 
 // Which engine runs the forward grouped expert GEMMs: 0 = tokens on the MMA's M side in row
