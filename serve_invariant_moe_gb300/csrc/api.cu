@@ -210,9 +210,12 @@ GemmVariant router_variant(int T, int E) {
 
 int shared_expert_run(const void* x, const void* ws13, const void* ws2, int T, int H, int F_shared, float* y_shared,
                       void* hs, unsigned int* status, cudaStream_t st, int* sched) {
+  // at most 64 tokens (decode): the small-M kernel, one 32-column tile of h (64 of y) per CTA and four K
+  // blocks per copy; the same MMA steps, K order and SwiGLU expression as the CTA-pair engine
+  const bool small = T <= 64 && F_shared % 32 == 0;
   GemmCall s1{};
   s1.name = "shared_gemm1_swiglu";
-  s1.variant = GV_PAIR_SWIGLU;
+  s1.variant = small ? GV_SWIGLU_SMALL64 : GV_PAIR_SWIGLU;
   s1.A = x; s1.a_rows = T; s1.B = ws13; s1.b_rows = 2LL * F_shared; s1.K = H;
   s1.N = F_shared; s1.M = T; s1.G = 0; s1.b_group_rows = 0; s1.b_up_rows = F_shared;
   s1.out = hs; s1.ldo = F_shared; s1.status = status; s1.sched = sched;
@@ -220,7 +223,7 @@ int shared_expert_run(const void* x, const void* ws13, const void* ws2, int T, i
   if (rc) return rc;
   GemmCall s2{};
   s2.name = "shared_gemm2";
-  s2.variant = GV_PAIR_F32;
+  s2.variant = small ? GV_F32_SMALL64 : GV_PAIR_F32;
   s2.A = hs; s2.a_rows = T; s2.B = ws2; s2.b_rows = H; s2.K = F_shared;
   s2.N = H; s2.M = T; s2.G = 0;
   s2.out = y_shared; s2.ldo = H; s2.status = status; s2.sched = sched;

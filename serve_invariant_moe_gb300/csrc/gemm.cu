@@ -298,20 +298,49 @@ int launch_tok(const GemmCall& c, cudaStream_t st) {
                     "tc_gemm_tok_kernel launch");
 }
 
-// At most 64 rows of A, dense, fp32 out: one 64-column tile per CTA (tc_gemm_small.cuh).
+// SwiGLU weights [2F, K] (gate rows, then up rows) for the small-M kernel: a rank-4 tensor (64 elements,
+// F rows, gate/up, K blocks) whose box (64, 32, 2, kblocks) holds, per K block, 32 gate rows followed by
+// the matching 32 up rows.
+int make_tmap_gate_up_small(CUtensorMap* m, const void* base, long long K, long long F, int kblocks) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return set_error(INVMOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  if (K % kBK != 0) return set_error(INVMOE_ERR_UNSUPPORTED_SHAPE, "K=%lld is not a multiple of 64", K);
+  const cuuint64_t row = static_cast<cuuint64_t>(K) * 2;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(kBK), static_cast<cuuint64_t>(F), 2, static_cast<cuuint64_t>(K / kBK)};
+  cuuint64_t strides[3] = {row, row * F, static_cast<cuuint64_t>(kBK) * 2};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(kBK), 32, 2, static_cast<cuuint32_t>(kblocks)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(INVMOE_ERR_CUDA, "cuTensorMapEncodeTiled (small gate/up) failed (%d)", (int)r);
+  return INVMOE_OK;
+}
+
+// At most 64 rows of A, dense: fp32 out in 64-column tiles, or SwiGLU h in 32-column tiles, one tile per
+// CTA (tc_gemm_small.cuh).
+template <int EPI>
 int launch_small(const GemmCall& c, cudaStream_t st) {
-  if (c.G != 0 || c.M > 64 || c.N % 4 != 0 || c.ldo % 4 != 0 || (reinterpret_cast<uintptr_t>(c.out) & 15) != 0)
+  const bool swiglu = EPI == EPI_SWIGLU;
+  const int cw = swiglu ? 32 : 64;
+  const int eb = swiglu ? 2 : 4;     // output element bytes
+  if (c.G != 0 || c.M > 64 || (swiglu ? c.N % 32 != 0 || c.b_up_rows != c.N : c.N % 4 != 0) ||
+      (c.ldo * eb) % 16 != 0 || (reinterpret_cast<uintptr_t>(c.out) & 15) != 0)
     return set_error(INVMOE_ERR_INVALID_ARG, "the small-M GEMM takes a dense A of at most 64 rows and an aligned output");
   CUtensorMap ta, tb;
   int rc = make_tmap_kblocks(&ta, c.A, c.K, c.a_rows, 64, kSmallKsub);
   if (rc) return rc;
-  if ((rc = make_tmap_kblocks(&tb, c.B, c.K, c.b_rows, 64, kSmallKsub))) return rc;
+  rc = swiglu ? make_tmap_gate_up_small(&tb, c.B, c.K, c.N, kSmallKsub)
+              : make_tmap_kblocks(&tb, c.B, c.K, c.b_rows, 64, kSmallKsub);
+  if (rc) return rc;
   static std::atomic<uint64_t> attr_set{0};
-  if ((rc = set_smem_attr(reinterpret_cast<const void*>(tc_gemm_small_kernel), kSmallSmemBytes, attr_set))) return rc;
-  const int grid = (c.N + 63) / 64;
+  if ((rc = set_smem_attr(reinterpret_cast<const void*>(tc_gemm_small_kernel<EPI>), kSmallSmemBytes, attr_set)))
+    return rc;
+  const int grid = (c.N + cw - 1) / cw;
   ProfScope prof(c.name ? c.name : "tc_gemm_small", st);
-  return check_cuda(launch_kernel(tc_gemm_small_kernel, dim3(grid), dim3(kSmallThreads), kSmallSmemBytes, st, ta, tb,
-                                  c.M, c.N, c.K, static_cast<float*>(c.out), c.ldo, c.status, kTimeoutNs),
+  return check_cuda(launch_kernel(tc_gemm_small_kernel<EPI>, dim3(grid), dim3(kSmallThreads), kSmallSmemBytes, st, ta,
+                                  tb, c.M, c.N, c.K, c.out, c.ldo, c.status, kTimeoutNs),
                     "tc_gemm_small_kernel launch");
 }
 
@@ -351,7 +380,8 @@ int gemm_run(const GemmCall& c, cudaStream_t st) {
       if (c.a_rows <= 1024 || c.a_rows <= 16LL * c.G) return launch_tok<EPI_SWIGLU, 5, 64>(c, st);
       if (c.a_rows <= 64LL * c.G) return launch_tok<EPI_SWIGLU, 4, 128>(c, st);
       return launch_tok<EPI_SWIGLU, 5, kTokChunk>(c, st);
-    case GV_F32_SMALL64: return launch_small(c, st);
+    case GV_F32_SMALL64: return launch_small<EPI_F32>(c, st);
+    case GV_SWIGLU_SMALL64: return launch_small<EPI_SWIGLU>(c, st);
     case GV_TOK_F32:
       if (c.a_rows <= 1024 || c.a_rows <= 16LL * c.G) return launch_tok<EPI_F32, 5, 64>(c, st);
       if (c.a_rows <= 64LL * c.G) return launch_tok<EPI_F32, 8, 128>(c, st);

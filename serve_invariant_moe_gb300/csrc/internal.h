@@ -90,7 +90,8 @@ enum GemmVariant : int {
   GV_PAIR_SWIGLU_BWD = 15, // CTA-pair gate+up recompute with the SwiGLU backward epilogue
   GV_TOK_SWIGLU = 16,      // grouped gate+up, tokens on the MMA's N side (CTA pair), SwiGLU -> bf16
   GV_TOK_F32 = 17,         // grouped, tokens on the MMA's N side (CTA pair), fp32 out
-  GV_F32_SMALL64 = 18      // dense fp32-out, at most 64 rows of A, one 64-column tile per CTA, 4 K blocks per copy
+  GV_F32_SMALL64 = 18,     // dense fp32-out, at most 64 rows of A, one 64-column tile per CTA, 4 K blocks per copy
+  GV_SWIGLU_SMALL64 = 19   // dense gate+up with SwiGLU -> bf16, at most 64 rows of A, 32 columns of h per CTA
 };
 
 // Which engine runs the forward grouped expert GEMMs: 0 = tokens on the MMA's M side in row

@@ -18,6 +18,11 @@
 //   Each 64-row x 128-byte slice of a box lands 8 KB apart in shared memory with the 128-byte
 //   swizzle of a 2-D box, which is the operand layout of one K block.
 //   * A last stage past K holds zero-filled blocks; their MMAs are not issued.
+// EPI_F32 writes D (fp32) for 64 columns per CTA.  EPI_SWIGLU computes h = silu(g) * u (the
+// expression of the other engines, bf16 round to nearest) for 32 columns of h per CTA: B is the gate
+// rows [32c, 32c + 32) and the matching up rows N + 32c.. in one rank-4 copy (64, 32 rows, gate/up,
+// K blocks), which lands per K block as 32 gate rows then 32 up rows, so one N = 64 MMA gives the
+// CTA's gate columns in accumulator columns [0, 32) and its up columns in [32, 64).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -36,6 +41,16 @@ constexpr int kSmallThreads = 64 + 128;                    // producer warp, MMA
 constexpr int kSmallSmemBytes = 1024 + kSmallStages * kSmallStageBytes + 8 * (2 * kSmallStages + 1) + 16;
 static_assert(kSmallSmemBytes <= 232448, "shared memory");
 
+// TMA load of rank 4 into this CTA's shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                            int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 // TMA load of rank 3 into this CTA's shared memory, completion counted on `bar`.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
                                             int c2) {
@@ -46,10 +61,12 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+template <int EPI>
 __global__ void __launch_bounds__(kSmallThreads, 1)
     tc_gemm_small_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                         int M, int N, int K, float* __restrict__ out, long long ldo, unsigned int* status,
+                         int M, int N, int K, void* __restrict__ out, long long ldo, unsigned int* status,
                          unsigned long long timeout_ns) {
+  static_assert(EPI == EPI_F32 || EPI == EPI_SWIGLU, "epilogue");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(ring + kSmallStages * kSmallStageBytes);
@@ -83,7 +100,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int num_kb = K / kBK;
   const int num_st = (num_kb + kSmallKsub - 1) / kSmallKsub;
-  const int n0 = static_cast<int>(blockIdx.x) * 64;
+  // first output column of this CTA: 64 per CTA (fp32 D), 32 per CTA (h)
+  const int n0 = static_cast<int>(blockIdx.x) * (EPI == EPI_SWIGLU ? 32 : 64);
   WaitCtl wc{s_abort, status, timeout_ns};
 
   if (warp == 0) {
@@ -100,7 +118,10 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         // a box counts its full size, zero-filled rows and blocks included
         mbar_arrive_expect_tx(&full_bar[stage], kSmallStageBytes);
         tma_load_3d(st, &tmA, &full_bar[stage], 0, 0, ks * kSmallKsub);
-        tma_load_3d(st + kSmallKsub * kSmallSlice, &tmB, &full_bar[stage], 0, n0, ks * kSmallKsub);
+        if (EPI == EPI_SWIGLU)
+          tma_load_4d(st + kSmallKsub * kSmallSlice, &tmB, &full_bar[stage], 0, n0, 0, ks * kSmallKsub);
+        else
+          tma_load_3d(st + kSmallKsub * kSmallSlice, &tmB, &full_bar[stage], 0, n0, ks * kSmallKsub);
         filled_phase[stage] = static_cast<int>(phase);
         if (++stage == kSmallStages) { stage = 0; phase ^= 1u; }
       }
@@ -157,13 +178,29 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       tmem_reg_fence(v1);
       const int row = q * 16 + lane;
       if (lane < 16 && row < M) {
-        float* o = out + static_cast<long long>(row) * ldo + n0;
+        if (EPI == EPI_SWIGLU) {
+          // h[row, n0 + j] = silu(g_j) * u_j, g in accumulator columns [0, 32), u in [32, 64)
+          uint32_t packed[16];
 #pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          if (n0 + c < N)
-            *reinterpret_cast<uint4*>(o + c) = make_uint4(v0[c], v0[c + 1], v0[c + 2], v0[c + 3]);
-          if (n0 + 32 + c < N)
-            *reinterpret_cast<uint4*>(o + 32 + c) = make_uint4(v1[c], v1[c + 1], v1[c + 2], v1[c + 3]);
+          for (int j = 0; j < 16; ++j) {
+            const float h0 = __fmul_rn(silu_f32(__uint_as_float(v0[2 * j])), __uint_as_float(v1[2 * j]));
+            const float h1 = __fmul_rn(silu_f32(__uint_as_float(v0[2 * j + 1])), __uint_as_float(v1[2 * j + 1]));
+            packed[j] = pack_bf16x2(h0, h1);
+          }
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + static_cast<long long>(row) * ldo + n0;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(o + 8 * c) =
+                make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+        } else {
+          float* o = static_cast<float*>(out) + static_cast<long long>(row) * ldo + n0;
+#pragma unroll
+          for (int c = 0; c < 32; c += 4) {
+            if (n0 + c < N)
+              *reinterpret_cast<uint4*>(o + c) = make_uint4(v0[c], v0[c + 1], v0[c + 2], v0[c + 3]);
+            if (n0 + 32 + c < N)
+              *reinterpret_cast<uint4*>(o + 32 + c) = make_uint4(v1[c], v1[c + 1], v1[c + 2], v1[c + 3]);
+          }
         }
       }
     }
