@@ -99,8 +99,9 @@ int invmoe_check(void* workspace, void* stream);
  * moe_route_topk -- router logits, top-k with lowest-index ties, gates, dispatch
  *
  *   logits[t, e] = sum_h x[t, h] * w_router[e, h]           (fp32 accumulate,
- *                  tcgen05 tile 128 x BN x 64 with BN = 64 for E <= 64, else 128;
- *                  K ascending, no split-K)
+ *                  tcgen05 tile 128 x BN x 64 with BN = 64 for E <= 64, else 128,
+ *                  or 64 x 64 x 64 for T <= 64; K ascending in 16-wide MMA steps,
+ *                  no split-K, so a logit has the same bits whatever T)
  *   topk_idx[t, 0..k-1]: the k largest logits of row t, largest first; exact
  *                  ties (and -0 vs +0) go to the lower expert index; NaN ranks
  *                  below -inf.
