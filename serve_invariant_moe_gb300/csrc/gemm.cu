@@ -379,7 +379,8 @@ int gemm_run(const GemmCall& c, cudaStream_t st) {
     case GV_TOK_SWIGLU:
       if (c.a_rows <= 1024 || c.a_rows <= 16LL * c.G) return launch_tok<EPI_SWIGLU, 5, 64>(c, st);
       if (c.a_rows <= 64LL * c.G) return launch_tok<EPI_SWIGLU, 4, 128>(c, st);
-      return launch_tok<EPI_SWIGLU, 5, kTokChunk>(c, st);
+      // a 6-stage ring for at most 256 experts (its chunk table), else 5 stages
+      return c.G <= 256 ? launch_tok<EPI_SWIGLU, 6, kTokChunk>(c, st) : launch_tok<EPI_SWIGLU, 5, kTokChunk>(c, st);
     case GV_F32_SMALL64: return launch_small<EPI_F32>(c, st);
     case GV_SWIGLU_SMALL64: return launch_small<EPI_SWIGLU>(c, st);
     case GV_TOK_F32:

@@ -34,6 +34,9 @@
 //     gate rows of h columns f0 + 16i + [0, 16), tile rows 32i + [16, 32) the
 //     up rows, so the warp on TMEM lanes 32i holds both halves of its 16 SwiGLU
 //     pairs and exchanges them with one shuffle.
+//   * Prefill-sized SwiGLU units of at most 256 experts run a 6-stage ring (216 KB of
+//     operands in flight per CTA; the GEMM is paced per SM by the bytes it keeps in
+//     flight), the fp32 ones 5 stages (their staging tiles are twice as large).
 //   * Smaller batches run the same kernel with smaller units (an expert with
 //     more tokens takes several): at most 1024 token slots or 16 per expert
 //     (decode), units of at most 64 tokens, a 32-row token tile per CTA, 20 KB
@@ -109,8 +112,12 @@ struct TokShape {
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
   static constexpr int THREADS = 64 + EPI_THREADS;
   static constexpr int QDEPTH = 4;
-  static constexpr int MAX_GROUPS = 1024;
-  static constexpr int OSTAGE_BYTES = EPI_WARPS * 2048;
+  // a sixth 36 KB stage for the 320-token SwiGLU units fits once each epilogue warp's staging tile
+  // is the 1,056 bytes the SwiGLU store uses and the chunk table holds at most 256 experts
+  static constexpr bool DEEP = EPI == EPI_SWIGLU && CHUNK == kTokChunk && STAGES >= 6;
+  static constexpr int MAX_GROUPS = DEEP ? 256 : 1024;
+  static constexpr int OST_WARP = DEEP ? 1088 : 2048;             // bytes of a warp's staging tile
+  static constexpr int OSTAGE_BYTES = EPI_WARPS * OST_WARP;
   static constexpr int BAR_BYTES = 8 * (2 * STAGES + 6 + 1 + 2 * QDEPTH);
   static constexpr int MISC_BYTES = 16 + 4 * QDEPTH;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + OSTAGE_BYTES + BAR_BYTES + MISC_BYTES +
@@ -444,7 +451,7 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES, CHUNK>::THREADS, 1)
     const int half = ew >> 2;               // every other chunk of each phase, starting at `half`
     const uint32_t accmid_leader0 = mapa_shared(smem_u32(accmid_bar), 0);
     const uint32_t accall_leader0 = mapa_shared(smem_u32(accall_bar), 0);
-    uint8_t* stg = ostage + ew * 2048;
+    uint8_t* stg = ostage + ew * S::OST_WARP;
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t nunit = 0;
     int qi = 0;
