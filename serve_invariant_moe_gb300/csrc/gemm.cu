@@ -386,7 +386,7 @@ int gemm_run(const GemmCall& c, cudaStream_t st) {
     case GV_TOK_F32:
       if (c.a_rows <= 1024 || c.a_rows <= 16LL * c.G) return launch_tok<EPI_F32, 5, 64>(c, st);
       if (c.a_rows <= 64LL * c.G) return launch_tok<EPI_F32, 8, 128>(c, st);
-      return launch_tok<EPI_F32, 5, kTokChunk>(c, st);
+      return c.G <= 256 ? launch_tok<EPI_F32, 6, kTokChunk>(c, st) : launch_tok<EPI_F32, 5, kTokChunk>(c, st);
   }
   return set_error(INVMOE_ERR_INVALID_ARG, "unknown GEMM variant %d", (int)c.variant);
 }

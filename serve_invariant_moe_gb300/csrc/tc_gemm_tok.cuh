@@ -34,9 +34,9 @@
 //     gate rows of h columns f0 + 16i + [0, 16), tile rows 32i + [16, 32) the
 //     up rows, so the warp on TMEM lanes 32i holds both halves of its 16 SwiGLU
 //     pairs and exchanges them with one shuffle.
-//   * Prefill-sized SwiGLU units of at most 256 experts run a 6-stage ring (216 KB of
-//     operands in flight per CTA; the GEMM is paced per SM by the bytes it keeps in
-//     flight), the fp32 ones 5 stages (their staging tiles are twice as large).
+//   * Prefill-sized units of at most 256 experts run a 6-stage ring (216 KB of operands
+//     in flight per CTA; the GEMM is paced per SM by the bytes it keeps in flight), with
+//     smaller epilogue staging tiles (the fp32 store then leaves in passes of 8 tokens).
 //   * Smaller batches run the same kernel with smaller units (an expert with
 //     more tokens takes several): at most 1024 token slots or 16 per expert
 //     (decode), units of at most 64 tokens, a 32-row token tile per CTA, 20 KB
@@ -112,11 +112,12 @@ struct TokShape {
   static constexpr int EPI_THREADS = 32 * EPI_WARPS;
   static constexpr int THREADS = 64 + EPI_THREADS;
   static constexpr int QDEPTH = 4;
-  // a sixth 36 KB stage for the 320-token SwiGLU units fits once each epilogue warp's staging tile
-  // is the 1,056 bytes the SwiGLU store uses and the chunk table holds at most 256 experts
-  static constexpr bool DEEP = EPI == EPI_SWIGLU && CHUNK == kTokChunk && STAGES >= 6;
+  // a sixth 36 KB stage for the 320-token units fits once the chunk table holds at most 256 experts
+  // and each epilogue warp's staging tile is the 1,056 bytes the SwiGLU store uses
+  // (SwiGLU), or 1 KB for the fp32 store in passes of 8 tokens (16 otherwise)
+  static constexpr bool DEEP = CHUNK == kTokChunk && STAGES >= 6;
   static constexpr int MAX_GROUPS = DEEP ? 256 : 1024;
-  static constexpr int OST_WARP = DEEP ? 1088 : 2048;             // bytes of a warp's staging tile
+  static constexpr int OST_WARP = DEEP ? (EPI == EPI_SWIGLU ? 1088 : 1024) : 2048;   // a warp's staging tile
   static constexpr int OSTAGE_BYTES = EPI_WARPS * OST_WARP;
   static constexpr int BAR_BYTES = 8 * (2 * STAGES + 6 + 1 + 2 * QDEPTH);
   static constexpr int MISC_BYTES = 16 + 4 * QDEPTH;
@@ -516,17 +517,18 @@ __global__ void __launch_bounds__(TokShape<EPI, STAGES, CHUNK>::THREADS, 1)
           // fp32 Y[token, h0 + lane] for the warp's 32 rows of this CTA's 128 weight rows
           const int h0 = U.wb * 256 + 128 * static_cast<int>(rank) + 32 * q;
           float* ys = reinterpret_cast<float*>(stg);
+          constexpr int TPP = S::OST_WARP / 128;    // tokens per staging pass (128 B of Y per token)
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
+          for (int hh = 0; hh < 32 / TPP; ++hh) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) ys[j * 32 + lane] = __uint_as_float(v[16 * hh + j]);
+            for (int j = 0; j < TPP; ++j) ys[j * 32 + lane] = __uint_as_float(v[TPP * hh + j]);
             __syncwarp();
             const int ch = lane & 7;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < TPP / 4; ++i) {
               const int r = 4 * i + (lane >> 3);
               const uint4 w = *reinterpret_cast<const uint4*>(stg + r * 128 + ch * 16);
-              const int t = tok_of(c, 16 * hh + r);
+              const int t = tok_of(c, TPP * hh + r);
               if (t < U.nv)
                 *reinterpret_cast<uint4*>(static_cast<float*>(p.out) +
                                           static_cast<long long>(U.tok0 + t) * p.ldo + h0 + ch * 4) = w;
