@@ -220,13 +220,15 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   }
   if (!do_permute) return;
   __syncthreads();
-  // permute: xp[slot_row[t, j]] = x[t], one warp per token, 16-byte vectors
-  for (int t = warp; t < T; t += 32) {
-    const uint4* src = (stage_x ? s_x : x) + static_cast<long long>(t) * vec_per_row;
-    for (int c = lane; c < vec_per_row; c += 32) {
-      const uint4 v = stage_x ? src[c] : __ldg(src + c);
-      for (int j = 0; j < k; ++j) xp[static_cast<long long>(s_pos[t * k + j]) * vec_per_row + c] = v;
-    }
+  // permute: xp[slot_row[t, j]] = x[t] in 16-byte vectors, one vector of one token per thread and
+  // step over the whole block (one warp per token left most of the block idle for a decode batch:
+  // 4.0-4.4 us for one token of H = 6144)
+  const int nvec = T * vec_per_row;
+  for (int i = tid; i < nvec; i += kSmallThreads) {
+    const int t = i / vec_per_row;
+    const int c = i - t * vec_per_row;
+    const uint4 v = stage_x ? s_x[i] : __ldg(x + i);
+    for (int j = 0; j < k; ++j) xp[static_cast<long long>(s_pos[t * k + j]) * vec_per_row + c] = v;
   }
 }
 
