@@ -320,8 +320,9 @@ int make_tmap_gate_up_small(CUtensorMap* m, const void* base, long long K, long 
 
 // At most 64 rows of A, dense: fp32 out in 64-column tiles, or SwiGLU h in 32-column tiles, one tile per
 // CTA (tc_gemm_small.cuh).
-template <int EPI>
-int launch_small(const GemmCall& c, cudaStream_t st) {
+template <int EPI, int ABOX>
+int launch_small_rows(const GemmCall& c, cudaStream_t st) {
+  using S = SmallShape<ABOX>;
   const bool swiglu = EPI == EPI_SWIGLU;
   const int cw = swiglu ? 32 : 64;
   const int eb = swiglu ? 2 : 4;     // output element bytes
@@ -329,19 +330,25 @@ int launch_small(const GemmCall& c, cudaStream_t st) {
       (c.ldo * eb) % 16 != 0 || (reinterpret_cast<uintptr_t>(c.out) & 15) != 0)
     return set_error(INVMOE_ERR_INVALID_ARG, "the small-M GEMM takes a dense A of at most 64 rows and an aligned output");
   CUtensorMap ta, tb;
-  int rc = make_tmap_kblocks(&ta, c.A, c.K, c.a_rows, 64, kSmallKsub);
+  int rc = make_tmap_kblocks(&ta, c.A, c.K, c.a_rows, ABOX, kSmallKsub);
   if (rc) return rc;
   rc = swiglu ? make_tmap_gate_up_small(&tb, c.B, c.K, c.N, kSmallKsub)
               : make_tmap_kblocks(&tb, c.B, c.K, c.b_rows, 64, kSmallKsub);
   if (rc) return rc;
   static std::atomic<uint64_t> attr_set{0};
-  if ((rc = set_smem_attr(reinterpret_cast<const void*>(tc_gemm_small_kernel<EPI>), kSmallSmemBytes, attr_set)))
+  if ((rc = set_smem_attr(reinterpret_cast<const void*>(tc_gemm_small_kernel<EPI, ABOX>), S::SMEM_BYTES, attr_set)))
     return rc;
   const int grid = (c.N + cw - 1) / cw;
   ProfScope prof(c.name ? c.name : "tc_gemm_small", st);
-  return check_cuda(launch_kernel(tc_gemm_small_kernel<EPI>, dim3(grid), dim3(kSmallThreads), kSmallSmemBytes, st, ta,
-                                  tb, c.M, c.N, c.K, c.out, c.ldo, c.status, kTimeoutNs),
+  return check_cuda(launch_kernel(tc_gemm_small_kernel<EPI, ABOX>, dim3(grid), dim3(kSmallThreads), S::SMEM_BYTES, st,
+                                  ta, tb, c.M, c.N, c.K, c.out, c.ldo, c.status, kTimeoutNs),
                     "tc_gemm_small_kernel launch");
+}
+
+// at most 16 rows of A: 16-row copies of A and a 5-stage ring; otherwise 64-row copies, 3 stages
+template <int EPI>
+int launch_small(const GemmCall& c, cudaStream_t st) {
+  return c.M <= 16 ? launch_small_rows<EPI, 16>(c, st) : launch_small_rows<EPI, 64>(c, st);
 }
 
 }  // namespace

@@ -34,12 +34,22 @@
 namespace invmoe {
 
 constexpr int kSmallKsub = 4;                              // K blocks per ring stage
-constexpr int kSmallStages = 3;
-constexpr int kSmallSlice = 64 * 128;                      // one operand's K block: 64 rows x 128 B
-constexpr int kSmallStageBytes = 2 * kSmallKsub * kSmallSlice;   // 64 KB: A blocks, then B blocks
 constexpr int kSmallThreads = 64 + 128;                    // producer warp, MMA warp, 4 epilogue warps
-constexpr int kSmallSmemBytes = 1024 + kSmallStages * kSmallStageBytes + 8 * (2 * kSmallStages + 1) + 16;
-static_assert(kSmallSmemBytes <= 232448, "shared memory");
+
+// ABOX: rows of A per copy, 64 or (for at most 16 rows) 16.  A stage holds A's kSmallKsub slices of
+// ABOX rows x 128 B, then B's of 64 rows x 128 B.  With 16-row slices (2 KB apart) the M = 64 MMA of
+// slice j also reads the next 48 rows' worth of bytes (other slices, or B): they only feed
+// accumulator rows 16..63, which are never stored; the smaller stage leaves room for 5 of them.
+template <int ABOX>
+struct SmallShape {
+  static_assert(ABOX == 64 || ABOX == 16, "A rows per copy");
+  static constexpr int A_SLICE = ABOX * 128;
+  static constexpr int B_SLICE = 64 * 128;
+  static constexpr int STAGE_BYTES = kSmallKsub * (A_SLICE + B_SLICE);   // 64 KB or 40 KB
+  static constexpr int STAGES = ABOX == 64 ? 3 : 5;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 1) + 16;
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
 
 // TMA load of rank 4 into this CTA's shared memory, completion counted on `bar`.
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
@@ -61,12 +71,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-template <int EPI>
+template <int EPI, int ABOX>
 __global__ void __launch_bounds__(kSmallThreads, 1)
     tc_gemm_small_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          int M, int N, int K, void* __restrict__ out, long long ldo, unsigned int* status,
                          unsigned long long timeout_ns) {
   static_assert(EPI == EPI_F32 || EPI == EPI_SWIGLU, "epilogue");
+  using S = SmallShape<ABOX>;
+  constexpr int kSmallStages = S::STAGES;
+  constexpr int kSmallStageBytes = S::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(ring + kSmallStages * kSmallStageBytes);
@@ -119,9 +132,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         mbar_arrive_expect_tx(&full_bar[stage], kSmallStageBytes);
         tma_load_3d(st, &tmA, &full_bar[stage], 0, 0, ks * kSmallKsub);
         if (EPI == EPI_SWIGLU)
-          tma_load_4d(st + kSmallKsub * kSmallSlice, &tmB, &full_bar[stage], 0, n0, 0, ks * kSmallKsub);
+          tma_load_4d(st + kSmallKsub * S::A_SLICE, &tmB, &full_bar[stage], 0, n0, 0, ks * kSmallKsub);
         else
-          tma_load_3d(st + kSmallKsub * kSmallSlice, &tmB, &full_bar[stage], 0, n0, ks * kSmallKsub);
+          tma_load_3d(st + kSmallKsub * S::A_SLICE, &tmB, &full_bar[stage], 0, n0, ks * kSmallKsub);
         filled_phase[stage] = static_cast<int>(phase);
         if (++stage == kSmallStages) { stage = 0; phase ^= 1u; }
       }
@@ -135,7 +148,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     if (lane == 0) {
       constexpr uint32_t IDESC = idesc_bf16_f32(64, 64);
       const uint64_t adesc0 = sdesc_k_sw128(smem_u32(ring));
-      const uint64_t bdesc0 = sdesc_k_sw128(smem_u32(ring + kSmallKsub * kSmallSlice));
+      const uint64_t bdesc0 = sdesc_k_sw128(smem_u32(ring + kSmallKsub * S::A_SLICE));
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -145,10 +158,11 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         const int nsub = min(kSmallKsub, num_kb - ks * kSmallKsub);
         for (int j = 0; j < nsub; ++j) {
           const int kb = ks * kSmallKsub + j;     // K blocks ascending, one accumulation chain
-          const uint64_t so = static_cast<uint64_t>((stage * kSmallStageBytes + j * kSmallSlice) >> 4);
+          const uint64_t sa = static_cast<uint64_t>((stage * kSmallStageBytes + j * S::A_SLICE) >> 4);
+          const uint64_t sb = static_cast<uint64_t>((stage * kSmallStageBytes + j * S::B_SLICE) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_bf16(tmem_base, adesc0 + so + 2u * kk, bdesc0 + so + 2u * kk, IDESC, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16(tmem_base, adesc0 + sa + 2u * kk, bdesc0 + sb + 2u * kk, IDESC, (kb | kk) != 0 ? 1u : 0u);
         }
         umma_commit(&empty_bar[stage]);
         if (++stage == kSmallStages) { stage = 0; phase ^= 1u; }
