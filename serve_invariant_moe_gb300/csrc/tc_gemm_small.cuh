@@ -13,7 +13,8 @@
 // chain of M = 64..128, N <= 64 MMAs runs at ~29 ns per MMA).  Here a ring stage holds kSmallKsub
 // consecutive K blocks of both operands, each operand loaded by ONE rank-3 TMA copy (64 elements x
 // 64 rows x kSmallKsub blocks of 64 columns of K): two copies per stage feed 4 * kSmallKsub MMAs.
-//   * A: the M <= 64 rows of X, as (64, rows, K / 64); rows past M are zero-filled by the copy.
+//   * A: the M <= 64 rows of X, as (64, rows, K / 64), in 64-row copies (16-row ones for M <= 16,
+//     see SmallShape); rows past M are zero-filled by the copy.
 //   * B: 64 rows of W starting at row 64 * blockIdx.x, as (64, rows, K / 64).
 //   Each 64-row x 128-byte slice of a box lands 8 KB apart in shared memory with the 128-byte
 //   swizzle of a 2-D box, which is the operand layout of one K block.
